@@ -1,0 +1,191 @@
+"""ctypes binding of the fa512 C ABI (``include/fa512.h``).
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the ``stream`` argument, and a non-zero status becomes a
+:class:`Fa512Error`.  Every step of the computation runs in the library's
+CUDA kernels; there is no fallback of any kind.  torch supplies device memory
+(outputs and the decode workspace when the caller passes none) and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+HEAD_DIM = 512
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libfa512.so"
+_lock = threading.Lock()
+_lib = None
+
+_STATUS = {
+    0: "FA512_OK",
+    1: "FA512_ERR_INVALID_ARG",
+    2: "FA512_ERR_UNSUPPORTED",
+    3: "FA512_ERR_CUDA",
+    4: "FA512_ERR_TIMEOUT",
+    5: "FA512_ERR_WORKSPACE",
+    6: "FA512_ERR_DEVICE_INDEX",
+}
+
+
+class Fa512Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s (%d): %s" % (_STATUS.get(status, "?"), status, message))
+        self.status = status
+
+
+def library_path() -> str:
+    return os.environ.get("FA512_LIBRARY", os.path.join(_HERE, _LIB_NAME))
+
+
+def load_library():
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise Fa512Error(3, "CUDA library %s is missing; build it with "
+                                "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+        lib = ctypes.CDLL(path)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa512_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P]
+        lib.fa512_prefill.restype = I
+        lib.fa512_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I,
+                                           P, Z, P]
+        lib.fa512_decode_paged.restype = I
+        lib.fa512_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
+        lib.fa512_decode_workspace_bytes.restype = Z
+        lib.fa512_decode_auto_splits.argtypes = [I, I, I, I]
+        lib.fa512_decode_auto_splits.restype = I
+        lib.fa512_device_status.argtypes = [P, I]
+        lib.fa512_device_status.restype = I
+        lib.fa512_status_string.argtypes = [I]
+        lib.fa512_status_string.restype = ctypes.c_char_p
+        lib.fa512_last_error_message.argtypes = []
+        lib.fa512_last_error_message.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        lib = load_library()
+        msg = lib.fa512_last_error_message()
+        raise Fa512Error(status, msg.decode() if msg else "")
+
+
+def _dptr(t: torch.Tensor | None, name: str, dtype=None) -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise Fa512Error(1, "%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise Fa512Error(1, "%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise Fa512Error(1, "%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def fa512_status_string(status: int) -> str:
+    return load_library().fa512_status_string(int(status)).decode()
+
+
+def fa512_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                  out: torch.Tensor | None = None, lse: torch.Tensor | None = None, *,
+                  q_offset: int = 0, scale: float | None = None, causal: bool = True,
+                  window: int = 0, return_lse: bool = True, stream=None):
+    """Attention forward of one prefill chunk; returns ``(out, lse)``.
+
+    q [seqlen_q, n_q_heads, 512], k/v [seqlen_k, n_kv_heads, 512], bf16 CUDA.
+    out is allocated when not given; lse [n_q_heads, seqlen_q] fp32 likewise
+    (``return_lse=False`` passes NULL).
+    """
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3 or k.shape != v.shape:
+        raise Fa512Error(1, "q, k, v must be [seq, heads, 512] with k.shape == v.shape")
+    sq, hq, d = q.shape
+    sk, hk, _ = k.shape
+    if out is None:
+        out = torch.empty((sq, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, sq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = d ** -0.5
+    lib = load_library()
+    _check(lib.fa512_prefill(_dptr(q, "q", torch.bfloat16), _dptr(k, "k", torch.bfloat16),
+                             _dptr(v, "v", torch.bfloat16), _dptr(out, "out", torch.bfloat16),
+                             _dptr(lse, "lse", torch.float32), sq, sk, int(q_offset), hq, hk,
+                             float(scale), 1 if causal else 0, int(window), _stream(stream)))
+    return out, lse
+
+
+def fa512_decode_workspace_bytes(batch: int, n_q_heads: int, n_kv_heads: int, page_size: int,
+                                 max_kv_len: int, num_splits: int = 0) -> int:
+    return int(load_library().fa512_decode_workspace_bytes(batch, n_q_heads, n_kv_heads,
+                                                           page_size, max_kv_len, num_splits))
+
+
+def fa512_decode_auto_splits(batch: int, n_kv_heads: int, page_size: int, max_kv_len: int) -> int:
+    return int(load_library().fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len))
+
+
+def fa512_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                       page_table: torch.Tensor, kv_lens: torch.Tensor,
+                       out: torch.Tensor | None = None, lse: torch.Tensor | None = None, *,
+                       max_kv_len: int | None = None, scale: float | None = None,
+                       window: int = 0, num_splits: int = 0,
+                       workspace: torch.Tensor | None = None, return_lse: bool = True,
+                       stream=None):
+    """One query token per sequence over a paged KV cache; returns ``(out, lse)``.
+
+    q [batch, n_q_heads, 512]; k_pages/v_pages [num_pages, page_size,
+    n_kv_heads, 512] bf16; page_table [batch, max_pages_per_seq] int32;
+    kv_lens [batch] int32 (all CUDA).  ``max_kv_len`` bounds kv_lens on the
+    host (default: the page table's capacity).
+    """
+    if q.dim() != 3 or k_pages.dim() != 4 or k_pages.shape != v_pages.shape:
+        raise Fa512Error(1, "q must be [batch, heads, 512], pages [n, page, heads, 512]")
+    bsz, hq, d = q.shape
+    npages, psz, hk, _ = k_pages.shape
+    if page_table.dim() != 2:
+        raise Fa512Error(1, "page_table must be [batch, max_pages_per_seq]")
+    mpps = page_table.shape[1]
+    if max_kv_len is None:
+        max_kv_len = mpps * psz
+    if out is None:
+        out = torch.empty((bsz, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((bsz, hq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = d ** -0.5
+    lib = load_library()
+    need = int(lib.fa512_decode_workspace_bytes(bsz, hq, hk, psz, int(max_kv_len),
+                                                int(num_splits)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.fa512_decode_paged(
+        _dptr(q, "q", torch.bfloat16), _dptr(k_pages, "k_pages", torch.bfloat16),
+        _dptr(v_pages, "v_pages", torch.bfloat16), _dptr(page_table, "page_table", torch.int32),
+        _dptr(kv_lens, "kv_lens", torch.int32), _dptr(out, "out", torch.bfloat16),
+        _dptr(lse, "lse", torch.float32), bsz, hq, hk, psz, npages, mpps, int(max_kv_len),
+        float(scale), int(window), int(num_splits), _dptr(workspace, "workspace"), ws_bytes,
+        _stream(stream)))
+    return out, lse
+
+
+def fa512_device_status(stream=None, clear: bool = True) -> int:
+    """Synchronise ``stream`` and return (optionally clearing) the device error word."""
+    return int(load_library().fa512_device_status(_stream(stream), 1 if clear else 0))

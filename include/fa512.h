@@ -1,0 +1,153 @@
+/*
+ * fa512 -- head-dim-512 FlashAttention forward for GB300 (sm_103a).
+ *
+ * C ABI of the library.  Plain pointers and sizes only; every device pointer
+ * is owned by the caller, the library allocates nothing and never
+ * synchronises the stream it is given.  All work is enqueued on `stream`.
+ *
+ * Operations (page title, then the part of the page that states them):
+ *
+ *  fa512_prefill -- causal GQA/MQA attention of a chunk of query rows against
+ *    the keys before them, with online softmax (running max m, running sum l,
+ *    rescaled O) so the [q x k] score matrix never reaches memory.
+ *    "Writing a FlashAttention Prefill Kernel for Gemma 4", sections "The
+ *    starting point" and "Head dim 512 breaks the textbook"; "A custom
+ *    attention kernel for Gemma 4 on the RTX PRO 6000", section "The kernel
+ *    in three steps" (query heads that share a KV head are packed into one
+ *    tile); pegainfer issue #1051, "Description" (one 8192-row chunk against
+ *    everything before it, 32 query heads over 4 KV heads).
+ *
+ *  fa512_decode_paged -- one query token per sequence against a paged KV
+ *    cache, split over the key sequence (Flash-Decoding): each split writes an
+ *    unnormalised (O, m, l) partial and a merge step combines them.
+ *    "Flash-Decoding for MQA in CUDA", section "One KV head breaks the
+ *    textbook"; vllm-project/flash-attention PR #199, "Performance" table
+ *    (q_len 1, 8 query heads over 4 KV heads, head dim 512, page size 64).
+ *
+ * Numerics: bf16 inputs and outputs, fp32 accumulation and softmax state.
+ * LSE is the natural logarithm of sum_j exp(scale * q.k_j) over the visible
+ * keys; a row with no visible key gets O = 0 and LSE = -inf
+ * (vllm-project/flash-attention PR #199, review item F4).
+ *
+ * Errors: arguments are validated before anything is enqueued; a rejected
+ * call returns a non-zero fa512_status and launches nothing.  A failed launch
+ * returns FA512_ERR_CUDA.  Faults that only the device can see (a page index
+ * outside the pool, a kv length beyond the page table, a pipeline wait that
+ * ran past its bound) are recorded in a device-side error word that
+ * fa512_device_status() reads; the kernels skip the offending access instead
+ * of trapping.
+ */
+#ifndef FA512_H
+#define FA512_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *fa512_stream_t;
+
+typedef enum {
+    FA512_OK = 0,
+    FA512_ERR_INVALID_ARG = 1, /* a pointer, size or alignment is unusable      */
+    FA512_ERR_UNSUPPORTED = 2, /* well-formed but outside what the kernels do    */
+    FA512_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed              */
+    FA512_ERR_TIMEOUT = 4,     /* device: a pipeline wait exceeded its bound     */
+    FA512_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required     */
+    FA512_ERR_DEVICE_INDEX = 6 /* device: page index or kv length out of range   */
+} fa512_status;
+
+/* Head dimension of every tensor this library accepts. */
+#define FA512_HEAD_DIM 512
+
+/*
+ * fa512_prefill -- attention forward of one prefill chunk (batch 1).
+ *
+ *   q    [seqlen_q, n_q_heads, 512]  bf16, device, contiguous
+ *   k, v [seqlen_k, n_kv_heads, 512] bf16, device, contiguous
+ *   out  [seqlen_q, n_q_heads, 512]  bf16, device, written
+ *   lse  [n_q_heads, seqlen_q]       fp32, device, written; may be NULL
+ *
+ * Query row i sits at absolute position q_offset + i.  Query head h reads KV
+ * head h / (n_q_heads / n_kv_heads).  Key j is visible to row i iff
+ *   (causal == 0 or j <= q_offset + i)  and
+ *   (window <= 0 or j > q_offset + i - window)        (window keys incl. own).
+ * scale multiplies q.k before the softmax (1/sqrt(512) for Gemma-4 shapes).
+ *
+ * Requirements: seqlen_q >= 0, seqlen_k >= 0, q_offset >= 0, n_kv_heads >= 1,
+ * n_q_heads a multiple of n_kv_heads with G = n_q_heads / n_kv_heads <= 128,
+ * every pointer 16-byte aligned.  seqlen_q == 0 is a no-op.
+ * Returns FA512_OK once the kernels are enqueued.
+ */
+fa512_status fa512_prefill(const void *q, const void *k, const void *v, void *out, float *lse,
+                           int seqlen_q, int seqlen_k, int q_offset, int n_q_heads,
+                           int n_kv_heads, float scale, int causal, int window,
+                           fa512_stream_t stream);
+
+/*
+ * fa512_decode_paged -- one query token per sequence over a paged KV cache.
+ *
+ *   q          [batch, n_q_heads, 512]                     bf16, device
+ *   k_pages    [num_pages, page_size, n_kv_heads, 512]      bf16, device
+ *   v_pages    same shape as k_pages                        bf16, device
+ *   page_table [batch, max_pages_per_seq] int32, device: logical page p of
+ *              sequence b is physical page page_table[b * max_pages_per_seq + p]
+ *   kv_lens    [batch] int32, device: live length of each sequence
+ *   out        [batch, n_q_heads, 512] bf16, device, written
+ *   lse        [batch, n_q_heads] fp32, device, written; may be NULL
+ *
+ * The query of sequence b sits at position kv_lens[b] - 1 and sees positions
+ * [max(0, kv_lens[b] - window), kv_lens[b]) (window <= 0: all of [0, len)).
+ * Only the pages that hold those positions are read.
+ *
+ * max_kv_len is a host-side upper bound of kv_lens (it sizes the split grid;
+ * no value is read back from the device).  kv_lens[b] > max_kv_len is an
+ * error recorded on the device; positions past max_kv_len are not read.
+ * num_splits: 0 picks fa512_decode_auto_splits(); otherwise 1 <= num_splits
+ * <= 1024.  workspace holds the (O, m, l) partials and must be at least
+ * fa512_decode_workspace_bytes(batch, n_q_heads, splits) bytes, 256-byte
+ * aligned, for the split count actually used.
+ *
+ * Requirements: batch >= 0, page_size a positive multiple of 16 and <= 256,
+ * n_q_heads a multiple of n_kv_heads with G <= 16, num_pages >= 1,
+ * max_kv_len <= max_pages_per_seq * page_size, tensors 16-byte aligned.
+ */
+fa512_status fa512_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *page_table, const int32_t *kv_lens, void *out,
+                                float *lse, int batch, int n_q_heads, int n_kv_heads,
+                                int page_size, int num_pages, int max_pages_per_seq,
+                                int max_kv_len, float scale, int window, int num_splits,
+                                void *workspace, size_t workspace_bytes,
+                                fa512_stream_t stream);
+
+/* Bytes of workspace fa512_decode_paged needs for this shape and split count
+ * (num_splits 0 means the automatic choice for max_kv_len).  Returns 0 for an
+ * invalid shape. */
+size_t fa512_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int page_size,
+                                    int max_kv_len, int num_splits);
+
+/* Split count chosen when num_splits == 0: enough (batch, KV head, split)
+ * work items to fill the current device's SMs about twice, each split at
+ * least one page.  Returns 1 when there is nothing to split. */
+int fa512_decode_auto_splits(int batch, int n_kv_heads, int page_size, int max_kv_len);
+
+/* Reads and optionally clears the device-side error word after
+ * synchronising `stream`.  Returns FA512_OK, FA512_ERR_TIMEOUT,
+ * FA512_ERR_DEVICE_INDEX or FA512_ERR_CUDA. */
+fa512_status fa512_device_status(fa512_stream_t stream, int clear);
+
+/* Static, human-readable name of a status code. */
+const char *fa512_status_string(fa512_status status);
+
+/* Detail of the last error returned on the calling thread (static storage,
+ * overwritten by the next failing call). */
+const char *fa512_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA512_H */

@@ -1,0 +1,161 @@
+"""fp64 CPU oracle for head-dim-512 attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library never does: it shares no
+code, header, table or helper with the CUDA path.
+
+The arithmetic lives in ``fa512_oracle.c`` (plain fp64 loops, one
+(row, head) pair at a time, the score vector materialised).  This module only
+compiles it with gcc, marshals arrays through ctypes and returns numpy fp64
+results.  Every input arrives as bf16 bit patterns and is widened exactly.
+
+Sources: "Writing a FlashAttention Prefill Kernel for Gemma 4" (the score
+matrix a classical attention materialises defines the result); "Flash-Decoding
+for MQA in CUDA", section "The test that catches what parity misses" (an FP64
+host reference over the same bf16-rounded inputs) and section "One KV head
+breaks the textbook" (the live band of a decode query); vllm-project/
+flash-attention PR #199, review item F4 (an empty row has LSE = -inf).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa512_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libfa512_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into oracle/_build (idempotent)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.check_call(cmd)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i = ctypes.c_int
+            lib.oracle_prefill.argtypes = [P, P, P, P, P, i, i, i, i, i, i,
+                                           ctypes.c_double, i, i, P, i, i]
+            lib.oracle_prefill.restype = i
+            lib.oracle_decode_paged.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, i,
+                                                ctypes.c_double, i, i]
+            lib.oracle_decode_paged.restype = i
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 tensor/array -> contiguous uint16 numpy array of its bit patterns."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            if x.dtype != torch.bfloat16:
+                raise TypeError("oracle inputs must be bf16, got %s" % x.dtype)
+            return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy()
+                                        .view(np.uint16))
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.asarray(x)
+    if a.dtype != np.uint16:
+        raise TypeError("expected bf16 bit patterns as uint16, got %s" % a.dtype)
+    return np.ascontiguousarray(a)
+
+
+def _i32(x) -> np.ndarray:
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def prefill(q, k, v, *, q_offset: int = 0, scale: float | None = None, causal: bool = True,
+            window: int = 0, rows=None, threads: int | None = None):
+    """Reference attention for a prefill chunk.
+
+    q [seqlen_q, n_q_heads, D], k/v [seqlen_k, n_kv_heads, D] (bf16).
+    Query row i sits at absolute position q_offset + i.  ``rows`` selects a
+    subset of query rows (default: all).  Returns ``(out, lse)``:
+    out [n_rows, n_q_heads, D] fp64 and lse [n_q_heads, n_rows] fp64.
+    """
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    if qb.ndim != 3 or kb.ndim != 3 or vb.shape != kb.shape:
+        raise ValueError("bad shapes")
+    sq, hq, d = qb.shape
+    sk, hk, d2 = kb.shape
+    if d2 != d:
+        raise ValueError("head_dim mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows_arr = None if rows is None else _i32(rows)
+    n_rows = sq if rows_arr is None else int(rows_arr.shape[0])
+    out = np.zeros((n_rows, hq, d), dtype=np.float64)
+    lse = np.zeros((hq, n_rows), dtype=np.float64)
+    rc = _load().oracle_prefill(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(out), _ptr(lse),
+                                sq, sk, int(q_offset), hq, hk, d, float(scale),
+                                1 if causal else 0, int(window),
+                                None if rows_arr is None else _ptr(rows_arr), n_rows,
+                                threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_prefill rejected its arguments")
+    return out, lse
+
+
+def decode_paged(q, k_pages, v_pages, page_table, kv_lens, *, scale: float | None = None,
+                 window: int = 0, threads: int | None = None):
+    """Reference attention of one query token per sequence over a paged cache.
+
+    q [batch, n_q_heads, D]; k_pages/v_pages [num_pages, page_size, n_kv_heads, D];
+    page_table [batch, max_pages_per_seq] int; kv_lens [batch] int.
+    Returns ``(out, lse)``: out [batch, n_q_heads, D] fp64, lse [batch, n_q_heads].
+    """
+    qb, kb, vb = _bits(q), _bits(k_pages), _bits(v_pages)
+    pt, kl = _i32(page_table), _i32(kv_lens)
+    bsz, hq, d = qb.shape
+    npages, psz, hk, d2 = kb.shape
+    if d2 != d or vb.shape != kb.shape or pt.ndim != 2 or pt.shape[0] != bsz:
+        raise ValueError("bad shapes")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((bsz, hq, d), dtype=np.float64)
+    lse = np.zeros((bsz, hq), dtype=np.float64)
+    rc = _load().oracle_decode_paged(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pt), _ptr(kl),
+                                     _ptr(out), _ptr(lse), bsz, hq, hk, d, psz, pt.shape[1],
+                                     npages, float(scale), int(window),
+                                     threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_decode_paged rejected its arguments")
+    return out, lse

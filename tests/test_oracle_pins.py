@@ -1,0 +1,347 @@
+"""Pins of the fp64 oracle against facts fixed by the pages and by mathematics.
+
+None of these re-types the oracle's formula: each case is built so that the
+answer follows from a closed form, an invariance or a special case, and so
+that a plausible slip in the oracle (a dropped max shift, a wrong head or
+key index, a transposed operand, a misplaced scale, an off-by-one mask)
+fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from head_dim_flashattention_gb300 import workloads
+
+D = 512
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16(x):
+    """Round to bf16 (nearest even).  Cases that need exact values build them
+    from small integers and dyadic fractions, or round first and reuse the
+    rounded values on both sides."""
+    return torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, val = line.split("=", 1)
+            vals[key.strip()] = val.strip()
+    return vals
+
+
+# ----------------------------------------------------------------- prefill
+
+def test_single_visible_key_returns_its_value():
+    """Causal row 0 (q_offset 0) sees only key 0: O = V[0], LSE = s_00."""
+    rng = np.random.default_rng(1)
+    sq, hq = 4, 2
+    q = np.zeros((sq, hq, D), np.float32)
+    q[:, :, 3] = 2.0
+    k = rng.integers(-4, 5, size=(sq, 1, D)).astype(np.float32)
+    k[0, 0, 3] = 3.0
+    v = rng.integers(-8, 9, size=(sq, 1, D)).astype(np.float32) / 4
+    q[0, :, 100] = 0.0
+    out, lse = oracle.prefill(bf16(q), bf16(k), bf16(v), scale=0.125, causal=True)
+    np.testing.assert_array_equal(out[0, 0], v[0, 0])
+    np.testing.assert_array_equal(out[0, 1], v[0, 0])
+    assert lse[0, 0] == pytest.approx(2.0 * 3.0 * 0.125, abs=1e-15)
+
+
+def test_uniform_logits_give_mean_and_log_count():
+    """q = 0: every visible key has logit 0, so O is the mean of the visible V
+    rows and LSE = ln(#visible)."""
+    rng = np.random.default_rng(2)
+    sq, sk, off = 5, 12, 7
+    q = np.zeros((sq, 2, D), np.float32)
+    k = rng.standard_normal((sk, 1, D)).astype(np.float32)
+    v = bf16(rng.standard_normal((sk, 1, D))).float().numpy()
+    out, lse = oracle.prefill(bf16(q), bf16(k), bf16(v), q_offset=off, causal=True)
+    for i in range(sq):
+        n = off + i + 1
+        np.testing.assert_allclose(out[i, 0], v[:n, 0].astype(np.float64).mean(0), atol=1e-14)
+        assert lse[1, i] == pytest.approx(math.log(n), abs=1e-14)
+
+
+def test_causal_positions_and_window_bands():
+    """V[j] = j with q = 0: row i (position p = q_offset + i) averages the
+    visible positions, p/2 causally and p - (W-1)/2 inside a window of W keys."""
+    sk, off, sq = 200, 40, 160
+    q = np.zeros((sq, 1, D), np.float32)
+    k = np.ones((sk, 1, D), np.float32)
+    v = np.repeat(np.arange(sk, dtype=np.float32)[:, None, None], D, axis=2)
+    out, _ = oracle.prefill(bf16(q), bf16(k), bf16(v), q_offset=off, causal=True)
+    for i in (0, 1, 17, 159):
+        p = off + i
+        assert out[i, 0, 0] == pytest.approx(p / 2, abs=1e-12)
+    W = 9
+    out, lse = oracle.prefill(bf16(q), bf16(k), bf16(v), q_offset=off, causal=True, window=W)
+    for i in (0, 5, 159):
+        p = off + i
+        assert out[i, 0, 7] == pytest.approx(p - (W - 1) / 2, abs=1e-12)
+        assert lse[0, i] == pytest.approx(math.log(W), abs=1e-13)
+    # window reaching before key 0 keeps only [0, p]
+    out, _ = oracle.prefill(bf16(q[:1]), bf16(k), bf16(v), q_offset=3, causal=True, window=W)
+    assert out[0, 0, 0] == pytest.approx(1.5, abs=1e-13)
+
+
+def test_q_offset_is_bottom_right_for_chunks():
+    """A chunk at q_offset = seqlen_k - seqlen_q: its last row sees every key."""
+    sk, sq = 64, 16
+    q = np.zeros((sq, 1, D), np.float32)
+    k = np.zeros((sk, 1, D), np.float32)
+    v = np.repeat(np.arange(sk, dtype=np.float32)[:, None, None], D, axis=2)
+    out, lse = oracle.prefill(bf16(q), bf16(k), bf16(v), q_offset=sk - sq)
+    assert out[-1, 0, 0] == pytest.approx((sk - 1) / 2, abs=1e-12)
+    assert lse[0, -1] == pytest.approx(math.log(sk), abs=1e-13)
+    assert lse[0, 0] == pytest.approx(math.log(sk - sq + 1), abs=1e-13)
+
+
+def test_head_mapping_is_consecutive_groups():
+    """Query head h reads KV head h // G: V of KV head c is the constant c+1."""
+    hq, hk, sk = 12, 3, 9
+    G = hq // hk
+    q = np.zeros((2, hq, D), np.float32)
+    k = np.zeros((sk, hk, D), np.float32)
+    v = np.zeros((sk, hk, D), np.float32)
+    for c in range(hk):
+        v[:, c, :] = c + 1
+    out, _ = oracle.prefill(bf16(q), bf16(k), bf16(v), q_offset=sk - 2)
+    for h in range(hq):
+        np.testing.assert_allclose(out[:, h, :], h // G + 1, atol=1e-14)
+
+
+def test_gqa_equals_mha_with_repeated_kv():
+    rng = np.random.default_rng(3)
+    sq, sk, hq, hk = 6, 11, 8, 2
+    q = bf16(rng.standard_normal((sq, hq, D)))
+    k = bf16(rng.standard_normal((sk, hk, D)))
+    v = bf16(rng.standard_normal((sk, hk, D)))
+    G = hq // hk
+    kr = k.repeat_interleave(G, dim=1)
+    vr = v.repeat_interleave(G, dim=1)
+    o1, l1 = oracle.prefill(q, k, v, q_offset=5)
+    o2, l2 = oracle.prefill(q, kr, vr, q_offset=5)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("a,b", [(2.0, 3.0), (-1.5, 4.0), (32.0, 25.0)])
+def test_two_keys_closed_form(a, b):
+    """Two keys with logits s0 = scale*a*b and s1 = 0 give weights
+    sigmoid(s0) and 1 - sigmoid(s0); LSE = ln(1 + e^s0).  The (32, 25) case
+    puts the logit at 800, beyond exp's range, so a missing max shift fails."""
+    rng = np.random.default_rng(4)
+    scale = 1.0 if a * b > 100 else 0.25
+    q = np.zeros((1, 1, D), np.float32)
+    q[0, 0, 0] = a
+    k = np.zeros((2, 1, D), np.float32)
+    k[0, 0, 0] = b
+    k[1, 0, 1] = 7.0          # orthogonal to q: logit 0
+    v = bf16(rng.standard_normal((2, 1, D))).float().numpy().astype(np.float64)
+    out, lse = oracle.prefill(bf16(q), bf16(k), bf16(v), q_offset=1, scale=scale)
+    s0 = scale * a * b
+    w0 = 1.0 / (1.0 + math.exp(-s0)) if s0 > -700 else 0.0
+    np.testing.assert_allclose(out[0, 0], w0 * v[0, 0] + (1 - w0) * v[1, 0], rtol=1e-13,
+                               atol=1e-14)
+    want = s0 + math.log1p(math.exp(-s0)) if s0 > 0 else math.log1p(math.exp(s0))
+    assert lse[0, 0] == pytest.approx(want, rel=1e-14)
+
+
+def test_dominant_key_returns_its_row_not_column():
+    """One key 60 logits above the rest: O equals that key's V row to ~e^-60.
+    V rows and columns differ everywhere, so a transposed V fails."""
+    rng = np.random.default_rng(5)
+    sk = 24
+    q = np.zeros((1, 1, D), np.float32)
+    q[0, 0, 5] = 6.0
+    k = np.zeros((sk, 1, D), np.float32)
+    k[13, 0, 5] = 10.0
+    v = bf16(rng.standard_normal((sk, 1, D))).float().numpy().astype(np.float64)
+    out, lse = oracle.prefill(bf16(q), bf16(k), bf16(v), q_offset=sk - 1, scale=1.0)
+    np.testing.assert_allclose(out[0, 0], v[13, 0], atol=1e-20 * sk + 1e-24, rtol=1e-15)
+    assert lse[0, 0] == pytest.approx(60.0 + math.log1p((sk - 1) * math.exp(-60)), abs=1e-14)
+
+
+def test_common_logit_shift_moves_lse_only():
+    """Adding c to every logit (through a spare dimension) leaves O unchanged
+    and adds c to LSE."""
+    rng = np.random.default_rng(6)
+    sq, sk = 3, 10
+    q = rng.standard_normal((sq, 1, D)).astype(np.float32)
+    k = rng.standard_normal((sk, 1, D)).astype(np.float32)
+    q[:, :, D - 1] = 0.0
+    k[:, :, D - 1] = 0.0
+    v = rng.standard_normal((sk, 1, D)).astype(np.float32)
+    q2, k2 = q.copy(), k.copy()
+    q2[:, :, D - 1] = 4.0
+    k2[:, :, D - 1] = 8.0
+    scale = 0.0625
+    o1, l1 = oracle.prefill(bf16(q), bf16(k), bf16(v), q_offset=sk - sq, scale=scale)
+    o2, l2 = oracle.prefill(bf16(q2), bf16(k2), bf16(v), q_offset=sk - sq, scale=scale)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l2 - l1, scale * 32.0, atol=1e-12)
+
+
+def test_key_order_is_irrelevant_without_mask():
+    rng = np.random.default_rng(7)
+    sq, sk = 4, 30
+    q = bf16(rng.standard_normal((sq, 2, D)))
+    k = bf16(rng.standard_normal((sk, 1, D)))
+    v = bf16(rng.standard_normal((sk, 1, D)))
+    perm = torch.as_tensor(rng.permutation(sk))
+    o1, l1 = oracle.prefill(q, k, v, causal=False)
+    o2, l2 = oracle.prefill(q, k[perm], v[perm], causal=False)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+def test_empty_rows_are_zero_with_minus_inf_lse():
+    """No visible key: O = 0, LSE = -inf (PR #199, review item F4)."""
+    q = bf16(np.ones((2, 2, D)))
+    k = bf16(np.ones((4, 1, D)))
+    out, lse = oracle.prefill(q, k, k, q_offset=10, causal=True, window=2)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+    out, lse = oracle.prefill(q, k[:0], k[:0], q_offset=0)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_sampled_rows_match_full_run():
+    """Asking for a subset of rows returns exactly those rows."""
+    cfg = workloads.PrefillConfig("t", 40, 40, 0, 4, 2, seed=11)
+    q, k, v = workloads.prefill_inputs(cfg)
+    o_all, l_all = oracle.prefill(q, k, v)
+    rows = [0, 7, 39]
+    o_s, l_s = oracle.prefill(q, k, v, rows=rows)
+    np.testing.assert_array_equal(o_s, o_all[rows])
+    np.testing.assert_array_equal(l_s, l_all[:, rows])
+
+
+def test_thread_count_does_not_change_bits():
+    cfg = workloads.PrefillConfig("t", 33, 33, 0, 4, 1, seed=12)
+    q, k, v = workloads.prefill_inputs(cfg)
+    o1, l1 = oracle.prefill(q, k, v, threads=1)
+    o2, l2 = oracle.prefill(q, k, v, threads=5)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+# ------------------------------------------------------- pages' worked cases
+
+def test_q_zero_v_one_is_one_at_every_length():
+    """PR #199 review: with q = 0 and V = 1 the exact output is 1.000 at any
+    key count (the page saw 0.500 at 32K and 0.125 at 128K from a
+    low-precision accumulator)."""
+    g = read_golden("q0_v1_long_split.txt")
+    for n in [int(x) for x in g["key_counts"].split(",")]:
+        q = torch.zeros((1, 1, D), dtype=torch.bfloat16)
+        k = workloads.randn_bf16((n, 1, D), 99)
+        v = torch.ones((n, 1, D), dtype=torch.bfloat16)
+        out, lse = oracle.prefill(q, k, v, q_offset=n - 1)
+        assert np.max(np.abs(out - float(g["expected_output"]))) < 1e-9
+        assert lse[0, 0] == pytest.approx(math.log(n), abs=1e-10)
+
+
+def test_softmax_tail_one_late_key_ahead():
+    """PR #199 review item F1: n keys, every logit 0 except one late key
+    ahead by delta.  Its weight is e^delta / (e^delta + n - 1) exactly."""
+    g = read_golden("late_key_tail.txt")
+    n = int(g["keys"])
+    for delta_s in g["deltas"].split(","):
+        delta = int(delta_s)
+        a, b = {12: (3.0, 4.0), 13: (1.0, 13.0)}[delta]
+        q = np.zeros((1, 1, D), np.float32)
+        q[0, 0, 0] = a
+        k = torch.zeros((n, 1, D), dtype=torch.bfloat16)
+        k[n - 1, 0, 0] = b
+        v = torch.zeros((n, 1, D), dtype=torch.bfloat16)
+        v[n - 1, 0, 0] = 1.0
+        v[:, 0, 1] = 1.0
+        out, lse = oracle.prefill(bf16(q), k, v, q_offset=n - 1, scale=1.0)
+        w = math.exp(delta) / (math.exp(delta) + n - 1)
+        assert out[0, 0, 0] == pytest.approx(w, rel=1e-12)
+        assert out[0, 0, 1] == pytest.approx(1.0, abs=1e-12)
+        assert lse[0, 0] == pytest.approx(math.log(math.exp(delta) + n - 1), abs=1e-12)
+
+
+# ------------------------------------------------------------------ decode
+
+def test_decode_band_and_positions():
+    """V at logical position j is the constant j / 8 and q = 0: the output is
+    the mean of the live band, (len - 1) / 2 / 8, or the window mean."""
+    page = 16
+    lens = [1, 15, 16, 17, 100]
+    pc = workloads.paged_decode_inputs(len(lens), lens, 4, 2, page, seed=21)
+    q = torch.zeros_like(pc.q)
+    for b, n in enumerate(lens):
+        for j in range(n):
+            pg = int(pc.page_table[b, j // page])
+            pc.v_pages[pg, j % page] = j / 8
+    out, lse = oracle.decode_paged(q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens)
+    for b, n in enumerate(lens):
+        np.testing.assert_allclose(out[b], (n - 1) / 2 / 8, atol=1e-12)
+        np.testing.assert_allclose(lse[b], math.log(n), atol=1e-13)
+    W = 5
+    out, lse = oracle.decode_paged(q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
+                                   window=W)
+    for b, n in enumerate(lens):
+        lo = max(0, n - W)
+        np.testing.assert_allclose(out[b], (lo + n - 1) / 2 / 8, atol=1e-12)
+        np.testing.assert_allclose(lse[b], math.log(n - lo), atol=1e-13)
+
+
+def test_decode_ignores_poisoned_slots_and_empty_sequences():
+    pc = workloads.paged_decode_inputs(3, [0, 70, 64], 8, 4, 64, seed=22)
+    out, lse = oracle.decode_paged(pc.q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens)
+    assert np.all(np.isfinite(out))
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(lse[1:]))
+
+
+def test_decode_page_permutation_invariance_and_prefill_agreement():
+    """The same logical cache laid out through two different page tables
+    gives the same result, equal to the last row of a contiguous prefill."""
+    page, n, hq, hk = 32, 150, 8, 4
+    pc = workloads.paged_decode_inputs(1, [n], hq, hk, page, seed=23)
+    o1, l1 = oracle.decode_paged(pc.q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens)
+    npg = (n + page - 1) // page
+    # gather the logical K/V contiguously, then re-page in reversed order
+    idx = pc.page_table[0, :npg].long()
+    k_lin = pc.k_pages[idx].reshape(npg * page, hk, D)[:n]
+    v_lin = pc.v_pages[idx].reshape(npg * page, hk, D)[:n]
+    o_pre, l_pre = oracle.prefill(pc.q[0][None], k_lin, v_lin, q_offset=n - 1)
+    np.testing.assert_array_equal(o1[0], o_pre[0])
+    np.testing.assert_array_equal(l1[0], l_pre[:, 0])
+    rev = torch.arange(npg - 1, -1, -1)
+    k2 = pc.k_pages[idx][rev]
+    v2 = pc.v_pages[idx][rev]
+    pt2 = (npg - 1 - torch.arange(npg, dtype=torch.int32))[None]
+    o2, l2 = oracle.decode_paged(pc.q, k2, v2, pt2, pc.kv_lens)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_decode_q0_v1_long():
+    n = 28672
+    pc = workloads.paged_decode_inputs(1, [n], 8, 4, 64, seed=24, spare_pages=1)
+    q = torch.zeros_like(pc.q)
+    v = torch.ones_like(pc.v_pages)
+    out, _ = oracle.decode_paged(q, pc.k_pages, v, pc.page_table, pc.kv_lens)
+    assert np.max(np.abs(out - 1.0)) < 1e-9
+
+
+def test_decode_rejects_out_of_range_tables():
+    pc = workloads.paged_decode_inputs(1, [10], 2, 1, 16, seed=25)
+    bad = pc.page_table.clone()
+    bad[0, 0] = 10_000
+    with pytest.raises(ValueError):
+        oracle.decode_paged(pc.q, pc.k_pages, pc.v_pages, bad, pc.kv_lens)
