@@ -1,0 +1,456 @@
+#!/usr/bin/env python3
+"""Benchmark of the hd512 attention hot path on GB300.
+
+One step = one pass of the whole path on synthetic inputs already resident in
+HBM: the chunked causal prefill (8192 query rows at positions 8192..16383
+against 16384 keys, 32 query heads over 4 KV heads, head dim 512) plus the
+paged split-K decode over the nine decode shapes (batch {1,16,64} x KV length
+{4096,16384,28672}, 8 query heads over 4 KV heads, page size 64).  L2 is
+flushed (a 512 MiB write) before every step; kernels are timed with CUDA
+events on the launching stream.
+
+Headline `value`: prefill TFLOP/s = 4 * 512 * n_q_heads * (visible query-key
+pairs) / prefill time (the FLOP convention that reproduces the 131 TFLOP the
+RTX PRO 6000 page states for 10 global layers of a 19,985-token prompt).
+Decode is reported as HBM GB/s of live K/V bytes.
+
+`--impl reference` times the fp64 CPU oracle on a bounded row sample of the
+same workload (the reference arm of this benchmark).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEAD_DIM = 512
+PREFILL = dict(name="chunked", seqlen_q=8192, seqlen_k=16384, q_offset=8192, n_q_heads=32,
+               n_kv_heads=4)
+DECODE_SHAPES = [(b, n) for b in (1, 16, 64) for n in (4096, 16384, 28672)]
+DECODE_HEADS = (8, 4)
+PAGE = 64
+METRIC = "hd512 causal prefill TFLOP/s (% of GB300 BF16 peak); decode HBM GB/s"
+
+
+def visible_pairs(seqlen_q: int, seqlen_k: int, q_offset: int, causal: bool = True,
+                  window: int = 0) -> int:
+    """Number of (query row, key) pairs the mask lets through, per query head."""
+    total = 0
+    # closed form per row is cheap enough in Python for these sizes
+    for i in range(seqlen_q):
+        p = q_offset + i
+        hi = min(seqlen_k, p + 1) if causal else seqlen_k
+        lo = max(0, p - window + 1) if window > 0 else 0
+        if hi > lo:
+            total += hi - lo
+    return total
+
+
+def prefill_flops(seqlen_q, seqlen_k, q_offset, n_q_heads, causal=True, window=0) -> int:
+    return 4 * HEAD_DIM * n_q_heads * visible_pairs(seqlen_q, seqlen_k, q_offset, causal, window)
+
+
+def decode_bytes(batch: int, kv_len: int, n_q_heads: int, n_kv_heads: int) -> int:
+    """Algorithmic HBM bytes of one decode call: live K and V rows, q, out, lse,
+    page table and lengths (the split partials are not counted)."""
+    kv = batch * kv_len * n_kv_heads * HEAD_DIM * 2 * 2
+    qo = batch * n_q_heads * HEAD_DIM * 2 * 2 + batch * n_q_heads * 4
+    pt = batch * ((kv_len + PAGE - 1) // PAGE) * 4 + batch * 4
+    return kv + qo + pt
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_digest(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "head_dim_flashattention_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, digest: str):
+    """DRAM bytes per launch recorded from an ncu capture of this exact kernel
+    source, or None when absent or taken on older source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        with open(path) as f:
+            for line in f:
+                if line.startswith("#") or not line.strip():
+                    continue
+                kv = dict(tok.split("=", 1) for tok in line.split())
+                if kv.get("kernel") == kernel and kv.get("src") == digest:
+                    return float(kv["bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        sms, maxes, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.tmp.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.tmp.name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        hi = max(sms)
+        loaded = [s for s in sms if s >= 0.5 * hi] or sms
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_sample(budget_rows: int = 24, decode_batch: int = 1, decode_len: int = 4096):
+    """Times the fp64 oracle on a bounded sample of the same workload.
+    Returns (flops, seconds, threads, description)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    from head_dim_flashattention_gb300 import workloads
+
+    cfg = workloads.PREFILL_CONFIGS["chunked"]
+    if "chunked" not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS["chunked"] = workloads.prefill_inputs(cfg)
+    q, k, v = _ORACLE_INPUTS["chunked"]
+    rows = [int(x) for x in np.linspace(0, cfg.seqlen_q - 1, budget_rows)]
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.prefill(q, k, v, q_offset=cfg.q_offset, scale=cfg.scale, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    flops = sum(4 * HEAD_DIM * cfg.n_q_heads * min(cfg.seqlen_k, cfg.q_offset + r + 1)
+                for r in rows)
+    desc = ("oracle_prefill on %d evenly spaced query rows (all 32 heads) of the chunked "
+            "config: %.3g GFLOP" % (len(rows), flops / 1e9))
+    return flops, dt, threads, desc
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    # warm-up steps, then K timed steps, each a bounded oracle sample
+    for _ in range(args.warmup):
+        oracle_sample(budget_rows=2)
+    flops_total, secs = 0, 0.0
+    threads, desc = 1, ""
+    for _ in range(args.steps):
+        f, dt, threads, desc = oracle_sample(budget_rows=args.ref_rows)
+        flops_total += f
+        secs += dt
+    value = flops_total / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "chunked prefill 8192 q rows at 8192..16383 vs 16384 keys, "
+                               "32/4 heads, d512, causal (row sample per step)",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import head_dim_flashattention_gb300 as fa
+    from head_dim_flashattention_gb300 import build as libbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        libbuild.build()
+    if world > 1:
+        dist.barrier()
+    fa.load_library()
+    stream = torch.cuda.current_stream()
+
+    # ---- resident inputs (seeded, drawn on the device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0x5EED + 2 + 1000 * rank)
+    P = PREFILL
+    q = torch.randn((P["seqlen_q"], P["n_q_heads"], HEAD_DIM), generator=g, device=dev,
+                    dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((P["seqlen_k"], P["n_kv_heads"], HEAD_DIM), generator=g, device=dev,
+                    dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn_like(k, dtype=torch.float32).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty((P["n_q_heads"], P["seqlen_q"]), dtype=torch.float32, device=dev)
+    pf_flops = prefill_flops(P["seqlen_q"], P["seqlen_k"], P["q_offset"], P["n_q_heads"])
+
+    hq, hk = DECODE_HEADS
+    dec = []
+    if not args.no_decode:
+        gcpu = torch.Generator()
+        gcpu.manual_seed(0x5EED + 5)
+        for b, n in DECODE_SHAPES:
+            npg = (n + PAGE - 1) // PAGE
+            num_pages = b * npg
+            kp = torch.randn((num_pages, PAGE, hk, HEAD_DIM), generator=g, device=dev,
+                             dtype=torch.float32).to(torch.bfloat16)
+            vp = torch.randn((num_pages, PAGE, hk, HEAD_DIM), generator=g, device=dev,
+                             dtype=torch.float32).to(torch.bfloat16)
+            perm = torch.randperm(num_pages, generator=gcpu).to(torch.int32)
+            pt = perm.view(b, npg).to(dev)
+            kl = torch.full((b,), n, dtype=torch.int32, device=dev)
+            dq = torch.randn((b, hq, HEAD_DIM), generator=g, device=dev,
+                             dtype=torch.float32).to(torch.bfloat16)
+            ws = torch.empty(fa.fa512_decode_workspace_bytes(b, hq, hk, PAGE, n, 0),
+                             dtype=torch.uint8, device=dev)
+            dec.append(dict(b=b, n=n, kp=kp, vp=vp, pt=pt, kl=kl, q=dq, ws=ws,
+                            out=torch.empty((b, hq, HEAD_DIM), dtype=torch.bfloat16, device=dev),
+                            lse=torch.empty((b, hq), dtype=torch.float32, device=dev),
+                            bytes=decode_bytes(b, n, hq, hk),
+                            splits=fa.fa512_decode_auto_splits(b, hk, PAGE, n)))
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+
+    def step(events):
+        flush.zero_()
+        events[0].record(stream)
+        fa.fa512_prefill(q, k, v, out, lse, q_offset=P["q_offset"], causal=True, stream=stream)
+        events[1].record(stream)
+        for i, d in enumerate(dec):
+            fa.fa512_decode_paged(d["q"], d["kp"], d["vp"], d["pt"], d["kl"], d["out"], d["lse"],
+                                  max_kv_len=d["n"], workspace=d["ws"], stream=stream)
+            events[2 + i].record(stream)
+
+    n_ev = 2 + len(dec)
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(n_ev)])
+    torch.cuda.synchronize()
+    assert fa.fa512_device_status() == 0
+
+    sampler = ClockSampler(local)
+    all_events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+                  for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        step(all_events[s])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = fa.fa512_device_status()
+
+    pf_ms = [e[0].elapsed_time(e[1]) for e in all_events]
+    dec_ms = [[e[1 + i].elapsed_time(e[2 + i]) for i in range(len(dec))] for e in all_events]
+    step_ms = [pf_ms[s] + sum(dec_ms[s]) for s in range(args.steps)]
+    t_pf = sum(pf_ms) / 1e3
+    t_dec = sum(sum(x) for x in dec_ms) / 1e3
+    t_step = sum(step_ms) / 1e3
+    if world > 1:
+        tt = torch.tensor([t_pf, t_dec, t_step, wall], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_pf, t_dec, t_step, wall = tt.tolist()
+
+    value = pf_flops * args.steps * world / t_pf / 1e12
+    dec_bytes = sum(d["bytes"] for d in dec)
+    dec_gbs = dec_bytes * args.steps * world / t_dec / 1e9 if dec else None
+
+    peaks, peak_kind = read_peaks()
+    pf_avg_s = t_pf / args.steps
+    pf_src = source_digest(["prefill_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
+    dec_src = source_digest(["decode_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
+    roofline = {"kernel": "fa512::prefill::prefill_kernel", "bound": "tensor",
+                "achieved": pf_flops / pf_avg_s / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": pf_flops / pf_avg_s / 1e12 / peaks["bf16_tflops"],
+                "peak_kind": "%s burst bf16 (MEASURED_PEAKS.json)" % peak_kind,
+                "frac_of_sustained": pf_flops / pf_avg_s / 1e12 / peaks["bf16_tflops_sustained"],
+                "frac_of_nominal_2250": pf_flops / pf_avg_s / 1e12 / 2250.0,
+                "traffic": recorded_traffic("prefill_kernel", pf_src), "src": pf_src}
+    decode_roofline = None
+    if dec:
+        per = {}
+        for i, d in enumerate(dec):
+            ms = sum(dec_ms[s][i] for s in range(args.steps)) / args.steps
+            per["b%d_kv%d" % (d["b"], d["n"])] = {"ms": ms, "GB/s": d["bytes"] / ms / 1e6,
+                                                  "splits": d["splits"]}
+        decode_roofline = {"kernel": "fa512::decode (split + merge)", "bound": "hbm",
+                           "achieved": dec_gbs / world, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": dec_gbs / world / peaks["hbm_gbs"],
+                           "frac_of_8000": dec_gbs / world / 8000.0,
+                           "traffic": recorded_traffic("decode_split_kernel", dec_src),
+                           "src": dec_src, "per_shape": per}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qh = q.cpu().pin_memory()
+        kh = k.cpu().pin_memory()
+        vh = v.cpu().pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            fa.fa512_prefill(qd, kd, vd, out, lse, q_offset=P["q_offset"], causal=True,
+                             stream=stream)
+            oh.copy_(out, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            flush.zero_()
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_e2e = e0.elapsed_time(e1) / 1e3
+        h2d = (q.numel() + k.numel() + v.numel()) * 2
+        d2h = out.numel() * 2 + lse.numel() * 4
+        e2e = {"value": pf_flops * args.steps * world / t_e2e / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "what": "fa512_prefill with pinned-host Q/K/V copied in and O/LSE copied out "
+                       "every step (L2 flush included)"}
+
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu:
+        f, dt, threads, desc = oracle_sample(budget_rows=args.ref_rows)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": desc, "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "chunked prefill: 8192 q rows at positions 8192..16383 vs "
+                                   "16384 keys, 32 q / 4 kv heads, d512, causal, bf16 N(0,1)"
+                                   + ("; paged decode b{1,16,64} x kv{4096,16384,28672}, 8/4 "
+                                      "heads, page 64, num_splits auto" if dec else ""),
+                       "l2": "flushed (512 MiB write) before every step",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "prefill_ms": t_pf / args.steps * 1e3,
+            "decode": ({"value": dec_gbs, "unit": "GB/s", "ms": t_dec / args.steps * 1e3,
+                        "bytes_per_step": dec_bytes} if dec else None),
+            "roofline": roofline,
+            "decode_roofline": decode_roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": (1 + 2 * len(dec)) * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_region": wall,
+            "device_status": status,
+            "context": "pages: FA4 hd512 chunked prefill 302-336 TFLOP/s on GH200 "
+                       "(44-49% of 686); not this hardware",
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=24)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,372 @@
+// C ABI of the fa512 library: argument validation, TMA tensor-map encoding,
+// split-count choice, workspace sizing and kernel launch on the caller's
+// stream.  See include/fa512.h for the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "fa512.h"
+#include "fa512_internal.h"
+
+// Device error word: bit 0 = a pipeline wait ran past its bound, bit 1 = a
+// page index or kv length outside the declared ranges.  One per device.
+__device__ unsigned fa512_device_error_word;
+
+namespace {
+
+constexpr int kHeadDim = FA512_HEAD_DIM;
+thread_local char g_last_error[512];
+
+fa512_status fail(fa512_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+
+fa512_status fail(fa512_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+fa512_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(FA512_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- per-device state: address of the device error word
+std::mutex g_mu;
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices];
+
+cudaError_t device_error_ptr(unsigned** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, fa512_device_error_word);
+        if (e != cudaSuccess) return e;
+        g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+    }
+    *out = g_err_ptr[dev];
+    return cudaSuccess;
+}
+
+// ---- tensor maps through the driver entry point (no link-time libcuda)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+fa512_status get_encoder(EncodeTiledFn* fn) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
+            return fail(FA512_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+        g_encode = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    *fn = g_encode;
+    return FA512_OK;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first,
+// strides in bytes for dims 1..rank-1.
+fa512_status encode_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides_bytes, const uint32_t* box) {
+    EncodeTiledFn enc;
+    fa512_status st = get_encoder(&enc);
+    if (st != FA512_OK) return st;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+    }
+    for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                     const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FA512_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return FA512_OK;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
+bool pow2_page(int ps) { return ps == 16 || ps == 32 || ps == 64 || ps == 128 || ps == 256; }
+
+// Tiles of the decode band (upper bound over sequences) for a host-side bound
+// on the kv length.  A window can straddle one extra tile boundary.
+long long band_tiles(int max_kv_len, int window) {
+    const int tk = fa512::decode_tile_positions();
+    long long band = max_kv_len;
+    if (window > 0 && window < band) band = window;
+    long long t = (band + tk - 1) / tk;
+    if (window > 0 && window < max_kv_len) t += 1;
+    return t;
+}
+
+int choose_splits(long long items, long long tiles, int n_sm) {
+    if (items <= 0 || tiles <= 1) return 1;
+    long long best_s = 1;
+    double best = 1e300;
+    const long long s_max = tiles < 1024 ? tiles : 1024;
+    for (long long s = 1; s <= s_max; ++s) {
+        const long long waves = (items * s + n_sm - 1) / n_sm;
+        const long long per = (tiles + s - 1) / s;
+        // time model: waves x (tiles per split + fixed cost of ~2 tiles)
+        const double cost = static_cast<double>(waves) * static_cast<double>(per + 2);
+        if (cost < best) {
+            best = cost;
+            best_s = s;
+        }
+    }
+    return static_cast<int>(best_s);
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t workspace_for(int batch, int n_q_heads, int splits) {
+    const size_t rows = static_cast<size_t>(batch) * n_q_heads * splits;
+    return round256(rows * kHeadDim * sizeof(float)) + round256(rows * 2 * sizeof(float));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa512_status_string(fa512_status s) {
+    switch (s) {
+        case FA512_OK: return "FA512_OK";
+        case FA512_ERR_INVALID_ARG: return "FA512_ERR_INVALID_ARG";
+        case FA512_ERR_UNSUPPORTED: return "FA512_ERR_UNSUPPORTED";
+        case FA512_ERR_CUDA: return "FA512_ERR_CUDA";
+        case FA512_ERR_TIMEOUT: return "FA512_ERR_TIMEOUT";
+        case FA512_ERR_WORKSPACE: return "FA512_ERR_WORKSPACE";
+        case FA512_ERR_DEVICE_INDEX: return "FA512_ERR_DEVICE_INDEX";
+    }
+    return "FA512_UNKNOWN_STATUS";
+}
+
+const char* fa512_last_error_message(void) { return g_last_error; }
+
+fa512_status fa512_prefill(const void* q, const void* k, const void* v, void* out, float* lse,
+                           int seqlen_q, int seqlen_k, int q_offset, int n_q_heads,
+                           int n_kv_heads, float scale, int causal, int window,
+                           fa512_stream_t stream) {
+    g_last_error[0] = 0;
+    if (seqlen_q < 0 || seqlen_k < 0 || q_offset < 0)
+        return fail(FA512_ERR_INVALID_ARG, "negative length or offset");
+    if (n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads != 0)
+        return fail(FA512_ERR_INVALID_ARG, "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)",
+                    n_q_heads, n_kv_heads);
+    const int G = n_q_heads / n_kv_heads;
+    if (G > 128) return fail(FA512_ERR_UNSUPPORTED, "more than 128 query heads per KV head");
+    if (!(scale == scale) || isinf(scale)) return fail(FA512_ERR_INVALID_ARG, "scale is not finite");
+    if (static_cast<long long>(q_offset) + seqlen_q > 0x7fffffffLL)
+        return fail(FA512_ERR_INVALID_ARG, "q_offset + seqlen_q overflows int32 positions");
+    if (seqlen_q == 0) return FA512_OK;
+    if (!q || !out || (seqlen_k > 0 && (!k || !v)))
+        return fail(FA512_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(out) || (seqlen_k > 0 && (!aligned16(k) || !aligned16(v))))
+        return fail(FA512_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(FA512_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+
+    unsigned* err = nullptr;
+    cudaError_t e = device_error_ptr(&err);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+
+    fa512::PrefillParams p;
+    memset(&p, 0, sizeof p);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.seqlen_q = seqlen_q;
+    p.seqlen_k = seqlen_k;
+    p.q_offset = q_offset;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = G;
+    p.tokens_per_tile = 128 / G;
+    p.rows_per_tile = p.tokens_per_tile * G;
+    p.num_q_tiles = (seqlen_q + p.tokens_per_tile - 1) / p.tokens_per_tile;
+    p.causal = causal ? 1 : 0;
+    p.window = window > 0 ? window : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    if (static_cast<long long>(p.num_q_tiles) * n_kv_heads * 2 > 0x7fffffffLL)
+        return fail(FA512_ERR_UNSUPPORTED, "grid too large");
+
+    CUtensorMap tmq, tmk, tmv;
+    memset(&tmk, 0, sizeof tmk);
+    memset(&tmv, 0, sizeof tmv);
+    {
+        const uint64_t dims[4] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(G),
+                                  static_cast<uint64_t>(n_kv_heads), static_cast<uint64_t>(seqlen_q)};
+        const uint64_t strides[3] = {kHeadDim * 2ull, static_cast<uint64_t>(G) * kHeadDim * 2ull,
+                                     static_cast<uint64_t>(n_q_heads) * kHeadDim * 2ull};
+        const uint32_t box[4] = {64u, static_cast<uint32_t>(G), 1u,
+                                 static_cast<uint32_t>(p.tokens_per_tile)};
+        fa512_status st = encode_bf16(&tmq, q, 4, dims, strides, box);
+        if (st != FA512_OK) return st;
+    }
+    if (seqlen_k > 0) {
+        const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(n_kv_heads),
+                                  static_cast<uint64_t>(seqlen_k)};
+        const uint64_t strides[2] = {kHeadDim * 2ull, static_cast<uint64_t>(n_kv_heads) * kHeadDim * 2ull};
+        const uint32_t box[3] = {64u, 1u, 64u};
+        fa512_status st = encode_bf16(&tmk, k, 3, dims, strides, box);
+        if (st != FA512_OK) return st;
+        st = encode_bf16(&tmv, v, 3, dims, strides, box);
+        if (st != FA512_OK) return st;
+    }
+    e = fa512::launch_prefill(tmq, tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return FA512_OK;
+}
+
+int fa512_decode_auto_splits(int batch, int n_kv_heads, int page_size, int max_kv_len) {
+    (void)page_size;
+    if (batch <= 0 || n_kv_heads <= 0 || max_kv_len <= 0) return 1;
+    return choose_splits(static_cast<long long>(batch) * n_kv_heads, band_tiles(max_kv_len, 0),
+                         sm_count());
+}
+
+size_t fa512_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int page_size,
+                                    int max_kv_len, int num_splits) {
+    if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_kv_len < 0 || num_splits < 0 ||
+        num_splits > 1024)
+        return 0;
+    const int s = num_splits > 0 ? num_splits
+                                 : fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len);
+    return workspace_for(batch, n_q_heads, s);
+}
+
+fa512_status fa512_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int32_t* page_table, const int32_t* kv_lens, void* out,
+                                float* lse, int batch, int n_q_heads, int n_kv_heads,
+                                int page_size, int num_pages, int max_pages_per_seq,
+                                int max_kv_len, float scale, int window, int num_splits,
+                                void* workspace, size_t workspace_bytes,
+                                fa512_stream_t stream) {
+    g_last_error[0] = 0;
+    if (batch < 0) return fail(FA512_ERR_INVALID_ARG, "negative batch");
+    if (n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads != 0)
+        return fail(FA512_ERR_INVALID_ARG, "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)",
+                    n_q_heads, n_kv_heads);
+    const int G = n_q_heads / n_kv_heads;
+    if (G > 16) return fail(FA512_ERR_UNSUPPORTED, "decode supports at most 16 query heads per KV head");
+    if (!pow2_page(page_size)) return fail(FA512_ERR_UNSUPPORTED, "page_size must be 16, 32, 64, 128 or 256");
+    if (num_pages < 1 || max_pages_per_seq < 1)
+        return fail(FA512_ERR_INVALID_ARG, "num_pages and max_pages_per_seq must be >= 1");
+    if (static_cast<long long>(num_pages) * page_size > 0x7fffffffLL)
+        return fail(FA512_ERR_UNSUPPORTED, "page pool larger than 2^31 rows");
+    if (max_kv_len < 0 || static_cast<long long>(max_kv_len) > static_cast<long long>(max_pages_per_seq) * page_size)
+        return fail(FA512_ERR_INVALID_ARG, "max_kv_len outside [0, max_pages_per_seq * page_size]");
+    if (num_splits < 0 || num_splits > 1024) return fail(FA512_ERR_INVALID_ARG, "num_splits outside [0, 1024]");
+    if (!(scale == scale) || isinf(scale)) return fail(FA512_ERR_INVALID_ARG, "scale is not finite");
+    if (batch == 0) return FA512_OK;
+    if (!q || !k_pages || !v_pages || !page_table || !kv_lens || !out)
+        return fail(FA512_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+        return fail(FA512_ERR_INVALID_ARG, "q, pages and out must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(page_table) & 3u) || (reinterpret_cast<uintptr_t>(kv_lens) & 3u) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return fail(FA512_ERR_INVALID_ARG, "page_table, kv_lens and lse must be 4-byte aligned");
+
+    const int splits = num_splits > 0 ? num_splits
+                                      : fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len);
+    const size_t need = workspace_for(batch, n_q_heads, splits);
+    if (!workspace || workspace_bytes < need)
+        return fail(FA512_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(FA512_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (static_cast<long long>(batch) * n_kv_heads > 65535LL * 65535LL)
+        return fail(FA512_ERR_UNSUPPORTED, "grid too large");
+    if (batch > 65535 || n_kv_heads > 65535) return fail(FA512_ERR_UNSUPPORTED, "grid too large");
+
+    unsigned* err = nullptr;
+    cudaError_t e = device_error_ptr(&err);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+
+    fa512::DecodeParams p;
+    memset(&p, 0, sizeof p);
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.page_table = page_table;
+    p.kv_lens = kv_lens;
+    const size_t rows = static_cast<size_t>(batch) * n_q_heads * splits;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * kHeadDim * sizeof(float)));
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.batch = batch;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = G;
+    p.page_size = page_size;
+    p.box_rows = page_size < 32 ? page_size : 32;
+    p.num_pages = num_pages;
+    p.max_pages_per_seq = max_pages_per_seq;
+    p.len_cap = max_kv_len;
+    p.window = window > 0 ? window : 0;
+    const long long tiles = band_tiles(max_kv_len, p.window);
+    p.num_splits = splits;
+    p.tiles_per_split = static_cast<int>((tiles + splits - 1) / splits);
+    if (p.tiles_per_split < 1) p.tiles_per_split = 1;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+
+    CUtensorMap tmk, tmv;
+    const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(n_kv_heads),
+                              static_cast<uint64_t>(num_pages) * page_size};
+    const uint64_t strides[2] = {kHeadDim * 2ull, static_cast<uint64_t>(n_kv_heads) * kHeadDim * 2ull};
+    const uint32_t box[3] = {64u, 1u, static_cast<uint32_t>(p.box_rows)};
+    fa512_status st = encode_bf16(&tmk, k_pages, 3, dims, strides, box);
+    if (st != FA512_OK) return st;
+    st = encode_bf16(&tmv, v_pages, 3, dims, strides, box);
+    if (st != FA512_OK) return st;
+    e = fa512::launch_decode(tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return FA512_OK;
+}
+
+fa512_status fa512_device_status(fa512_stream_t stream, int clear) {
+    g_last_error[0] = 0;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    unsigned word = 0;
+    e = cudaMemcpyFromSymbol(&word, fa512_device_error_word, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (clear && word) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(fa512_device_error_word, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+    }
+    if (word & 1u) return fail(FA512_ERR_TIMEOUT, "a kernel pipeline wait exceeded its bound");
+    if (word & 2u) return fail(FA512_ERR_DEVICE_INDEX, "a page index or kv length was out of range");
+    return FA512_OK;
+}
+
+}  // extern "C"

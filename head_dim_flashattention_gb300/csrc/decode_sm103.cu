@@ -1,0 +1,452 @@
+// Paged split-K decode for head dim 512 (Flash-Decoding), sm_103a.
+//
+// "Flash-Decoding for MQA in CUDA" (mila.toddt.me), section "One KV head
+// breaks the textbook": the key sequence of each (sequence, KV head) is split
+// across CTAs; each split writes an unnormalised (O, m, l) partial and a
+// small fixup kernel applies the online-softmax merge.  The same section:
+// walk absolute positions, read only the live band [max(0, len - window),
+// len), keep K/V tiles double-buffered and rescale once per tile.
+// vllm-project/flash-attention PR #199, "Performance": the cache is paged
+// (page size 64), 8 query heads over 4 KV heads, q_len 1.
+//
+// Work item = (split, KV head, sequence).  One CTA streams its split's key
+// tiles of TILE_K = 32 positions through a NUM_STAGES-deep ring in shared
+// memory filled by TMA (one 64-column box per page run), computes
+// S = Q K^T and O += P V for the G query heads of its KV head with bf16
+// mma.sync (rows padded to 16), and keeps the softmax state in the log2
+// domain.  HBM traffic per position and KV head: 1 KiB of K + 1 KiB of V.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fa512_device.cuh"
+#include "fa512_internal.h"
+
+namespace fa512 {
+namespace decode {
+
+constexpr int D = 512;
+constexpr int TILE_K = 32;                       // key positions per tile
+constexpr int NUM_STAGES = 3;
+constexpr int NUM_WARPS = 8;
+constexpr int NUM_THREADS = NUM_WARPS * 32;
+constexpr int CHUNK_BYTES = TILE_K * 128;        // one 64-column box column
+constexpr int TILE_BYTES = 8 * CHUNK_BYTES;      // 32 x 512 bf16 = 32 KiB
+constexpr int STAGE_BYTES = 2 * TILE_BYTES;      // K + V
+constexpr int Q_BYTES = 16 * D * 2;              // 16 padded query rows
+constexpr int P_STRIDE = 80;                     // bytes per P row (64 + pad)
+constexpr int P_BYTES = 16 * P_STRIDE;
+
+struct Smem {
+    // Offsets inside the dynamic shared memory block (1024-byte aligned base).
+    static constexpr int stages = 0;
+    static constexpr int q = NUM_STAGES * STAGE_BYTES;
+    static constexpr int p = q + Q_BYTES;
+    static constexpr int xs = p + P_BYTES;                    // 4 warps x 32 lanes x float4
+    static constexpr int redm = xs + 4 * 32 * 16;            // [4][16] float
+    static constexpr int redl = redm + 4 * 16 * 4;           // [4][16] float
+    static constexpr int full_bar = redl + 4 * 16 * 4;       // NUM_STAGES x u64
+    static constexpr int total = full_bar + NUM_STAGES * 8;
+};
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk16) {
+    // byte offset of 16-byte chunk `chunk16` (0..7) of 128-byte line `row`
+    // under the TMA 128-byte swizzle
+    return static_cast<uint32_t>(row * 128 + ((chunk16 ^ (row & 7)) << 4));
+}
+
+// Which positions of tile t (absolute positions [32t, 32t+32)) are loaded:
+// a run of box_rows positions is loaded iff it overlaps [lo, hi) and its page
+// index is valid.  Returns a 32-bit mask of loaded positions and the number
+// of loaded runs.
+struct TilePlan {
+    uint32_t loaded;   // bit r: position 32t + r was loaded
+    int runs;
+};
+
+__device__ __forceinline__ TilePlan plan_tile(const DecodeParams& p, int b, int t, int lo,
+                                              int hi, bool record) {
+    TilePlan plan{0u, 0};
+    const int box_rows = p.box_rows;
+    for (int r0 = 0; r0 < TILE_K; r0 += box_rows) {
+        const int pos0 = t * TILE_K + r0;
+        if (pos0 + box_rows <= lo || pos0 >= hi) continue;
+        const int lp = pos0 / p.page_size;
+        const int page = p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
+        if (page < 0 || page >= p.num_pages) {
+            if (record) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+            continue;
+        }
+        const uint32_t bits = (box_rows >= 32) ? 0xffffffffu : ((1u << box_rows) - 1u);
+        plan.loaded |= bits << r0;
+        plan.runs += 1;
+    }
+    return plan;
+}
+
+__device__ __forceinline__ void issue_tile(const DecodeParams& p, const CUtensorMap* tmk,
+                                           const CUtensorMap* tmv, uint8_t* stage,
+                                           uint64_t* bar, int b, int kvh, int t, int lo, int hi) {
+    const TilePlan plan = plan_tile(p, b, t, lo, hi, true);
+    const int box_rows = p.box_rows;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(plan.runs) * 8u * box_rows * 128u * 2u);
+    for (int r0 = 0; r0 < TILE_K; r0 += box_rows) {
+        if (!((plan.loaded >> r0) & 1u)) continue;
+        const int pos0 = t * TILE_K + r0;
+        const int lp = pos0 / p.page_size;
+        const int page = p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
+        const int row = page * p.page_size + (pos0 - lp * p.page_size);
+        for (int c = 0; c < 8; ++c) {
+            tma_load_3d(stage + c * CHUNK_BYTES + r0 * 128, tmk, bar, c * 64, kvh, row);
+            tma_load_3d(stage + TILE_BYTES + c * CHUNK_BYTES + r0 * 128, tmv, bar, c * 64, kvh,
+                        row);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Smem::full_bar);
+    float* redm = reinterpret_cast<float*>(smem + Smem::redm);
+    float* redl = reinterpret_cast<float*>(smem + Smem::redl);
+    float4* xs = reinterpret_cast<float4*>(smem + Smem::xs);
+
+    const int split = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int b = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int G = p.group;
+
+    // ---- live band of this sequence
+    int len = p.kv_lens[b];
+    if (len < 0 || len > p.len_cap) {
+        if (tid == 0 && split == 0 && kvh == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+        len = len < 0 ? 0 : p.len_cap;
+    }
+    const int hi = len;
+    const int lo = (p.window > 0 && len - p.window > 0) ? len - p.window : 0;
+    const int t_lo = lo / TILE_K;
+    const int t_hi = (hi + TILE_K - 1) / TILE_K;
+    const int t_begin = t_lo + split * p.tiles_per_split;
+    int t_end = t_begin + p.tiles_per_split;
+    if (t_end > t_hi) t_end = t_hi;
+    const int n_tiles = t_end > t_begin ? t_end - t_begin : 0;
+
+    if (tid == 0) {
+        for (int s = 0; s < NUM_STAGES; ++s) mbar_init(&full_bar[s], 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    // ---- Q rows of the G heads of this KV head, zero-padded to 16, swizzled
+    {
+        uint8_t* qs = smem + Smem::q;
+        for (int i = tid; i < 16 * 64; i += NUM_THREADS) {
+            const int row = i >> 6, c = i & 63;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (row < G) {
+                const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + row;
+                v = reinterpret_cast<const uint4*>(p.q + h * D)[c];
+            }
+            *reinterpret_cast<uint4*>(qs + row * 1024 + (((c & ~7) | ((c ^ row) & 7)) << 4)) = v;
+        }
+    }
+    __syncthreads();
+
+    // prologue loads
+    if (tid == 0) {
+        for (int s = 0; s < NUM_STAGES - 1 && s < n_tiles; ++s)
+            issue_tile(p, &tmk, &tmv, smem + s * STAGE_BYTES, &full_bar[s], b, kvh, t_begin + s,
+                       lo, hi);
+    }
+
+    // ---- Q fragments (A operand) for this warp's half of the head dim
+    const int nt = warp & 3;       // QK: n-tile (8 positions) of the tile
+    const int dh = warp >> 2;      // QK: half of the head dim
+    uint32_t qa[16][4];
+    {
+        const uint32_t qbase = smem_u32(smem + Smem::q);
+        const int mi = lane >> 3, rr = lane & 7;
+        const int row = rr + 8 * (mi & 1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int kk = dh * 16 + j;
+            const int c = 2 * kk + (mi >> 1);
+            ldmatrix_x4(qa[j][0], qa[j][1], qa[j][2], qa[j][3],
+                        qbase + row * 1024 + (((c & ~7) | ((c ^ row) & 7)) << 4));
+        }
+    }
+
+    float o[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float m_run0 = -INFINITY, m_run1 = -INFINITY;   // rows lane/4 and lane/4 + 8
+    float l_run0 = 0.f, l_run1 = 0.f;               // partial over this thread's positions
+    bool ok = true;
+    int failed_it = n_tiles;
+
+    for (int it = 0; it < n_tiles; ++it) {
+        const int t = t_begin + it;
+        const int st = it % NUM_STAGES;
+        uint8_t* stage = smem + st * STAGE_BYTES;
+        // refill the stage consumed in the previous iteration
+        if (tid == 0 && it + NUM_STAGES - 1 < n_tiles) {
+            const int nst = (it + NUM_STAGES - 1) % NUM_STAGES;
+            issue_tile(p, &tmk, &tmv, smem + nst * STAGE_BYTES, &full_bar[nst], b, kvh,
+                       t + NUM_STAGES - 1, lo, hi);
+        }
+        const TilePlan plan = plan_tile(p, b, t, lo, hi, false);
+        // live positions of this tile: loaded and inside [lo, hi)
+        uint32_t valid = plan.loaded;
+        {
+            const int pos0 = t * TILE_K;
+            const int a = lo - pos0 > 0 ? lo - pos0 : 0;
+            const int e = hi - pos0 < TILE_K ? hi - pos0 : TILE_K;
+            const uint32_t upto = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
+            const uint32_t from = a >= 32 ? 0u : ~((1u << a) - 1u);
+            valid &= upto & from;
+        }
+        if (!mbar_wait(&full_bar[st], static_cast<uint32_t>((it / NUM_STAGES) & 1), p.err)) {
+            ok = false;
+        }
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            failed_it = it;
+            break;
+        }
+
+        // zero V rows that hold no live position (stale or poisoned data)
+        if (valid != 0xffffffffu) {
+            uint8_t* vt = stage + TILE_BYTES;
+            for (int i = tid; i < TILE_K * 64; i += NUM_THREADS) {
+                const int r = i & 31, cc = i >> 5;   // cc: 0..63 16-byte chunks of the row
+                if (!((valid >> r) & 1u))
+                    *reinterpret_cast<uint4*>(vt + (cc >> 3) * CHUNK_BYTES + r * 128 +
+                                              ((cc & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+        }
+
+        // ---- S = Q K^T for n-tile nt over head-dim half dh
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const uint32_t kbase = smem_u32(stage);
+            const int mi = lane >> 3;
+            const int row = nt * 8 + (lane & 7);
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const int kk = dh * 16 + j + (mi >> 1);
+                const int sub = 2 * (kk & 3) + (mi & 1);
+                uint32_t r0, r1, r2, r3;
+                ldmatrix_x4(r0, r1, r2, r3, kbase + (kk >> 2) * CHUNK_BYTES + swz(row, sub));
+                mma_bf16_16816(sc, qa[j], r0, r1);
+                mma_bf16_16816(sc, qa[j + 1], r2, r3);
+            }
+        }
+        if (dh == 1) xs[nt * 32 + lane] = make_float4(sc[0], sc[1], sc[2], sc[3]);
+        __syncthreads();
+        float pr[4];
+        if (dh == 0) {
+            const float4 x = xs[nt * 32 + lane];
+            sc[0] += x.x;
+            sc[1] += x.y;
+            sc[2] += x.z;
+            sc[3] += x.w;
+            const int r = nt * 8 + 2 * (lane & 3);
+            const bool v0 = (valid >> r) & 1u, v1 = (valid >> (r + 1)) & 1u;
+            sc[0] = v0 ? sc[0] * p.scale_log2 : -INFINITY;
+            sc[1] = v1 ? sc[1] * p.scale_log2 : -INFINITY;
+            sc[2] = v0 ? sc[2] * p.scale_log2 : -INFINITY;
+            sc[3] = v1 ? sc[3] * p.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(sc[0], sc[1]), mx1 = fmaxf(sc[2], sc[3]);
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            if ((lane & 3) == 0) {
+                redm[nt * 16 + (lane >> 2)] = mx0;
+                redm[nt * 16 + (lane >> 2) + 8] = mx1;
+            }
+        }
+        __syncthreads();
+        const int row0 = lane >> 2, row1 = row0 + 8;
+        float tm0 = fmaxf(fmaxf(redm[row0], redm[16 + row0]), fmaxf(redm[32 + row0], redm[48 + row0]));
+        float tm1 = fmaxf(fmaxf(redm[row1], redm[16 + row1]), fmaxf(redm[32 + row1], redm[48 + row1]));
+        const float mn0 = fmaxf(m_run0, tm0), mn1 = fmaxf(m_run1, tm1);
+        // a row that has seen no key yet keeps m = -inf; use 0 as its shift
+        const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float a0 = fast_exp2(m_run0 - sh0), a1 = fast_exp2(m_run1 - sh1);
+        m_run0 = mn0;
+        m_run1 = mn1;
+        if (dh == 0) {
+            pr[0] = fast_exp2(sc[0] - sh0);
+            pr[1] = fast_exp2(sc[1] - sh0);
+            pr[2] = fast_exp2(sc[2] - sh1);
+            pr[3] = fast_exp2(sc[3] - sh1);
+            l_run0 = l_run0 * a0 + pr[0] + pr[1];
+            l_run1 = l_run1 * a1 + pr[2] + pr[3];
+            uint8_t* ps = smem + Smem::p;
+            const int col = nt * 8 + 2 * (lane & 3);
+            *reinterpret_cast<uint32_t*>(ps + row0 * P_STRIDE + col * 2) = pack_bf16x2(pr[0], pr[1]);
+            *reinterpret_cast<uint32_t*>(ps + row1 * P_STRIDE + col * 2) = pack_bf16x2(pr[2], pr[3]);
+        }
+        __syncthreads();
+
+        // ---- O += P V for head-dim columns [64 warp, 64 warp + 64)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            o[j][0] *= a0;
+            o[j][1] *= a0;
+            o[j][2] *= a1;
+            o[j][3] *= a1;
+        }
+        {
+            const uint32_t pbase = smem_u32(smem + Smem::p);
+            const uint32_t vbase = smem_u32(stage + TILE_BYTES + warp * CHUNK_BYTES);
+            const int mi = lane >> 3;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t a[4];
+                {
+                    const int row = (lane & 7) + 8 * (mi & 1);
+                    const int col = 16 * kk + 8 * (mi >> 1);
+                    ldmatrix_x4(a[0], a[1], a[2], a[3], pbase + row * P_STRIDE + col * 2);
+                }
+                const int pos = 16 * kk + (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                    uint32_t r0, r1, r2, r3;
+                    ldmatrix_x4_trans(r0, r1, r2, r3, vbase + swz(pos, j + (mi >> 1)));
+                    mma_bf16_16816(o[j], a, r0, r1);
+                    mma_bf16_16816(o[j + 1], a, r2, r3);
+                }
+            }
+        }
+        __syncthreads();   // stage, P and the reduction buffers are free again
+    }
+
+    // Timeout path: before leaving, wait (bounded) for every tile load that
+    // was issued but not consumed, so no copy lands in shared memory after
+    // this CTA has exited.
+    if (!ok && tid == 0) {
+        for (int k = failed_it; k < n_tiles && k < failed_it + NUM_STAGES; ++k)
+            if (!mbar_wait(&full_bar[k % NUM_STAGES], static_cast<uint32_t>((k / NUM_STAGES) & 1),
+                           p.err))
+                break;
+    }
+
+    // ---- l: sum over quad lanes and the 4 score warps
+    if (warp < 4) {
+        l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, 1);
+        l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, 2);
+        l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 1);
+        l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 2);
+        if ((lane & 3) == 0) {
+            redl[warp * 16 + (lane >> 2)] = l_run0;
+            redl[warp * 16 + (lane >> 2) + 8] = l_run1;
+        }
+    }
+    __syncthreads();
+    const size_t S = static_cast<size_t>(p.num_splits);
+    const int row0 = lane >> 2, row1 = row0 + 8;
+    // partial O (unnormalised), this warp's 64 columns
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int d = warp * 64 + 8 * j + 2 * (lane & 3);
+        if (row0 < G) {
+            const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + row0;
+            *reinterpret_cast<float2*>(p.ws_o + (h * S + split) * D + d) =
+                make_float2(ok ? o[j][0] : 0.f, ok ? o[j][1] : 0.f);
+        }
+        if (row1 < G) {
+            const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + row1;
+            *reinterpret_cast<float2*>(p.ws_o + (h * S + split) * D + d) =
+                make_float2(ok ? o[j][2] : 0.f, ok ? o[j][3] : 0.f);
+        }
+    }
+    // every thread holds the running max of rows lane/4 and lane/4 + 8;
+    // warp 0 publishes them for the partial record
+    if (warp == 0 && (lane & 3) == 0) {
+        redm[lane >> 2] = m_run0;
+        redm[(lane >> 2) + 8] = m_run1;
+    }
+    __syncthreads();
+    if (tid < G) {
+        const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + tid;
+        const float l = redl[tid] + redl[16 + tid] + redl[32 + tid] + redl[48 + tid];
+        const float m = redm[tid];
+        p.ws_ml[(h * S + split) * 2 + 0] = ok && n_tiles > 0 ? m : -INFINITY;
+        p.ws_ml[(h * S + split) * 2 + 1] = ok && n_tiles > 0 ? l : 0.f;
+    }
+}
+
+// One block per (sequence, query head): merges the splits' (O, m, l).
+__global__ void __launch_bounds__(128)
+decode_merge_kernel(const DecodeParams p) {
+    const int h = blockIdx.x;
+    const int b = blockIdx.y;
+    const size_t bh = static_cast<size_t>(b) * p.n_q_heads + h;
+    const int S = p.num_splits;
+    const float* ml = p.ws_ml + bh * S * 2;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, ml[2 * s]);
+    const int d = threadIdx.x * 4;
+    __nv_bfloat16* out = p.out + bh * D + d;
+    if (M == -INFINITY) {
+        *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
+        if (p.lse && threadIdx.x == 0) p.lse[bh] = -INFINITY;
+        return;
+    }
+    float L = 0.f, acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    const float* ob = p.ws_o + bh * S * D + d;
+    for (int s = 0; s < S; ++s) {
+        const float w = fast_exp2(ml[2 * s] - M);   // 0 for an empty split (m = -inf)
+        L += w * ml[2 * s + 1];
+        if (w != 0.f) {
+            const float4 x = *reinterpret_cast<const float4*>(ob + static_cast<size_t>(s) * D);
+            acc0 += w * x.x;
+            acc1 += w * x.y;
+            acc2 += w * x.z;
+            acc3 += w * x.w;
+        }
+    }
+    const float inv = 1.f / L;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc0 * inv, acc1 * inv);
+    packed.y = pack_bf16x2(acc2 * inv, acc3 * inv);
+    *reinterpret_cast<uint2*>(out) = packed;
+    if (p.lse && threadIdx.x == 0) p.lse[bh] = (M + log2f(L)) * 0.69314718055994530942f;
+}
+
+}  // namespace decode
+
+int decode_smem_bytes() { return decode::Smem::total + 1024; }
+
+int decode_tile_positions() { return decode::TILE_K; }
+
+cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                          cudaStream_t stream) {
+    const int smem = decode_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(decode::decode_split_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.num_splits, p.n_kv_heads, p.batch);
+    decode::decode_split_kernel<<<grid, decode::NUM_THREADS, smem, stream>>>(tmk, tmv, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 mgrid(p.n_q_heads, p.batch);
+    decode::decode_merge_kernel<<<mgrid, 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa512

