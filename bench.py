@@ -253,7 +253,7 @@ def run_ours(args):
                     dtype=torch.float32).to(torch.bfloat16)
     k = torch.randn((P["seqlen_k"], P["n_kv_heads"], HEAD_DIM), generator=g, device=dev,
                     dtype=torch.float32).to(torch.bfloat16)
-    v = torch.randn_like(k, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn(k.shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
     out = torch.empty_like(q)
     lse = torch.empty((P["n_q_heads"], P["seqlen_q"]), dtype=torch.float32, device=dev)
     pf_flops = prefill_flops(P["seqlen_q"], P["seqlen_k"], P["q_offset"], P["n_q_heads"])
