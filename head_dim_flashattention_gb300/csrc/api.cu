@@ -155,6 +155,10 @@ size_t workspace_for(int batch, int n_q_heads, int splits) {
 
 }  // namespace
 
+void fa512::set_last_error_message(const char* msg) {
+    snprintf(g_last_error, sizeof g_last_error, "%s", msg ? msg : "");
+}
+
 extern "C" {
 
 const char* fa512_status_string(fa512_status s) {

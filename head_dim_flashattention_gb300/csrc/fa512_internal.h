@@ -44,6 +44,9 @@ struct PrefillParams {
 };
 
 int prefill_smem_bytes();
+
+// Sets the text fa512_last_error_message() returns on this thread.
+void set_last_error_message(const char* msg);
 cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                            const PrefillParams& p, cudaStream_t stream);
 

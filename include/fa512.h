@@ -111,7 +111,7 @@ fa512_status fa512_prefill(const void *q, const void *k, const void *v, void *ou
  * fa512_decode_workspace_bytes(batch, n_q_heads, splits) bytes, 256-byte
  * aligned, for the split count actually used.
  *
- * Requirements: batch >= 0, page_size a positive multiple of 16 and <= 256,
+ * Requirements: batch >= 0, page_size one of 16, 32, 64, 128, 256,
  * n_q_heads a multiple of n_kv_heads with G <= 16, num_pages >= 1,
  * max_kv_len <= max_pages_per_seq * page_size, tensors 16-byte aligned.
  */
@@ -133,6 +133,43 @@ size_t fa512_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, in
  * work items to fill the current device's SMs about twice, each split at
  * least one page.  Returns 1 when there is nothing to split. */
 int fa512_decode_auto_splits(int batch, int n_kv_heads, int page_size, int max_kv_len);
+
+/*
+ * fa512_decode_paged_noalloc -- fa512_decode_paged without a workspace
+ * argument.  (The pages have no counterpart: this is a convenience of the
+ * library, not a step of the method.)
+ *
+ * For callers that cannot call cudaMalloc: code that only receives device
+ * pointers for its inputs and outputs from another framework and has no
+ * allocator of its own, or that runs where every byte of device memory
+ * belongs to a pool it does not control.  The (O, m, l) split partials go to
+ * a file-scope device array of FA512_DECODE_STATIC_SCRATCH_BYTES that the
+ * library holds on every GPU it is loaded on until the process exits.  The
+ * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
+ *
+ * Arguments, layouts and errors are those of fa512_decode_paged.  A shape
+ * whose partials need more than FA512_DECODE_STATIC_SCRATCH_BYTES
+ * (fa512_decode_workspace_bytes) is rejected with FA512_ERR_WORKSPACE before
+ * anything is enqueued; lower num_splits or the batch to fit.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  All calls share the one array and it
+ * keeps the last call's contents; nothing in it has to start at zero, since
+ * every split writes its whole partial before the merge reads it.  Calls
+ * whose kernels overlap on the GPU (different streams, or different host
+ * threads without ordering) race on the array: order them.
+ */
+#define FA512_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+fa512_status fa512_decode_paged_noalloc(const void *q, const void *k_pages,
+                                        const void *v_pages, const int32_t *page_table,
+                                        const int32_t *kv_lens, void *out, float *lse,
+                                        int batch, int n_q_heads, int n_kv_heads, int page_size,
+                                        int num_pages, int max_pages_per_seq, int max_kv_len,
+                                        float scale, int window, int num_splits,
+                                        fa512_stream_t stream);
 
 /* Reads and optionally clears the device-side error word after
  * synchronising `stream`.  Returns FA512_OK, FA512_ERR_TIMEOUT,
