@@ -5,38 +5,35 @@
 // memory ("Writing a FlashAttention Prefill Kernel for Gemma 4", sections
 // "The starting point" and "Head dim 512 breaks the textbook").
 //
-// Geometry of one work item (a cluster of two CTAs on two SMs):
-//   * GQA row packing: the pair owns one 128-row tile of T = 128 / G query
-//     tokens times the G query heads that share one KV head, so every K/V
-//     tile serves all of them ("A custom attention kernel for Gemma 4 on the
-//     RTX PRO 6000", "The kernel in three steps", step 1).  TMA gathers the
-//     packed rows from q[seq, Hq, 512] with a 4-D box {64, G, 1, T}.
-//   * Head-dim split across the pair: CTA h holds Q[:, 256h:256h+256] and
-//     O[:, 256h:256h+256] in its tensor memory and reads only the matching
-//     256 columns of K and V.  It computes the partial scores
-//     S_h = Q_h K_h^T; the two CTAs swap S_h through distributed shared
-//     memory and both run the same softmax on S_0 + S_1 (the head-dim split
-//     of "Head dim 512 breaks the textbook" and of step 2 on the RTX PRO 6000
-//     page, lifted from a warp pair to an SM pair).  A 128 x 512 fp32 O would
-//     fill all 512 TMEM columns on its own; split this way each SM holds
-//     O half (256 columns) + Q half (128 columns of bf16 pairs) + two S
-//     buffers (2 x 64 columns).
-//   * The swap moves 32 KiB per tile each way and the SM-to-SM network
-//     carries about 20 B/clk per SM, so it is kept off the critical path: a
-//     tile's partial scores are sent while the softmax of the previous tile
-//     runs, S buffers are released as soon as they are read, and P goes to
-//     shared memory, so S(j+2) = Q K(j+2)^T never waits behind O += P(j) V(j).
+// Geometry of one work item (one CTA on one SM):
+//   * GQA row packing: a 128-row tile holds T = 128 / G query tokens times
+//     the G query heads that share one KV head, so every K/V tile serves all
+//     of them ("A custom attention kernel for Gemma 4 on the RTX PRO 6000",
+//     "The kernel in three steps", step 1).  TMA gathers the packed rows
+//     from q[seq, Hq, 512] with a 4-D box {64, G, 1, T}.
+//   * Output head-dim split: a 128 x 512 fp32 O would fill all 512 TMEM
+//     columns on its own, so each q tile is served by two CTAs that each own
+//     one 256-column half of O (the head-dim split of "Head dim 512 breaks
+//     the textbook" and of step 2 on the RTX PRO 6000 page, lifted from
+//     warps to SMs).  Both CTAs compute the same full S = Q K^T and the same
+//     softmax, so no scores cross between SMs; the pair's only duplicated
+//     work is S.  (Swapping half-width partial scores instead is bound by the
+//     SM-to-SM network, about 20 B/clk per SM against 32 B/clk needed.)
+//   * Operand placement: the tensor core reads shared-memory operands through
+//     a 128 B/clk path, so as much as possible comes from TMEM.  TMEM holds O
+//     half (256 columns), Q[:, 0:256] as bf16 pairs (128 columns) and two S
+//     buffers (2 x 64 columns; P overwrites S in place).  Q[:, 256:512]
+//     stays in shared memory.  S = Q_lo K_lo^T (A from TMEM) + Q_hi K_hi^T
+//     (A from shared memory); O += P V_half with P from TMEM.
 //   * Causal / sliding-window tile skipping: only key tiles that intersect
 //     the visible band of the tile's rows are visited; only tiles that cross
 //     the band's edge are masked element by element.
 //
-// Roles per CTA (256 threads): warp 0 lane 0 issues TMA loads, warp 1 lane 0
-// issues tcgen05.mma (warp 1 also owns the TMEM allocation), warps 4-7 own
-// TMEM lanes 0-127 (one packed row per thread) and run the score exchange,
-// the softmax, the O correction and the epilogue.
-//
-// Shared memory: K half-tiles in a 3-deep ring, V half-tile single-buffered,
-// two exchange buffers (also the Q staging area), two P buffers.
+// Roles (256 threads): warp 0 lane 0 issues TMA loads, warp 1 lane 0 issues
+// tcgen05.mma (warp 1 owns the TMEM allocation), warps 4-7 own TMEM lanes
+// 0-127 (one packed row per thread) and run the softmax, the O correction
+// and the epilogue.  S is double-buffered so S(j+1) is computed while the
+// softmax works on tile j.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -52,41 +49,36 @@ namespace prefill {
 constexpr int D = 512;
 constexpr int BM = 128;                 // packed rows per tile
 constexpr int BN = 64;                  // keys per KV tile
-constexpr int DH = 256;                 // head-dim columns per CTA
+constexpr int DH = 256;                 // O columns per CTA
 constexpr int NUM_THREADS = 256;
-constexpr int K_STAGES = 3;
-constexpr int HALF_CHUNK = BN * 128;    // one 64-column box of a K or V tile: 8 KiB
-constexpr int HALF_TILE = 4 * HALF_CHUNK;   // 64 keys x 256 columns: 32 KiB
-constexpr int X_BYTES = BM * BN * 4;        // one exchanged partial S: 32 KiB
-constexpr int P_BYTES = BM * BN * 2;        // one P tile (bf16): 16 KiB
+constexpr int K_STAGES = 2;
+constexpr int Q_CHUNK = BM * 128;       // one 64-column box of Q: 16 KiB
+constexpr int KV_CHUNK = BN * 128;      // one 64-column box of K or V: 8 KiB
+constexpr int K_TILE = 8 * KV_CHUNK;    // 64 keys x 512 columns: 64 KiB
+constexpr int V_TILE = 4 * KV_CHUNK;    // 64 keys x 256 columns: 32 KiB
 
 constexpr uint32_t TM_O = 0;            // 256 columns fp32
-constexpr uint32_t TM_Q = 256;          // 128 columns (256 bf16 per row)
-constexpr uint32_t TM_S = 384;          // 2 x 64 columns fp32
+constexpr uint32_t TM_Q = 256;          // 128 columns: Q[:, 0:256] as bf16 pairs
+constexpr uint32_t TM_S = 384;          // 2 x 64 columns fp32; P (bf16) reuses the first 32
 
 // Rescale O only when the row max grows by more than this (log2 units);
 // until then the stale max stays the reference and p <= 2^8.
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
 struct Smem {
-    static constexpr int k = 0;                                  // K_STAGES x 32 KiB
-    static constexpr int v = k + K_STAGES * HALF_TILE;           // 32 KiB
-    static constexpr int x = v + HALF_TILE;                      // 2 x 32 KiB (Q staging first)
-    static constexpr int pbuf = x + 2 * X_BYTES;                 // 2 x 16 KiB
-    static constexpr int bars = pbuf + 2 * P_BYTES;
+    static constexpr int qhi = 0;                             // Q[:, 256:512]: 64 KiB
+    static constexpr int k = qhi + 4 * Q_CHUNK;               // K_STAGES x 64 KiB
+    static constexpr int v = k + K_STAGES * K_TILE;           // 32 KiB
+    static constexpr int bars = v + V_TILE;
     enum {
         K_FULL = 0,
         K_EMPTY = K_FULL + K_STAGES,
         V_FULL = K_EMPTY + K_STAGES,
         V_EMPTY = V_FULL + 1,
-        S_FULL = V_EMPTY + 1,            // 2: S(j) computed
-        S_FREE = S_FULL + 2,             // 2: S(j) read into registers
-        P_FULL = S_FREE + 2,             // 2: P(j) written to shared memory
-        P_EMPTY = P_FULL + 2,            // 2: O += P(j) V(j) done with P(j)
-        X_FULL = P_EMPTY + 2,            // 2: the peer's partial S has landed here
-        X_EMPTY = X_FULL + 2,            // 2: the peer has consumed what we wrote there
-        Q_FULL = X_EMPTY + 2,
-        Q_READY = Q_FULL + 1,
+        S_FULL = V_EMPTY + 1,            // 2
+        P_FULL = S_FULL + 2,             // 2
+        Q_FULL = P_FULL + 2,             // Q_hi and the Q_lo staging copy landed
+        Q_READY = Q_FULL + 1,            // Q_lo is in TMEM, staging free
         O_DONE = Q_READY + 1,
         DRAIN = O_DONE + 1,
         N_BARS = DRAIN + 1
@@ -94,25 +86,23 @@ struct Smem {
     static constexpr int tmem_addr = bars + N_BARS * 8;
     static constexpr int abort_flag = tmem_addr + 4;
     static constexpr int total = abort_flag + 4;
+    // Q[:, 0:256] is staged in K stage 1 before the first K tiles arrive
+    static constexpr int qlo_staging = k + K_TILE;
 };
 static_assert(Smem::total + 1024 <= 232448, "shared memory budget");
+static_assert(4 * Q_CHUNK <= K_TILE, "Q staging fits one K stage");
 
 constexpr uint32_t IDESC_QK = make_idesc_bf16(BM, BN, 0);
 constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, DH, 1);
 
 // Bounded wait that also gives up when another role of this CTA has aborted.
-// `cluster_scope` uses acquire.cluster so that data a peer CTA released with
-// its arrival is visible after the wait.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, unsigned* err,
-                                              volatile int* abort, bool cluster_scope = false) {
+                                              volatile int* abort) {
     const uint32_t a = smem_u32(bar);
-    auto try_once = [&]() {
-        return cluster_scope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity);
-    };
-    if (try_once()) return true;
+    if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (try_once()) return true;
+        if (mbar_try_wait(a, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -128,7 +118,7 @@ __device__ __forceinline__ bool key_visible(int j, int qpos, const PrefillParams
     return j < p.seqlen_k && (!p.causal || j <= qpos) && (p.window <= 0 || j > qpos - p.window);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -141,13 +131,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const uint32_t half = cluster_ctarank();     // head-dim half of this CTA
-    const uint32_t peer = half ^ 1u;
 
-    // ---- work item: (q tile, KV head); heaviest (latest) q tiles first
-    const int pair = blockIdx.x >> 1;
-    const int kvh = pair % p.n_kv_heads;
-    const int qt = p.num_q_tiles - 1 - pair / p.n_kv_heads;
+    // ---- work item: (q tile, KV head, O half); heaviest (latest) q tiles first
+    const int half = blockIdx.x & 1;
+    const int rest = blockIdx.x >> 1;
+    const int kvh = rest % p.n_kv_heads;
+    const int qt = p.num_q_tiles - 1 - rest / p.n_kv_heads;
     const int G = p.group;
     const int t0 = qt * p.tokens_per_tile;
     const int ntok = min(p.tokens_per_tile, p.seqlen_q - t0);
@@ -169,10 +158,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int qpos = p.q_offset + t0 + tok;
     const int hq = kvh * G + g;
 
-    if (n_kt == 0) {
+    if (n_kt == 0 || timed_out_before(p.err)) {
         // no key is visible to any row of this tile: O = 0, LSE = -inf
-        // (both CTAs of the pair take this branch together)
-        if (valid_row) {
+        // (after an earlier pipeline timeout: skip the work)
+        if (n_kt == 0 && valid_row) {
             uint4* dst = reinterpret_cast<uint4*>(
                 p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + half * DH);
             for (int i = 0; i < DH / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -183,17 +172,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < Smem::N_BARS; ++i) {
-            uint32_t count = 1;
-            if (i == Smem::Q_READY || (i >= Smem::S_FREE && i < Smem::S_FREE + 2) ||
-                (i >= Smem::P_FULL && i < Smem::P_FULL + 2))
-                count = 128;                                           // every softmax thread
-            if (i >= Smem::X_FULL && i < Smem::X_EMPTY + 2) count = 4;   // the peer's 4 softmax warps
-            mbar_init(&bars[i], count);
+            const bool per_thread = i == Smem::Q_READY || i == Smem::P_FULL || i == Smem::P_FULL + 1;
+            mbar_init(&bars[i], per_thread ? 128 : 1);
         }
-        // after any earlier timeout skip the work (both CTAs still meet at
-        // the cluster barriers; a peer that did start gives up at its first
-        // bounded wait)
-        *abort = timed_out_before(p.err) ? 1 : 0;
+        *abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
@@ -204,45 +186,43 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         tmem_relinquish();
     }
     tc_fence_before_sync();
-    // both CTAs' barriers exist before either side arrives remotely
-    cluster_sync_all();
+    __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_addr_smem;
 
-    const bool skip = *abort != 0;
-    if (skip) {
-        // nothing to do; fall through to the teardown
-    } else if (warp == 0) {
+    if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------------ TMA producer
-            mbar_arrive_expect_tx(&bars[Smem::Q_FULL], static_cast<uint32_t>(4 * 128 * p.rows_per_tile));
-            for (int c = 0; c < 4; ++c)
-                tma_load_4d(smem + Smem::x + c * (BM * 128), &tmq, &bars[Smem::Q_FULL],
-                            static_cast<int>(half * 4 + c) * 64, 0, kvh, t0);
+            mbar_arrive_expect_tx(&bars[Smem::Q_FULL], static_cast<uint32_t>(8 * 128 * p.rows_per_tile));
+            for (int c = 0; c < 4; ++c) {
+                tma_load_4d(smem + Smem::qlo_staging + c * Q_CHUNK, &tmq, &bars[Smem::Q_FULL], c * 64, 0,
+                            kvh, t0);
+                tma_load_4d(smem + Smem::qhi + c * Q_CHUNK, &tmq, &bars[Smem::Q_FULL], (4 + c) * 64, 0, kvh,
+                            t0);
+            }
             auto load_k = [&](int j) -> bool {
                 const int s = j % K_STAGES;
                 if (!wait_or_abort(&bars[Smem::K_EMPTY + s], ((j / K_STAGES) & 1) ^ 1, p.err, abort))
                     return false;
-                mbar_arrive_expect_tx(&bars[Smem::K_FULL + s], HALF_TILE);
+                mbar_arrive_expect_tx(&bars[Smem::K_FULL + s], K_TILE);
                 const int key0 = (kt_begin + j) * BN;
-                for (int c = 0; c < 4; ++c)
-                    tma_load_3d(smem + Smem::k + s * HALF_TILE + c * HALF_CHUNK, &tmk,
-                                &bars[Smem::K_FULL + s], static_cast<int>(half * 4 + c) * 64, kvh, key0);
+                for (int c = 0; c < 8; ++c)
+                    tma_load_3d(smem + Smem::k + s * K_TILE + c * KV_CHUNK, &tmk, &bars[Smem::K_FULL + s],
+                                c * 64, kvh, key0);
                 return true;
             };
             auto load_v = [&](int j) -> bool {
                 if (!wait_or_abort(&bars[Smem::V_EMPTY], (j & 1) ^ 1, p.err, abort)) return false;
-                mbar_arrive_expect_tx(&bars[Smem::V_FULL], HALF_TILE);
+                mbar_arrive_expect_tx(&bars[Smem::V_FULL], V_TILE);
                 const int key0 = (kt_begin + j) * BN;
                 for (int c = 0; c < 4; ++c)
-                    tma_load_3d(smem + Smem::v + c * HALF_CHUNK, &tmv, &bars[Smem::V_FULL],
-                                static_cast<int>(half * 4 + c) * 64, kvh, key0);
+                    tma_load_3d(smem + Smem::v + c * KV_CHUNK, &tmv, &bars[Smem::V_FULL], (half * 4 + c) * 64,
+                                kvh, key0);
                 return true;
             };
-            // K runs up to three tiles ahead, V one: K(j+3) is free to load once
-            // S(j) is computed, V(j+1) once O += P(j) V(j) is done
             bool ok = load_k(0) && load_v(0);
-            for (int j = 1; ok && j < K_STAGES && j < n_kt; ++j) ok = load_k(j);
+            // K stage 1 holds the Q staging copy until Q[:, 0:256] is in TMEM
+            if (ok && n_kt > 1) ok = wait_or_abort(&bars[Smem::Q_READY], 0, p.err, abort) && load_k(1);
             for (int j = 0; ok && j < n_kt; ++j) {
                 if (j + K_STAGES < n_kt) ok = load_k(j + K_STAGES);
                 if (ok && j + 1 < n_kt) ok = load_v(j + 1);
@@ -255,44 +235,47 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             tc_fence_after_sync();
             const uint32_t k_base = smem_u32(smem + Smem::k);
             const uint32_t v_base = smem_u32(smem + Smem::v);
-            const uint32_t p_base = smem_u32(smem + Smem::pbuf);
+            const uint32_t qhi_base = smem_u32(smem + Smem::qhi);
             auto issue_qk = [&](int j) -> bool {
                 const int s = j % K_STAGES;
-                if (j >= 2 &&
-                    !wait_or_abort(&bars[Smem::S_FREE + (j & 1)], ((j - 2) >> 1) & 1, p.err, abort))
-                    return false;
                 if (!wait_or_abort(&bars[Smem::K_FULL + s], (j / K_STAGES) & 1, p.err, abort)) return false;
                 tc_fence_after_sync();
                 const uint32_t sb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
-                const uint32_t kb = k_base + s * HALF_TILE;
+                const uint32_t kb = k_base + s * K_TILE;
+                // head-dim columns 0..255: A = Q_lo from TMEM
 #pragma unroll
-                for (int kk = 0; kk < DH / 16; ++kk) {
-                    const uint64_t bd = make_sdesc_sw128(kb + (kk >> 2) * HALF_CHUNK + (kk & 3) * 32, 16, 1024);
+                for (int kk = 0; kk < 16; ++kk) {
+                    const uint64_t bd = make_sdesc_sw128(kb + (kk >> 2) * KV_CHUNK + (kk & 3) * 32, 16, 1024);
                     tc_mma_ts(sb, tmem + TM_Q + kk * 8, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+                }
+                // head-dim columns 256..511: A = Q_hi from shared memory
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint64_t ad = make_sdesc_sw128(qhi_base + (kk >> 2) * Q_CHUNK + off, 16, 1024);
+                    const uint64_t bd = make_sdesc_sw128(kb + (4 + (kk >> 2)) * KV_CHUNK + off, 16, 1024);
+                    tc_mma_ss(sb, ad, bd, IDESC_QK, 1u);
                 }
                 tc_commit(&bars[Smem::S_FULL + (j & 1)]);
                 tc_commit(&bars[Smem::K_EMPTY + s]);
                 return true;
             };
             if (ok) ok = issue_qk(0);
-            if (ok && n_kt > 1) ok = issue_qk(1);
             for (int j = 0; ok && j < n_kt; ++j) {
-                // S(j+2) as soon as S(j) has been read, ahead of O += P(j) V(j)
-                if (j + 2 < n_kt && !(ok = issue_qk(j + 2))) break;
+                // S(j+1) runs while the softmax works on tile j; its buffer last
+                // held P(j-1), consumed by O += P(j-1) V(j-1) issued before it
+                if (j + 1 < n_kt && !(ok = issue_qk(j + 1))) break;
                 if (!(ok = wait_or_abort(&bars[Smem::P_FULL + (j & 1)], (j >> 1) & 1, p.err, abort))) break;
                 if (!(ok = wait_or_abort(&bars[Smem::V_FULL], j & 1, p.err, abort))) break;
                 tc_fence_after_sync();
-                const uint32_t pb = p_base + static_cast<uint32_t>(j & 1) * P_BYTES;
+                const uint32_t pb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    // P: K-major rows of 128 B; V: MN-major, 64-column boxes
-                    // HALF_CHUNK apart, 8-key groups 1 KiB apart
-                    const uint64_t ad = make_sdesc_sw128(pb + kk * 32, 16, 1024);
-                    const uint64_t bd = make_sdesc_sw128(v_base + kk * 16 * 128, HALF_CHUNK, 1024);
-                    tc_mma_ss(tmem + TM_O, ad, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    // V is MN-major: 64-column boxes KV_CHUNK apart, 8-key groups 1 KiB apart
+                    const uint64_t bd = make_sdesc_sw128(v_base + kk * 16 * 128, KV_CHUNK, 1024);
+                    tc_mma_ts(tmem + TM_O, pb + kk * 8, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&bars[Smem::O_DONE]);
-                tc_commit(&bars[Smem::P_EMPTY + (j & 1)]);
                 tc_commit(&bars[Smem::V_EMPTY]);
             }
             // let every issued MMA finish before TMEM can be released
@@ -300,24 +283,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err);
         }
     } else if (softmax_warp) {
-        // ---------------------------------------------- exchange + softmax + epilogue
+        // ---------------------------------------------- softmax + correction + epilogue
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t x_remote = map_to_cta(smem_u32(smem + Smem::x), peer);
-        const uint32_t bar_remote = map_to_cta(smem_u32(bars), peer);
         float m_ref = -INFINITY;   // log2 units
         float l = 0.f;             // sum of the fp32 probabilities (for LSE)
         float l_b = 0.f;           // sum of the bf16-rounded probabilities (normalises O)
         bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort);
         if (ok) {
-            // Q half of this row: shared memory (TMA swizzle) -> TMEM as bf16 pairs
-            const uint8_t* qs = smem + Smem::x;
+            // Q[:, 0:256] of this row: staging copy (TMA swizzle) -> TMEM as bf16 pairs
+            const uint8_t* qs = smem + Smem::qlo_staging;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t w[32];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const uint4 v = *reinterpret_cast<const uint4*>(
-                        qs + c * (BM * 128) + row * 128 + ((i ^ (row & 7)) << 4));
+                        qs + c * Q_CHUNK + row * 128 + ((i ^ (row & 7)) << 4));
                     w[4 * i + 0] = v.x;
                     w[4 * i + 1] = v.y;
                     w[4 * i + 2] = v.z;
@@ -327,72 +308,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             }
             tmem_st_wait();
         }
+        // the staging area becomes K stage 1: order these generic reads
+        // before the TMA writes that follow the arrival
+        fence_proxy_async_smem();
         tc_fence_before_sync();
         mbar_arrive(&bars[Smem::Q_READY]);
-        // the staging area is now free for the peer's partial scores; one
-        // release-arrival per warp covers the reads of all its lanes
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive_remote(bar_remote + 8 * Smem::X_EMPTY);
-            mbar_arrive_remote(bar_remote + 8 * (Smem::X_EMPTY + 1));
-        }
 
-        // Send this CTA's partial scores of tile j to the peer: read S(j) from
-        // TMEM into `own`, release the S buffer, store into the peer's
-        // exchange buffer j % 2 (layout [16-byte chunk][row], so each warp
-        // store covers 512 contiguous bytes).  The arrival that publishes the
-        // data is issued later, after the softmax of the previous tile.
-        auto send_partial = [&](int j, float (&own)[64]) -> bool {
+        for (int j = 0; ok && j < n_kt; ++j) {
             const int b = j & 1;
             const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-            if (!wait_or_abort(&bars[Smem::S_FULL + b], ph, p.err, abort)) return false;
+            if (!(ok = wait_or_abort(&bars[Smem::S_FULL + b], ph, p.err, abort))) break;
             tc_fence_after_sync();
             uint32_t sr[2][32];
             const uint32_t s_col = TM_S + static_cast<uint32_t>(b) * BN;
             tmem_ld32(tmem + lane_base + s_col, sr[0]);
             tmem_ld32(tmem + lane_base + s_col + 32, sr[1]);
             tmem_ld_wait();
-            tc_fence_before_sync();
-            mbar_arrive(&bars[Smem::S_FREE + b]);
-#pragma unroll
-            for (int c = 0; c < 64; ++c) own[c] = __uint_as_float(sr[c >> 5][c & 31]);
-            if (!wait_or_abort(&bars[Smem::X_EMPTY + b], ph, p.err, abort, true)) return false;
-            const uint32_t xrow = static_cast<uint32_t>(b * X_BYTES + row * 16);
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                st_cluster_v4(x_remote + xrow + static_cast<uint32_t>(c) * (BM * 16), own[4 * c],
-                              own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]);
-            return true;
-        };
-        auto publish_partial = [&](int j) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(bar_remote + 8 * (Smem::X_FULL + (j & 1)));
-        };
-
-        float own_cur[64], own_next[64];
-        if (ok) ok = send_partial(0, own_cur);
-        if (ok) publish_partial(0);
-        for (int j = 0; ok && j < n_kt; ++j) {
-            const int b = j & 1;
-            const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-            const bool more = j + 1 < n_kt;
-            // the next tile's partial travels while this tile's softmax runs
-            if (more && !(ok = send_partial(j + 1, own_next))) break;
-
-            // S = S_0 + S_1: the peer's partial for tile j
-            if (!(ok = wait_or_abort(&bars[Smem::X_FULL + b], ph, p.err, abort, true))) break;
-            const uint8_t* xs = smem + Smem::x + b * X_BYTES + row * 16;
             float s[64];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float4 v = *reinterpret_cast<const float4*>(xs + c * (BM * 16));
-                // fp32 addition is commutative, so both CTAs obtain bitwise-equal
-                // S = S_0 + S_1 and hence identical P, m and l
-                s[4 * c + 0] = own_cur[4 * c + 0] + v.x;
-                s[4 * c + 1] = own_cur[4 * c + 1] + v.y;
-                s[4 * c + 2] = own_cur[4 * c + 2] + v.z;
-                s[4 * c + 3] = own_cur[4 * c + 3] + v.w;
-            }
+            for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
             const int key0 = (kt_begin + j) * BN;
             const bool tile_full = key0 + BN <= p.seqlen_k && (!p.causal || key0 + BN - 1 <= p_first) &&
@@ -466,28 +400,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                     tmem_st32(tmem + lane_base + TM_O + c * 32, o);
                 }
-                tmem_st_wait();
             }
-            // P(j) -> shared memory buffer b, K-major with the 128-byte swizzle
-            // the MMA descriptor expects; buffer b last held P(j-2)
-            if (j >= 2 && !(ok = wait_or_abort(&bars[Smem::P_EMPTY + b], ((j - 2) >> 1) & 1, p.err, abort)))
-                break;
-            {
-                uint8_t* pdst = smem + Smem::pbuf + b * P_BYTES + row * 128;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(pdst + ((c ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            }
-            fence_proxy_async_smem();
+            // P(j) overwrites the first 32 columns of S buffer b (already read)
+            tmem_st32(tmem + lane_base + s_col, pk);
+            tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(&bars[Smem::P_FULL + b]);
-            // publish the next tile's partial, then hand buffer b back to the peer
-            if (more) publish_partial(j + 1);
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(bar_remote + 8 * (Smem::X_EMPTY + b));
-#pragma unroll
-            for (int c = 0; c < 64; ++c) own_cur[c] = own_next[c];
         }
         if (ok) ok = wait_or_abort(&bars[Smem::O_DONE], static_cast<uint32_t>((n_kt - 1) & 1), p.err, abort);
         if (ok) {
@@ -520,8 +438,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 
     tc_fence_before_sync();
     __syncthreads();
-    // no CTA leaves while its peer may still write into its shared memory
-    cluster_sync_all();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, 512);
@@ -538,7 +454,7 @@ cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const
     cudaError_t e = cudaFuncSetAttribute(prefill::prefill_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int n_blocks = p.num_q_tiles * p.n_kv_heads * 2;   // one cluster of 2 per tile
+    const int n_blocks = p.num_q_tiles * p.n_kv_heads * 2;   // two O halves per q tile
     prefill::prefill_kernel<<<n_blocks, prefill::NUM_THREADS, smem, stream>>>(tmq, tmk, tmv, p);
     return cudaGetLastError();
 }
