@@ -240,10 +240,13 @@ fa512_status fa512_prefill(const void* q, const void* k, const void* v, void* ou
         const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(n_kv_heads),
                                   static_cast<uint64_t>(seqlen_k)};
         const uint64_t strides[2] = {kHeadDim * 2ull, static_cast<uint64_t>(n_kv_heads) * kHeadDim * 2ull};
-        const uint32_t box[3] = {64u, 1u, 64u};
-        fa512_status st = encode_bf16(&tmk, k, 3, dims, strides, box);
+        // the kernel streams K in head-dim chunks of a whole key tile and V
+        // in key slices; it states the box height of each
+        const uint32_t kbox[3] = {64u, 1u, static_cast<uint32_t>(fa512::prefill_k_box_rows())};
+        const uint32_t vbox[3] = {64u, 1u, static_cast<uint32_t>(fa512::prefill_v_box_rows())};
+        fa512_status st = encode_bf16(&tmk, k, 3, dims, strides, kbox);
         if (st != FA512_OK) return st;
-        st = encode_bf16(&tmv, v, 3, dims, strides, box);
+        st = encode_bf16(&tmv, v, 3, dims, strides, vbox);
         if (st != FA512_OK) return st;
     }
     e = fa512::launch_prefill(tmq, tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));

@@ -44,6 +44,8 @@ struct PrefillParams {
 };
 
 int prefill_smem_bytes();
+int prefill_k_box_rows();   // keys per K box (one head-dim chunk of a key tile)
+int prefill_v_box_rows();   // keys per V box (one key slice)
 
 // Sets the text fa512_last_error_message() returns on this thread.
 void set_last_error_message(const char* msg);

@@ -132,11 +132,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // ---- work item: (q tile, KV head, O half); heaviest (latest) q tiles first
+    // ---- work item: (q tile, KV head, O half).  KV heads run one after the
+    // other so that the CTAs resident at any time share one head's K and V
+    // in L2; within a head the heaviest (latest) q tiles go first.
     const int half = blockIdx.x & 1;
     const int rest = blockIdx.x >> 1;
-    const int kvh = rest % p.n_kv_heads;
-    const int qt = p.num_q_tiles - 1 - rest / p.n_kv_heads;
+    const int kvh = rest / p.num_q_tiles;
+    const int qt = p.num_q_tiles - 1 - rest % p.num_q_tiles;
     const int G = p.group;
     const int t0 = qt * p.tokens_per_tile;
     const int ntok = min(p.tokens_per_tile, p.seqlen_q - t0);
@@ -242,19 +244,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 tc_fence_after_sync();
                 const uint32_t sb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
                 const uint32_t kb = k_base + s * K_TILE;
-                // head-dim columns 0..255: A = Q_lo from TMEM
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t bd = make_sdesc_sw128(kb + (kk >> 2) * KV_CHUNK + (kk & 3) * 32, 16, 1024);
-                    tc_mma_ts(sb, tmem + TM_Q + kk * 8, bd, IDESC_QK, kk > 0 ? 1u : 0u);
-                }
-                // head-dim columns 256..511: A = Q_hi from shared memory
+                // Alternate the two halves of the contraction: columns 0..255
+                // take A = Q_lo from TMEM (2 KiB of shared-memory reads per
+                // MMA), columns 256..511 A = Q_hi from shared memory (6 KiB),
+                // which keeps the shared-memory read rate even and leaves room
+                // for the TMA writes of the next tiles.
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
                     const uint32_t off = (kk & 3) * 32;
+                    const uint64_t bl = make_sdesc_sw128(kb + (kk >> 2) * KV_CHUNK + off, 16, 1024);
+                    tc_mma_ts(sb, tmem + TM_Q + kk * 8, bl, IDESC_QK, kk > 0 ? 1u : 0u);
                     const uint64_t ad = make_sdesc_sw128(qhi_base + (kk >> 2) * Q_CHUNK + off, 16, 1024);
-                    const uint64_t bd = make_sdesc_sw128(kb + (4 + (kk >> 2)) * KV_CHUNK + off, 16, 1024);
-                    tc_mma_ss(sb, ad, bd, IDESC_QK, 1u);
+                    const uint64_t bh = make_sdesc_sw128(kb + (4 + (kk >> 2)) * KV_CHUNK + off, 16, 1024);
+                    tc_mma_ss(sb, ad, bh, IDESC_QK, 1u);
                 }
                 tc_commit(&bars[Smem::S_FULL + (j & 1)]);
                 tc_commit(&bars[Smem::K_EMPTY + s]);
@@ -447,6 +449,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 }  // namespace prefill
 
 int prefill_smem_bytes() { return prefill::Smem::total + 1024; }
+int prefill_k_box_rows() { return prefill::BN; }
+int prefill_v_box_rows() { return prefill::BN; }
 
 cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                            const PrefillParams& p, cudaStream_t stream) {
