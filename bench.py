@@ -260,10 +260,14 @@ def run_ours(args):
 
     hq, hk = DECODE_HEADS
     dec = []
+    shapes = DECODE_SHAPES
+    if args.decode_shapes:
+        want = set(args.decode_shapes.split(","))
+        shapes = [(b, n) for b, n in DECODE_SHAPES if "b%d_kv%d" % (b, n) in want]
     if not args.no_decode:
         gcpu = torch.Generator()
         gcpu.manual_seed(0x5EED + 5)
-        for b, n in DECODE_SHAPES:
+        for b, n in shapes:
             npg = (n + PAGE - 1) // PAGE
             num_pages = b * npg
             kp = torch.randn((num_pages, PAGE, hk, HEAD_DIM), generator=g, device=dev,
@@ -288,7 +292,8 @@ def run_ours(args):
     def step(events):
         flush.zero_()
         events[0].record(stream)
-        fa.fa512_prefill(q, k, v, out, lse, q_offset=P["q_offset"], causal=True, stream=stream)
+        if not args.no_prefill:
+            fa.fa512_prefill(q, k, v, out, lse, q_offset=P["q_offset"], causal=True, stream=stream)
         events[1].record(stream)
         for i, d in enumerate(dec):
             fa.fa512_decode_paged(d["q"], d["kp"], d["vp"], d["pt"], d["kl"], d["out"], d["lse"],
@@ -330,12 +335,12 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_pf, t_dec, t_step, wall = tt.tolist()
 
-    value = pf_flops * args.steps * world / t_pf / 1e12
+    value = pf_flops * args.steps * world / t_pf / 1e12 if not args.no_prefill else None
     dec_bytes = sum(d["bytes"] for d in dec)
     dec_gbs = dec_bytes * args.steps * world / t_dec / 1e9 if dec else None
 
     peaks, peak_kind = read_peaks()
-    pf_avg_s = t_pf / args.steps
+    pf_avg_s = t_pf / args.steps if not args.no_prefill else float("nan")
     pf_src = source_digest(["prefill_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
     dec_src = source_digest(["decode_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
     roofline = {"kernel": "fa512::prefill::prefill_kernel", "bound": "tensor",
@@ -361,7 +366,7 @@ def run_ours(args):
 
     # ---- end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.no_prefill:
         qh = q.cpu().pin_memory()
         kh = k.cpu().pin_memory()
         vh = v.cpu().pin_memory()
@@ -421,7 +426,7 @@ def run_ours(args):
             "decode_roofline": decode_roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (1 + 2 * len(dec)) * args.steps,
+            "gpu_launches": ((0 if args.no_prefill else 1) + 2 * len(dec)) * args.steps,
             "clocks": clocks,
             "wall_s_timed_region": wall,
             "device_status": status,
@@ -444,6 +449,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling)")
+    ap.add_argument("--decode-shapes", default="", help="comma list such as b64_kv28672")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -321,6 +321,8 @@ fa512_status fa512_decode_paged(const void* q, const void* k_pages, const void* 
     fa512::DecodeParams p;
     memset(&p, 0, sizeof p);
     p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
+    p.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
     p.page_table = page_table;
     p.kv_lens = kv_lens;
     const size_t rows = static_cast<size_t>(batch) * n_q_heads * splits;

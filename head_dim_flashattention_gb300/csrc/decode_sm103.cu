@@ -390,6 +390,221 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Streaming variant for small query groups (G <= 2 query heads per KV head).
+//
+// With two query heads per KV head the split is a pure stream of 2 KiB per
+// position (K row + V row) and about 2 FLOP per byte, so it runs on the FP32
+// units without any CTA-wide synchronisation: each warp owns every 8th chunk
+// of 4 positions of the split, copies its lanes' 32-byte slices of the K and
+// V rows into a private shared-memory ring with cp.async (positions outside
+// the live band are zero-filled, never read), and keeps its own online
+// softmax state with one (m, l) rescale per chunk ("Flash-Decoding for MQA in
+// CUDA", "One KV head breaks the textbook": tile-granular rescale).  The 8
+// warps' (m, l, O) are merged once at the end into the split's partial.
+namespace stream {
+
+constexpr int POS = 4;                   // positions per chunk
+constexpr int STAGES = 3;                // chunks in flight per warp
+constexpr int WARPS = 8;
+constexpr int CHUNK_BYTES = 2 * POS * D * 2;          // K and V rows: 8 KiB
+constexpr int RING_BYTES = WARPS * STAGES * CHUNK_BYTES;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    // src-size 0 fills the 16 bytes with zeros without touching global memory
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void unpack8(const uint4 a, const uint4 b, float (&f)[16]) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(WARPS * 32, 1)
+decode_stream_kernel(const DecodeParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    int len = p.kv_lens[b];
+    if (len < 0 || len > p.len_cap) {
+        if (threadIdx.x == 0 && split == 0 && kvh == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+        len = len < 0 ? 0 : p.len_cap;
+    }
+    const int hi = len;
+    const int lo = (p.window > 0 && len - p.window > 0) ? len - p.window : 0;
+    // the split covers tiles of TILE_K positions, as in the tiled variant
+    const int t_begin = lo / TILE_K + split * p.tiles_per_split;
+    const int pb = max(lo, t_begin * TILE_K);
+    const int pe = min(hi, (t_begin + p.tiles_per_split) * TILE_K);
+    const int n_chunks = pe > pb ? (pe - pb + POS - 1) / POS : 0;
+
+    // this lane's 16 head-dim columns of the G query rows, in fp32
+    float q[G][16];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + (static_cast<size_t>(b) * p.n_q_heads + kvh * G + g) * D + lane * 16);
+        unpack8(src[0], src[1], q[g]);
+    }
+    float m[G], l[G], o[G][16];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int d = 0; d < 16; ++d) o[g][d] = 0.f;
+    }
+
+    const uint32_t ring = smem_u32(smem) + warp * STAGES * CHUNK_BYTES;
+    // chunk k of this warp covers positions pb + (warp + 8k) * POS ...
+    const int my_chunks = n_chunks > warp ? (n_chunks - warp + WARPS - 1) / WARPS : 0;
+    auto issue = [&](int k) {
+        if (k < my_chunks) {
+            const int pos0 = pb + (warp + WARPS * k) * POS;
+            const uint32_t st = ring + (k % STAGES) * CHUNK_BYTES;
+#pragma unroll
+            for (int i = 0; i < POS; ++i) {
+                const int pos = pos0 + i;
+                bool valid = pos < pe;
+                size_t row = 0;
+                if (valid) {
+                    const int page = p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size];
+                    if (page < 0 || page >= p.num_pages) {
+                        report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                        valid = false;
+                    } else {
+                        row = (static_cast<size_t>(page) * p.page_size + (pos & (p.page_size - 1))) * p.n_kv_heads + kvh;
+                    }
+                }
+                const __nv_bfloat16* ks = p.k_pages + row * D + lane * 16;
+                const __nv_bfloat16* vs = p.v_pages + row * D + lane * 16;
+                const uint32_t kd = st + i * (D * 2) + lane * 32;
+                const uint32_t vd = st + (POS + i) * (D * 2) + lane * 32;
+                cp_async16(kd, ks, valid);
+                cp_async16(kd + 16, ks + 8, valid);
+                cp_async16(vd, vs, valid);
+                cp_async16(vd + 16, vs + 8, valid);
+            }
+        }
+        cp_async_commit();   // one group per chunk slot, empty past the end
+    };
+#pragma unroll
+    for (int k = 0; k < STAGES - 1; ++k) issue(k);
+
+    for (int k = 0; k < my_chunks; ++k) {
+        issue(k + STAGES - 1);
+        cp_async_wait<STAGES - 1>();   // this lane's copies of chunk k have landed
+        const uint8_t* st = smem + (warp * STAGES + (k % STAGES)) * CHUNK_BYTES;
+        const int pos0 = pb + (warp + WARPS * k) * POS;
+        float s[POS][G];
+#pragma unroll
+        for (int i = 0; i < POS; ++i) {
+            float kf[16];
+            const uint4* kr = reinterpret_cast<const uint4*>(st + i * (D * 2) + lane * 32);
+            unpack8(kr[0], kr[1], kf);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float acc = 0.f;
+#pragma unroll
+                for (int d = 0; d < 16; ++d) acc = fmaf(q[g][d], kf[d], acc);
+                s[i][g] = acc;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < POS; ++i)
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float v = s[i][g];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                s[i][g] = (pos0 + i < pe) ? v * p.scale_log2 : -INFINITY;
+            }
+        float pr[POS][G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float cm = s[0][g];
+#pragma unroll
+            for (int i = 1; i < POS; ++i) cm = fmaxf(cm, s[i][g]);
+            const float mn = fmaxf(m[g], cm);
+            const float sh = mn == -INFINITY ? 0.f : mn;   // no key seen yet
+            const float a = fast_exp2(m[g] - sh);
+            float ps = 0.f;
+#pragma unroll
+            for (int i = 0; i < POS; ++i) {
+                pr[i][g] = fast_exp2(s[i][g] - sh);
+                ps += pr[i][g];
+            }
+            l[g] = l[g] * a + ps;
+            m[g] = mn;
+#pragma unroll
+            for (int d = 0; d < 16; ++d) o[g][d] *= a;
+        }
+#pragma unroll
+        for (int i = 0; i < POS; ++i) {
+            float vf[16];
+            const uint4* vr = reinterpret_cast<const uint4*>(st + (POS + i) * (D * 2) + lane * 32);
+            unpack8(vr[0], vr[1], vf);
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int d = 0; d < 16; ++d) o[g][d] = fmaf(pr[i][g], vf[d], o[g][d]);
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();   // every warp is done with its ring: reuse it for the merge
+
+    float* so = reinterpret_cast<float*>(smem);                 // [WARPS][G][512]
+    float* sml = so + WARPS * G * D;                             // [WARPS][G][2]
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float4* dst = reinterpret_cast<float4*>(so + (warp * G + g) * D + lane * 16);
+#pragma unroll
+        for (int d = 0; d < 4; ++d)
+            dst[d] = make_float4(o[g][4 * d], o[g][4 * d + 1], o[g][4 * d + 2], o[g][4 * d + 3]);
+        if (lane == 0) {
+            sml[(warp * G + g) * 2] = m[g];
+            sml[(warp * G + g) * 2 + 1] = l[g];
+        }
+    }
+    __syncthreads();
+    const size_t S = static_cast<size_t>(p.num_splits);
+    for (int idx = threadIdx.x; idx < G * D; idx += WARPS * 32) {
+        const int g = idx / D, d = idx - g * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sml[(w * G + g) * 2]);
+        float acc = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < WARPS; ++w) {
+                const float wt = fast_exp2(sml[(w * G + g) * 2] - M);   // 0 for a warp with no key
+                acc += wt * so[(w * G + g) * D + d];
+                L += wt * sml[(w * G + g) * 2 + 1];
+            }
+        }
+        const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + g;
+        p.ws_o[(h * S + split) * D + d] = acc;
+        if (d == 0) {
+            p.ws_ml[(h * S + split) * 2 + 0] = M;
+            p.ws_ml[(h * S + split) * 2 + 1] = M == -INFINITY ? 0.f : L;
+        }
+    }
+}
+
+}  // namespace stream
+
 // One block per (sequence, query head): merges the splits' (O, m, l).
 __global__ void __launch_bounds__(128)
 decode_merge_kernel(const DecodeParams p) {
@@ -434,15 +649,34 @@ int decode_smem_bytes() { return decode::Smem::total + 1024; }
 
 int decode_tile_positions() { return decode::TILE_K; }
 
-cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
-                          cudaStream_t stream) {
-    const int smem = decode_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(decode::decode_split_kernel,
+template <int G>
+static cudaError_t launch_stream(const DecodeParams& p, cudaStream_t stream) {
+    const int smem = decode::stream::RING_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(decode::stream::decode_stream_kernel<G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.num_splits, p.n_kv_heads, p.batch);
-    decode::decode_split_kernel<<<grid, decode::NUM_THREADS, smem, stream>>>(tmk, tmv, p);
-    e = cudaGetLastError();
+    decode::stream::decode_stream_kernel<G><<<grid, decode::stream::WARPS * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                          cudaStream_t stream) {
+    cudaError_t e;
+    if (p.group == 1) {
+        e = launch_stream<1>(p, stream);
+    } else if (p.group == 2) {
+        e = launch_stream<2>(p, stream);
+    } else {
+        // larger query groups: S and PV on the tensor cores (rows padded to 16)
+        const int smem = decode_smem_bytes();
+        e = cudaFuncSetAttribute(decode::decode_split_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        dim3 grid(p.num_splits, p.n_kv_heads, p.batch);
+        decode::decode_split_kernel<<<grid, decode::NUM_THREADS, smem, stream>>>(tmk, tmv, p);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     dim3 mgrid(p.n_q_heads, p.batch);
     decode::decode_merge_kernel<<<mgrid, 128, 0, stream>>>(p);

@@ -11,6 +11,8 @@ namespace fa512 {
 
 struct DecodeParams {
     const __nv_bfloat16* q;        // [batch, n_q_heads, 512]
+    const __nv_bfloat16* k_pages;  // [num_pages, page_size, n_kv_heads, 512]
+    const __nv_bfloat16* v_pages;
     const int32_t* page_table;     // [batch, max_pages_per_seq]
     const int32_t* kv_lens;        // [batch]
     float* ws_o;                   // [batch, n_q_heads, num_splits, 512] unnormalised O
