@@ -40,6 +40,10 @@ DECODE_SHAPES = [(b, n) for b in (1, 16, 64) for n in (4096, 16384, 28672)]
 DECODE_HEADS = (8, 4)
 PAGE = 64
 METRIC = "hd512 causal prefill TFLOP/s (% of GB300 BF16 peak); decode HBM GB/s"
+PREFILL_WORKLOAD = ("chunked prefill: 8192 q rows at positions 8192..16383 vs 16384 keys, "
+                    "32 q / 4 kv heads, d512, causal, bf16 N(0,1)")
+DECODE_WORKLOAD = ("; paged decode b{1,16,64} x kv{4096,16384,28672}, 8/4 heads, page 64, "
+                   "num_splits auto")
 
 
 def visible_pairs(seqlen_q: int, seqlen_k: int, q_offset: int, causal: bool = True,
@@ -121,7 +125,7 @@ class ClockSampler:
             self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.tmp, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -208,9 +212,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "chunked prefill 8192 q rows at 8192..16383 vs 16384 keys, "
-                               "32/4 heads, d512, causal (row sample per step)",
-                   "l2": "n/a (CPU)"},
+        "config": {"workload": PREFILL_WORKLOAD, "l2": "n/a (host CPU)",
+                   "parallelism": "host threads"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -413,10 +416,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "chunked prefill: 8192 q rows at positions 8192..16383 vs "
-                                   "16384 keys, 32 q / 4 kv heads, d512, causal, bf16 N(0,1)"
-                                   + ("; paged decode b{1,16,64} x kv{4096,16384,28672}, 8/4 "
-                                      "heads, page 64, num_splits auto" if dec else ""),
+            "config": {"workload": PREFILL_WORKLOAD + (DECODE_WORKLOAD if dec else ""),
                        "l2": "flushed (512 MiB write) before every step",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "prefill_ms": t_pf / args.steps * 1e3,
@@ -442,7 +442,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=24)
