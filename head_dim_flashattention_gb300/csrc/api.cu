@@ -375,6 +375,7 @@ fa512_status fa512_device_status(fa512_stream_t stream, int clear) {
     }
     if (word & 1u) return fail(FA512_ERR_TIMEOUT, "a kernel pipeline wait exceeded its bound");
     if (word & 2u) return fail(FA512_ERR_DEVICE_INDEX, "a page index or kv length was out of range");
+    if (word & 4u) return fail(FA512_ERR_UNSUPPORTED, "the dynamic shared-memory window was not 1 KiB aligned");
     return FA512_OK;
 }
 

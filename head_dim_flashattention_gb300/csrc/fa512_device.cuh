@@ -13,6 +13,7 @@
 
 #define FA512_DEVICE_ERR_TIMEOUT 1u
 #define FA512_DEVICE_ERR_INDEX 2u
+#define FA512_DEVICE_ERR_LAYOUT 4u
 
 namespace fa512 {
 

@@ -19,21 +19,26 @@
 //     softmax, so no scores cross between SMs; the pair's only duplicated
 //     work is S.  (Swapping half-width partial scores instead is bound by the
 //     SM-to-SM network, about 20 B/clk per SM against 32 B/clk needed.)
-//   * Operand placement: the tensor core reads shared-memory operands through
-//     a 128 B/clk path, so as much as possible comes from TMEM.  TMEM holds O
-//     half (256 columns), Q[:, 0:256] as bf16 pairs (128 columns) and two S
-//     buffers (2 x 64 columns; P overwrites S in place).  Q[:, 256:512]
-//     stays in shared memory.  S = Q_lo K_lo^T (A from TMEM) + Q_hi K_hi^T
-//     (A from shared memory); O += P V_half with P from TMEM.
+//   * 128-key tiles: an M128 x N64 tcgen05.mma keeps the tensor pipe only
+//     about 55-70% busy, N128 keeps it full, so S is computed 128 keys at a
+//     time.  TMEM then holds the O half (256 columns) and two 128-column S
+//     buffers; P (bf16 pairs) overwrites S in place.  Q (128 x 512 bf16,
+//     128 KiB) stays in shared memory for the whole item and both QK^T
+//     operands come from shared memory.
+//   * K and V stream through one ring of 16 KiB slots in the order the MMAs
+//     consume them: a K slot is one 64-column head-dim chunk of 128 keys
+//     (8 per tile), a V slot is 64 keys x 128 output columns (4 per tile).
 //   * Causal / sliding-window tile skipping: only key tiles that intersect
-//     the visible band of the tile's rows are visited; only tiles that cross
-//     the band's edge are masked element by element.
+//     the visible band of the tile's rows are visited; only the 64-key halves
+//     that cross the band's edge are masked element by element.
 //
-// Roles (256 threads): warp 0 lane 0 issues TMA loads, warp 1 lane 0 issues
-// tcgen05.mma (warp 1 owns the TMEM allocation), warps 4-7 own TMEM lanes
-// 0-127 (one packed row per thread) and run the softmax, the O correction
-// and the epilogue.  S is double-buffered so S(j+1) is computed while the
-// softmax works on tile j.
+// Roles (320 threads): warp 0 lane 0 issues TMA loads, warp 1 lane 0 issues
+// tcgen05.mma (warp 1 owns the TMEM allocation), warps 2-9 run the softmax,
+// the O correction and the epilogue.  TMEM lane quadrant (warp % 4) gives a
+// softmax warp its 32 rows; warps 2-5 take keys 0-63 of each tile, warps 6-9
+// keys 64-127, and the two warps of a quadrant swap their row maxima through
+// shared memory each tile.  S is double-buffered so S(j+1) is computed while
+// the softmax works on tile j.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -48,49 +53,52 @@ namespace prefill {
 
 constexpr int D = 512;
 constexpr int BM = 128;                 // packed rows per tile
-constexpr int BN = 64;                  // keys per KV tile
+constexpr int BN = 128;                 // keys per KV tile
+constexpr int BH = BN / 2;              // keys per softmax warp
 constexpr int DH = 256;                 // O columns per CTA
-constexpr int NUM_THREADS = 256;
-constexpr int K_STAGES = 2;
+constexpr int NUM_THREADS = 320;
+constexpr int N_SOFTMAX_THREADS = 256;  // warps 2-9
 constexpr int Q_CHUNK = BM * 128;       // one 64-column box of Q: 16 KiB
-constexpr int KV_CHUNK = BN * 128;      // one 64-column box of K or V: 8 KiB
-constexpr int K_TILE = 8 * KV_CHUNK;    // 64 keys x 512 columns: 64 KiB
-constexpr int V_TILE = 4 * KV_CHUNK;    // 64 keys x 256 columns: 32 KiB
+constexpr int SLOT = 32768;             // ring slot
+constexpr int N_SLOTS = 3;
+constexpr int K_BOX_ROWS = BN;          // K slot: two {64 columns, 128 keys} boxes
+constexpr int K_BOX = K_BOX_ROWS * 128; // 16 KiB
+constexpr int V_BOX_ROWS = 64;          // V slot: four {64 columns, 64 keys} boxes
+constexpr int V_BOX = V_BOX_ROWS * 128; // 8 KiB
+constexpr int K_SLOTS_PER_TILE = D / 128;                         // 4
+constexpr int V_SLOTS_PER_TILE = BN / V_BOX_ROWS;                 // 2
 
 constexpr uint32_t TM_O = 0;            // 256 columns fp32
-constexpr uint32_t TM_Q = 256;          // 128 columns: Q[:, 0:256] as bf16 pairs
-constexpr uint32_t TM_S = 384;          // 2 x 64 columns fp32; P (bf16) reuses the first 32
+constexpr uint32_t TM_S = 256;          // 2 x 128 columns fp32; P (bf16) reuses them
 
 // Rescale O only when the row max grows by more than this (log2 units);
 // until then the stale max stays the reference and p <= 2^8.
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
 struct Smem {
-    static constexpr int qhi = 0;                             // Q[:, 256:512]: 64 KiB
-    static constexpr int k = qhi + 4 * Q_CHUNK;               // K_STAGES x 64 KiB
-    static constexpr int v = k + K_STAGES * K_TILE;           // 32 KiB
-    static constexpr int bars = v + V_TILE;
+    static constexpr int q = 0;                               // 8 x 16 KiB
+    static constexpr int ring = q + 8 * Q_CHUNK;              // N_SLOTS x 16 KiB
+    static constexpr int xmax = ring + N_SLOTS * SLOT;        // [2 buffers][2 halves][128 rows] fp32
+    static constexpr int bars = xmax + 2 * 2 * BM * 4;
     enum {
-        K_FULL = 0,
-        K_EMPTY = K_FULL + K_STAGES,
-        V_FULL = K_EMPTY + K_STAGES,
-        V_EMPTY = V_FULL + 1,
-        S_FULL = V_EMPTY + 1,            // 2
+        FULL = 0,
+        EMPTY = FULL + N_SLOTS,
+        S_FULL = EMPTY + N_SLOTS,        // 2
         P_FULL = S_FULL + 2,             // 2
-        Q_FULL = P_FULL + 2,             // Q_hi and the Q_lo staging copy landed
-        Q_READY = Q_FULL + 1,            // Q_lo is in TMEM, staging free
-        O_DONE = Q_READY + 1,
-        DRAIN = O_DONE + 1,
+        XCHG = P_FULL + 2,               // 2: row-max swap between the two softmax halves
+        Q_FULL = XCHG + 2,
+        O_DONE = Q_FULL + 1,
+        L_XCHG = O_DONE + 1,             // final row-sum swap
+        DRAIN = L_XCHG + 1,
         N_BARS = DRAIN + 1
     };
     static constexpr int tmem_addr = bars + N_BARS * 8;
     static constexpr int abort_flag = tmem_addr + 4;
     static constexpr int total = abort_flag + 4;
-    // Q[:, 0:256] is staged in K stage 1 before the first K tiles arrive
-    static constexpr int qlo_staging = k + K_TILE;
 };
-static_assert(Smem::total + 1024 <= 232448, "shared memory budget");
-static_assert(4 * Q_CHUNK <= K_TILE, "Q staging fits one K stage");
+// The dynamic shared-memory window starts 1 KiB aligned (checked at run
+// time), which the 128-byte swizzle atoms need.
+static_assert(Smem::total <= 232448, "shared memory budget");
 
 constexpr uint32_t IDESC_QK = make_idesc_bf16(BM, BN, 0);
 constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, DH, 1);
@@ -121,9 +129,11 @@ __device__ __forceinline__ bool key_visible(int j, int qpos, const PrefillParams
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {
+        if (threadIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_LAYOUT);
+        return;
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::bars);
     uint32_t* tmem_addr_smem = reinterpret_cast<uint32_t*>(smem + Smem::tmem_addr);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + Smem::abort_flag);
@@ -151,11 +161,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int kt_begin = j_lo / BN;
     const int n_kt = j_hi > j_lo ? (j_hi + BN - 1) / BN - kt_begin : 0;
 
-    // this thread's packed row (warps 4-7)
+    // this thread's packed row and key half (warps 2-9)
+    const bool softmax_warp = warp >= 2;
     const int row = (warp & 3) * 32 + lane;
+    const int kh = warp >= 6 ? 1 : 0;
     const int tok = row / G;
     const int g = row - tok * G;
-    const bool softmax_warp = warp >= 4;
     const bool valid_row = softmax_warp && row < p.rows_per_tile && tok < ntok;
     const int qpos = p.q_offset + t0 + tok;
     const int hq = kvh * G + g;
@@ -165,17 +176,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         // (after an earlier pipeline timeout: skip the work)
         if (n_kt == 0 && valid_row) {
             uint4* dst = reinterpret_cast<uint4*>(
-                p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + half * DH);
-            for (int i = 0; i < DH / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (half == 0 && p.lse) p.lse[static_cast<size_t>(hq) * p.seqlen_q + t0 + tok] = -INFINITY;
+                p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + half * DH + kh * 128);
+            for (int i = 0; i < 128 / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (half == 0 && kh == 0 && p.lse)
+                p.lse[static_cast<size_t>(hq) * p.seqlen_q + t0 + tok] = -INFINITY;
         }
         return;
     }
 
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < Smem::N_BARS; ++i) {
-            const bool per_thread = i == Smem::Q_READY || i == Smem::P_FULL || i == Smem::P_FULL + 1;
-            mbar_init(&bars[i], per_thread ? 128 : 1);
+            const bool per_thread = (i >= Smem::P_FULL && i < Smem::Q_FULL) || i == Smem::L_XCHG;
+            mbar_init(&bars[i], per_thread ? N_SOFTMAX_THREADS : 1);
         }
         *abort = 0;
         fence_mbar_init();
@@ -196,70 +208,98 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         if (lane == 0) {
             // ------------------------------------------------------------ TMA producer
             mbar_arrive_expect_tx(&bars[Smem::Q_FULL], static_cast<uint32_t>(8 * 128 * p.rows_per_tile));
-            for (int c = 0; c < 4; ++c) {
-                tma_load_4d(smem + Smem::qlo_staging + c * Q_CHUNK, &tmq, &bars[Smem::Q_FULL], c * 64, 0,
-                            kvh, t0);
-                tma_load_4d(smem + Smem::qhi + c * Q_CHUNK, &tmq, &bars[Smem::Q_FULL], (4 + c) * 64, 0, kvh,
-                            t0);
-            }
+            for (int c = 0; c < 8; ++c)
+                tma_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, &bars[Smem::Q_FULL], c * 64, 0, kvh, t0);
+            uint32_t item = 0;
+            // next ring slot in consumption order, once the MMAs have released it
+            auto next_slot = [&](int& s) -> bool {
+                s = static_cast<int>(item % N_SLOTS);
+                const uint32_t ph = (item / N_SLOTS) & 1u;
+                ++item;
+                if (!wait_or_abort(&bars[Smem::EMPTY + s], ph ^ 1u, p.err, abort)) return false;
+                mbar_arrive_expect_tx(&bars[Smem::FULL + s], SLOT);
+                return true;
+            };
             auto load_k = [&](int j) -> bool {
-                const int s = j % K_STAGES;
-                if (!wait_or_abort(&bars[Smem::K_EMPTY + s], ((j / K_STAGES) & 1) ^ 1, p.err, abort))
-                    return false;
-                mbar_arrive_expect_tx(&bars[Smem::K_FULL + s], K_TILE);
                 const int key0 = (kt_begin + j) * BN;
-                for (int c = 0; c < 8; ++c)
-                    tma_load_3d(smem + Smem::k + s * K_TILE + c * KV_CHUNK, &tmk, &bars[Smem::K_FULL + s],
-                                c * 64, kvh, key0);
+                for (int c = 0; c < K_SLOTS_PER_TILE; ++c) {
+                    int s;
+                    if (!next_slot(s)) return false;
+                    for (int b = 0; b < 2; ++b)
+                        tma_load_3d(smem + Smem::ring + s * SLOT + b * K_BOX, &tmk, &bars[Smem::FULL + s],
+                                    (c * 2 + b) * 64, kvh, key0);
+                }
                 return true;
             };
             auto load_v = [&](int j) -> bool {
-                if (!wait_or_abort(&bars[Smem::V_EMPTY], (j & 1) ^ 1, p.err, abort)) return false;
-                mbar_arrive_expect_tx(&bars[Smem::V_FULL], V_TILE);
                 const int key0 = (kt_begin + j) * BN;
-                for (int c = 0; c < 4; ++c)
-                    tma_load_3d(smem + Smem::v + c * KV_CHUNK, &tmv, &bars[Smem::V_FULL], (half * 4 + c) * 64,
-                                kvh, key0);
+                for (int vk = 0; vk < V_SLOTS_PER_TILE; ++vk) {
+                    int s;
+                    if (!next_slot(s)) return false;
+                    for (int b = 0; b < 4; ++b)
+                        tma_load_3d(smem + Smem::ring + s * SLOT + b * V_BOX, &tmv, &bars[Smem::FULL + s],
+                                    (half * 4 + b) * 64, kvh, key0 + vk * V_BOX_ROWS);
+                }
                 return true;
             };
-            bool ok = load_k(0) && load_v(0);
-            // K stage 1 holds the Q staging copy until Q[:, 0:256] is in TMEM
-            if (ok && n_kt > 1) ok = wait_or_abort(&bars[Smem::Q_READY], 0, p.err, abort) && load_k(1);
+            bool ok = load_k(0);
             for (int j = 0; ok && j < n_kt; ++j) {
-                if (j + K_STAGES < n_kt) ok = load_k(j + K_STAGES);
-                if (ok && j + 1 < n_kt) ok = load_v(j + 1);
+                if (j + 1 < n_kt) ok = load_k(j + 1);
+                if (ok) ok = load_v(j);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issue
-            bool ok = wait_or_abort(&bars[Smem::Q_READY], 0, p.err, abort);
-            tc_fence_after_sync();
-            const uint32_t k_base = smem_u32(smem + Smem::k);
-            const uint32_t v_base = smem_u32(smem + Smem::v);
-            const uint32_t qhi_base = smem_u32(smem + Smem::qhi);
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j % K_STAGES;
-                if (!wait_or_abort(&bars[Smem::K_FULL + s], (j / K_STAGES) & 1, p.err, abort)) return false;
+            bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort);
+            const uint32_t ring_base = smem_u32(smem + Smem::ring);
+            const uint32_t q_base = smem_u32(smem + Smem::q);
+            uint32_t item = 0;
+            auto take_slot = [&](int& s) -> bool {
+                s = static_cast<int>(item % N_SLOTS);
+                const uint32_t ph = (item / N_SLOTS) & 1u;
+                ++item;
+                if (!wait_or_abort(&bars[Smem::FULL + s], ph, p.err, abort)) return false;
                 tc_fence_after_sync();
+                return true;
+            };
+            auto issue_qk = [&](int j) -> bool {
                 const uint32_t sb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
-                const uint32_t kb = k_base + s * K_TILE;
-                // Alternate the two halves of the contraction: columns 0..255
-                // take A = Q_lo from TMEM (2 KiB of shared-memory reads per
-                // MMA), columns 256..511 A = Q_hi from shared memory (6 KiB),
-                // which keeps the shared-memory read rate even and leaves room
-                // for the TMA writes of the next tiles.
+                for (int c = 0; c < K_SLOTS_PER_TILE; ++c) {
+                    int s;
+                    if (!take_slot(s)) return false;
+                    const uint32_t kb = ring_base + s * SLOT;
+                    const uint32_t qa = q_base + c * 2 * Q_CHUNK;
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t bl = make_sdesc_sw128(kb + (kk >> 2) * KV_CHUNK + off, 16, 1024);
-                    tc_mma_ts(sb, tmem + TM_Q + kk * 8, bl, IDESC_QK, kk > 0 ? 1u : 0u);
-                    const uint64_t ad = make_sdesc_sw128(qhi_base + (kk >> 2) * Q_CHUNK + off, 16, 1024);
-                    const uint64_t bh = make_sdesc_sw128(kb + (4 + (kk >> 2)) * KV_CHUNK + off, 16, 1024);
-                    tc_mma_ss(sb, ad, bh, IDESC_QK, 1u);
+                    for (int k8 = 0; k8 < 8; ++k8) {
+                        // head-dim chunk 2c + (k8 >> 2), 16 columns at a time
+                        const uint32_t off = (k8 >> 2) * Q_CHUNK + (k8 & 3) * 32;
+                        const uint64_t ad = make_sdesc_sw128(qa + off, 16, 1024);
+                        const uint64_t bd = make_sdesc_sw128(kb + (k8 >> 2) * K_BOX + (k8 & 3) * 32, 16, 1024);
+                        tc_mma_ss(sb, ad, bd, IDESC_QK, (c | k8) ? 1u : 0u);
+                    }
+                    tc_commit(&bars[Smem::EMPTY + s]);
                 }
                 tc_commit(&bars[Smem::S_FULL + (j & 1)]);
-                tc_commit(&bars[Smem::K_EMPTY + s]);
+                return true;
+            };
+            auto issue_pv = [&](int j) -> bool {
+                const uint32_t pb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
+                for (int vk = 0; vk < V_SLOTS_PER_TILE; ++vk) {
+                    int s;
+                    if (!take_slot(s)) return false;
+                    const uint32_t vb = ring_base + s * SLOT;
+#pragma unroll
+                    for (int kk = 0; kk < V_BOX_ROWS / 16; ++kk) {
+                        // V is MN-major: 64-column boxes V_BOX apart, 8-key groups 1 KiB apart;
+                        // P of keys [64 vk, 64 vk + 64) sits at S columns [64 vk, 64 vk + 32)
+                        const uint64_t bd = make_sdesc_sw128(vb + kk * 16 * 128, V_BOX, 1024);
+                        tc_mma_ts(tmem + TM_O, pb + vk * BH + kk * 8, bd, IDESC_PV,
+                                  (j > 0 || vk > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&bars[Smem::EMPTY + s]);
+                }
+                tc_commit(&bars[Smem::O_DONE]);
                 return true;
             };
             if (ok) ok = issue_qk(0);
@@ -268,53 +308,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 // held P(j-1), consumed by O += P(j-1) V(j-1) issued before it
                 if (j + 1 < n_kt && !(ok = issue_qk(j + 1))) break;
                 if (!(ok = wait_or_abort(&bars[Smem::P_FULL + (j & 1)], (j >> 1) & 1, p.err, abort))) break;
-                if (!(ok = wait_or_abort(&bars[Smem::V_FULL], j & 1, p.err, abort))) break;
                 tc_fence_after_sync();
-                const uint32_t pb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // V is MN-major: 64-column boxes KV_CHUNK apart, 8-key groups 1 KiB apart
-                    const uint64_t bd = make_sdesc_sw128(v_base + kk * 16 * 128, KV_CHUNK, 1024);
-                    tc_mma_ts(tmem + TM_O, pb + kk * 8, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(&bars[Smem::O_DONE]);
-                tc_commit(&bars[Smem::V_EMPTY]);
+                ok = issue_pv(j);
             }
             // let every issued MMA finish before TMEM can be released
             tc_commit(&bars[Smem::DRAIN]);
             (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err);
         }
-    } else if (softmax_warp) {
+    } else {
         // ---------------------------------------------- softmax + correction + epilogue
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        float m_ref = -INFINITY;   // log2 units
-        float l = 0.f;             // sum of the fp32 probabilities (for LSE)
-        float l_b = 0.f;           // sum of the bf16-rounded probabilities (normalises O)
-        bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort);
-        if (ok) {
-            // Q[:, 0:256] of this row: staging copy (TMA swizzle) -> TMEM as bf16 pairs
-            const uint8_t* qs = smem + Smem::qlo_staging;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[32];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(
-                        qs + c * Q_CHUNK + row * 128 + ((i ^ (row & 7)) << 4));
-                    w[4 * i + 0] = v.x;
-                    w[4 * i + 1] = v.y;
-                    w[4 * i + 2] = v.z;
-                    w[4 * i + 3] = v.w;
-                }
-                tmem_st32(tmem + lane_base + TM_Q + c * 32, w);
-            }
-            tmem_st_wait();
-        }
-        // the staging area becomes K stage 1: order these generic reads
-        // before the TMA writes that follow the arrival
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        mbar_arrive(&bars[Smem::Q_READY]);
+        float* xmax = reinterpret_cast<float*>(smem + Smem::xmax);
+        float m_ref = -INFINITY;   // log2 units, the same in both key halves
+        float l = 0.f;             // this half's sum of the fp32 probabilities (for LSE)
+        float l_b = 0.f;           // this half's sum of the bf16-rounded probabilities
+        bool ok = true;
+        const bool neg_scale = p.scale_log2 < 0.f;
 
         for (int j = 0; ok && j < n_kt; ++j) {
             const int b = j & 1;
@@ -322,7 +331,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             if (!(ok = wait_or_abort(&bars[Smem::S_FULL + b], ph, p.err, abort))) break;
             tc_fence_after_sync();
             uint32_t sr[2][32];
-            const uint32_t s_col = TM_S + static_cast<uint32_t>(b) * BN;
+            const uint32_t s_col = TM_S + static_cast<uint32_t>(b) * BN + kh * BH;
             tmem_ld32(tmem + lane_base + s_col, sr[0]);
             tmem_ld32(tmem + lane_base + s_col + 32, sr[1]);
             tmem_ld_wait();
@@ -330,13 +339,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 #pragma unroll
             for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
-            const int key0 = (kt_begin + j) * BN;
-            const bool tile_full = key0 + BN <= p.seqlen_k && (!p.causal || key0 + BN - 1 <= p_first) &&
+            const int key0 = (kt_begin + j) * BN + kh * BH;
+            const bool half_full = key0 + BH <= p.seqlen_k && (!p.causal || key0 + BH - 1 <= p_first) &&
                                    (p.window <= 0 || key0 > p_last - p.window);
             // scores stay unscaled until the exponent; a hidden key gets the
             // value that scales to -inf whatever the sign of the scale
-            const bool neg_scale = p.scale_log2 < 0.f;
-            if (!tile_full) {
+            if (!half_full) {
                 const float hidden = neg_scale ? INFINITY : -INFINITY;
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
@@ -360,7 +368,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 #pragma unroll
                     for (int c = 0; c < w; ++c) mx[c] = fminf(mx[c], mx[c + w]);
             }
-            const float tmax = mx[0] * p.scale_log2;   // row max in log2 units
+            // row max over the whole tile: swap the halves' maxima (log2 units).
+            // Both halves then take the same decision on the same numbers.
+            const float own_max = mx[0] * p.scale_log2;
+            xmax[(b * 2 + kh) * BM + row] = own_max;
+            mbar_arrive(&bars[Smem::XCHG + b]);
+            if (!(ok = wait_or_abort(&bars[Smem::XCHG + b], ph, p.err, abort))) break;
+            const float tmax = fmaxf(own_max, xmax[(b * 2 + (kh ^ 1)) * BM + row]);
+
             float m_use = m_ref, alpha = 1.f;
             if (tmax > m_ref + RESCALE_THRESHOLD) {
                 m_use = tmax;
@@ -390,35 +405,52 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             l_b = l_b * alpha + (pb01.x + pb01.y);
             m_ref = m_use;
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                // PV of the previous tile must be done before O is corrected
+                // PV of the previous tile must be done before O is corrected;
+                // each key half corrects its own 128 O columns
                 if (!(ok = wait_or_abort(&bars[Smem::O_DONE], static_cast<uint32_t>((j - 1) & 1), p.err, abort)))
                     break;
                 tc_fence_after_sync();
-                for (int c = 0; c < DH / 32; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + TM_O + c * 32, o);
+                    const uint32_t oc = TM_O + kh * 128 + c * 32;
+                    tmem_ld32(tmem + lane_base + oc, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tmem + lane_base + TM_O + c * 32, o);
+                    tmem_st32(tmem + lane_base + oc, o);
                 }
             }
-            // P(j) overwrites the first 32 columns of S buffer b (already read)
+            // P of this key half overwrites the first 32 of its own 64 S columns
             tmem_st32(tmem + lane_base + s_col, pk);
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(&bars[Smem::P_FULL + b]);
         }
+        // O is final once PV(n_kt - 1) has completed.  PV(n_kt - 2) may still
+        // be running here, and a parity wait can only tell the pending phase
+        // from the one before it, so wait for the two phases in turn.
+        if (ok && n_kt >= 2)
+            ok = wait_or_abort(&bars[Smem::O_DONE], static_cast<uint32_t>((n_kt - 2) & 1), p.err, abort);
         if (ok) ok = wait_or_abort(&bars[Smem::O_DONE], static_cast<uint32_t>((n_kt - 1) & 1), p.err, abort);
+        // Swap the halves' row sums through the Q area, idle once every MMA
+        // has completed.  Each thread arrives exactly once, so the wait ends.
+        float* lsum = reinterpret_cast<float*>(smem + Smem::q);
+        lsum[(kh * BM + row) * 2 + 0] = l;
+        lsum[(kh * BM + row) * 2 + 1] = l_b;
+        mbar_arrive(&bars[Smem::L_XCHG]);
+        if (ok) ok = wait_or_abort(&bars[Smem::L_XCHG], 0, p.err, abort);
         if (ok) {
             tc_fence_after_sync();
+            const float l_all = l + lsum[((kh ^ 1) * BM + row) * 2 + 0];
+            const float lb_all = l_b + lsum[((kh ^ 1) * BM + row) * 2 + 1];
             // O / sum(p~) with p~ the rounded weights PV used: O stays an exact
             // convex combination of V rows whatever the rounding of P
-            const float inv_l = l_b > 0.f ? 1.f / l_b : 0.f;
-            __nv_bfloat16* dst = p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + half * DH;
-            for (int c = 0; c < DH / 32; ++c) {
+            const float inv_l = lb_all > 0.f ? 1.f / lb_all : 0.f;
+            __nv_bfloat16* dst =
+                p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + half * DH + kh * 128;
+            for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_base + TM_O + c * 32, o);
+                tmem_ld32(tmem + lane_base + TM_O + kh * 128 + c * 32, o);
                 tmem_ld_wait();
                 if (valid_row) {
                     uint32_t pk[16];
@@ -432,9 +464,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                         d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
             }
-            if (valid_row && half == 0 && p.lse)
+            if (valid_row && half == 0 && kh == 0 && p.lse)
                 p.lse[static_cast<size_t>(hq) * p.seqlen_q + t0 + tok] =
-                    l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+                    l_all > 0.f ? (m_ref + log2f(l_all)) * 0.69314718055994530942f : -INFINITY;
         }
     }
 
@@ -448,9 +480,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 
 }  // namespace prefill
 
-int prefill_smem_bytes() { return prefill::Smem::total + 1024; }
-int prefill_k_box_rows() { return prefill::BN; }
-int prefill_v_box_rows() { return prefill::BN; }
+int prefill_smem_bytes() { return prefill::Smem::total; }
+int prefill_k_box_rows() { return prefill::K_BOX_ROWS; }
+int prefill_v_box_rows() { return prefill::V_BOX_ROWS; }
 
 cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                            const PrefillParams& p, cudaStream_t stream) {
