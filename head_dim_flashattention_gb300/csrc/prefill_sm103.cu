@@ -5,7 +5,7 @@
 // memory ("Writing a FlashAttention Prefill Kernel for Gemma 4", sections
 // "The starting point" and "Head dim 512 breaks the textbook").
 //
-// Geometry of one work item (one CTA on one SM):
+// Geometry of one work item:
 //   * GQA row packing: a 128-row tile holds T = 128 / G query tokens times
 //     the G query heads that share one KV head, so every K/V tile serves all
 //     of them ("A custom attention kernel for Gemma 4 on the RTX PRO 6000",
@@ -15,30 +15,33 @@
 //     columns on its own, so each q tile is served by two CTAs that each own
 //     one 256-column half of O (the head-dim split of "Head dim 512 breaks
 //     the textbook" and of step 2 on the RTX PRO 6000 page, lifted from
-//     warps to SMs).  Both CTAs compute the same full S = Q K^T and the same
-//     softmax, so no scores cross between SMs; the pair's only duplicated
-//     work is S.  (Swapping half-width partial scores instead is bound by the
-//     SM-to-SM network, about 20 B/clk per SM against 32 B/clk needed.)
-//   * 128-key tiles: an M128 x N64 tcgen05.mma keeps the tensor pipe only
-//     about 55-70% busy, N128 keeps it full, so S is computed 128 keys at a
-//     time.  TMEM then holds the O half (256 columns) and two 128-column S
-//     buffers; P (bf16 pairs) overwrites S in place.  Q (128 x 512 bf16,
-//     128 KiB) stays in shared memory for the whole item and both QK^T
-//     operands come from shared memory.
-//   * K and V stream through one ring of 16 KiB slots in the order the MMAs
-//     consume them: a K slot is one 64-column head-dim chunk of 128 keys
-//     (8 per tile), a V slot is 64 keys x 128 output columns (4 per tile).
-//   * Causal / sliding-window tile skipping: only key tiles that intersect
-//     the visible band of the tile's rows are visited; only the 64-key halves
-//     that cross the band's edge are masked element by element.
+//     warps to SMs).  Both compute the same S = Q K^T and the same softmax,
+//     so no scores cross between SMs.
+//   * SM pairs: a cluster of two CTAs takes two consecutive q tiles with the
+//     same O half and issues 2-SM MMAs (tcgen05 cta_group::2, M = 256): each
+//     CTA keeps its own 128 rows of Q in shared memory and its own S, P and
+//     O in TMEM, and holds one half of every K and V operand tile (K: half
+//     of the keys, V: half of the output columns).  One MMA then does both
+//     SMs' work from half the shared memory per SM, and the issuing thread --
+//     whose barrier waits cost tensor-pipe time -- waits once per 16 (QK^T)
+//     or 8 (PV) MMAs.
+//   * 128-key tiles; S = Q K^T with M256 x N128 MMAs (both operands in
+//     shared memory), O_half += P V_half with M256 x N256 MMAs (P from
+//     TMEM).  TMEM: O half (256 columns) and two 128-column S buffers, P
+//     (bf16 pairs) over S.  K and V stream through a 3-slot ring of 32 KiB
+//     per CTA in the order the MMAs consume them: two K slots (256 head-dim
+//     columns x this CTA's 64 keys each) then one V slot (128 keys x this
+//     CTA's 128 output columns) per tile.
+//   * Causal / sliding-window tile skipping over the pair's visible band;
+//     only the 64-key halves that cross a row's band edge are masked
+//     element by element.
 //
-// Roles (320 threads): warp 0 lane 0 issues TMA loads, warp 1 lane 0 issues
-// tcgen05.mma (warp 1 owns the TMEM allocation), warps 2-9 run the softmax,
-// the O correction and the epilogue.  TMEM lane quadrant (warp % 4) gives a
-// softmax warp its 32 rows; warps 2-5 take keys 0-63 of each tile, warps 6-9
-// keys 64-127, and the two warps of a quadrant swap their row maxima through
-// shared memory each tile.  S is double-buffered so S(j+1) is computed while
-// the softmax works on tile j.
+// Roles (320 threads per CTA): warp 0 lane 0 issues this CTA's TMA loads;
+// warp 1 owns the TMEM allocation and, in the even CTA, lane 0 issues every
+// MMA of the pair; warps 2-9 run the softmax, the O correction and the
+// epilogue of this CTA's rows: TMEM lane quadrant (warp % 4) gives a warp its
+// 32 rows, warps 2-5 take keys 0-63 of each tile and warps 6-9 keys 64-127,
+// and the two warps of a quadrant swap row maxima through shared memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -52,21 +55,20 @@ namespace fa512 {
 namespace prefill {
 
 constexpr int D = 512;
-constexpr int BM = 128;                 // packed rows per tile
+constexpr int BM = 128;                 // packed rows per CTA tile
 constexpr int BN = 128;                 // keys per KV tile
 constexpr int BH = BN / 2;              // keys per softmax warp
 constexpr int DH = 256;                 // O columns per CTA
 constexpr int NUM_THREADS = 320;
-constexpr int N_SOFTMAX_THREADS = 256;  // warps 2-9
+constexpr int N_SOFTMAX_WARPS = 8;      // warps 2-9
 constexpr int Q_CHUNK = BM * 128;       // one 64-column box of Q: 16 KiB
-constexpr int SLOT = 32768;             // ring slot
+constexpr int SLOT = 32768;             // ring slot (this CTA's half of a pair slot)
 constexpr int N_SLOTS = 3;
-constexpr int K_BOX_ROWS = BN;          // K slot: two {64 columns, 128 keys} boxes
-constexpr int K_BOX = K_BOX_ROWS * 128; // 16 KiB
-constexpr int V_BOX_ROWS = 64;          // V slot: four {64 columns, 64 keys} boxes
-constexpr int V_BOX = V_BOX_ROWS * 128; // 8 KiB
-constexpr int K_SLOTS_PER_TILE = D / 128;                         // 4
-constexpr int V_SLOTS_PER_TILE = BN / V_BOX_ROWS;                 // 2
+constexpr int K_BOX_ROWS = BN / 2;      // K slot: four {64 columns, 64 keys} boxes
+constexpr int K_BOX = K_BOX_ROWS * 128; // 8 KiB
+constexpr int V_BOX_ROWS = BN;          // V slot: two {64 columns, 128 keys} boxes
+constexpr int V_BOX = V_BOX_ROWS * 128; // 16 KiB
+constexpr int K_SLOTS_PER_TILE = 2;     // 256 head-dim columns each
 
 constexpr uint32_t TM_O = 0;            // 256 columns fp32
 constexpr uint32_t TM_S = 256;          // 2 x 128 columns fp32; P (bf16) reuses them
@@ -77,31 +79,97 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 
 struct Smem {
     static constexpr int q = 0;                               // 8 x 16 KiB
-    static constexpr int ring = q + 8 * Q_CHUNK;              // N_SLOTS x 16 KiB
+    static constexpr int ring = q + 8 * Q_CHUNK;              // N_SLOTS x 32 KiB
     static constexpr int xmax = ring + N_SLOTS * SLOT;        // [2 buffers][2 halves][128 rows] fp32
     static constexpr int bars = xmax + 2 * 2 * BM * 4;
     enum {
-        FULL = 0,
-        EMPTY = FULL + N_SLOTS,
+        FULL = 0,                        // even CTA: both halves of a pair slot landed
+        EMPTY = FULL + N_SLOTS,          // this CTA's half of a slot may be refilled
         S_FULL = EMPTY + N_SLOTS,        // 2
-        P_FULL = S_FULL + 2,             // 2
+        P_FULL = S_FULL + 2,             // 2, even CTA: P of both CTAs in TMEM
         XCHG = P_FULL + 2,               // 2: row-max swap between the two softmax halves
-        Q_FULL = XCHG + 2,
+        Q_FULL = XCHG + 2,               // even CTA: Q of both CTAs landed
         O_DONE = Q_FULL + 1,
         L_XCHG = O_DONE + 1,             // final row-sum swap
-        DRAIN = L_XCHG + 1,
+        DRAIN = L_XCHG + 1,              // every issued MMA has completed
         N_BARS = DRAIN + 1
     };
     static constexpr int tmem_addr = bars + N_BARS * 8;
     static constexpr int abort_flag = tmem_addr + 4;
-    static constexpr int total = abort_flag + 4;
+    static constexpr int skip_flag = abort_flag + 4;         // written by the even CTA into both
+    static constexpr int total = skip_flag + 4;
 };
 // The dynamic shared-memory window starts 1 KiB aligned (checked at run
 // time), which the 128-byte swizzle atoms need.
 static_assert(Smem::total <= 232448, "shared memory budget");
 
-constexpr uint32_t IDESC_QK = make_idesc_bf16(BM, BN, 0);
-constexpr uint32_t IDESC_PV = make_idesc_bf16(BM, DH, 1);
+constexpr uint32_t IDESC_QK = make_idesc_bf16(2 * BM, BN, 0);
+constexpr uint32_t IDESC_PV = make_idesc_bf16(2 * BM, DH, 1);
+
+// ---------------------------------------------------------------- 2-SM forms
+
+// D (+)= A B^T on the CTA pair: A rows 0-127 from the even CTA, 128-255 from
+// the odd one (same shared-memory / TMEM offsets), B's N columns split in
+// halves between the two CTAs; each CTA's TMEM receives its 128 rows.
+__device__ __forceinline__ void mma2_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+__device__ __forceinline__ void mma2_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+// Arrives on the barrier at this offset in both CTAs once every MMA issued so
+// far has completed.
+__device__ __forceinline__ void commit2_both(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+// Arrives only on this CTA's barrier.
+__device__ __forceinline__ void commit2_local(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(static_cast<uint16_t>(1))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// TMA tile loads into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (bar_cluster: shared::cluster address).
+__device__ __forceinline__ void tma2_load_3d(void* smem_dst, const CUtensorMap* m, uint32_t bar_cluster,
+                                             int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tma2_load_4d(void* smem_dst, const CUtensorMap* m, uint32_t bar_cluster,
+                                             int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 // Bounded wait that also gives up when another role of this CTA has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, unsigned* err,
@@ -126,10 +194,11 @@ __device__ __forceinline__ bool key_visible(int j, int qpos, const PrefillParams
     return j < p.seqlen_k && (!p.causal || j <= qpos) && (p.window <= 0 || j > qpos - p.window);
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    // The alignment does not depend on the CTA, so both CTAs of a pair leave here together.
     if (smem_u32(smem) & 1023u) {
         if (threadIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_LAYOUT);
         return;
@@ -142,21 +211,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // ---- work item: (q tile, KV head, O half).  KV heads run one after the
-    // other so that the CTAs resident at any time share one head's K and V
-    // in L2; within a head the heaviest (latest) q tiles go first.
-    const int half = blockIdx.x & 1;
-    const int rest = blockIdx.x >> 1;
-    const int kvh = rest / p.num_q_tiles;
-    const int qt = p.num_q_tiles - 1 - rest % p.num_q_tiles;
+    // ---- work item: (q-tile pair, KV head, O half, rank in the pair).  KV
+    // heads run one after the other so that the CTAs resident at any time
+    // share one head's K and V in L2; within a head the heaviest (latest) q
+    // tiles go first.
+    const uint32_t rank = cluster_ctarank();            // == blockIdx.x & 1
+    const int half = (blockIdx.x >> 1) & 1;
+    const int rest = blockIdx.x >> 2;
+    const int n_pairs = (p.num_q_tiles + 1) / 2;
+    const int kvh = rest / n_pairs;
+    const int pair = n_pairs - 1 - rest % n_pairs;
+    const int qt = 2 * pair + static_cast<int>(rank);   // may equal num_q_tiles: no rows
     const int G = p.group;
-    const int t0 = qt * p.tokens_per_tile;
-    const int ntok = min(p.tokens_per_tile, p.seqlen_q - t0);
+    const int T = p.tokens_per_tile;
+    const int t0 = qt * T;
+    const int ntok = min(T, p.seqlen_q - t0);            // <= 0 for a missing second tile
     const int p_first = p.q_offset + t0;
     const int p_last = p.q_offset + t0 + ntok - 1;
+    // the pair's visible band (the same in both CTAs)
+    const int pair_first = p.q_offset + 2 * pair * T;
+    const int pair_last = p.q_offset + min(p.seqlen_q, (2 * pair + 2) * T) - 1;
     int j_lo = 0, j_hi = p.seqlen_k;
-    if (p.causal) j_hi = min(j_hi, p_last + 1);
-    if (p.window > 0) j_lo = max(0, p_first - p.window + 1);
+    if (p.causal) j_hi = min(j_hi, pair_last + 1);
+    if (p.window > 0) j_lo = max(0, pair_first - p.window + 1);
     if (j_hi < j_lo) j_hi = j_lo;
     const int kt_begin = j_lo / BN;
     const int n_kt = j_hi > j_lo ? (j_hi + BN - 1) / BN - kt_begin : 0;
@@ -171,10 +248,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int qpos = p.q_offset + t0 + tok;
     const int hq = kvh * G + g;
 
-    if (n_kt == 0 || timed_out_before(p.err)) {
-        // no key is visible to any row of this tile: O = 0, LSE = -inf
-        // (after an earlier pipeline timeout: skip the work)
-        if (n_kt == 0 && valid_row) {
+    if (n_kt == 0) {
+        // no key is visible to any row of the pair: O = 0, LSE = -inf
+        if (valid_row) {
             uint4* dst = reinterpret_cast<uint4*>(
                 p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + half * DH + kh * 128);
             for (int i = 0; i < 128 / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -186,8 +262,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < Smem::N_BARS; ++i) {
-            const bool per_thread = (i >= Smem::P_FULL && i < Smem::Q_FULL) || i == Smem::L_XCHG;
-            mbar_init(&bars[i], per_thread ? N_SOFTMAX_THREADS : 1);
+            uint32_t count = 1;
+            if (i == Smem::XCHG || i == Smem::XCHG + 1 || i == Smem::L_XCHG) count = N_SOFTMAX_WARPS * 32;
+            if (i == Smem::P_FULL || i == Smem::P_FULL + 1) count = 2 * N_SOFTMAX_WARPS;   // one lane per warp, both CTAs
+            mbar_init(&bars[i], count);
         }
         *abort = 0;
         fence_mbar_init();
@@ -195,51 +273,64 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
     }
+    __syncthreads();
+    cluster_sync_all();   // both CTAs running, barriers initialised
+    // After an earlier pipeline timeout the pair skips its work; the even CTA
+    // decides for both so that the two never part ways.
+    if (rank == 0 && tid == 0) {
+        const uint32_t skip = timed_out_before(p.err) ? 1u : 0u;
+        st_cluster_u32(map_to_cta(smem_u32(smem + Smem::skip_flag), 0), skip);
+        st_cluster_u32(map_to_cta(smem_u32(smem + Smem::skip_flag), 1), skip);
+    }
+    cluster_sync_all();
+    if (*reinterpret_cast<volatile uint32_t*>(smem + Smem::skip_flag)) return;
+
     if (warp == 1) {
-        tmem_alloc(tmem_addr_smem, 512);
-        tmem_relinquish();
+        tmem_alloc2(tmem_addr_smem, 512);
+        tmem_relinquish2();
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_addr_smem;
+    // barriers of the even CTA, addressed from either CTA
+    auto leader_bar = [&](int i) -> uint32_t { return map_to_cta(smem_u32(&bars[i]), 0); };
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------------ TMA producer
-            mbar_arrive_expect_tx(&bars[Smem::Q_FULL], static_cast<uint32_t>(8 * 128 * p.rows_per_tile));
+            const uint32_t q_bytes = static_cast<uint32_t>(8 * 128 * p.rows_per_tile);
+            if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::Q_FULL], 2 * q_bytes);
             for (int c = 0; c < 8; ++c)
-                tma_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, &bars[Smem::Q_FULL], c * 64, 0, kvh, t0);
+                tma2_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, leader_bar(Smem::Q_FULL), c * 64, 0, kvh, t0);
             uint32_t item = 0;
-            // next ring slot in consumption order, once the MMAs have released it
+            // next ring slot in consumption order, once the MMAs have released this CTA's half
             auto next_slot = [&](int& s) -> bool {
-                s = static_cast<int>(item % N_SLOTS);
-                const uint32_t ph = (item / N_SLOTS) & 1u;
-                ++item;
-                if (!wait_or_abort(&bars[Smem::EMPTY + s], ph ^ 1u, p.err, abort)) return false;
-                mbar_arrive_expect_tx(&bars[Smem::FULL + s], SLOT);
+                const uint32_t it = item++;
+                s = static_cast<int>(it % N_SLOTS);
+                if (!wait_or_abort(&bars[Smem::EMPTY + s], ((it / N_SLOTS) & 1u) ^ 1u, p.err, abort))
+                    return false;
+                if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::FULL + s], 2 * SLOT);
                 return true;
             };
             auto load_k = [&](int j) -> bool {
-                const int key0 = (kt_begin + j) * BN;
+                const int key0 = (kt_begin + j) * BN + static_cast<int>(rank) * K_BOX_ROWS;
                 for (int c = 0; c < K_SLOTS_PER_TILE; ++c) {
                     int s;
                     if (!next_slot(s)) return false;
-                    for (int b = 0; b < 2; ++b)
-                        tma_load_3d(smem + Smem::ring + s * SLOT + b * K_BOX, &tmk, &bars[Smem::FULL + s],
-                                    (c * 2 + b) * 64, kvh, key0);
+                    for (int b = 0; b < 4; ++b)
+                        tma2_load_3d(smem + Smem::ring + s * SLOT + b * K_BOX, &tmk, leader_bar(Smem::FULL + s),
+                                     (c * 4 + b) * 64, kvh, key0);
                 }
                 return true;
             };
             auto load_v = [&](int j) -> bool {
                 const int key0 = (kt_begin + j) * BN;
-                for (int vk = 0; vk < V_SLOTS_PER_TILE; ++vk) {
-                    int s;
-                    if (!next_slot(s)) return false;
-                    for (int b = 0; b < 4; ++b)
-                        tma_load_3d(smem + Smem::ring + s * SLOT + b * V_BOX, &tmv, &bars[Smem::FULL + s],
-                                    (half * 4 + b) * 64, kvh, key0 + vk * V_BOX_ROWS);
-                }
+                int s;
+                if (!next_slot(s)) return false;
+                for (int b = 0; b < 2; ++b)
+                    tma2_load_3d(smem + Smem::ring + s * SLOT + b * V_BOX, &tmv, leader_bar(Smem::FULL + s),
+                                 (half * 4 + static_cast<int>(rank) * 2 + b) * 64, kvh, key0);
                 return true;
             };
             bool ok = load_k(0);
@@ -249,8 +340,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------------------ MMA issue
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------------------ MMA issue (both SMs)
             bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort);
             const uint32_t ring_base = smem_u32(smem + Smem::ring);
             const uint32_t q_base = smem_u32(smem + Smem::q);
@@ -269,37 +360,35 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     int s;
                     if (!take_slot(s)) return false;
                     const uint32_t kb = ring_base + s * SLOT;
-                    const uint32_t qa = q_base + c * 2 * Q_CHUNK;
+                    const uint32_t qa = q_base + c * 4 * Q_CHUNK;
 #pragma unroll
-                    for (int k8 = 0; k8 < 8; ++k8) {
-                        // head-dim chunk 2c + (k8 >> 2), 16 columns at a time
-                        const uint32_t off = (k8 >> 2) * Q_CHUNK + (k8 & 3) * 32;
-                        const uint64_t ad = make_sdesc_sw128(qa + off, 16, 1024);
-                        const uint64_t bd = make_sdesc_sw128(kb + (k8 >> 2) * K_BOX + (k8 & 3) * 32, 16, 1024);
-                        tc_mma_ss(sb, ad, bd, IDESC_QK, (c | k8) ? 1u : 0u);
+                    for (int k16 = 0; k16 < 16; ++k16) {
+                        // head-dim chunk 4c + (k16 >> 2), 16 columns at a time
+                        const uint32_t off = (k16 & 3) * 32;
+                        const uint64_t ad = make_sdesc_sw128(qa + (k16 >> 2) * Q_CHUNK + off, 16, 1024);
+                        const uint64_t bd = make_sdesc_sw128(kb + (k16 >> 2) * K_BOX + off, 16, 1024);
+                        mma2_ss(sb, ad, bd, IDESC_QK, (c | k16) ? 1u : 0u);
                     }
-                    tc_commit(&bars[Smem::EMPTY + s]);
+                    commit2_both(&bars[Smem::EMPTY + s]);
                 }
-                tc_commit(&bars[Smem::S_FULL + (j & 1)]);
+                commit2_both(&bars[Smem::S_FULL + (j & 1)]);
                 return true;
             };
             auto issue_pv = [&](int j) -> bool {
                 const uint32_t pb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
-                for (int vk = 0; vk < V_SLOTS_PER_TILE; ++vk) {
-                    int s;
-                    if (!take_slot(s)) return false;
-                    const uint32_t vb = ring_base + s * SLOT;
+                int s;
+                if (!take_slot(s)) return false;
+                const uint32_t vb = ring_base + s * SLOT;
 #pragma unroll
-                    for (int kk = 0; kk < V_BOX_ROWS / 16; ++kk) {
-                        // V is MN-major: 64-column boxes V_BOX apart, 8-key groups 1 KiB apart;
-                        // P of keys [64 vk, 64 vk + 64) sits at S columns [64 vk, 64 vk + 32)
-                        const uint64_t bd = make_sdesc_sw128(vb + kk * 16 * 128, V_BOX, 1024);
-                        tc_mma_ts(tmem + TM_O, pb + vk * BH + kk * 8, bd, IDESC_PV,
-                                  (j > 0 || vk > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&bars[Smem::EMPTY + s]);
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    // V is MN-major: 64-column boxes V_BOX apart, 8-key groups 1 KiB apart;
+                    // P of keys [64 h, 64 h + 64) sits at S columns [64 h, 64 h + 32)
+                    const uint64_t bd = make_sdesc_sw128(vb + kk * 16 * 128, V_BOX, 1024);
+                    mma2_ts(tmem + TM_O, pb + (kk >> 2) * BH + (kk & 3) * 8, bd, IDESC_PV,
+                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(&bars[Smem::O_DONE]);
+                commit2_both(&bars[Smem::EMPTY + s]);
+                commit2_both(&bars[Smem::O_DONE]);
                 return true;
             };
             if (ok) ok = issue_qk(0);
@@ -312,7 +401,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 ok = issue_pv(j);
             }
             // let every issued MMA finish before TMEM can be released
-            tc_commit(&bars[Smem::DRAIN]);
+            commit2_local(&bars[Smem::DRAIN]);
             (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err);
         }
     } else {
@@ -328,7 +417,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         for (int j = 0; ok && j < n_kt; ++j) {
             const int b = j & 1;
             const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-            if (!(ok = wait_or_abort(&bars[Smem::S_FULL + b], ph, p.err, abort))) break;
+            // (every wait of a softmax warp is made warp-uniform: the warp
+            // synchronises below and must leave the loop as one)
+            if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::S_FULL + b], ph, p.err, abort)))) break;
             tc_fence_after_sync();
             uint32_t sr[2][32];
             const uint32_t s_col = TM_S + static_cast<uint32_t>(b) * BN + kh * BH;
@@ -340,7 +431,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
             const int key0 = (kt_begin + j) * BN + kh * BH;
-            const bool half_full = key0 + BH <= p.seqlen_k && (!p.causal || key0 + BH - 1 <= p_first) &&
+            const bool half_full = ntok > 0 && key0 + BH <= p.seqlen_k &&
+                                   (!p.causal || key0 + BH - 1 <= p_first) &&
                                    (p.window <= 0 || key0 > p_last - p.window);
             // scores stay unscaled until the exponent; a hidden key gets the
             // value that scales to -inf whatever the sign of the scale
@@ -373,7 +465,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const float own_max = mx[0] * p.scale_log2;
             xmax[(b * 2 + kh) * BM + row] = own_max;
             mbar_arrive(&bars[Smem::XCHG + b]);
-            if (!(ok = wait_or_abort(&bars[Smem::XCHG + b], ph, p.err, abort))) break;
+            if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::XCHG + b], ph, p.err, abort)))) break;
             const float tmax = fmaxf(own_max, xmax[(b * 2 + (kh ^ 1)) * BM + row]);
 
             float m_use = m_ref, alpha = 1.f;
@@ -407,7 +499,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 // PV of the previous tile must be done before O is corrected;
                 // each key half corrects its own 128 O columns
-                if (!(ok = wait_or_abort(&bars[Smem::O_DONE], static_cast<uint32_t>((j - 1) & 1), p.err, abort)))
+                if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::O_DONE],
+                                                                 static_cast<uint32_t>((j - 1) & 1), p.err, abort))))
                     break;
                 tc_fence_after_sync();
                 for (int c = 0; c < 4; ++c) {
@@ -424,7 +517,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             tmem_st32(tmem + lane_base + s_col, pk);
             tmem_st_wait();
             tc_fence_before_sync();
-            mbar_arrive(&bars[Smem::P_FULL + b]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(leader_bar(Smem::P_FULL + b));
         }
         // O is final once PV(n_kt - 1) has completed.  PV(n_kt - 2) may still
         // be running here, and a parity wait can only tell the pending phase
@@ -470,11 +564,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         }
     }
 
+    // Neither CTA leaves (or frees TMEM) while the pair's MMAs, loads or
+    // remote arrivals may still touch it: every role above ends with bounded
+    // waits, then both CTAs meet here.
     tc_fence_before_sync();
     __syncthreads();
+    cluster_sync_all();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc2(tmem, 512);
     }
 }
 
@@ -490,7 +588,9 @@ cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const
     cudaError_t e = cudaFuncSetAttribute(prefill::prefill_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int n_blocks = p.num_q_tiles * p.n_kv_heads * 2;   // two O halves per q tile
+    // (q-tile pair, O half, rank) per KV head; clusters of two consecutive CTAs
+    const int n_pairs = (p.num_q_tiles + 1) / 2;
+    const int n_blocks = n_pairs * 4 * p.n_kv_heads;
     prefill::prefill_kernel<<<n_blocks, prefill::NUM_THREADS, smem, stream>>>(tmq, tmk, tmv, p);
     return cudaGetLastError();
 }
