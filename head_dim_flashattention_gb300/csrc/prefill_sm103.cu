@@ -28,10 +28,13 @@
 //   * 128-key tiles; S = Q K^T with M256 x N128 MMAs (both operands in
 //     shared memory), O_half += P V_half with M256 x N256 MMAs (P from
 //     TMEM).  TMEM: O half (256 columns) and two 128-column S buffers, P
-//     (bf16 pairs) over S.  K and V stream through a 3-slot ring of 32 KiB
-//     per CTA in the order the MMAs consume them: two K slots (256 head-dim
-//     columns x this CTA's 64 keys each) then one V slot (128 keys x this
-//     CTA's 128 output columns) per tile.
+//     (bf16 pairs) over S.  K and V stream through three 32 KiB slots per
+//     CTA, each with one role: K head-dim columns 0-255, K columns 256-511
+//     (this CTA's 64 keys each) and V (128 keys x this CTA's 128 output
+//     columns).  The second K slot is released by the commit that marks S
+//     ready and the V slot by the one that marks O done, and V's load is
+//     counted on the barrier that marks P ready, so the issuing thread
+//     waits three times and commits three times per tile.
 //   * Causal / sliding-window tile skipping over the pair's visible band;
 //     only the 64-key halves that cross a row's band edge are masked
 //     element by element.
@@ -62,8 +65,8 @@ constexpr int DH = 256;                 // O columns per CTA
 constexpr int NUM_THREADS = 320;
 constexpr int N_SOFTMAX_WARPS = 8;      // warps 2-9
 constexpr int Q_CHUNK = BM * 128;       // one 64-column box of Q: 16 KiB
-constexpr int SLOT = 32768;             // ring slot (this CTA's half of a pair slot)
-constexpr int N_SLOTS = 3;
+constexpr int SLOT = 32768;             // one slot (this CTA's half of the pair's operand tile)
+constexpr int SLOT_KA = 0, SLOT_KB = 1, SLOT_V = 2;
 constexpr int K_BOX_ROWS = BN / 2;      // K slot: four {64 columns, 64 keys} boxes
 constexpr int K_BOX = K_BOX_ROWS * 128; // 8 KiB
 constexpr int V_BOX_ROWS = BN;          // V slot: two {64 columns, 128 keys} boxes
@@ -79,17 +82,18 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 
 struct Smem {
     static constexpr int q = 0;                               // 8 x 16 KiB
-    static constexpr int ring = q + 8 * Q_CHUNK;              // N_SLOTS x 32 KiB
-    static constexpr int xmax = ring + N_SLOTS * SLOT;        // [2 buffers][2 halves][128 rows] fp32
+    static constexpr int ring = q + 8 * Q_CHUNK;              // 3 slots x 32 KiB
+    static constexpr int xmax = ring + 3 * SLOT;              // [2 buffers][2 halves][128 rows] fp32
     static constexpr int bars = xmax + 2 * 2 * BM * 4;
     enum {
-        FULL = 0,                        // even CTA: both halves of a pair slot landed
-        EMPTY = FULL + N_SLOTS,          // this CTA's half of a slot may be refilled
-        S_FULL = EMPTY + N_SLOTS,        // 2
-        P_FULL = S_FULL + 2,             // 2, even CTA: P of both CTAs in TMEM
+        FULL_KA = 0,                     // even CTA: both halves of K columns 0-255 landed
+        FULL_KB = FULL_KA + 1,           // even CTA: ... columns 256-511
+        EMPTY_KA = FULL_KB + 1,          // the first K slot may be refilled
+        S_FULL = EMPTY_KA + 1,           // 2; also: the second K slot may be refilled
+        P_FULL = S_FULL + 2,             // 2, even CTA: P of both CTAs in TMEM and V landed
         XCHG = P_FULL + 2,               // 2: row-max swap between the two softmax halves
         Q_FULL = XCHG + 2,               // even CTA: Q of both CTAs landed
-        O_DONE = Q_FULL + 1,
+        O_DONE = Q_FULL + 1,             // also: the V slot may be refilled
         L_XCHG = O_DONE + 1,             // final row-sum swap
         DRAIN = L_XCHG + 1,              // every issued MMA has completed
         N_BARS = DRAIN + 1
@@ -264,7 +268,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         for (int i = 0; i < Smem::N_BARS; ++i) {
             uint32_t count = 1;
             if (i == Smem::XCHG || i == Smem::XCHG + 1 || i == Smem::L_XCHG) count = N_SOFTMAX_WARPS * 32;
-            if (i == Smem::P_FULL || i == Smem::P_FULL + 1) count = 2 * N_SOFTMAX_WARPS;   // one lane per warp, both CTAs
+            // one lane per softmax warp of both CTAs, plus the even CTA's V load
+            if (i == Smem::P_FULL || i == Smem::P_FULL + 1) count = 2 * N_SOFTMAX_WARPS + 1;
             mbar_init(&bars[i], count);
         }
         *abort = 0;
@@ -303,40 +308,38 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::Q_FULL], 2 * q_bytes);
             for (int c = 0; c < 8; ++c)
                 tma2_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, leader_bar(Smem::Q_FULL), c * 64, 0, kvh, t0);
-            uint32_t item = 0;
-            // next ring slot in consumption order, once the MMAs have released this CTA's half
-            auto next_slot = [&](int& s) -> bool {
-                const uint32_t it = item++;
-                s = static_cast<int>(it % N_SLOTS);
-                if (!wait_or_abort(&bars[Smem::EMPTY + s], ((it / N_SLOTS) & 1u) ^ 1u, p.err, abort))
-                    return false;
-                if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::FULL + s], 2 * SLOT);
-                return true;
-            };
-            auto load_k = [&](int j) -> bool {
+            // K columns 0-255 of tile j (slot KA), columns 256-511 (slot KB)
+            auto load_k = [&](int j, int slot, int c, uint32_t full) {
                 const int key0 = (kt_begin + j) * BN + static_cast<int>(rank) * K_BOX_ROWS;
-                for (int c = 0; c < K_SLOTS_PER_TILE; ++c) {
-                    int s;
-                    if (!next_slot(s)) return false;
-                    for (int b = 0; b < 4; ++b)
-                        tma2_load_3d(smem + Smem::ring + s * SLOT + b * K_BOX, &tmk, leader_bar(Smem::FULL + s),
-                                     (c * 4 + b) * 64, kvh, key0);
-                }
-                return true;
+                for (int b = 0; b < 4; ++b)
+                    tma2_load_3d(smem + Smem::ring + slot * SLOT + b * K_BOX, &tmk, full, (c * 4 + b) * 64, kvh,
+                                 key0);
             };
-            auto load_v = [&](int j) -> bool {
-                const int key0 = (kt_begin + j) * BN;
-                int s;
-                if (!next_slot(s)) return false;
-                for (int b = 0; b < 2; ++b)
-                    tma2_load_3d(smem + Smem::ring + s * SLOT + b * V_BOX, &tmv, leader_bar(Smem::FULL + s),
-                                 (half * 4 + static_cast<int>(rank) * 2 + b) * 64, kvh, key0);
-                return true;
-            };
-            bool ok = load_k(0);
+            if (rank == 0) {
+                mbar_arrive_expect_tx(&bars[Smem::FULL_KA], 2 * SLOT);
+                mbar_arrive_expect_tx(&bars[Smem::FULL_KB], 2 * SLOT);
+            }
+            load_k(0, SLOT_KA, 0, leader_bar(Smem::FULL_KA));
+            load_k(0, SLOT_KB, 1, leader_bar(Smem::FULL_KB));
+            bool ok = true;
             for (int j = 0; ok && j < n_kt; ++j) {
-                if (j + 1 < n_kt) ok = load_k(j + 1);
-                if (ok) ok = load_v(j);
+                const uint32_t ph = static_cast<uint32_t>(j & 1);
+                if (j + 1 < n_kt) {
+                    // slot KA once the first half of S(j) is done, slot KB once S(j) is
+                    if (!(ok = wait_or_abort(&bars[Smem::EMPTY_KA], ph, p.err, abort))) break;
+                    if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::FULL_KA], 2 * SLOT);
+                    load_k(j + 1, SLOT_KA, 0, leader_bar(Smem::FULL_KA));
+                    if (!(ok = wait_or_abort(&bars[Smem::S_FULL + (j & 1)], (j >> 1) & 1, p.err, abort))) break;
+                    if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::FULL_KB], 2 * SLOT);
+                    load_k(j + 1, SLOT_KB, 1, leader_bar(Smem::FULL_KB));
+                }
+                // V(j) once O += P(j-1) V(j-1) is done; counted on P ready of tile j
+                if (j > 0 && !(ok = wait_or_abort(&bars[Smem::O_DONE], (j - 1) & 1, p.err, abort))) break;
+                if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::P_FULL + (j & 1)], 2 * SLOT);
+                for (int b = 0; b < 2; ++b)
+                    tma2_load_3d(smem + Smem::ring + SLOT_V * SLOT + b * V_BOX, &tmv,
+                                 leader_bar(Smem::P_FULL + (j & 1)), (half * 4 + static_cast<int>(rank) * 2 + b) * 64,
+                                 kvh, (kt_begin + j) * BN);
             }
         }
     } else if (warp == 1) {
@@ -345,21 +348,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort);
             const uint32_t ring_base = smem_u32(smem + Smem::ring);
             const uint32_t q_base = smem_u32(smem + Smem::q);
-            uint32_t item = 0;
-            auto take_slot = [&](int& s) -> bool {
-                s = static_cast<int>(item % N_SLOTS);
-                const uint32_t ph = (item / N_SLOTS) & 1u;
-                ++item;
-                if (!wait_or_abort(&bars[Smem::FULL + s], ph, p.err, abort)) return false;
-                tc_fence_after_sync();
-                return true;
-            };
             auto issue_qk = [&](int j) -> bool {
                 const uint32_t sb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
-                for (int c = 0; c < K_SLOTS_PER_TILE; ++c) {
-                    int s;
-                    if (!take_slot(s)) return false;
-                    const uint32_t kb = ring_base + s * SLOT;
+                for (int c = 0; c < 2; ++c) {
+                    if (!wait_or_abort(&bars[c == 0 ? Smem::FULL_KA : Smem::FULL_KB], j & 1, p.err, abort))
+                        return false;
+                    tc_fence_after_sync();
+                    const uint32_t kb = ring_base + (c == 0 ? SLOT_KA : SLOT_KB) * SLOT;
                     const uint32_t qa = q_base + c * 4 * Q_CHUNK;
 #pragma unroll
                     for (int k16 = 0; k16 < 16; ++k16) {
@@ -369,16 +364,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                         const uint64_t bd = make_sdesc_sw128(kb + (k16 >> 2) * K_BOX + off, 16, 1024);
                         mma2_ss(sb, ad, bd, IDESC_QK, (c | k16) ? 1u : 0u);
                     }
-                    commit2_both(&bars[Smem::EMPTY + s]);
+                    commit2_both(&bars[c == 0 ? Smem::EMPTY_KA : Smem::S_FULL + (j & 1)]);
                 }
-                commit2_both(&bars[Smem::S_FULL + (j & 1)]);
                 return true;
             };
-            auto issue_pv = [&](int j) -> bool {
+            auto issue_pv = [&](int j) {
                 const uint32_t pb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
-                int s;
-                if (!take_slot(s)) return false;
-                const uint32_t vb = ring_base + s * SLOT;
+                const uint32_t vb = ring_base + SLOT_V * SLOT;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     // V is MN-major: 64-column boxes V_BOX apart, 8-key groups 1 KiB apart;
@@ -387,18 +379,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     mma2_ts(tmem + TM_O, pb + (kk >> 2) * BH + (kk & 3) * 8, bd, IDESC_PV,
                             (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                commit2_both(&bars[Smem::EMPTY + s]);
                 commit2_both(&bars[Smem::O_DONE]);
-                return true;
             };
             if (ok) ok = issue_qk(0);
             for (int j = 0; ok && j < n_kt; ++j) {
                 // S(j+1) runs while the softmax works on tile j; its buffer last
                 // held P(j-1), consumed by O += P(j-1) V(j-1) issued before it
                 if (j + 1 < n_kt && !(ok = issue_qk(j + 1))) break;
+                // P(j) from both CTAs' softmax and V(j) in both CTAs' V slot
                 if (!(ok = wait_or_abort(&bars[Smem::P_FULL + (j & 1)], (j >> 1) & 1, p.err, abort))) break;
                 tc_fence_after_sync();
-                ok = issue_pv(j);
+                issue_pv(j);
             }
             // let every issued MMA finish before TMEM can be released
             commit2_local(&bars[Smem::DRAIN]);
@@ -518,7 +509,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(leader_bar(Smem::P_FULL + b));
+            // one arrival per warp on the even CTA's barrier (a cluster-scope
+            // release only where the barrier is the other CTA's)
+            if (lane == 0) {
+                if (rank == 0) mbar_arrive(&bars[Smem::P_FULL + b]);
+                else mbar_arrive_remote(leader_bar(Smem::P_FULL + b));
+            }
         }
         // O is final once PV(n_kt - 1) has completed.  PV(n_kt - 2) may still
         // be running here, and a parity wait can only tell the pending phase
