@@ -91,6 +91,24 @@ def source_digest(names) -> str:
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(values, device):
+    """Each timing taken as the slowest rank's (an all-reduce MAX over the
+    process group when one is initialised with more than one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(units_per_step_per_rank: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_step_per_rank * steps * world / seconds
+
+
 def recorded_traffic(kernel: str, digest: str):
     """DRAM bytes per launch recorded from an ncu capture of this exact kernel
     source, or None when absent or taken on older source."""
@@ -333,14 +351,11 @@ def run_ours(args):
     t_pf = sum(pf_ms) / 1e3
     t_dec = sum(sum(x) for x in dec_ms) / 1e3
     t_step = sum(step_ms) / 1e3
-    if world > 1:
-        tt = torch.tensor([t_pf, t_dec, t_step, wall], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_pf, t_dec, t_step, wall = tt.tolist()
+    t_pf, t_dec, t_step, wall = max_over_ranks([t_pf, t_dec, t_step, wall], dev)
 
-    value = pf_flops * args.steps * world / t_pf / 1e12 if not args.no_prefill else None
+    value = job_rate(pf_flops, args.steps, world, t_pf) / 1e12 if not args.no_prefill else None
     dec_bytes = sum(d["bytes"] for d in dec)
-    dec_gbs = dec_bytes * args.steps * world / t_dec / 1e9 if dec else None
+    dec_gbs = job_rate(dec_bytes, args.steps, world, t_dec) / 1e9 if dec else None
 
     peaks, peak_kind = read_peaks()
     pf_avg_s = t_pf / args.steps if not args.no_prefill else float("nan")
