@@ -356,13 +356,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     tc_fence_after_sync();
                     const uint32_t kb = ring_base + (c == 0 ? SLOT_KA : SLOT_KB) * SLOT;
                     const uint32_t qa = q_base + c * 4 * Q_CHUNK;
+                    const uint64_t ad0 = make_sdesc_sw128(qa, 16, 1024);
+                    const uint64_t bd0 = make_sdesc_sw128(kb, 16, 1024);
 #pragma unroll
                     for (int k16 = 0; k16 < 16; ++k16) {
-                        // head-dim chunk 4c + (k16 >> 2), 16 columns at a time
-                        const uint32_t off = (k16 & 3) * 32;
-                        const uint64_t ad = make_sdesc_sw128(qa + (k16 >> 2) * Q_CHUNK + off, 16, 1024);
-                        const uint64_t bd = make_sdesc_sw128(kb + (k16 >> 2) * K_BOX + off, 16, 1024);
-                        mma2_ss(sb, ad, bd, IDESC_QK, (c | k16) ? 1u : 0u);
+                        // head-dim chunk 4c + (k16 >> 2), 16 columns at a time (start field in 16 B units)
+                        const uint64_t off = static_cast<uint64_t>((k16 & 3) * 2);
+                        mma2_ss(sb, ad0 + static_cast<uint64_t>((k16 >> 2) * (Q_CHUNK >> 4)) + off,
+                                bd0 + static_cast<uint64_t>((k16 >> 2) * (K_BOX >> 4)) + off, IDESC_QK,
+                                (c | k16) ? 1u : 0u);
                     }
                     commit2_both(&bars[c == 0 ? Smem::EMPTY_KA : Smem::S_FULL + (j & 1)]);
                 }
@@ -375,7 +377,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     // V is MN-major: 64-column boxes V_BOX apart, 8-key groups 1 KiB apart;
                     // P of keys [64 h, 64 h + 64) sits at S columns [64 h, 64 h + 32)
-                    const uint64_t bd = make_sdesc_sw128(vb + kk * 16 * 128, V_BOX, 1024);
+                    const uint64_t bd = make_sdesc_sw128(vb, V_BOX, 1024) + static_cast<uint64_t>(kk * (16 * 128 >> 4));
                     mma2_ts(tmem + TM_O, pb + (kk >> 2) * BH + (kk & 3) * 8, bd, IDESC_PV,
                             (j > 0 || kk > 0) ? 1u : 0u);
                 }
