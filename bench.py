@@ -382,42 +382,65 @@ def run_ours(args):
                            "traffic": recorded_traffic("decode_split_kernel", dec_src),
                            "src": dec_src, "per_shape": per}
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Every step
+    # copies its Q/K/V in from pinned host memory and its O/LSE back out; the
+    # copies of neighbouring steps overlap the kernel on their own streams
+    # (inputs and outputs double-buffered on the device), as a serving loop
+    # would run them.
     e2e = None
     if not args.no_e2e and not args.no_prefill:
         qh = q.cpu().pin_memory()
         kh = k.cpu().pin_memory()
         vh = v.cpu().pin_memory()
-        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dev_in = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)) for _ in range(2)]
+        dev_out = [(torch.empty_like(out), torch.empty_like(lse)) for _ in range(2)]
+        host_out = [(torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                     torch.empty(lse.shape, dtype=lse.dtype).pin_memory()) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-        def e2e_step():
-            qd.copy_(qh, non_blocking=True)
-            kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-            fa.fa512_prefill(qd, kd, vd, out, lse, q_offset=P["q_offset"], causal=True,
-                             stream=stream)
-            oh.copy_(out, non_blocking=True)
-            lh.copy_(lse, non_blocking=True)
+        def e2e_run(n_steps):
+            in_ready = [torch.cuda.Event() for _ in range(2)]
+            done = [torch.cuda.Event() for _ in range(2)]
+            copied = [torch.cuda.Event() for _ in range(2)]
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(s_in)
+            for i in range(n_steps):
+                b = i & 1
+                qd, kd, vd = dev_in[b]
+                od, ld = dev_out[b]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(done[b])          # step i-2 finished reading dev_in[b]
+                    qd.copy_(qh, non_blocking=True)
+                    kd.copy_(kh, non_blocking=True)
+                    vd.copy_(vh, non_blocking=True)
+                    in_ready[b].record(s_in)
+                stream.wait_event(in_ready[b])
+                if i >= 2:
+                    stream.wait_event(copied[b])          # step i-2's result left dev_out[b]
+                flush.zero_()
+                fa.fa512_prefill(qd, kd, vd, od, ld, q_offset=P["q_offset"], causal=True,
+                                 stream=stream)
+                done[b].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done[b])
+                    host_out[b][0].copy_(od, non_blocking=True)
+                    host_out[b][1].copy_(ld, non_blocking=True)
+                    copied[b].record(s_out)
+            s_out.wait_event(done[(n_steps - 1) & 1])
+            t1.record(s_out)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / 1e3
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            flush.zero_()
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        t_e2e = e0.elapsed_time(e1) / 1e3
+        e2e_run(3)
+        (t_e2e,) = max_over_ranks([e2e_run(args.steps)], dev)
         h2d = (q.numel() + k.numel() + v.numel()) * 2
         d2h = out.numel() * 2 + lse.numel() * 4
-        e2e = {"value": pf_flops * args.steps * world / t_e2e / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_rate(pf_flops, args.steps, world, t_e2e) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "what": "fa512_prefill with pinned-host Q/K/V copied in and O/LSE copied out "
-                       "every step (L2 flush included)"}
+                       "every step, copies of neighbouring steps overlapping the kernel on two "
+                       "more streams (L2 flush included)"}
 
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu:
