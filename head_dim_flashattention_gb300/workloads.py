@@ -154,6 +154,12 @@ def paged_decode_inputs(batch: int, kv_lens, n_q_heads: int = 8, n_kv_heads: int
                              "n_q_heads": n_q_heads, "n_kv_heads": n_kv_heads})
 
 
+def draft_queries(batch: int, q_len: int, n_q_heads: int, seed: int) -> torch.Tensor:
+    """q_len query tokens per sequence (the last q_len positions of each
+    cache, e.g. draft tokens being verified): [batch, q_len, n_q_heads, D] bf16."""
+    return randn_bf16((batch, q_len, n_q_heads, HEAD_DIM), seed * 7 + 5)
+
+
 def decode_inputs(cfg: DecodeConfig, poison: bool = True) -> PagedCache:
     return paged_decode_inputs(cfg.batch, [cfg.kv_len] * cfg.batch, cfg.n_q_heads,
                                cfg.n_kv_heads, cfg.page_size, cfg.seed, cfg.spare_pages, poison)

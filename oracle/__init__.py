@@ -60,6 +60,9 @@ def _load():
             lib.oracle_decode_paged.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, i,
                                                 ctypes.c_double, i, i]
             lib.oracle_decode_paged.restype = i
+            lib.oracle_decode_paged_q.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, i, i,
+                                                  ctypes.c_double, i, i]
+            lib.oracle_decode_paged_q.restype = i
             _lib = lib
     return _lib
 
@@ -158,4 +161,33 @@ def decode_paged(q, k_pages, v_pages, page_table, kv_lens, *, scale: float | Non
                                      threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_decode_paged rejected its arguments")
+    return out, lse
+
+
+def decode_paged_q(q, k_pages, v_pages, page_table, kv_lens, *, scale: float | None = None,
+                   window: int = 0, threads: int | None = None):
+    """Reference attention of the last q_len tokens of each sequence over a paged cache.
+
+    q [batch, q_len, n_q_heads, D]: query t of sequence b sits at position
+    kv_lens[b] - q_len + t and sees the cache causally (and through the window).
+    k_pages/v_pages [num_pages, page_size, n_kv_heads, D]; page_table
+    [batch, max_pages_per_seq] int; kv_lens [batch] int.
+    Returns ``(out, lse)``: out [batch, q_len, n_q_heads, D] fp64, lse [batch, q_len, n_q_heads].
+    """
+    qb, kb, vb = _bits(q), _bits(k_pages), _bits(v_pages)
+    pt, kl = _i32(page_table), _i32(kv_lens)
+    bsz, qlen, hq, d = qb.shape
+    npages, psz, hk, d2 = kb.shape
+    if d2 != d or vb.shape != kb.shape or pt.ndim != 2 or pt.shape[0] != bsz:
+        raise ValueError("bad shapes")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((bsz, qlen, hq, d), dtype=np.float64)
+    lse = np.zeros((bsz, qlen, hq), dtype=np.float64)
+    rc = _load().oracle_decode_paged_q(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pt), _ptr(kl),
+                                       _ptr(out), _ptr(lse), bsz, qlen, hq, hk, d, psz,
+                                       pt.shape[1], npages, float(scale), int(window),
+                                       threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_decode_paged_q rejected its arguments")
     return out, lse

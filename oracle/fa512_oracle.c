@@ -199,6 +199,7 @@ typedef struct {
     int window;
     int n_threads, tid;
     int max_len;
+    int q_len;
 } decode_job;
 
 static void *decode_worker(void *arg)
@@ -209,15 +210,20 @@ static void *decode_worker(void *arg)
     const uint16_t **krows = (const uint16_t **)malloc(sizeof(void *) * (size_t)(J->max_len + 1));
     const uint16_t **vrows = (const uint16_t **)malloc(sizeof(void *) * (size_t)(J->max_len + 1));
     double *s = (double *)malloc(sizeof(double) * (size_t)(J->max_len + 1));
-    long total = (long)J->batch * J->n_q_heads;
+    long total = (long)J->batch * J->q_len * J->n_q_heads;
     for (long w = J->tid; w < total; w += J->n_threads) {
-        int b = (int)(w / J->n_q_heads);
+        int bt = (int)(w / J->n_q_heads);      /* b * q_len + t */
         int h = (int)(w % J->n_q_heads);
+        int b = bt / J->q_len;
+        int t = bt % J->q_len;
         int hk = h / G;
         int len = J->kv_lens[b];
-        /* the query is the sequence's last position, len - 1 */
+        /* the q_len queries are the sequence's last q_len positions:
+           query t sits at len - q_len + t (negative: no key is visible) */
+        long p = (long)len - J->q_len + t;
         long lo, hi;
-        visible_range((long)len - 1, len, 1, J->window, &lo, &hi);
+        visible_range(p, len, 1, J->window, &lo, &hi);
+        if (p < 0) hi = lo = 0;
         int n = 0;
         for (long j = lo; j < hi; ++j, ++n) {
             /* logical position j lives in page page_table[b][j / page_size],
@@ -228,9 +234,9 @@ static void *decode_worker(void *arg)
             krows[n] = J->kp + row * D;
             vrows[n] = J->vp + row * D;
         }
-        const uint16_t *qr = J->q + ((size_t)b * J->n_q_heads + h) * D;
-        double *o = J->out + ((size_t)b * J->n_q_heads + h) * D;
-        double *l = J->lse + (size_t)b * J->n_q_heads + h;
+        const uint16_t *qr = J->q + ((size_t)bt * J->n_q_heads + h) * D;
+        double *o = J->out + ((size_t)bt * J->n_q_heads + h) * D;
+        double *l = J->lse + (size_t)bt * J->n_q_heads + h;
         attend_one(qr, krows, vrows, n, D, J->scale, o, l, s);
     }
     free(krows);
@@ -249,13 +255,40 @@ static void *decode_worker(void *arg)
  * Returns 0, or -1 on invalid arguments (including a page index or length
  * outside the table; num_pages bounds the page indices).
  */
+int oracle_decode_paged_q(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                          const int *page_table, const int *kv_lens, double *out, double *lse,
+                          int batch, int q_len, int n_q_heads, int n_kv_heads, int head_dim,
+                          int page_size, int max_pages_per_seq, int num_pages, double scale,
+                          int window, int n_threads);
+
 int oracle_decode_paged(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                         const int *page_table, const int *kv_lens, double *out, double *lse,
                         int batch, int n_q_heads, int n_kv_heads, int head_dim, int page_size,
                         int max_pages_per_seq, int num_pages, double scale, int window,
                         int n_threads)
 {
-    if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || page_size <= 0)
+    return oracle_decode_paged_q(q, k_pages, v_pages, page_table, kv_lens, out, lse, batch, 1,
+                                 n_q_heads, n_kv_heads, head_dim, page_size, max_pages_per_seq,
+                                 num_pages, scale, window, n_threads);
+}
+
+/*
+ * Several query tokens per sequence (draft tokens being verified, a short
+ * chunk appended to a paged cache): the q_len queries of sequence b are its
+ * last q_len positions, query t at position kv_lens[b] - q_len + t, each
+ * causal over the cache (and windowed like any query).
+ * q   [batch, q_len, n_q_heads, head_dim]   bf16 bits
+ * out [batch, q_len, n_q_heads, head_dim] fp64;  lse [batch, q_len, n_q_heads] fp64.
+ * Other arguments as oracle_decode_paged; q_len = 1 is that function.
+ */
+int oracle_decode_paged_q(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                          const int *page_table, const int *kv_lens, double *out, double *lse,
+                          int batch, int q_len, int n_q_heads, int n_kv_heads, int head_dim,
+                          int page_size, int max_pages_per_seq, int num_pages, double scale,
+                          int window, int n_threads)
+{
+    if (batch < 0 || q_len < 1 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
+        page_size <= 0)
         return -1;
     if (n_q_heads % n_kv_heads != 0) return -1;
     int max_len = 0;
@@ -275,7 +308,7 @@ int oracle_decode_paged(const uint16_t *q, const uint16_t *k_pages, const uint16
     for (int t = 0; t < n_threads; ++t) {
         decode_job J = {q, k_pages, v_pages, page_table, kv_lens, out, lse, batch,
                         n_q_heads, n_kv_heads, head_dim, page_size, max_pages_per_seq,
-                        scale, window, n_threads, t, max_len};
+                        scale, window, n_threads, t, max_len, q_len};
         jobs[t] = J;
         pthread_create(&th[t], NULL, decode_worker, &jobs[t]);
     }

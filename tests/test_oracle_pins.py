@@ -345,3 +345,63 @@ def test_decode_rejects_out_of_range_tables():
     bad[0, 0] = 10_000
     with pytest.raises(ValueError):
         oracle.decode_paged(pc.q, pc.k_pages, pc.v_pages, bad, pc.kv_lens)
+
+
+# ----------------------------------------------- decode with several query tokens
+
+def test_decode_q_positions_and_window_closed_form():
+    """q = 0, V at logical position j is the constant j / 8: query t of a
+    q_len-token decode sits at p = len - q_len + t and averages the positions
+    [lo, p] it sees (lo = 0, or p - W + 1 under a window W); a query whose
+    position is negative (len < q_len) sees nothing."""
+    page, q_len = 16, 4
+    lens = [1, 3, 4, 15, 17, 100]
+    pc = workloads.paged_decode_inputs(len(lens), lens, 4, 2, page, seed=31)
+    q = torch.zeros((len(lens), q_len, 4, D), dtype=torch.bfloat16)
+    for b, n in enumerate(lens):
+        for j in range(n):
+            pg = int(pc.page_table[b, j // page])
+            pc.v_pages[pg, j % page] = j / 8
+    for W in (0, 3):
+        out, lse = oracle.decode_paged_q(q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
+                                         window=W)
+        for b, n in enumerate(lens):
+            for t in range(q_len):
+                p = n - q_len + t
+                if p < 0:
+                    assert np.all(out[b, t] == 0) and np.all(np.isneginf(lse[b, t]))
+                    continue
+                lo = max(0, p - W + 1) if W > 0 else 0
+                np.testing.assert_allclose(out[b, t], (lo + p) / 2 / 8, atol=1e-12)
+                np.testing.assert_allclose(lse[b, t], math.log(p - lo + 1), atol=1e-13)
+
+
+def test_decode_q_rows_are_the_last_prefill_rows():
+    """A q_len-token decode over a paged cache equals the last q_len rows of a
+    causal prefill over the same keys laid out contiguously (q_offset = len - q_len)."""
+    page, n, hq, hk, q_len = 32, 150, 8, 4, 5
+    pc = workloads.paged_decode_inputs(1, [n], hq, hk, page, seed=32)
+    q = workloads.draft_queries(1, q_len, hq, seed=32)
+    out, lse = oracle.decode_paged_q(q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens)
+    npg = (n + page - 1) // page
+    idx = pc.page_table[0, :npg].long()
+    k_lin = pc.k_pages[idx].reshape(npg * page, hk, D)[:n]
+    v_lin = pc.v_pages[idx].reshape(npg * page, hk, D)[:n]
+    o_pre, l_pre = oracle.prefill(q[0], k_lin, v_lin, q_offset=n - q_len)
+    np.testing.assert_array_equal(out[0], o_pre)
+    np.testing.assert_array_equal(lse[0], l_pre.T)
+    # the same with a window: row t keeps its own band
+    out_w, lse_w = oracle.decode_paged_q(q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
+                                         window=40)
+    o_prw, l_prw = oracle.prefill(q[0], k_lin, v_lin, q_offset=n - q_len, window=40)
+    np.testing.assert_array_equal(out_w[0], o_prw)
+    np.testing.assert_array_equal(lse_w[0], l_prw.T)
+
+
+def test_decode_q_len_one_is_single_token_decode():
+    pc = workloads.paged_decode_inputs(3, [5, 64, 90], 8, 4, 32, seed=33)
+    o1, l1 = oracle.decode_paged(pc.q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens)
+    o2, l2 = oracle.decode_paged_q(pc.q[:, None], pc.k_pages, pc.v_pages, pc.page_table,
+                                   pc.kv_lens)
+    np.testing.assert_array_equal(o1, o2[:, 0])
+    np.testing.assert_array_equal(l1, l2[:, 0])
