@@ -60,6 +60,11 @@ def load_library():
         lib.fa512_decode_paged.restype = I
         lib.fa512_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
         lib.fa512_decode_workspace_bytes.restype = Z
+        lib.fa512_decode_paged_q.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I,
+                                             P, Z, P]
+        lib.fa512_decode_paged_q.restype = I
+        lib.fa512_decode_workspace_bytes_q.argtypes = [I, I, I, I, I, I, I]
+        lib.fa512_decode_workspace_bytes_q.restype = Z
         lib.fa512_decode_auto_splits.argtypes = [I, I, I, I]
         lib.fa512_decode_auto_splits.restype = I
         lib.fa512_device_status.argtypes = [P, I]
@@ -181,6 +186,50 @@ def fa512_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Te
         _dptr(v_pages, "v_pages", torch.bfloat16), _dptr(page_table, "page_table", torch.int32),
         _dptr(kv_lens, "kv_lens", torch.int32), _dptr(out, "out", torch.bfloat16),
         _dptr(lse, "lse", torch.float32), bsz, hq, hk, psz, npages, mpps, int(max_kv_len),
+        float(scale), int(window), int(num_splits), _dptr(workspace, "workspace"), ws_bytes,
+        _stream(stream)))
+    return out, lse
+
+
+def fa512_decode_paged_q(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                         page_table: torch.Tensor, kv_lens: torch.Tensor,
+                         out: torch.Tensor | None = None, lse: torch.Tensor | None = None, *,
+                         max_kv_len: int | None = None, scale: float | None = None,
+                         window: int = 0, num_splits: int = 0,
+                         workspace: torch.Tensor | None = None, return_lse: bool = True,
+                         stream=None):
+    """q_len query tokens per sequence (its last q_len positions) over a paged
+    KV cache; returns ``(out, lse)``.
+
+    q [batch, q_len, n_q_heads, 512]; out like q; lse [batch, q_len, n_q_heads].
+    Other arguments as :func:`fa512_decode_paged`.
+    """
+    if q.dim() != 4 or k_pages.dim() != 4 or k_pages.shape != v_pages.shape:
+        raise Fa512Error(1, "q must be [batch, q_len, heads, 512], pages [n, page, heads, 512]")
+    bsz, qlen, hq, d = q.shape
+    npages, psz, hk, _ = k_pages.shape
+    if page_table.dim() != 2:
+        raise Fa512Error(1, "page_table must be [batch, max_pages_per_seq]")
+    mpps = page_table.shape[1]
+    if max_kv_len is None:
+        max_kv_len = mpps * psz
+    if out is None:
+        out = torch.empty((bsz, qlen, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((bsz, qlen, hq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = d ** -0.5
+    lib = load_library()
+    need = int(lib.fa512_decode_workspace_bytes_q(bsz, qlen, hq, hk, psz, int(max_kv_len),
+                                                  int(num_splits)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.fa512_decode_paged_q(
+        _dptr(q, "q", torch.bfloat16), _dptr(k_pages, "k_pages", torch.bfloat16),
+        _dptr(v_pages, "v_pages", torch.bfloat16), _dptr(page_table, "page_table", torch.int32),
+        _dptr(kv_lens, "kv_lens", torch.int32), _dptr(out, "out", torch.bfloat16),
+        _dptr(lse, "lse", torch.float32), bsz, qlen, hq, hk, psz, npages, mpps, int(max_kv_len),
         float(scale), int(window), int(num_splits), _dptr(workspace, "workspace"), ws_bytes,
         _stream(stream)))
     return out, lse

@@ -261,30 +261,40 @@ int fa512_decode_auto_splits(int batch, int n_kv_heads, int page_size, int max_k
                          sm_count());
 }
 
-size_t fa512_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int page_size,
-                                    int max_kv_len, int num_splits) {
-    if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_kv_len < 0 || num_splits < 0 ||
-        num_splits > 1024)
+size_t fa512_decode_workspace_bytes_q(int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                      int page_size, int max_kv_len, int num_splits) {
+    if (batch < 0 || q_len < 1 || n_q_heads <= 0 || n_kv_heads <= 0 || max_kv_len < 0 ||
+        num_splits < 0 || num_splits > 1024)
         return 0;
     const int s = num_splits > 0 ? num_splits
                                  : fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len);
-    return workspace_for(batch, n_q_heads, s);
+    return workspace_for(batch * q_len, n_q_heads, s);
 }
 
-fa512_status fa512_decode_paged(const void* q, const void* k_pages, const void* v_pages,
-                                const int32_t* page_table, const int32_t* kv_lens, void* out,
-                                float* lse, int batch, int n_q_heads, int n_kv_heads,
-                                int page_size, int num_pages, int max_pages_per_seq,
-                                int max_kv_len, float scale, int window, int num_splits,
-                                void* workspace, size_t workspace_bytes,
-                                fa512_stream_t stream) {
+size_t fa512_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int page_size,
+                                    int max_kv_len, int num_splits) {
+    return fa512_decode_workspace_bytes_q(batch, 1, n_q_heads, n_kv_heads, page_size, max_kv_len,
+                                          num_splits);
+}
+
+fa512_status fa512_decode_paged_q(const void* q, const void* k_pages, const void* v_pages,
+                                  const int32_t* page_table, const int32_t* kv_lens, void* out,
+                                  float* lse, int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                  int page_size, int num_pages, int max_pages_per_seq,
+                                  int max_kv_len, float scale, int window, int num_splits,
+                                  void* workspace, size_t workspace_bytes,
+                                  fa512_stream_t stream) {
     g_last_error[0] = 0;
     if (batch < 0) return fail(FA512_ERR_INVALID_ARG, "negative batch");
+    if (q_len < 1) return fail(FA512_ERR_INVALID_ARG, "q_len must be >= 1");
     if (n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads != 0)
         return fail(FA512_ERR_INVALID_ARG, "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)",
                     n_q_heads, n_kv_heads);
     const int G = n_q_heads / n_kv_heads;
     if (G > 16) return fail(FA512_ERR_UNSUPPORTED, "decode supports at most 16 query heads per KV head");
+    if (q_len * G > 16)
+        return fail(FA512_ERR_UNSUPPORTED, "q_len x query heads per KV head (%d x %d) must be at most 16",
+                    q_len, G);
     if (!pow2_page(page_size)) return fail(FA512_ERR_UNSUPPORTED, "page_size must be 16, 32, 64, 128 or 256");
     if (num_pages < 1 || max_pages_per_seq < 1)
         return fail(FA512_ERR_INVALID_ARG, "num_pages and max_pages_per_seq must be >= 1");
@@ -305,7 +315,7 @@ fa512_status fa512_decode_paged(const void* q, const void* k_pages, const void* 
 
     const int splits = num_splits > 0 ? num_splits
                                       : fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len);
-    const size_t need = workspace_for(batch, n_q_heads, splits);
+    const size_t need = workspace_for(batch * q_len, n_q_heads, splits);
     if (!workspace || workspace_bytes < need)
         return fail(FA512_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
@@ -325,7 +335,7 @@ fa512_status fa512_decode_paged(const void* q, const void* k_pages, const void* 
     p.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
     p.page_table = page_table;
     p.kv_lens = kv_lens;
-    const size_t rows = static_cast<size_t>(batch) * n_q_heads * splits;
+    const size_t rows = static_cast<size_t>(batch) * q_len * n_q_heads * splits;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * kHeadDim * sizeof(float)));
     p.out = static_cast<__nv_bfloat16*>(out);
@@ -334,6 +344,7 @@ fa512_status fa512_decode_paged(const void* q, const void* k_pages, const void* 
     p.n_q_heads = n_q_heads;
     p.n_kv_heads = n_kv_heads;
     p.group = G;
+    p.q_len = q_len;
     p.page_size = page_size;
     p.box_rows = page_size < 32 ? page_size : 32;
     p.num_pages = num_pages;
@@ -359,6 +370,19 @@ fa512_status fa512_decode_paged(const void* q, const void* k_pages, const void* 
     e = fa512::launch_decode(tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return FA512_OK;
+}
+
+fa512_status fa512_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int32_t* page_table, const int32_t* kv_lens, void* out,
+                                float* lse, int batch, int n_q_heads, int n_kv_heads,
+                                int page_size, int num_pages, int max_pages_per_seq,
+                                int max_kv_len, float scale, int window, int num_splits,
+                                void* workspace, size_t workspace_bytes,
+                                fa512_stream_t stream) {
+    return fa512_decode_paged_q(q, k_pages, v_pages, page_table, kv_lens, out, lse, batch, 1,
+                                n_q_heads, n_kv_heads, page_size, num_pages, max_pages_per_seq,
+                                max_kv_len, scale, window, num_splits, workspace, workspace_bytes,
+                                stream);
 }
 
 fa512_status fa512_device_status(fa512_stream_t stream, int clear) {

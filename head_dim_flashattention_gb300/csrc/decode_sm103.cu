@@ -15,6 +15,9 @@
 // S = Q K^T and O += P V for the G query heads of its KV head with bf16
 // mma.sync (rows padded to 16), and keeps the softmax state in the log2
 // domain.  HBM traffic per position and KV head: 1 KiB of K + 1 KiB of V.
+// With q_len query tokens per sequence (the last q_len positions of its
+// cache) the rows are (token, head) pairs, q_len * G <= 16, each masked at
+// its own position.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -124,6 +127,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int G = p.group;
+    const int R = p.q_len * G;      // query rows: (token t, head g) -> row t * G + g
 
     // ---- live band of this sequence
     int len = p.kv_lens[b];
@@ -131,8 +135,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
         if (tid == 0 && split == 0 && kvh == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
         len = len < 0 ? 0 : p.len_cap;
     }
+    // union of the rows' bands: row t sees [pos_t - window + 1, pos_t] with
+    // pos_t = len - q_len + t
     const int hi = len;
-    const int lo = (p.window > 0 && len - p.window > 0) ? len - p.window : 0;
+    const int w_lo = len - p.q_len + 1 - p.window;
+    const int lo = (p.window > 0 && w_lo > 0) ? w_lo : 0;
     const int t_lo = lo / TILE_K;
     const int t_hi = (hi + TILE_K - 1) / TILE_K;
     const int t_begin = t_lo + split * p.tiles_per_split;
@@ -152,8 +159,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
         for (int i = tid; i < 16 * 64; i += NUM_THREADS) {
             const int row = i >> 6, c = i & 63;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (row < G) {
-                const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + row;
+            if (row < R) {
+                const size_t h = (static_cast<size_t>(b) * p.q_len + row / G) * p.n_q_heads + kvh * G + row % G;
                 v = reinterpret_cast<const uint4*>(p.q + h * D)[c];
             }
             *reinterpret_cast<uint4*>(qs + row * 1024 + (((c & ~7) | ((c ^ row) & 7)) << 4)) = v;
@@ -188,6 +195,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
     float o[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    // positions of this thread's score rows lane/4 and lane/4 + 8 (-1: padding row, sees nothing)
+    const int qpos0 = (lane >> 2) < R ? len - p.q_len + (lane >> 2) / G : -1;
+    const int qpos1 = (lane >> 2) + 8 < R ? len - p.q_len + ((lane >> 2) + 8) / G : -1;
     float m_run0 = -INFINITY, m_run1 = -INFINITY;   // rows lane/4 and lane/4 + 8
     float l_run0 = 0.f, l_run1 = 0.f;               // partial over this thread's positions
     bool ok = true;
@@ -263,10 +273,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
             sc[3] += x.w;
             const int r = nt * 8 + 2 * (lane & 3);
             const bool v0 = (valid >> r) & 1u, v1 = (valid >> (r + 1)) & 1u;
-            sc[0] = v0 ? sc[0] * p.scale_log2 : -INFINITY;
-            sc[1] = v1 ? sc[1] * p.scale_log2 : -INFINITY;
-            sc[2] = v0 ? sc[2] * p.scale_log2 : -INFINITY;
-            sc[3] = v1 ? sc[3] * p.scale_log2 : -INFINITY;
+            // each row sees the live keys up to its own position (and inside its window)
+            const int pos = t * TILE_K + r;
+            auto sees = [&](int kpos, int qp) {
+                return kpos <= qp && (p.window <= 0 || kpos > qp - p.window);
+            };
+            sc[0] = v0 && sees(pos, qpos0) ? sc[0] * p.scale_log2 : -INFINITY;
+            sc[1] = v1 && sees(pos + 1, qpos0) ? sc[1] * p.scale_log2 : -INFINITY;
+            sc[2] = v0 && sees(pos, qpos1) ? sc[2] * p.scale_log2 : -INFINITY;
+            sc[3] = v1 && sees(pos + 1, qpos1) ? sc[3] * p.scale_log2 : -INFINITY;
             float mx0 = fmaxf(sc[0], sc[1]), mx1 = fmaxf(sc[2], sc[3]);
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
@@ -363,13 +378,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int d = warp * 64 + 8 * j + 2 * (lane & 3);
-        if (row0 < G) {
-            const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + row0;
+        if (row0 < R) {
+            const size_t h = (static_cast<size_t>(b) * p.q_len + row0 / G) * p.n_q_heads + kvh * G + row0 % G;
             *reinterpret_cast<float2*>(p.ws_o + (h * S + split) * D + d) =
                 make_float2(ok ? o[j][0] : 0.f, ok ? o[j][1] : 0.f);
         }
-        if (row1 < G) {
-            const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + row1;
+        if (row1 < R) {
+            const size_t h = (static_cast<size_t>(b) * p.q_len + row1 / G) * p.n_q_heads + kvh * G + row1 % G;
             *reinterpret_cast<float2*>(p.ws_o + (h * S + split) * D + d) =
                 make_float2(ok ? o[j][2] : 0.f, ok ? o[j][3] : 0.f);
         }
@@ -381,8 +396,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
         redm[(lane >> 2) + 8] = m_run1;
     }
     __syncthreads();
-    if (tid < G) {
-        const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + tid;
+    if (tid < R) {
+        const size_t h = (static_cast<size_t>(b) * p.q_len + tid / G) * p.n_q_heads + kvh * G + tid % G;
         const float l = redl[tid] + redl[16 + tid] + redl[32 + tid] + redl[48 + tid];
         const float m = redm[tid];
         p.ws_ml[(h * S + split) * 2 + 0] = ok && n_tiles > 0 ? m : -INFINITY;
@@ -605,12 +620,12 @@ decode_stream_kernel(const DecodeParams p) {
 
 }  // namespace stream
 
-// One block per (sequence, query head): merges the splits' (O, m, l).
+// One block per (sequence, query token, query head): merges the splits' (O, m, l).
 __global__ void __launch_bounds__(128)
 decode_merge_kernel(const DecodeParams p) {
     const int h = blockIdx.x;
-    const int b = blockIdx.y;
-    const size_t bh = static_cast<size_t>(b) * p.n_q_heads + h;
+    const int bt = blockIdx.y;      // sequence * q_len + token
+    const size_t bh = static_cast<size_t>(bt) * p.n_q_heads + h;
     const int S = p.num_splits;
     const float* ml = p.ws_ml + bh * S * 2;
     float M = -INFINITY;
@@ -663,12 +678,13 @@ static cudaError_t launch_stream(const DecodeParams& p, cudaStream_t stream) {
 cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
                           cudaStream_t stream) {
     cudaError_t e;
-    if (p.group == 1) {
+    if (p.q_len == 1 && p.group == 1) {
         e = launch_stream<1>(p, stream);
-    } else if (p.group == 2) {
+    } else if (p.q_len == 1 && p.group == 2) {
         e = launch_stream<2>(p, stream);
     } else {
-        // larger query groups: S and PV on the tensor cores (rows padded to 16)
+        // larger query groups or several tokens: S and PV on the tensor cores
+        // (q_len * G rows padded to 16)
         const int smem = decode_smem_bytes();
         e = cudaFuncSetAttribute(decode::decode_split_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -678,7 +694,7 @@ cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const 
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    dim3 mgrid(p.n_q_heads, p.batch);
+    dim3 mgrid(p.n_q_heads, p.batch * p.q_len);
     decode::decode_merge_kernel<<<mgrid, 128, 0, stream>>>(p);
     return cudaGetLastError();
 }

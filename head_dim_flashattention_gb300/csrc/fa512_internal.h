@@ -10,16 +10,17 @@
 namespace fa512 {
 
 struct DecodeParams {
-    const __nv_bfloat16* q;        // [batch, n_q_heads, 512]
+    const __nv_bfloat16* q;        // [batch, q_len, n_q_heads, 512]
     const __nv_bfloat16* k_pages;  // [num_pages, page_size, n_kv_heads, 512]
     const __nv_bfloat16* v_pages;
     const int32_t* page_table;     // [batch, max_pages_per_seq]
     const int32_t* kv_lens;        // [batch]
-    float* ws_o;                   // [batch, n_q_heads, num_splits, 512] unnormalised O
-    float* ws_ml;                  // [batch, n_q_heads, num_splits, 2] (m in log2 units, l)
-    __nv_bfloat16* out;            // [batch, n_q_heads, 512]
-    float* lse;                    // [batch, n_q_heads] or null
+    float* ws_o;                   // [batch, q_len, n_q_heads, num_splits, 512] unnormalised O
+    float* ws_ml;                  // [batch, q_len, n_q_heads, num_splits, 2] (m in log2 units, l)
+    __nv_bfloat16* out;            // [batch, q_len, n_q_heads, 512]
+    float* lse;                    // [batch, q_len, n_q_heads] or null
     int batch, n_q_heads, n_kv_heads, group;
+    int q_len;                     // query tokens per sequence: its last q_len positions
     int page_size, box_rows, num_pages, max_pages_per_seq;
     int len_cap;                   // min(max_kv_len, max_pages_per_seq * page_size)
     int window;

@@ -129,6 +129,40 @@ fa512_status fa512_decode_paged(const void *q, const void *k_pages, const void *
 size_t fa512_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int page_size,
                                     int max_kv_len, int num_splits);
 
+/*
+ * fa512_decode_paged_q -- q_len query tokens per sequence over a paged KV
+ * cache: the tokens just appended to each cache (draft tokens being
+ * verified, a short chunk), each attending causally to the cache.  The pages
+ * list multi-token decode among the next steps of the decode path
+ * (vllm-project/flash-attention PR #199, "Notes": varlen Q over a paged
+ * cache; "A custom attention kernel for Gemma 4 on the RTX PRO 6000", the
+ * draft of 4 tokens).
+ *
+ *   q    [batch, q_len, n_q_heads, 512] bf16, device
+ *   out  [batch, q_len, n_q_heads, 512] bf16, device, written
+ *   lse  [batch, q_len, n_q_heads] fp32, device, written; may be NULL
+ *   other tensors and arguments as fa512_decode_paged.
+ *
+ * Query t of sequence b sits at position kv_lens[b] - q_len + t and sees
+ * positions [max(0, pos - window + 1), pos] (window <= 0: [0, pos]); a query
+ * whose position is negative (kv_lens[b] < q_len) sees nothing and returns
+ * O = 0, LSE = -inf.  The workspace must be at least
+ * fa512_decode_workspace_bytes_q(batch, q_len, ...) bytes.  Requirements as
+ * fa512_decode_paged, plus q_len >= 1 and q_len * (n_q_heads / n_kv_heads)
+ * <= 16 (FA512_ERR_UNSUPPORTED otherwise).  q_len = 1 is fa512_decode_paged.
+ */
+fa512_status fa512_decode_paged_q(const void *q, const void *k_pages, const void *v_pages,
+                                  const int32_t *page_table, const int32_t *kv_lens, void *out,
+                                  float *lse, int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                  int page_size, int num_pages, int max_pages_per_seq,
+                                  int max_kv_len, float scale, int window, int num_splits,
+                                  void *workspace, size_t workspace_bytes,
+                                  fa512_stream_t stream);
+
+/* Workspace bytes fa512_decode_paged_q needs (0 for an invalid shape). */
+size_t fa512_decode_workspace_bytes_q(int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                      int page_size, int max_kv_len, int num_splits);
+
 /* Split count chosen when num_splits == 0: enough (batch, KV head, split)
  * work items to fill the current device's SMs about twice, each split at
  * least one page.  Returns 1 when there is nothing to split. */

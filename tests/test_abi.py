@@ -99,3 +99,28 @@ def test_workspace_size_and_auto_splits(lib):
     # more work per sequence never asks for fewer splits of a single sequence
     assert fa.fa512_decode_auto_splits(1, 4, 64, 28672) >= s
     assert fa.fa512_decode_workspace_bytes(-1, 8, 4, 64, 10, 0) == 0
+
+
+def _decode_q(lib, **kw):
+    a = dict(q=16, kp=16, vp=16, pt=16, kl=16, out=16, lse=None, b=2, ql=4, hq=8, hk=4, ps=64,
+             npages=10, mpps=4, maxlen=200, scale=0.05, window=0, splits=0, ws=256,
+             wsb=1 << 30)
+    a.update(kw)
+    return lib.fa512_decode_paged_q(a["q"], a["kp"], a["vp"], a["pt"], a["kl"], a["out"],
+                                    a["lse"], a["b"], a["ql"], a["hq"], a["hk"], a["ps"],
+                                    a["npages"], a["mpps"], a["maxlen"], a["scale"], a["window"],
+                                    a["splits"], a["ws"], a["wsb"], None)
+
+
+def test_multi_token_decode_validation_and_workspace(lib):
+    assert _decode_q(lib, ql=0) == 1                 # q_len >= 1
+    assert _decode_q(lib, ql=9, hq=8, hk=4) == 2     # 9 tokens x G 2 > 16 rows
+    assert _decode_q(lib, ql=3, hq=48, hk=8) == 2    # 3 x G 6 = 18 > 16
+    assert _decode_q(lib, wsb=16) == 5
+    assert _decode_q(lib, b=0, q=None) == 0
+    # the workspace covers batch x q_len query rows; q_len 1 is the single-token size
+    n4 = lib.fa512_decode_workspace_bytes_q(4, 4, 8, 4, 64, 4096, 3)
+    assert n4 == 16 * 8 * 3 * 512 * 4 + ((16 * 8 * 3 * 2 * 4 + 255) // 256) * 256
+    assert (lib.fa512_decode_workspace_bytes_q(4, 1, 8, 4, 64, 4096, 3)
+            == fa.fa512_decode_workspace_bytes(4, 8, 4, 64, 4096, 3))
+    assert lib.fa512_decode_workspace_bytes_q(4, 0, 8, 4, 64, 4096, 3) == 0
