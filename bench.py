@@ -38,6 +38,8 @@ PREFILL = dict(name="chunked", seqlen_q=8192, seqlen_k=16384, q_offset=8192, n_q
                n_kv_heads=4)
 DECODE_SHAPES = [(b, n) for b in (1, 16, 64) for n in (4096, 16384, 28672)]
 DECODE_HEADS = (8, 4)
+# several query tokens per sequence (the last q_len positions of the cache)
+DECODE_Q_SHAPE = {"batch": 64, "kv_len": 16384, "q_len": 4}
 PAGE = 64
 METRIC = "hd512 causal prefill TFLOP/s (% of GB300 BF16 peak); decode HBM GB/s"
 PREFILL_WORKLOAD = ("chunked prefill: 8192 q rows at positions 8192..16383 vs 16384 keys, "
@@ -64,11 +66,11 @@ def prefill_flops(seqlen_q, seqlen_k, q_offset, n_q_heads, causal=True, window=0
     return 4 * HEAD_DIM * n_q_heads * visible_pairs(seqlen_q, seqlen_k, q_offset, causal, window)
 
 
-def decode_bytes(batch: int, kv_len: int, n_q_heads: int, n_kv_heads: int) -> int:
+def decode_bytes(batch: int, kv_len: int, n_q_heads: int, n_kv_heads: int, q_len: int = 1) -> int:
     """Algorithmic HBM bytes of one decode call: live K and V rows, q, out, lse,
     page table and lengths (the split partials are not counted)."""
     kv = batch * kv_len * n_kv_heads * HEAD_DIM * 2 * 2
-    qo = batch * n_q_heads * HEAD_DIM * 2 * 2 + batch * n_q_heads * 4
+    qo = q_len * (batch * n_q_heads * HEAD_DIM * 2 * 2 + batch * n_q_heads * 4)
     pt = batch * ((kv_len + PAGE - 1) // PAGE) * 4 + batch * 4
     return kv + qo + pt
 
@@ -442,6 +444,50 @@ def run_ours(args):
                        "every step, copies of neighbouring steps overlapping the kernel on two "
                        "more streams (L2 flush included)"}
 
+    # ---- paged decode of q_len tokens per sequence, timed on its own
+    decode_q = None
+    if not args.no_decode and not args.decode_shapes:
+        b, n, ql = DECODE_Q_SHAPE["batch"], DECODE_Q_SHAPE["kv_len"], DECODE_Q_SHAPE["q_len"]
+        npg = (n + PAGE - 1) // PAGE
+        gcpu = torch.Generator()
+        gcpu.manual_seed(0x5EED + 6)
+        kp = torch.randn((b * npg, PAGE, hk, HEAD_DIM), generator=g, device=dev,
+                         dtype=torch.float32).to(torch.bfloat16)
+        vp = torch.randn(kp.shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        pt = torch.randperm(b * npg, generator=gcpu).to(torch.int32).view(b, npg).to(dev)
+        kl = torch.full((b,), n, dtype=torch.int32, device=dev)
+        dq = torch.randn((b, ql, hq, HEAD_DIM), generator=g, device=dev,
+                         dtype=torch.float32).to(torch.bfloat16)
+        dout = torch.empty_like(dq)
+        dlse = torch.empty((b, ql, hq), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(256, int(fa.load_library().fa512_decode_workspace_bytes_q(
+            b, ql, hq, hk, PAGE, n, 0))), dtype=torch.uint8, device=dev)
+
+        def dq_call():
+            fa.fa512_decode_paged_q(dq, kp, vp, pt, kl, dout, dlse, max_kv_len=n, workspace=ws,
+                                    stream=stream)
+
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            dq_call()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            dq_call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        (t_dq,) = max_over_ranks([sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3], dev)
+        dq_bytes = decode_bytes(b, n, hq, hk, ql)
+        gbs = job_rate(dq_bytes, args.steps, world, t_dq) / 1e9
+        decode_q = {"workload": "paged decode of %d tokens per sequence: batch %d x kv %d, "
+                                "%d/%d heads, page %d, num_splits auto" % (ql, b, n, hq, hk, PAGE),
+                    "value": gbs, "unit": "GB/s", "ms": t_dq / args.steps * 1e3,
+                    "bytes_per_call": dq_bytes, "frac_of_measured_hbm": gbs / world / peaks["hbm_gbs"],
+                    "l2": "flushed before every call"}
+
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu:
         f, dt, threads, desc = oracle_sample(budget_rows=args.ref_rows)
@@ -462,6 +508,7 @@ def run_ours(args):
                         "bytes_per_step": dec_bytes} if dec else None),
             "roofline": roofline,
             "decode_roofline": decode_roofline,
+            "decode_q": decode_q,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": ((0 if args.no_prefill else 1) + 2 * len(dec)) * args.steps,
