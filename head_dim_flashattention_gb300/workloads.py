@@ -160,6 +160,18 @@ def draft_queries(batch: int, q_len: int, n_q_heads: int, seed: int) -> torch.Te
     return randn_bf16((batch, q_len, n_q_heads, HEAD_DIM), seed * 7 + 5)
 
 
+def varlen_queries(seqlens_q, n_q_heads: int, seed: int):
+    """Packed query rows of a batch of prefill chunks: (q [total_q, n_q_heads,
+    D] bf16, cu_seqlens_q [batch + 1] int32), chunk b at rows
+    cu_seqlens_q[b] .. cu_seqlens_q[b + 1] - 1."""
+    lens = [int(x) for x in seqlens_q]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    q = randn_bf16((cu[-1], n_q_heads, HEAD_DIM), seed * 7 + 6)
+    return q, torch.tensor(cu, dtype=torch.int32)
+
+
 def decode_inputs(cfg: DecodeConfig, poison: bool = True) -> PagedCache:
     return paged_decode_inputs(cfg.batch, [cfg.kv_len] * cfg.batch, cfg.n_q_heads,
                                cfg.n_kv_heads, cfg.page_size, cfg.seed, cfg.spare_pages, poison)

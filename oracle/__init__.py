@@ -14,7 +14,8 @@ matrix a classical attention materialises defines the result); "Flash-Decoding
 for MQA in CUDA", section "The test that catches what parity misses" (an FP64
 host reference over the same bf16-rounded inputs) and section "One KV head
 breaks the textbook" (the live band of a decode query); vllm-project/
-flash-attention PR #199, review item F4 (an empty row has LSE = -inf).
+flash-attention PR #199, review item F4 (an empty row has LSE = -inf);
+pegainfer issue #1051, "Proposed Plan" (a varlen prefill over the paged pool).
 """
 from __future__ import annotations
 
@@ -190,4 +191,60 @@ def decode_paged_q(q, k_pages, v_pages, page_table, kv_lens, *, scale: float | N
                                        threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_decode_paged_q rejected its arguments")
+    return out, lse
+
+
+def prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqused_k, *,
+                  scale: float | None = None, causal: bool = True, window: int = 0,
+                  threads: int | None = None):
+    """Reference attention of a batch of prefill chunks over a paged KV cache.
+
+    q [total_q, n_q_heads, D]: the chunk of sequence b is
+    q[cu_seqlens_q[b]:cu_seqlens_q[b + 1]].  k_pages/v_pages [num_pages,
+    page_size, n_kv_heads, D]; page_table [batch, max_pages_per_seq] int;
+    seqused_k [batch] int.  The cache of sequence b holds positions
+    0 .. seqused_k[b] - 1, position j in slot j % page_size of physical page
+    page_table[b, j // page_size] (pegainfer issue #1051, "Proposed Plan": a
+    varlen prefill reading the paged pool).  A chunk is the tail of its
+    sequence, as in the chunked prefill of the same issue's "Description"
+    (one chunk against everything before it): its row i sits at position
+    seqused_k[b] - seqlen_q_b + i; a negative position sees no key under the
+    causal mask.
+
+    Steps: gather the used positions of each sequence in order through its
+    page table (numpy indexing), then the contiguous prefill reference.
+    Returns ``(out, lse)``: out [total_q, n_q_heads, D] fp64,
+    lse [n_q_heads, total_q] fp64.
+    """
+    qb, kb, vb = _bits(q), _bits(k_pages), _bits(v_pages)
+    pt, cu, used = _i32(page_table), _i32(cu_seqlens_q), _i32(seqused_k)
+    total_q, hq, d = qb.shape
+    npages, psz, hk, d2 = kb.shape
+    batch = int(used.shape[0])
+    if (d2 != d or vb.shape != kb.shape or pt.ndim != 2 or pt.shape[0] != batch
+            or cu.shape != (batch + 1,)):
+        raise ValueError("bad shapes")
+    if cu[0] != 0 or np.any(np.diff(cu) < 0) or cu[-1] > total_q:
+        raise ValueError("cu_seqlens_q must rise from 0 to at most total_q")
+    if np.any(used < 0) or np.any(used > pt.shape[1] * psz):
+        raise ValueError("seqused_k outside [0, max_pages_per_seq * page_size]")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((total_q, hq, d), dtype=np.float64)
+    lse = np.zeros((hq, total_q), dtype=np.float64)
+    for b in range(batch):
+        r0, r1 = int(cu[b]), int(cu[b + 1])
+        if r1 == r0:
+            continue
+        n = int(used[b])
+        pos = np.arange(n)
+        phys = pt[b, pos // psz]
+        if np.any(phys < 0) or np.any(phys >= npages):
+            raise ValueError("page table of sequence %d points outside the pool" % b)
+        k_lin = np.ascontiguousarray(kb[phys, pos % psz])
+        v_lin = np.ascontiguousarray(vb[phys, pos % psz])
+        o_b, l_b = prefill(qb[r0:r1], k_lin, v_lin, q_offset=n - (r1 - r0), scale=scale,
+                           causal=causal, window=window, threads=threads)
+        out[r0:r1] = o_b
+        lse[:, r0:r1] = l_b
     return out, lse

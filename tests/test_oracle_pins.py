@@ -405,3 +405,120 @@ def test_decode_q_len_one_is_single_token_decode():
                                    pc.kv_lens)
     np.testing.assert_array_equal(o1, o2[:, 0])
     np.testing.assert_array_equal(l1, l2[:, 0])
+
+
+# ------------------------------------------------ varlen prefill over a paged cache
+
+def _paged_v_positions(pc, lens, page):
+    """V channel 0 at logical position j of sequence b is j / 8, channel 1 is b
+    (both exact in bf16); the other channels keep their random values."""
+    for b, n in enumerate(lens):
+        for j in range(n):
+            pg = int(pc.page_table[b, j // page])
+            pc.v_pages[pg, j % page, :, 0] = j / 8
+            pc.v_pages[pg, j % page, :, 1] = b
+
+
+def test_prefill_paged_positions_closed_form():
+    """q = 0: every visible key has logit 0, so channel 0 of O is the mean of
+    the visible positions / 8 and channel 1 names the sequence.  Row i of a
+    chunk of S rows over a cache of n positions sits at p = n - S + i (the
+    chunk is the tail of its sequence) and sees [lo, p]; a negative p sees
+    nothing.  Slots outside the live positions are NaN, so a read past a
+    sequence's length or through an unused table entry shows up."""
+    page = 16
+    lens_k = [37, 5, 64, 0, 20]
+    lens_q = [6, 9, 1, 3, 0]
+    pc = workloads.paged_decode_inputs(len(lens_k), lens_k, 4, 2, page, seed=41)
+    _paged_v_positions(pc, lens_k, page)
+    _, cu = workloads.varlen_queries(lens_q, 4, seed=41)
+    q = torch.zeros((int(cu[-1]), 4, D), dtype=torch.bfloat16)
+    used = torch.tensor(lens_k, dtype=torch.int32)
+    for W in (0, 3):
+        out, lse = oracle.prefill_paged(q, pc.k_pages, pc.v_pages, pc.page_table, cu, used,
+                                        window=W)
+        assert np.all(np.isfinite(out))
+        for b, (n, s) in enumerate(zip(lens_k, lens_q)):
+            for i in range(s):
+                r, p = int(cu[b]) + i, n - s + i
+                if p < 0:
+                    assert np.all(out[r] == 0) and np.all(np.isneginf(lse[:, r]))
+                    continue
+                lo = max(0, p - W + 1) if W > 0 else 0
+                np.testing.assert_allclose(out[r, :, 0], (lo + p) / 2 / 8, atol=1e-12)
+                np.testing.assert_allclose(out[r, :, 1], b, atol=1e-12)
+                np.testing.assert_allclose(lse[:, r], math.log(p - lo + 1), atol=1e-13)
+    # without the causal mask every row sees the whole cache of its sequence
+    out, lse = oracle.prefill_paged(q, pc.k_pages, pc.v_pages, pc.page_table, cu, used,
+                                    causal=False)
+    for b, (n, s) in enumerate(zip(lens_k, lens_q)):
+        for i in range(s):
+            r = int(cu[b]) + i
+            if n == 0:
+                assert np.all(out[r] == 0) and np.all(np.isneginf(lse[:, r]))
+                continue
+            np.testing.assert_allclose(out[r, :, 0], (n - 1) / 2 / 8, atol=1e-12)
+            np.testing.assert_allclose(lse[:, r], math.log(n), atol=1e-13)
+
+
+def test_prefill_paged_equals_multi_token_decode():
+    """Chunks of S rows each equal an S-token decode over the same cache (a
+    separate code path that walks the page table itself), bit for bit."""
+    page, s, hq, hk = 32, 4, 8, 4
+    lens_k = [40, 100, 7]
+    pc = workloads.paged_decode_inputs(len(lens_k), lens_k, hq, hk, page, seed=42)
+    q, cu = workloads.varlen_queries([s] * len(lens_k), hq, seed=42)
+    used = torch.tensor(lens_k, dtype=torch.int32)
+    for W in (0, 20):
+        o_p, l_p = oracle.prefill_paged(q, pc.k_pages, pc.v_pages, pc.page_table, cu, used,
+                                        window=W)
+        o_d, l_d = oracle.decode_paged_q(q.reshape(len(lens_k), s, hq, D), pc.k_pages,
+                                         pc.v_pages, pc.page_table, used, window=W)
+        np.testing.assert_array_equal(o_p, o_d.reshape(-1, hq, D))
+        np.testing.assert_array_equal(l_p, l_d.reshape(-1, hq).T)
+
+
+def test_prefill_paged_page_permutation_invariance():
+    """Moving every physical page elsewhere in the pool and rewriting the
+    table to match leaves the result unchanged, bit for bit."""
+    page, hq, hk = 16, 4, 1
+    lens_k, lens_q = [50, 33], [20, 33]
+    pc = workloads.paged_decode_inputs(2, lens_k, hq, hk, page, seed=43)
+    q, cu = workloads.varlen_queries(lens_q, hq, seed=43)
+    used = torch.tensor(lens_k, dtype=torch.int32)
+    o1, l1 = oracle.prefill_paged(q, pc.k_pages, pc.v_pages, pc.page_table, cu, used)
+    npg = pc.k_pages.shape[0]
+    perm = torch.randperm(npg, generator=torch.Generator().manual_seed(43))
+    k2 = torch.empty_like(pc.k_pages)
+    v2 = torch.empty_like(pc.v_pages)
+    k2[perm] = pc.k_pages
+    v2[perm] = pc.v_pages
+    pt2 = pc.page_table.clone()
+    live = pt2 < npg
+    pt2[live] = perm[pt2[live].long()].to(torch.int32)
+    o2, l2 = oracle.prefill_paged(q, k2, v2, pt2, cu, used)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    # and a contiguous prefill over the gathered keys agrees for a full-length chunk
+    idx = pc.page_table[1, :3].long()
+    k_lin = pc.k_pages[idx].reshape(3 * page, hk, D)[:33]
+    v_lin = pc.v_pages[idx].reshape(3 * page, hk, D)[:33]
+    o3, l3 = oracle.prefill(q[20:53], k_lin, v_lin, q_offset=0)
+    np.testing.assert_array_equal(o1[20:53], o3)
+    np.testing.assert_array_equal(l1[:, 20:53], l3)
+
+
+def test_prefill_paged_rejects_bad_tables_and_offsets():
+    pc = workloads.paged_decode_inputs(2, [10, 30], 2, 1, 16, seed=44)
+    q, cu = workloads.varlen_queries([4, 5], 2, seed=44)
+    used = torch.tensor([10, 30], dtype=torch.int32)
+    bad = pc.page_table.clone()
+    bad[1, 1] = 10_000
+    with pytest.raises(ValueError):
+        oracle.prefill_paged(q, pc.k_pages, pc.v_pages, bad, cu, used)
+    with pytest.raises(ValueError):
+        oracle.prefill_paged(q, pc.k_pages, pc.v_pages, pc.page_table,
+                             torch.tensor([0, 5, 4], dtype=torch.int32), used)
+    with pytest.raises(ValueError):
+        oracle.prefill_paged(q, pc.k_pages, pc.v_pages, pc.page_table, cu,
+                             torch.tensor([10, 33], dtype=torch.int32))
