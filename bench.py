@@ -41,6 +41,12 @@ DECODE_HEADS = (8, 4)
 # several query tokens per sequence (the last q_len positions of the cache)
 DECODE_Q_SHAPE = {"batch": 64, "kv_len": 16384, "q_len": 4}
 PAGE = 64
+# prefill over a paged cache: (chunk rows, cached positions incl. the chunk) per sequence.
+# "chunked": the headline chunk through shuffled 64-key pages; "varlen": a mixed batch.
+PAGED_PREFILL = {
+    "chunked": [(8192, 16384)],
+    "varlen": [(8192, 8192), (4096, 12288), (2048, 20480), (1024, 1024), (3000, 7000)],
+}
 METRIC = "hd512 causal prefill TFLOP/s (% of GB300 BF16 peak); decode HBM GB/s"
 PREFILL_WORKLOAD = ("chunked prefill: 8192 q rows at positions 8192..16383 vs 16384 keys, "
                     "32 q / 4 kv heads, d512, causal, bf16 N(0,1)")
@@ -444,6 +450,65 @@ def run_ours(args):
                        "every step, copies of neighbouring steps overlapping the kernel on two "
                        "more streams (L2 flush included)"}
 
+    # ---- prefill over a paged cache (varlen batches), timed on its own
+    prefill_paged = None
+    if not args.no_prefill and not args.no_paged:
+        prefill_paged = {}
+        gcpu = torch.Generator()
+        gcpu.manual_seed(0x5EED + 7)
+        hq_p, hk_p = P["n_q_heads"], P["n_kv_heads"]
+        for name, seqs in PAGED_PREFILL.items():
+            npgs = [(n + PAGE - 1) // PAGE for _, n in seqs]
+            num_pages = sum(npgs)
+            kp = torch.randn((num_pages, PAGE, hk_p, HEAD_DIM), generator=g, device=dev,
+                             dtype=torch.float32).to(torch.bfloat16)
+            vp = torch.randn(kp.shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            perm = torch.randperm(num_pages, generator=gcpu).to(torch.int32)
+            pt = torch.zeros((len(seqs), max(npgs)), dtype=torch.int32)
+            c = 0
+            for i, m in enumerate(npgs):
+                pt[i, :m] = perm[c:c + m]
+                c += m
+            pt = pt.to(dev)
+            cu = [0]
+            for sq, _ in seqs:
+                cu.append(cu[-1] + sq)
+            pq = torch.randn((cu[-1], hq_p, HEAD_DIM), generator=g, device=dev,
+                             dtype=torch.float32).to(torch.bfloat16)
+            pout = torch.empty_like(pq)
+            plse = torch.empty((hq_p, cu[-1]), dtype=torch.float32, device=dev)
+            cu_t = torch.tensor(cu, dtype=torch.int32, device=dev)
+            used = torch.tensor([n for _, n in seqs], dtype=torch.int32, device=dev)
+            max_q = max(sq for sq, _ in seqs)
+            flops = sum(prefill_flops(sq, n, n - sq, hq_p) for sq, n in seqs)
+
+            def pp_call():
+                fa.fa512_prefill_paged(pq, kp, vp, pt, cu_t, used, pout, plse, max_seqlen_q=max_q,
+                                       stream=stream)
+
+            for _ in range(max(3, args.warmup)):
+                flush.zero_()
+                pp_call()
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for e0, e1 in evs:
+                flush.zero_()
+                e0.record(stream)
+                pp_call()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            (t_pp,) = max_over_ranks([sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3], dev)
+            tf = job_rate(flops, args.steps, world, t_pp) / 1e12
+            prefill_paged[name] = {
+                "workload": "%d chunk(s) (rows, cached keys) %s over shuffled %d-key pages, "
+                            "%d/%d heads, causal" % (len(seqs), seqs, PAGE, hq_p, hk_p),
+                "value": tf, "unit": "TFLOP/s", "ms": t_pp / args.steps * 1e3,
+                "flops_per_call": flops, "frac_of_measured_bf16": tf / world / peaks["bf16_tflops"],
+                "l2": "flushed before every call"}
+            del kp, vp, pq, pout
+        assert fa.fa512_device_status() == 0
+
     # ---- paged decode of q_len tokens per sequence, timed on its own
     decode_q = None
     if not args.no_decode and not args.decode_shapes:
@@ -509,6 +574,7 @@ def run_ours(args):
             "roofline": roofline,
             "decode_roofline": decode_roofline,
             "decode_q": decode_q,
+            "prefill_paged": prefill_paged,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": ((0 if args.no_prefill else 1) + 2 * len(dec)) * args.steps,
@@ -534,6 +600,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-paged", action="store_true", help="skip the paged-prefill legs")
     ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling)")
     ap.add_argument("--decode-shapes", default="", help="comma list such as b64_kv28672")
     args = ap.parse_args()

@@ -55,6 +55,9 @@ def load_library():
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa512_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P]
         lib.fa512_prefill.restype = I
+        lib.fa512_prefill_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F,
+                                            I, I, P]
+        lib.fa512_prefill_paged.restype = I
         lib.fa512_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I,
                                            P, Z, P]
         lib.fa512_decode_paged.restype = I
@@ -133,6 +136,47 @@ def fa512_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                              _dptr(v, "v", torch.bfloat16), _dptr(out, "out", torch.bfloat16),
                              _dptr(lse, "lse", torch.float32), sq, sk, int(q_offset), hq, hk,
                              float(scale), 1 if causal else 0, int(window), _stream(stream)))
+    return out, lse
+
+
+def fa512_prefill_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                        page_table: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                        seqused_k: torch.Tensor, out: torch.Tensor | None = None,
+                        lse: torch.Tensor | None = None, *, max_seqlen_q: int,
+                        scale: float | None = None, causal: bool = True, window: int = 0,
+                        return_lse: bool = True, stream=None):
+    """Attention forward of a batch of prefill chunks (varlen rows) over a
+    paged KV cache; returns ``(out, lse)``.
+
+    q [total_q, n_q_heads, 512] bf16; k_pages/v_pages [num_pages, page_size,
+    n_kv_heads, 512] bf16; page_table [batch, max_pages_per_seq] int32;
+    cu_seqlens_q [batch + 1] int32; seqused_k [batch] int32 (all CUDA).
+    ``max_seqlen_q`` bounds the chunk lengths on the host.  out is allocated
+    when not given; lse [n_q_heads, total_q] fp32 likewise.
+    """
+    if q.dim() != 3 or k_pages.dim() != 4 or k_pages.shape != v_pages.shape:
+        raise Fa512Error(1, "q must be [total_q, heads, 512], pages [n, page, heads, 512]")
+    if page_table.dim() != 2 or cu_seqlens_q.dim() != 1 or seqused_k.dim() != 1:
+        raise Fa512Error(1, "page_table [batch, pages], cu_seqlens_q [batch + 1], seqused_k [batch]")
+    total_q, hq, d = q.shape
+    npages, psz, hk, _ = k_pages.shape
+    bsz, mpps = page_table.shape
+    if cu_seqlens_q.shape[0] != bsz + 1 or seqused_k.shape[0] != bsz:
+        raise Fa512Error(1, "cu_seqlens_q must have batch + 1 entries and seqused_k batch")
+    if out is None:
+        out = torch.empty((total_q, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, total_q), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = d ** -0.5
+    lib = load_library()
+    _check(lib.fa512_prefill_paged(
+        _dptr(q, "q", torch.bfloat16), _dptr(k_pages, "k_pages", torch.bfloat16),
+        _dptr(v_pages, "v_pages", torch.bfloat16), _dptr(page_table, "page_table", torch.int32),
+        _dptr(cu_seqlens_q, "cu_seqlens_q", torch.int32),
+        _dptr(seqused_k, "seqused_k", torch.int32), _dptr(out, "out", torch.bfloat16),
+        _dptr(lse, "lse", torch.float32), bsz, total_q, int(max_seqlen_q), hq, hk, psz, npages,
+        mpps, float(scale), 1 if causal else 0, int(window), _stream(stream)))
     return out, lse
 
 

@@ -208,6 +208,7 @@ fa512_status fa512_prefill(const void* q, const void* k, const void* v, void* ou
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
     p.seqlen_q = seqlen_q;
+    p.total_q = seqlen_q;
     p.seqlen_k = seqlen_k;
     p.q_offset = q_offset;
     p.n_q_heads = n_q_heads;
@@ -251,6 +252,101 @@ fa512_status fa512_prefill(const void* q, const void* k, const void* v, void* ou
     }
     e = fa512::launch_prefill(tmq, tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return FA512_OK;
+}
+
+fa512_status fa512_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* page_table, const int32_t* cu_seqlens_q,
+                                 const int32_t* seqused_k, void* out, float* lse, int batch,
+                                 int total_q, int max_seqlen_q, int n_q_heads, int n_kv_heads,
+                                 int page_size, int num_pages, int max_pages_per_seq, float scale,
+                                 int causal, int window, fa512_stream_t stream) {
+    g_last_error[0] = 0;
+    if (batch < 0 || total_q < 0 || max_seqlen_q < 0)
+        return fail(FA512_ERR_INVALID_ARG, "negative batch, total_q or max_seqlen_q");
+    if (n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads != 0)
+        return fail(FA512_ERR_INVALID_ARG, "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)",
+                    n_q_heads, n_kv_heads);
+    const int G = n_q_heads / n_kv_heads;
+    if (G > 128) return fail(FA512_ERR_UNSUPPORTED, "more than 128 query heads per KV head");
+    if (page_size != 64 && page_size != 128 && page_size != 256)
+        return fail(FA512_ERR_UNSUPPORTED, "prefill over a paged cache needs page_size 64, 128 or 256");
+    if (num_pages < 1 || max_pages_per_seq < 1)
+        return fail(FA512_ERR_INVALID_ARG, "num_pages and max_pages_per_seq must be >= 1");
+    if (static_cast<long long>(num_pages) * page_size > 0x7fffffffLL - 256 ||
+        static_cast<long long>(max_pages_per_seq) * page_size > 0x7fffffffLL - 256)
+        return fail(FA512_ERR_UNSUPPORTED, "page pool or page table too large for int32 key rows");
+    if (!(scale == scale) || isinf(scale)) return fail(FA512_ERR_INVALID_ARG, "scale is not finite");
+    if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return FA512_OK;
+    if (!q || !out || !k_pages || !v_pages || !page_table || !cu_seqlens_q || !seqused_k)
+        return fail(FA512_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(q) || !aligned16(out) || !aligned16(k_pages) || !aligned16(v_pages))
+        return fail(FA512_ERR_INVALID_ARG, "q, k_pages, v_pages and out must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(page_table) | reinterpret_cast<uintptr_t>(cu_seqlens_q) |
+         reinterpret_cast<uintptr_t>(seqused_k)) & 3u)
+        return fail(FA512_ERR_INVALID_ARG, "int32 arrays must be 4-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(FA512_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+
+    unsigned* err = nullptr;
+    cudaError_t e = device_error_ptr(&err);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+
+    fa512::PrefillParams p;
+    memset(&p, 0, sizeof p);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.total_q = total_q;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = G;
+    p.tokens_per_tile = 128 / G;
+    p.rows_per_tile = p.tokens_per_tile * G;
+    p.causal = causal ? 1 : 0;
+    p.window = window > 0 ? window : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    p.page_table = page_table;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.seqused_k = seqused_k;
+    p.batch = batch;
+    p.max_seqlen_q = max_seqlen_q;
+    const long long tiles = (static_cast<long long>(max_seqlen_q) + p.tokens_per_tile - 1) / p.tokens_per_tile;
+    p.max_pairs = static_cast<int>((tiles + 1) / 2);
+    int shift = 0;
+    while ((1 << shift) < page_size) ++shift;
+    p.page_shift = shift;
+    p.num_pages = num_pages;
+    p.max_pages_per_seq = max_pages_per_seq;
+    p.oob_row = num_pages * page_size;
+    if (static_cast<long long>(batch) * n_kv_heads * p.max_pairs * 4 > 0x7fffffffLL)
+        return fail(FA512_ERR_UNSUPPORTED, "grid too large");
+
+    CUtensorMap tmq, tmk, tmv;
+    {
+        const uint64_t dims[4] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(G),
+                                  static_cast<uint64_t>(n_kv_heads), static_cast<uint64_t>(total_q)};
+        const uint64_t strides[3] = {kHeadDim * 2ull, static_cast<uint64_t>(G) * kHeadDim * 2ull,
+                                     static_cast<uint64_t>(n_q_heads) * kHeadDim * 2ull};
+        const uint32_t box[4] = {64u, static_cast<uint32_t>(G), 1u,
+                                 static_cast<uint32_t>(p.tokens_per_tile)};
+        fa512_status st = encode_bf16(&tmq, q, 4, dims, strides, box);
+        if (st != FA512_OK) return st;
+    }
+    {
+        // the pool as rows of keys: [num_pages * page_size, n_kv_heads, 512]
+        const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(n_kv_heads),
+                                  static_cast<uint64_t>(num_pages) * page_size};
+        const uint64_t strides[2] = {kHeadDim * 2ull, static_cast<uint64_t>(n_kv_heads) * kHeadDim * 2ull};
+        const uint32_t kbox[3] = {64u, 1u, static_cast<uint32_t>(fa512::prefill_k_box_rows())};
+        const uint32_t vbox[3] = {64u, 1u, static_cast<uint32_t>(fa512::prefill_paged_v_box_rows())};
+        fa512_status st = encode_bf16(&tmk, k_pages, 3, dims, strides, kbox);
+        if (st != FA512_OK) return st;
+        st = encode_bf16(&tmv, v_pages, 3, dims, strides, vbox);
+        if (st != FA512_OK) return st;
+    }
+    e = fa512::launch_prefill_paged(tmq, tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
     return FA512_OK;
 }
 

@@ -35,15 +35,23 @@ cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const 
                           cudaStream_t stream);
 
 struct PrefillParams {
-    __nv_bfloat16* out;            // [seqlen_q, n_q_heads, 512]
-    float* lse;                    // [n_q_heads, seqlen_q] or null
+    __nv_bfloat16* out;            // [total_q, n_q_heads, 512]
+    float* lse;                    // [n_q_heads, total_q] or null
     int seqlen_q, seqlen_k, q_offset, n_q_heads, n_kv_heads, group;
     int tokens_per_tile;           // query tokens packed per 128-row tile
     int rows_per_tile;             // tokens_per_tile * group (<= 128)
-    int num_q_tiles;               // per KV head
+    int num_q_tiles;               // per KV head (contiguous mode)
     int causal, window;
     float scale_log2;              // scale * log2(e)
     unsigned* err;
+    int total_q;                   // rows of q / out (contiguous mode: seqlen_q)
+    // varlen mode over a paged cache (the contiguous kernel ignores these)
+    const int32_t* page_table;     // [batch, max_pages_per_seq]
+    const int32_t* cu_seqlens_q;   // [batch + 1]
+    const int32_t* seqused_k;      // [batch]
+    int batch, max_seqlen_q, max_pairs;
+    int page_shift, num_pages, max_pages_per_seq;
+    int oob_row;                   // num_pages * page_size: a row past the pool (TMA fills zeros)
 };
 
 int prefill_smem_bytes();
@@ -54,5 +62,8 @@ int prefill_v_box_rows();   // keys per V box (one key slice)
 void set_last_error_message(const char* msg);
 cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                            const PrefillParams& p, cudaStream_t stream);
+int prefill_paged_v_box_rows();   // keys per V box over a paged cache (one page-aligned half tile)
+cudaError_t launch_prefill_paged(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                 const PrefillParams& p, cudaStream_t stream);
 
 }  // namespace fa512

@@ -51,6 +51,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "fa512_device.cuh"
 #include "fa512_internal.h"
 
@@ -71,7 +73,6 @@ constexpr int K_BOX_ROWS = BN / 2;      // K slot: four {64 columns, 64 keys} bo
 constexpr int K_BOX = K_BOX_ROWS * 128; // 8 KiB
 constexpr int V_BOX_ROWS = BN;          // V slot: two {64 columns, 128 keys} boxes
 constexpr int V_BOX = V_BOX_ROWS * 128; // 16 KiB
-constexpr int K_SLOTS_PER_TILE = 2;     // 256 head-dim columns each
 
 constexpr uint32_t TM_O = 0;            // 256 columns fp32
 constexpr uint32_t TM_S = 256;          // 2 x 128 columns fp32; P (bf16) reuses them
@@ -96,7 +97,8 @@ struct Smem {
         O_DONE = Q_FULL + 1,             // also: the V slot may be refilled
         L_XCHG = O_DONE + 1,             // final row-sum swap
         DRAIN = L_XCHG + 1,              // every issued MMA has completed
-        N_BARS = DRAIN + 1
+        V_TAIL = DRAIN + 1,              // paged: this CTA's V of the tile that holds the cache's end landed
+        N_BARS = V_TAIL + 1
     };
     static constexpr int tmem_addr = bars + N_BARS * 8;
     static constexpr int abort_flag = tmem_addr + 4;
@@ -194,10 +196,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, un
     }
 }
 
-__device__ __forceinline__ bool key_visible(int j, int qpos, const PrefillParams& p) {
-    return j < p.seqlen_k && (!p.causal || j <= qpos) && (p.window <= 0 || j > qpos - p.window);
+__device__ __forceinline__ bool key_visible(int j, int qpos, int seqlen_k, const PrefillParams& p) {
+    return j < seqlen_k && (!p.causal || j <= qpos) && (p.window <= 0 || j > qpos - p.window);
 }
 
+// PAGED: a batch of chunks (varlen rows through cu_seqlens_q) over a paged
+// cache; K and V rows are found through the page table one 64-key half tile
+// at a time (a page holds a whole number of half tiles).
+template <bool PAGED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
@@ -215,27 +221,125 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // ---- work item: (q-tile pair, KV head, O half, rank in the pair).  KV
-    // heads run one after the other so that the CTAs resident at any time
-    // share one head's K and V in L2; within a head the heaviest (latest) q
-    // tiles go first.
+    // ---- work item: (q-tile pair, KV head, O half, rank in the pair), and in
+    // varlen mode the sequence.  KV heads run one after the other so that
+    // the CTAs resident at any time share one head's K and V in L2; within a
+    // head the heaviest (latest) q tiles go first.
     const uint32_t rank = cluster_ctarank();            // == blockIdx.x & 1
     const int half = (blockIdx.x >> 1) & 1;
     const int rest = blockIdx.x >> 2;
-    const int n_pairs = (p.num_q_tiles + 1) / 2;
-    const int kvh = rest / n_pairs;
-    const int pair = n_pairs - 1 - rest % n_pairs;
-    const int qt = 2 * pair + static_cast<int>(rank);   // may equal num_q_tiles: no rows
     const int G = p.group;
     const int T = p.tokens_per_tile;
+    int kvh, pair, seq = 0, q_start = 0;
+    int seqlen_q = p.seqlen_q, seqlen_k = p.seqlen_k, q_offset = p.q_offset;
+    if constexpr (PAGED) {
+        // Work items are numbered sequence by sequence, KV head by KV head,
+        // heaviest pair first, with no gaps: warp 0 finds this CTA's
+        // sequence by a scan of the chunk lengths (one contiguous block of
+        // sequences per lane), the others wait at the barrier below.
+        int* found = reinterpret_cast<int*>(smem + Smem::xmax);   // idle until the pipeline starts
+        const int two_t = 2 * T;
+        // pairs of a chunk with rows [s0, s1) (0 for a malformed entry; block 0 records those)
+        auto chunk_pairs = [&](int s0, int s1) -> int {
+            int n = s1 - s0;
+            if (s0 < 0 || n < 0 || s0 > p.total_q - n) {
+                if (blockIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                return 0;
+            }
+            if (n > p.max_seqlen_q) {
+                if (blockIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                n = p.max_seqlen_q;
+            }
+            return (n + two_t - 1) / two_t;
+        };
+        if (warp == 0) {
+            const int item = rest;
+            const int per = (p.batch + 31) >> 5;
+            const int lo = min(p.batch, lane * per), hi = min(p.batch, lo + per);
+            // up to 32 sequences: one sequence per lane, all loads in flight at once
+            int s0 = 0, s1 = 0, kv = 0;
+            if (per == 1 && lo < hi) {
+                s0 = p.cu_seqlens_q[lo];
+                s1 = p.cu_seqlens_q[lo + 1];
+                kv = p.seqused_k[lo];
+            }
+            int cnt = 0;
+            if (per == 1) {
+                if (lo < hi) cnt = chunk_pairs(s0, s1) * p.n_kv_heads;
+            } else {
+                for (int b = lo; b < hi; ++b)
+                    cnt += chunk_pairs(p.cu_seqlens_q[b], p.cu_seqlens_q[b + 1]) * p.n_kv_heads;
+            }
+            int incl = cnt;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += t;
+            }
+            const int excl = incl - cnt;
+            const unsigned owner_mask = __ballot_sync(0xffffffffu, item >= excl && item < incl);
+            if (owner_mask) {
+                const int owner = __ffs(owner_mask) - 1;
+                if (lane == owner) {
+                    int f_seq = lo, acc = excl;
+                    if (per > 1) {
+                        for (int b = lo; b < hi; ++b) {
+                            s0 = p.cu_seqlens_q[b];
+                            s1 = p.cu_seqlens_q[b + 1];
+                            const int c = chunk_pairs(s0, s1) * p.n_kv_heads;
+                            if (item < acc + c) {
+                                f_seq = b;
+                                break;
+                            }
+                            acc += c;
+                        }
+                        kv = p.seqused_k[f_seq];
+                    }
+                    found[0] = f_seq;
+                    found[1] = item - acc;
+                    found[2] = s0;
+                    found[3] = s1;
+                    found[4] = kv;
+                }
+            } else if (lane == 0) {
+                found[0] = -1;
+            }
+        }
+        __syncthreads();
+        seq = found[0];
+        if (seq < 0) return;                            // past the last item: both CTAs of the pair
+        const int off = found[1];
+        q_start = found[2];
+        seqlen_q = min(found[3] - q_start, p.max_seqlen_q);
+        seqlen_k = found[4];
+        const int n_pairs_seq = (seqlen_q + two_t - 1) / two_t;
+        kvh = off / n_pairs_seq;
+        const int order = off - kvh * n_pairs_seq;     // 0 = heaviest pair
+        pair = n_pairs_seq - 1 - order;
+        q_offset = seqlen_k - (found[3] - q_start);    // the chunk is its sequence's tail
+        const int kv_cap = p.max_pages_per_seq << p.page_shift;
+        if (seqlen_k < 0 || seqlen_k > kv_cap) {
+            // recorded once per sequence; read up to the table's capacity
+            if (tid == 0 && off == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+            seqlen_k = seqlen_k < 0 ? 0 : kv_cap;
+        }
+    } else {
+        const int n_pairs = (p.num_q_tiles + 1) / 2;
+        kvh = rest / n_pairs;
+        pair = n_pairs - 1 - rest % n_pairs;
+    }
+    const int qt = 2 * pair + static_cast<int>(rank);   // may be one past the last tile: no rows
     const int t0 = qt * T;
-    const int ntok = min(T, p.seqlen_q - t0);            // <= 0 for a missing second tile
-    const int p_first = p.q_offset + t0;
-    const int p_last = p.q_offset + t0 + ntok - 1;
+    const int ntok = min(T, seqlen_q - t0);              // <= 0 for a missing second tile
+    const int p_first = q_offset + t0;
+    const int p_last = q_offset + t0 + ntok - 1;
     // the pair's visible band (the same in both CTAs)
-    const int pair_first = p.q_offset + 2 * pair * T;
-    const int pair_last = p.q_offset + min(p.seqlen_q, (2 * pair + 2) * T) - 1;
-    int j_lo = 0, j_hi = p.seqlen_k;
+    const int pair_first = q_offset + 2 * pair * T;
+    const int pair_last = q_offset + min(seqlen_q, (2 * pair + 2) * T) - 1;
+    // paged: the tile that holds the cache's last key when that key does not
+    // end a half tile (its V rows past the end are live pool memory)
+    const int tail_tile = (PAGED && (seqlen_k & (K_BOX_ROWS - 1))) ? (seqlen_k - 1) / BN : -1;
+    int j_lo = 0, j_hi = seqlen_k;
     if (p.causal) j_hi = min(j_hi, pair_last + 1);
     if (p.window > 0) j_lo = max(0, pair_first - p.window + 1);
     if (j_hi < j_lo) j_hi = j_lo;
@@ -249,17 +353,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int tok = row / G;
     const int g = row - tok * G;
     const bool valid_row = softmax_warp && row < p.rows_per_tile && tok < ntok;
-    const int qpos = p.q_offset + t0 + tok;
+    const int qpos = q_offset + t0 + tok;
     const int hq = kvh * G + g;
 
     if (n_kt == 0) {
         // no key is visible to any row of the pair: O = 0, LSE = -inf
         if (valid_row) {
             uint4* dst = reinterpret_cast<uint4*>(
-                p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + half * DH + kh * 128);
+                p.out + (static_cast<size_t>(q_start + t0 + tok) * p.n_q_heads + hq) * D + half * DH + kh * 128);
             for (int i = 0; i < 128 / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
             if (half == 0 && kh == 0 && p.lse)
-                p.lse[static_cast<size_t>(hq) * p.seqlen_q + t0 + tok] = -INFINITY;
+                p.lse[static_cast<size_t>(hq) * p.total_q + q_start + t0 + tok] = -INFINITY;
         }
         return;
     }
@@ -307,39 +411,86 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const uint32_t q_bytes = static_cast<uint32_t>(8 * 128 * p.rows_per_tile);
             if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::Q_FULL], 2 * q_bytes);
             for (int c = 0; c < 8; ++c)
-                tma2_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, leader_bar(Smem::Q_FULL), c * 64, 0, kvh, t0);
-            // K columns 0-255 of tile j (slot KA), columns 256-511 (slot KB)
-            auto load_k = [&](int j, int slot, int c, uint32_t full) {
-                const int key0 = (kt_begin + j) * BN + static_cast<int>(rank) * K_BOX_ROWS;
+                tma2_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, leader_bar(Smem::Q_FULL), c * 64, 0, kvh,
+                             q_start + t0);
+            // Row of the tensor map holding the first key of the 64-key half
+            // tile that starts at logical key `key`: the key itself, or in
+            // paged mode its slot in the pool.  Halves past the cache's end
+            // (and pages outside the pool) read a row past the pool, which
+            // the TMA unit fills with zeros.
+            auto half_row = [&](int key) -> int {
+                if constexpr (PAGED) {
+                    if (key >= seqlen_k) return p.oob_row;
+                    const int pg = p.page_table[static_cast<size_t>(seq) * p.max_pages_per_seq + (key >> p.page_shift)];
+                    if (static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages)) {
+                        report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                        return p.oob_row;
+                    }
+                    return (pg << p.page_shift) + (key & ((1 << p.page_shift) - 1));
+                } else {
+                    return key;
+                }
+            };
+            // rows of the two half tiles of tile j (paged: looked up one tile ahead)
+            int row_lo = half_row(kt_begin * BN), row_hi = half_row(kt_begin * BN + K_BOX_ROWS);
+            int next_lo = 0, next_hi = 0;
+            // K columns 0-255 of tile j (slot KA), columns 256-511 (slot KB): this CTA's half tile
+            auto load_k = [&](int row, int slot, int c, uint32_t full) {
                 for (int b = 0; b < 4; ++b)
                     tma2_load_3d(smem + Smem::ring + slot * SLOT + b * K_BOX, &tmk, full, (c * 4 + b) * 64, kvh,
-                                 key0);
+                                 row);
             };
+
             if (rank == 0) {
                 mbar_arrive_expect_tx(&bars[Smem::FULL_KA], 2 * SLOT);
                 mbar_arrive_expect_tx(&bars[Smem::FULL_KB], 2 * SLOT);
             }
-            load_k(0, SLOT_KA, 0, leader_bar(Smem::FULL_KA));
-            load_k(0, SLOT_KB, 1, leader_bar(Smem::FULL_KB));
+            load_k(rank ? row_hi : row_lo, SLOT_KA, 0, leader_bar(Smem::FULL_KA));
+            load_k(rank ? row_hi : row_lo, SLOT_KB, 1, leader_bar(Smem::FULL_KB));
             bool ok = true;
             for (int j = 0; ok && j < n_kt; ++j) {
                 const uint32_t ph = static_cast<uint32_t>(j & 1);
                 if (j + 1 < n_kt) {
+                    next_lo = half_row((kt_begin + j + 1) * BN);
+                    next_hi = half_row((kt_begin + j + 1) * BN + K_BOX_ROWS);
                     // slot KA once the first half of S(j) is done, slot KB once S(j) is
                     if (!(ok = wait_or_abort(&bars[Smem::EMPTY_KA], ph, p.err, abort))) break;
                     if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::FULL_KA], 2 * SLOT);
-                    load_k(j + 1, SLOT_KA, 0, leader_bar(Smem::FULL_KA));
+                    load_k(rank ? next_hi : next_lo, SLOT_KA, 0, leader_bar(Smem::FULL_KA));
                     if (!(ok = wait_or_abort(&bars[Smem::S_FULL + (j & 1)], (j >> 1) & 1, p.err, abort))) break;
                     if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::FULL_KB], 2 * SLOT);
-                    load_k(j + 1, SLOT_KB, 1, leader_bar(Smem::FULL_KB));
+                    load_k(rank ? next_hi : next_lo, SLOT_KB, 1, leader_bar(Smem::FULL_KB));
                 }
                 // V(j) once O += P(j-1) V(j-1) is done; counted on P ready of tile j
                 if (j > 0 && !(ok = wait_or_abort(&bars[Smem::O_DONE], (j - 1) & 1, p.err, abort))) break;
-                if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::P_FULL + (j & 1)], 2 * SLOT);
-                for (int b = 0; b < 2; ++b)
-                    tma2_load_3d(smem + Smem::ring + SLOT_V * SLOT + b * V_BOX, &tmv,
-                                 leader_bar(Smem::P_FULL + (j & 1)), (half * 4 + static_cast<int>(rank) * 2 + b) * 64,
-                                 kvh, (kt_begin + j) * BN);
+                if constexpr (PAGED) {
+                    // Each V box is one half tile (one page or part of one).
+                    // The tail tile's V lands on this CTA's own barrier: the
+                    // softmax warps clear the rows past the cache's end before
+                    // they mark P ready (a NaN there would survive a zero weight).
+                    const bool tail = kt_begin + j == tail_tile;
+                    uint32_t vbar;
+                    if (tail) {
+                        if (rank == 0) mbar_arrive(&bars[Smem::P_FULL + (j & 1)]);
+                        mbar_arrive_expect_tx(&bars[Smem::V_TAIL], SLOT);
+                        vbar = map_to_cta(smem_u32(&bars[Smem::V_TAIL]), rank);
+                    } else {
+                        if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::P_FULL + (j & 1)], 2 * SLOT);
+                        vbar = leader_bar(Smem::P_FULL + (j & 1));
+                    }
+                    for (int r = 0; r < 2; ++r)
+                        for (int b = 0; b < 2; ++b)
+                            tma2_load_3d(smem + Smem::ring + SLOT_V * SLOT + b * V_BOX + r * K_BOX, &tmv, vbar,
+                                         (half * 4 + static_cast<int>(rank) * 2 + b) * 64, kvh, r ? row_hi : row_lo);
+                } else {
+                    if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::P_FULL + (j & 1)], 2 * SLOT);
+                    for (int b = 0; b < 2; ++b)
+                        tma2_load_3d(smem + Smem::ring + SLOT_V * SLOT + b * V_BOX, &tmv,
+                                     leader_bar(Smem::P_FULL + (j & 1)),
+                                     (half * 4 + static_cast<int>(rank) * 2 + b) * 64, kvh, row_lo);
+                }
+                row_lo = next_lo;
+                row_hi = next_hi;
             }
         }
     } else if (warp == 1) {
@@ -424,7 +575,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
             const int key0 = (kt_begin + j) * BN + kh * BH;
-            const bool half_full = ntok > 0 && key0 + BH <= p.seqlen_k &&
+            const bool half_full = ntok > 0 && key0 + BH <= seqlen_k &&
                                    (!p.causal || key0 + BH - 1 <= p_first) &&
                                    (p.window <= 0 || key0 > p_last - p.window);
             // scores stay unscaled until the exponent; a hidden key gets the
@@ -433,7 +584,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 const float hidden = neg_scale ? INFINITY : -INFINITY;
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
-                    if (!key_visible(key0 + c, qpos, p)) s[c] = hidden;
+                    if (!key_visible(key0 + c, qpos, seqlen_k, p)) s[c] = hidden;
             }
             float mx[16];
             if (!neg_scale) {
@@ -508,6 +659,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             }
             // P of this key half overwrites the first 32 of its own 64 S columns
             tmem_st32(tmem + lane_base + s_col, pk);
+            if constexpr (PAGED) {
+                if (kt_begin + j == tail_tile) {
+                    // the tile holding the cache's end: zero this CTA's V rows
+                    // from the end to the end of its half tile, then hand them
+                    // to the tensor core (async proxy)
+                    if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::V_TAIL], 0, p.err, abort)))) break;
+                    const int r0 = seqlen_k - tail_tile * BN;       // 1 .. 127, not 64
+                    const int n16 = (((r0 + K_BOX_ROWS - 1) & ~(K_BOX_ROWS - 1)) - r0) * 8;   // 16-byte chunks per box
+                    uint8_t* vs = smem + Smem::ring + SLOT_V * SLOT + r0 * 128;
+                    for (int i = tid - 64; i < 2 * n16; i += N_SOFTMAX_WARPS * 32) {
+                        const int b = i >= n16 ? 1 : 0;
+                        *reinterpret_cast<uint4*>(vs + b * V_BOX + (i - b * n16) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
@@ -539,7 +706,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             // convex combination of V rows whatever the rounding of P
             const float inv_l = lb_all > 0.f ? 1.f / lb_all : 0.f;
             __nv_bfloat16* dst =
-                p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + half * DH + kh * 128;
+                p.out + (static_cast<size_t>(q_start + t0 + tok) * p.n_q_heads + hq) * D + half * DH + kh * 128;
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tmem + lane_base + TM_O + kh * 128 + c * 32, o);
@@ -557,7 +724,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 }
             }
             if (valid_row && half == 0 && kh == 0 && p.lse)
-                p.lse[static_cast<size_t>(hq) * p.seqlen_q + t0 + tok] =
+                p.lse[static_cast<size_t>(hq) * p.total_q + q_start + t0 + tok] =
                     l_all > 0.f ? (m_ref + log2f(l_all)) * 0.69314718055994530942f : -INFINITY;
         }
     }
@@ -579,17 +746,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 int prefill_smem_bytes() { return prefill::Smem::total; }
 int prefill_k_box_rows() { return prefill::K_BOX_ROWS; }
 int prefill_v_box_rows() { return prefill::V_BOX_ROWS; }
+int prefill_paged_v_box_rows() { return prefill::K_BOX_ROWS; }
 
 cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                            const PrefillParams& p, cudaStream_t stream) {
     const int smem = prefill_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(prefill::prefill_kernel,
+    cudaError_t e = cudaFuncSetAttribute(prefill::prefill_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // (q-tile pair, O half, rank) per KV head; clusters of two consecutive CTAs
     const int n_pairs = (p.num_q_tiles + 1) / 2;
     const int n_blocks = n_pairs * 4 * p.n_kv_heads;
-    prefill::prefill_kernel<<<n_blocks, prefill::NUM_THREADS, smem, stream>>>(tmq, tmk, tmv, p);
+    prefill::prefill_kernel<false><<<n_blocks, prefill::NUM_THREADS, smem, stream>>>(tmq, tmk, tmv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_paged(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                 const PrefillParams& p, cudaStream_t stream) {
+    const int smem = prefill_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(prefill::prefill_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // (sequence, KV head, q-tile pair, O half, rank) numbered without gaps; the
+    // chunks hold at most total_q / (2 T) + batch pairs
+    const long long per_head = std::min(static_cast<long long>(p.batch) * p.max_pairs,
+                                        (static_cast<long long>(p.total_q) + 2 * p.tokens_per_tile - 1) /
+                                                (2 * p.tokens_per_tile) + p.batch);
+    const long long n_blocks = per_head * p.n_kv_heads * 4;
+    if (n_blocks == 0) return cudaSuccess;
+    prefill::prefill_kernel<true><<<static_cast<unsigned>(n_blocks), prefill::NUM_THREADS, smem, stream>>>(
+        tmq, tmk, tmv, p);
     return cudaGetLastError();
 }
 

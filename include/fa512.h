@@ -17,6 +17,9 @@
  *    tile); pegainfer issue #1051, "Description" (one 8192-row chunk against
  *    everything before it, 32 query heads over 4 KV heads).
  *
+ *  fa512_prefill_paged -- the same for a batch of chunks of different
+ *    lengths over a paged KV cache (pegainfer issue #1051, "Proposed Plan").
+ *
  *  fa512_decode_paged -- one query token per sequence against a paged KV
  *    cache, split over the key sequence (Flash-Decoding): each split writes an
  *    unnormalised (O, m, l) partial and a merge step combines them.
@@ -86,6 +89,52 @@ fa512_status fa512_prefill(const void *q, const void *k, const void *v, void *ou
                            int seqlen_q, int seqlen_k, int q_offset, int n_q_heads,
                            int n_kv_heads, float scale, int causal, int window,
                            fa512_stream_t stream);
+
+/*
+ * fa512_prefill_paged -- attention forward of a batch of prefill chunks
+ * (varlen rows) over a paged KV cache.  pegainfer issue #1051, "Proposed
+ * Plan" (a varlen paged prefill for head dim 512; the pool paged at the key
+ * block, so a block of keys is one copy); vllm-project/flash-attention PR
+ * #199, review (call shapes: varlen Q, paged K/V, prefix prefill).
+ *
+ *   q            [total_q, n_q_heads, 512]              bf16, device
+ *   k_pages      [num_pages, page_size, n_kv_heads, 512] bf16, device
+ *   v_pages      same shape as k_pages                  bf16, device
+ *   page_table   [batch, max_pages_per_seq] int32, device: logical page p of
+ *                sequence b is physical page page_table[b * max_pages_per_seq + p]
+ *   cu_seqlens_q [batch + 1] int32, device: the chunk of sequence b is rows
+ *                cu_seqlens_q[b] .. cu_seqlens_q[b + 1] - 1 of q and out
+ *   seqused_k    [batch] int32, device: cached positions of sequence b,
+ *                the chunk's own keys included
+ *   out          [total_q, n_q_heads, 512] bf16, device, written
+ *   lse          [n_q_heads, total_q] fp32, device, written; may be NULL
+ *
+ * A chunk is the tail of its sequence: row i of a chunk of S rows sits at
+ * position seqused_k[b] - S + i, and key j < seqused_k[b] is visible to it
+ * under the same causal / window rule as fa512_prefill (a negative position
+ * sees no key when causal: O = 0, LSE = -inf).  Only the pages that hold
+ * visible positions are read; slots past seqused_k[b] may hold anything
+ * (NaN included) without reaching the output.
+ *
+ * max_seqlen_q is a host-side upper bound of the chunk lengths (it sizes the
+ * grid; nothing is read back).  On the device, a chunk longer than
+ * max_seqlen_q, seqused_k[b] outside [0, max_pages_per_seq * page_size],
+ * cu_seqlens_q not rising within [0, total_q], or a page index outside
+ * [0, num_pages) is recorded in the device error word; the offending rows or
+ * pages are clipped or read as zeros, never out of bounds.
+ *
+ * Requirements: page_size 64, 128 or 256 (a page holds whole 64-key half
+ * tiles); num_pages, max_pages_per_seq >= 1; n_q_heads a multiple of
+ * n_kv_heads with at most 128 query heads per KV head; tensors 16-byte
+ * aligned, int32 arrays 4-byte aligned.  batch, total_q or max_seqlen_q == 0
+ * is a no-op.
+ */
+fa512_status fa512_prefill_paged(const void *q, const void *k_pages, const void *v_pages,
+                                 const int32_t *page_table, const int32_t *cu_seqlens_q,
+                                 const int32_t *seqused_k, void *out, float *lse, int batch,
+                                 int total_q, int max_seqlen_q, int n_q_heads, int n_kv_heads,
+                                 int page_size, int num_pages, int max_pages_per_seq, float scale,
+                                 int causal, int window, fa512_stream_t stream);
 
 /*
  * fa512_decode_paged -- one query token per sequence over a paged KV cache.

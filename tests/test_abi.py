@@ -124,3 +124,35 @@ def test_multi_token_decode_validation_and_workspace(lib):
     assert (lib.fa512_decode_workspace_bytes_q(4, 1, 8, 4, 64, 4096, 3)
             == fa.fa512_decode_workspace_bytes(4, 8, 4, 64, 4096, 3))
     assert lib.fa512_decode_workspace_bytes_q(4, 0, 8, 4, 64, 4096, 3) == 0
+
+
+def _prefill_paged(lib, **kw):
+    args = dict(q=16, k=16, v=16, pt=16, cu=16, used=16, out=16, lse=None, batch=2, total_q=8,
+                max_q=4, hq=8, hk=2, page=64, npages=4, mpps=2, scale=0.05, causal=1, window=0)
+    args.update(kw)
+    a = args
+    return lib.fa512_prefill_paged(a["q"], a["k"], a["v"], a["pt"], a["cu"], a["used"], a["out"],
+                                   a["lse"], a["batch"], a["total_q"], a["max_q"], a["hq"],
+                                   a["hk"], a["page"], a["npages"], a["mpps"], a["scale"],
+                                   a["causal"], a["window"], None)
+
+
+def test_prefill_paged_rejects_bad_arguments_before_any_launch(lib):
+    assert _prefill_paged(lib, batch=-1) == 1
+    assert _prefill_paged(lib, total_q=-1) == 1
+    assert _prefill_paged(lib, hq=6, hk=4) == 1
+    assert _prefill_paged(lib, page=32) == 2          # a page must hold whole 64-key half tiles
+    assert _prefill_paged(lib, page=100) == 2
+    assert _prefill_paged(lib, npages=0) == 1
+    assert _prefill_paged(lib, mpps=0) == 1
+    assert _prefill_paged(lib, npages=1 << 24, page=256) == 2   # pool rows past int32
+    assert _prefill_paged(lib, scale=float("inf")) == 1
+    assert _prefill_paged(lib, q=None) == 1
+    assert _prefill_paged(lib, cu=None) == 1
+    assert _prefill_paged(lib, out=24) == 1           # misaligned
+    assert _prefill_paged(lib, used=18) == 1          # int32 array misaligned
+    assert _prefill_paged(lib, hq=256, hk=1) == 2
+    # empty batches are no-ops that touch nothing
+    assert _prefill_paged(lib, batch=0, q=None) == 0
+    assert _prefill_paged(lib, total_q=0, q=None) == 0
+    assert _prefill_paged(lib, max_q=0, q=None) == 0
