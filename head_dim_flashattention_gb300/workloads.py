@@ -37,10 +37,11 @@ class PrefillConfig:
     window: int = 0
     stress: bool = False          # every 64th K row multiplied by 8
     seed: int = SEED_BASE
+    head_dim: int = HEAD_DIM
 
     @property
     def scale(self) -> float:
-        return HEAD_DIM ** -0.5
+        return self.head_dim ** -0.5
 
 
 @dataclass(frozen=True)
@@ -67,6 +68,11 @@ PREFILL_CONFIGS = {
     "full_stress": PrefillConfig("full_stress", 20480, 20480, 0, 32, 4, stress=True,
                                  seed=SEED_BASE + 3),
     "mqa": PrefillConfig("mqa", 49152, 49152, 0, 16, 1, seed=SEED_BASE + 4),
+    # the sliding-window local layers: heads of 256 dimensions over the last
+    # 1,024 tokens, a 20k-token prompt (RTX PRO 6000 page, "The deployment");
+    # the head counts are the global layers' (the pages give none for these)
+    "local256": PrefillConfig("local256", 20480, 20480, 0, 32, 4, window=1024,
+                              seed=SEED_BASE + 8, head_dim=256),
 }
 
 DECODE_CONFIGS = {
@@ -87,10 +93,10 @@ def randn_bf16(shape, seed: int) -> torch.Tensor:
 
 
 def prefill_inputs(cfg: PrefillConfig):
-    """(q, k, v) on the CPU: q [sq, Hq, 512], k/v [sk, Hkv, 512], bf16."""
-    q = randn_bf16((cfg.seqlen_q, cfg.n_q_heads, HEAD_DIM), cfg.seed * 3 + 0)
-    k = randn_bf16((cfg.seqlen_k, cfg.n_kv_heads, HEAD_DIM), cfg.seed * 3 + 1)
-    v = randn_bf16((cfg.seqlen_k, cfg.n_kv_heads, HEAD_DIM), cfg.seed * 3 + 2)
+    """(q, k, v) on the CPU: q [sq, Hq, D], k/v [sk, Hkv, D], bf16 (D = cfg.head_dim)."""
+    q = randn_bf16((cfg.seqlen_q, cfg.n_q_heads, cfg.head_dim), cfg.seed * 3 + 0)
+    k = randn_bf16((cfg.seqlen_k, cfg.n_kv_heads, cfg.head_dim), cfg.seed * 3 + 1)
+    v = randn_bf16((cfg.seqlen_k, cfg.n_kv_heads, cfg.head_dim), cfg.seed * 3 + 2)
     if cfg.stress:
         # x8 is exact in bf16 (an exponent change), so the stressed rows stay
         # exact copies of 8 * (the unstressed bf16 value).

@@ -522,3 +522,67 @@ def test_prefill_paged_rejects_bad_tables_and_offsets():
     with pytest.raises(ValueError):
         oracle.prefill_paged(q, pc.k_pages, pc.v_pages, pc.page_table, cu,
                              torch.tensor([10, 33], dtype=torch.int32))
+
+
+# --------------------------------------- head dim 256 (the sliding-window local layers)
+
+D256 = 256
+
+
+def test_d256_window_band_closed_form():
+    """Head dim 256, window 1024 ("A custom attention kernel for Gemma 4 on the
+    RTX PRO 6000", "The deployment": the local layers attend to the last 1,024
+    tokens with heads of 256 dimensions).  q = 0 and V channel c at position j
+    equal to j / 64 (exact in bf16 for j < 2048): row i at p = q_offset + i
+    averages the (bf16-rounded) values of [max(0, p - W + 1), p] and
+    LSE = ln(count)."""
+    sk, off, sq, W = 1500, 300, 1200, 1024
+    q = np.zeros((sq, 2, D256), np.float32)
+    k = np.ones((sk, 1, D256), np.float32)
+    vb = bf16(np.repeat((np.arange(sk, dtype=np.float32) / 64)[:, None, None], D256, axis=2))
+    vr = vb.float().numpy().astype(np.float64)[:, 0, D256 - 1]
+    rows = [0, 1, 700, 723, 724, 725, 1199]
+    out, lse = oracle.prefill(bf16(q), bf16(k), vb, q_offset=off, window=W, rows=rows)
+    for r, i in enumerate(rows):
+        p = off + i
+        lo = max(0, p - W + 1)
+        np.testing.assert_allclose(out[r, :, D256 - 1], vr[lo:p + 1].mean(), atol=1e-12)
+        np.testing.assert_allclose(lse[:, r], math.log(p - lo + 1), atol=1e-12)
+
+
+def test_d256_two_keys_and_scale():
+    """Two visible keys with q.k0 = a * b over one channel and q.k1 = 0: the
+    weights are sigmoid(+-s), s = a * b / 16, the default scale 1/sqrt(256)."""
+    a, b = 3.0, 5.0
+    q = np.zeros((1, 1, D256), np.float32)
+    q[0, 0, 255] = a
+    k = np.zeros((2, 1, D256), np.float32)
+    k[0, 0, 255] = b
+    v = np.zeros((2, 1, D256), np.float32)
+    v[0, 0, 0] = 1.0
+    v[1, 0, 1] = 1.0
+    out, lse = oracle.prefill(bf16(q), bf16(k), bf16(v), q_offset=1)
+    s = a * b / 16
+    w0 = 1 / (1 + math.exp(-s))
+    assert out[0, 0, 0] == pytest.approx(w0, rel=1e-13)
+    assert out[0, 0, 1] == pytest.approx(1 - w0, rel=1e-12)
+    assert lse[0, 0] == pytest.approx(math.log(math.exp(s) + 1), rel=1e-13)
+
+
+def test_d256_head_mapping_and_last_channel():
+    """Query head h reads KV head h // G and every one of the 256 channels:
+    V of KV head c is c + 1 + channel / 256, rounded to bf16 once and used
+    rounded on both sides."""
+    hq, hk, sk = 8, 2, 5
+    q = np.zeros((3, hq, D256), np.float32)
+    k = np.zeros((sk, hk, D256), np.float32)
+    ch = np.arange(D256, dtype=np.float32) / 256
+    v = np.zeros((sk, hk, D256), np.float32)
+    for c in range(hk):
+        v[:, c, :] = c + 1 + ch
+    vb = bf16(v)
+    vr = vb.float().numpy().astype(np.float64)
+    out, _ = oracle.prefill(bf16(q), bf16(k), vb, q_offset=sk - 3)
+    for h in range(hq):
+        np.testing.assert_allclose(out[:, h, :], np.broadcast_to(vr[0, h // (hq // hk)], (3, D256)),
+                                   atol=1e-14)
