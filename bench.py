@@ -43,6 +43,8 @@ DECODE_Q_SHAPE = {"batch": 64, "kv_len": 16384, "q_len": 4}
 PAGE = 64
 # prefill over a paged cache: (chunk rows, cached positions incl. the chunk) per sequence.
 # "chunked": the headline chunk through shuffled 64-key pages; "varlen": a mixed batch.
+# the sliding-window local layers: heads of 256 dimensions over the last 1,024 tokens
+LOCAL256 = {"seqlen": 20480, "window": 1024, "n_q_heads": 32, "n_kv_heads": 4}
 PAGED_PREFILL = {
     "chunked": [(8192, 16384)],
     "varlen": [(8192, 8192), (4096, 12288), (2048, 20480), (1024, 1024), (3000, 7000)],
@@ -68,8 +70,9 @@ def visible_pairs(seqlen_q: int, seqlen_k: int, q_offset: int, causal: bool = Tr
     return total
 
 
-def prefill_flops(seqlen_q, seqlen_k, q_offset, n_q_heads, causal=True, window=0) -> int:
-    return 4 * HEAD_DIM * n_q_heads * visible_pairs(seqlen_q, seqlen_k, q_offset, causal, window)
+def prefill_flops(seqlen_q, seqlen_k, q_offset, n_q_heads, causal=True, window=0,
+                  head_dim=HEAD_DIM) -> int:
+    return 4 * head_dim * n_q_heads * visible_pairs(seqlen_q, seqlen_k, q_offset, causal, window)
 
 
 def decode_bytes(batch: int, kv_len: int, n_q_heads: int, n_kv_heads: int, q_len: int = 1) -> int:
@@ -367,7 +370,7 @@ def run_ours(args):
 
     peaks, peak_kind = read_peaks()
     pf_avg_s = t_pf / args.steps if not args.no_prefill else float("nan")
-    pf_src = source_digest(["prefill_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
+    pf_src = source_digest(["prefill_sm103.cu", "fa512_pair.cuh", "fa512_device.cuh", "fa512_internal.h"])
     dec_src = source_digest(["decode_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
     roofline = {"kernel": "fa512::prefill::prefill_kernel", "bound": "tensor",
                 "achieved": pf_flops / pf_avg_s / 1e12, "peak": peaks["bf16_tflops"],
@@ -509,6 +512,45 @@ def run_ours(args):
             del kp, vp, pq, pout
         assert fa.fa512_device_status() == 0
 
+    # ---- the local layers: heads of 256 dimensions over a 1,024-key window
+    local256 = None
+    if not args.no_prefill and not args.no_paged:
+        L = LOCAL256
+        lq = torch.randn((L["seqlen"], L["n_q_heads"], 256), generator=g, device=dev,
+                         dtype=torch.float32).to(torch.bfloat16)
+        lk = torch.randn((L["seqlen"], L["n_kv_heads"], 256), generator=g, device=dev,
+                         dtype=torch.float32).to(torch.bfloat16)
+        lv = torch.randn(lk.shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        lout = torch.empty_like(lq)
+        llse = torch.empty((L["n_q_heads"], L["seqlen"]), dtype=torch.float32, device=dev)
+        lflops = prefill_flops(L["seqlen"], L["seqlen"], 0, L["n_q_heads"], window=L["window"],
+                               head_dim=256)
+
+        def l_call():
+            fa.fa512_prefill_d256(lq, lk, lv, lout, llse, window=L["window"], stream=stream)
+
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            l_call()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            l_call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        (t_l,) = max_over_ranks([sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3], dev)
+        tf = job_rate(lflops, args.steps, world, t_l) / 1e12
+        local256 = {"workload": "local layer: %d tokens from 0, window %d, %d/%d heads, head dim 256, "
+                                "causal" % (L["seqlen"], L["window"], L["n_q_heads"], L["n_kv_heads"]),
+                    "value": tf, "unit": "TFLOP/s", "ms": t_l / args.steps * 1e3,
+                    "flops_per_call": lflops, "frac_of_measured_bf16": tf / world / peaks["bf16_tflops"],
+                    "l2": "flushed before every call"}
+        del lq, lk, lv, lout
+        assert fa.fa512_device_status() == 0
+
     # ---- paged decode of q_len tokens per sequence, timed on its own
     decode_q = None
     if not args.no_decode and not args.decode_shapes:
@@ -575,6 +617,7 @@ def run_ours(args):
             "decode_roofline": decode_roofline,
             "decode_q": decode_q,
             "prefill_paged": prefill_paged,
+            "local256": local256,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": ((0 if args.no_prefill else 1) + 2 * len(dec)) * args.steps,

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     fa512_decode_workspace_bytes,
     fa512_device_status,
     fa512_prefill,
+    fa512_prefill_d256,
     fa512_prefill_paged,
     fa512_status_string,
     library_path,

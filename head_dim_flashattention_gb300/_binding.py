@@ -55,6 +55,8 @@ def load_library():
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa512_prefill.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P]
         lib.fa512_prefill.restype = I
+        lib.fa512_prefill_d256.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P]
+        lib.fa512_prefill_d256.restype = I
         lib.fa512_prefill_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F,
                                             I, I, P]
         lib.fa512_prefill_paged.restype = I
@@ -136,6 +138,35 @@ def fa512_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                              _dptr(v, "v", torch.bfloat16), _dptr(out, "out", torch.bfloat16),
                              _dptr(lse, "lse", torch.float32), sq, sk, int(q_offset), hq, hk,
                              float(scale), 1 if causal else 0, int(window), _stream(stream)))
+    return out, lse
+
+
+def fa512_prefill_d256(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                       out: torch.Tensor | None = None, lse: torch.Tensor | None = None, *,
+                       q_offset: int = 0, scale: float | None = None, causal: bool = True,
+                       window: int = 0, return_lse: bool = True, stream=None):
+    """Attention forward of one prefill chunk with heads of 256 dimensions
+    (the sliding-window local layers); returns ``(out, lse)``.
+
+    q [seqlen_q, n_q_heads, 256], k/v [seqlen_k, n_kv_heads, 256], bf16 CUDA.
+    """
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3 or k.shape != v.shape:
+        raise Fa512Error(1, "q, k, v must be [seq, heads, 256] with k.shape == v.shape")
+    sq, hq, d = q.shape
+    sk, hk, dk = k.shape
+    if d != 256 or dk != 256:
+        raise Fa512Error(1, "fa512_prefill_d256 takes heads of 256 dimensions")
+    if out is None:
+        out = torch.empty((sq, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, sq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = d ** -0.5
+    lib = load_library()
+    _check(lib.fa512_prefill_d256(_dptr(q, "q", torch.bfloat16), _dptr(k, "k", torch.bfloat16),
+                                  _dptr(v, "v", torch.bfloat16), _dptr(out, "out", torch.bfloat16),
+                                  _dptr(lse, "lse", torch.float32), sq, sk, int(q_offset), hq, hk,
+                                  float(scale), 1 if causal else 0, int(window), _stream(stream)))
     return out, lse
 
 

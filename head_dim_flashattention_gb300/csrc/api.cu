@@ -255,6 +255,91 @@ fa512_status fa512_prefill(const void* q, const void* k, const void* v, void* ou
     return FA512_OK;
 }
 
+fa512_status fa512_prefill_d256(const void* q, const void* k, const void* v, void* out, float* lse,
+                                int seqlen_q, int seqlen_k, int q_offset, int n_q_heads,
+                                int n_kv_heads, float scale, int causal, int window,
+                                fa512_stream_t stream) {
+    g_last_error[0] = 0;
+    constexpr int kD = 256;
+    if (seqlen_q < 0 || seqlen_k < 0 || q_offset < 0)
+        return fail(FA512_ERR_INVALID_ARG, "negative length or offset");
+    if (n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads != 0)
+        return fail(FA512_ERR_INVALID_ARG, "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)",
+                    n_q_heads, n_kv_heads);
+    const int G = n_q_heads / n_kv_heads;
+    if (G > 128) return fail(FA512_ERR_UNSUPPORTED, "more than 128 query heads per KV head");
+    if (!(scale == scale) || isinf(scale)) return fail(FA512_ERR_INVALID_ARG, "scale is not finite");
+    if (static_cast<long long>(q_offset) + seqlen_q > 0x7fffffffLL)
+        return fail(FA512_ERR_INVALID_ARG, "q_offset + seqlen_q overflows int32 positions");
+    if (seqlen_q == 0) return FA512_OK;
+    if (!q || !out || (seqlen_k > 0 && (!k || !v)))
+        return fail(FA512_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(out) || (seqlen_k > 0 && (!aligned16(k) || !aligned16(v))))
+        return fail(FA512_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(FA512_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+
+    unsigned* err = nullptr;
+    cudaError_t e = device_error_ptr(&err);
+    if (e != cudaSuccess) return cuda_fail(e, "device error word");
+
+    fa512::Prefill256Params p;
+    memset(&p, 0, sizeof p);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.seqlen_q = seqlen_q;
+    p.seqlen_k = seqlen_k;
+    p.q_offset = q_offset;
+    p.n_q_heads = n_q_heads;
+    p.n_kv_heads = n_kv_heads;
+    p.group = G;
+    p.tokens_per_tile = 128 / G;
+    p.rows_per_tile = p.tokens_per_tile * G;
+    p.num_q_tiles = (seqlen_q + p.tokens_per_tile - 1) / p.tokens_per_tile;
+    p.n_pairs = (p.num_q_tiles + 1) / 2;
+    if (static_cast<long long>(p.n_pairs) * n_kv_heads > 0x7fffffffLL)
+        return fail(FA512_ERR_UNSUPPORTED, "too many work items");
+    p.n_items = p.n_pairs * n_kv_heads;
+    p.causal = causal ? 1 : 0;
+    p.window = window > 0 ? window : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    fa512::plan_prefill256(p, sm_count());
+
+    CUtensorMap tmq, tmk, tmv, tmo;
+    memset(&tmk, 0, sizeof tmk);
+    memset(&tmv, 0, sizeof tmv);
+    {
+        const uint64_t dims[4] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(G),
+                                  static_cast<uint64_t>(n_kv_heads), static_cast<uint64_t>(seqlen_q)};
+        const uint64_t strides[3] = {kD * 2ull, static_cast<uint64_t>(G) * kD * 2ull,
+                                     static_cast<uint64_t>(n_q_heads) * kD * 2ull};
+        const uint32_t box[4] = {64u, static_cast<uint32_t>(G), 1u,
+                                 static_cast<uint32_t>(p.tokens_per_tile)};
+        fa512_status st = encode_bf16(&tmq, q, 4, dims, strides, box);
+        if (st != FA512_OK) return st;
+        // O leaves through the same box shape (a staged tile per TMA store)
+        st = encode_bf16(&tmo, out, 4, dims, strides, box);
+        if (st != FA512_OK) return st;
+    }
+    if (seqlen_k > 0) {
+        const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(n_kv_heads),
+                                  static_cast<uint64_t>(seqlen_k)};
+        const uint64_t strides[2] = {kD * 2ull, static_cast<uint64_t>(n_kv_heads) * kD * 2ull};
+        // K in {64 columns, 48 keys} boxes (each CTA of a pair holds half a
+        // 96-key tile), V in {64 columns, 96 keys} boxes
+        const uint32_t kbox[3] = {64u, 1u, static_cast<uint32_t>(fa512::prefill256_k_box_rows())};
+        const uint32_t vbox[3] = {64u, 1u, static_cast<uint32_t>(fa512::prefill256_v_box_rows())};
+        fa512_status st = encode_bf16(&tmk, k, 3, dims, strides, kbox);
+        if (st != FA512_OK) return st;
+        st = encode_bf16(&tmv, v, 3, dims, strides, vbox);
+        if (st != FA512_OK) return st;
+    }
+    e = fa512::launch_prefill256(tmq, tmk, tmv, tmo, p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "head-dim-256 prefill launch");
+    return FA512_OK;
+}
+
 fa512_status fa512_prefill_paged(const void* q, const void* k_pages, const void* v_pages,
                                  const int32_t* page_table, const int32_t* cu_seqlens_q,
                                  const int32_t* seqused_k, void* out, float* lse, int batch,

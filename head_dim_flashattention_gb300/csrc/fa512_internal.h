@@ -58,6 +58,30 @@ int prefill_smem_bytes();
 int prefill_k_box_rows();   // keys per K box (one head-dim chunk of a key tile)
 int prefill_v_box_rows();   // keys per V box (one key slice)
 
+// Head dim 256 (the sliding-window local layers): a persistent kernel, one
+// cluster of two CTAs per SM pair, each walking a contiguous range of
+// (KV head, q-tile pair) items.
+constexpr int kMaxPersistentClusters = 128;
+
+struct Prefill256Params {
+    __nv_bfloat16* out;            // [seqlen_q, n_q_heads, 256]
+    float* lse;                    // [n_q_heads, seqlen_q] or null
+    int seqlen_q, seqlen_k, q_offset, n_q_heads, n_kv_heads, group;
+    int tokens_per_tile, rows_per_tile, num_q_tiles, n_pairs, n_items;
+    int causal, window;
+    float scale_log2;
+    unsigned* err;
+    int n_clusters;
+    int range_start[kMaxPersistentClusters + 1];   // items of cluster c: [range_start[c], range_start[c + 1])
+};
+
+int prefill256_smem_bytes();
+int prefill256_k_box_rows();
+int prefill256_v_box_rows();
+void plan_prefill256(Prefill256Params& p, int n_sm);
+cudaError_t launch_prefill256(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const CUtensorMap& tmo, const Prefill256Params& p, cudaStream_t stream);
+
 // Sets the text fa512_last_error_message() returns on this thread.
 void set_last_error_message(const char* msg);
 cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,

@@ -55,9 +55,11 @@
 
 #include "fa512_device.cuh"
 #include "fa512_internal.h"
+#include "fa512_pair.cuh"
 
 namespace fa512 {
 namespace prefill {
+using namespace pair;
 
 constexpr int D = 512;
 constexpr int BM = 128;                 // packed rows per CTA tile
@@ -98,7 +100,8 @@ struct Smem {
         L_XCHG = O_DONE + 1,             // final row-sum swap
         DRAIN = L_XCHG + 1,              // every issued MMA has completed
         V_TAIL = DRAIN + 1,              // paged: this CTA's V of the tile that holds the cache's end landed
-        N_BARS = V_TAIL + 1
+        O_FINAL = V_TAIL + 1,            // the last O += P V has completed
+        N_BARS = O_FINAL + 1
     };
     static constexpr int tmem_addr = bars + N_BARS * 8;
     static constexpr int abort_flag = tmem_addr + 4;
@@ -111,90 +114,6 @@ static_assert(Smem::total <= 232448, "shared memory budget");
 
 constexpr uint32_t IDESC_QK = make_idesc_bf16(2 * BM, BN, 0);
 constexpr uint32_t IDESC_PV = make_idesc_bf16(2 * BM, DH, 1);
-
-// ---------------------------------------------------------------- 2-SM forms
-
-// D (+)= A B^T on the CTA pair: A rows 0-127 from the even CTA, 128-255 from
-// the odd one (same shared-memory / TMEM offsets), B's N columns split in
-// halves between the two CTAs; each CTA's TMEM receives its 128 rows.
-__device__ __forceinline__ void mma2_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
-                 : "memory");
-}
-__device__ __forceinline__ void mma2_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                 ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-                 : "memory");
-}
-// Arrives on the barrier at this offset in both CTAs once every MMA issued so
-// far has completed.
-__device__ __forceinline__ void commit2_both(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-        ::"r"(smem_u32(bar)), "h"(static_cast<uint16_t>(3))
-        : "memory");
-}
-// Arrives only on this CTA's barrier.
-__device__ __forceinline__ void commit2_local(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-        ::"r"(smem_u32(bar)), "h"(static_cast<uint16_t>(1))
-        : "memory");
-}
-__device__ __forceinline__ void tmem_alloc2(uint32_t* dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish2() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// TMA tile loads into this CTA's shared memory whose completion is counted on
-// an mbarrier of either CTA of the pair (bar_cluster: shared::cluster address).
-__device__ __forceinline__ void tma2_load_3d(void* smem_dst, const CUtensorMap* m, uint32_t bar_cluster,
-                                             int c0, int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-__device__ __forceinline__ void tma2_load_4d(void* smem_dst, const CUtensorMap* m, uint32_t bar_cluster,
-                                             int c0, int c1, int c2, int c3) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-        : "memory");
-}
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// Bounded wait that also gives up when another role of this CTA has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, unsigned* err,
-                                              volatile int* abort) {
-    const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                report_error(err, FA512_DEVICE_ERR_TIMEOUT);
-                *abort = 1;
-                return false;
-            }
-        }
-    }
-}
 
 __device__ __forceinline__ bool key_visible(int j, int qpos, int seqlen_k, const PrefillParams& p) {
     return j < seqlen_k && (!p.causal || j <= qpos) && (p.window <= 0 || j > qpos - p.window);
@@ -544,6 +463,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 tc_fence_after_sync();
                 issue_pv(j);
             }
+            if (ok) commit2_both(&bars[Smem::O_FINAL]);
             // let every issued MMA finish before TMEM can be released
             commit2_local(&bars[Smem::DRAIN]);
             (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err);
@@ -685,12 +605,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 else mbar_arrive_remote(leader_bar(Smem::P_FULL + b));
             }
         }
-        // O is final once PV(n_kt - 1) has completed.  PV(n_kt - 2) may still
-        // be running here, and a parity wait can only tell the pending phase
-        // from the one before it, so wait for the two phases in turn.
-        if (ok && n_kt >= 2)
-            ok = wait_or_abort(&bars[Smem::O_DONE], static_cast<uint32_t>((n_kt - 2) & 1), p.err, abort);
-        if (ok) ok = wait_or_abort(&bars[Smem::O_DONE], static_cast<uint32_t>((n_kt - 1) & 1), p.err, abort);
+        // O is final once PV(n_kt - 1) has completed: a barrier of its own,
+        // committed once after the last PV, so no phase can be mistaken
+        if (ok) ok = wait_or_abort(&bars[Smem::O_FINAL], 0, p.err, abort);
         // Swap the halves' row sums through the Q area, idle once every MMA
         // has completed.  Each thread arrives exactly once, so the wait ends.
         float* lsum = reinterpret_cast<float*>(smem + Smem::q);

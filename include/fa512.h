@@ -17,6 +17,9 @@
  *    tile); pegainfer issue #1051, "Description" (one 8192-row chunk against
  *    everything before it, 32 query heads over 4 KV heads).
  *
+ *  fa512_prefill_d256 -- the same for heads of 256 dimensions (the
+ *    sliding-window local layers, window 1,024), from a persistent kernel.
+ *
  *  fa512_prefill_paged -- the same for a batch of chunks of different
  *    lengths over a paged KV cache (pegainfer issue #1051, "Proposed Plan").
  *
@@ -89,6 +92,26 @@ fa512_status fa512_prefill(const void *q, const void *k, const void *v, void *ou
                            int seqlen_q, int seqlen_k, int q_offset, int n_q_heads,
                            int n_kv_heads, float scale, int causal, int window,
                            fa512_stream_t stream);
+
+/*
+ * fa512_prefill_d256 -- the same forward for heads of 256 dimensions, the
+ * sliding-window local layers ("A custom attention kernel for Gemma 4 on the
+ * RTX PRO 6000", "The deployment": they attend to the last 1,024 tokens with
+ * heads of 256 dimensions).
+ *
+ *   q    [seqlen_q, n_q_heads, 256]  bf16, device, contiguous
+ *   k, v [seqlen_k, n_kv_heads, 256] bf16, device, contiguous
+ *   out  [seqlen_q, n_q_heads, 256]  bf16, device, written
+ *   lse  [n_q_heads, seqlen_q]       fp32, device, written; may be NULL
+ *
+ * Positions, visibility (causal, window), scale, requirements and errors are
+ * those of fa512_prefill; a window of 1024 is the local layers' setting and
+ * window <= 0 attends causally (or fully) to every key.
+ */
+fa512_status fa512_prefill_d256(const void *q, const void *k, const void *v, void *out, float *lse,
+                                int seqlen_q, int seqlen_k, int q_offset, int n_q_heads,
+                                int n_kv_heads, float scale, int causal, int window,
+                                fa512_stream_t stream);
 
 /*
  * fa512_prefill_paged -- attention forward of a batch of prefill chunks

@@ -156,3 +156,21 @@ def test_prefill_paged_rejects_bad_arguments_before_any_launch(lib):
     assert _prefill_paged(lib, batch=0, q=None) == 0
     assert _prefill_paged(lib, total_q=0, q=None) == 0
     assert _prefill_paged(lib, max_q=0, q=None) == 0
+
+
+def test_prefill_d256_rejects_bad_arguments_before_any_launch(lib):
+    def call(**kw):
+        a = dict(q=16, k=16, v=16, out=16, lse=None, sq=4, sk=4, off=0, hq=8, hk=2,
+                 scale=0.05, causal=1, window=1024)
+        a.update(kw)
+        return lib.fa512_prefill_d256(a["q"], a["k"], a["v"], a["out"], a["lse"], a["sq"],
+                                      a["sk"], a["off"], a["hq"], a["hk"], a["scale"],
+                                      a["causal"], a["window"], None)
+    assert call(hq=6, hk=4) == 1
+    assert call(sq=-1) == 1
+    assert call(off=-1) == 1
+    assert call(q=None) == 1
+    assert call(out=8) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(hq=256, hk=1) == 2
+    assert call(sq=0, q=None) == 0
