@@ -160,6 +160,41 @@ def paged_decode_inputs(batch: int, kv_lens, n_q_heads: int = 8, n_kv_heads: int
                              "n_q_heads": n_q_heads, "n_kv_heads": n_kv_heads})
 
 
+E4M3_NAN = 0x7F
+
+
+def to_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """x / scale rounded to the nearest FP8 E4M3 value (torch's float8_e4m3fn
+    cast), returned as the uint8 codes; |x / scale| must stay below 448."""
+    return (x.float() / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def paged_fp8_inputs(batch: int, kv_lens, n_q_heads: int = 8, n_kv_heads: int = 4,
+                     page_size: int = 64, seed: int = SEED_BASE + 9, spare_pages: int = 8,
+                     poison: bool = True, k_scale: float = 1 / 32, v_scale: float = 1 / 32):
+    """The paged layout of paged_decode_inputs with an FP8 E4M3 cache: K and V
+    are N(0,1) draws stored as e4m3(x / scale) with per-tensor scales (the
+    dequantised element is scale * e4m3).  With ``poison`` every slot outside
+    a live band holds the E4M3 NaN code.  Returns (PagedCache with uint8
+    k_pages / v_pages, k_scale, v_scale)."""
+    pc = paged_decode_inputs(batch, kv_lens, n_q_heads, n_kv_heads, page_size, seed,
+                             spare_pages, poison=False)
+    g = _gen(seed * 7 + 8)
+    shape = tuple(pc.k_pages.shape)
+    k8 = to_e4m3(torch.randn(shape, generator=g, dtype=torch.float32), k_scale)
+    v8 = to_e4m3(torch.randn(shape, generator=g, dtype=torch.float32), v_scale)
+    if poison:
+        live = torch.zeros(shape[:2], dtype=torch.bool)
+        for b in range(batch):
+            n = int(pc.kv_lens[b])
+            for lp in range((n + page_size - 1) // page_size):
+                live[int(pc.page_table[b, lp]), :min(page_size, n - lp * page_size)] = True
+        k8[~live] = E4M3_NAN
+        v8[~live] = E4M3_NAN
+    pc.k_pages, pc.v_pages = k8, v8
+    return pc, k_scale, v_scale
+
+
 def draft_queries(batch: int, q_len: int, n_q_heads: int, seed: int) -> torch.Tensor:
     """q_len query tokens per sequence (the last q_len positions of each
     cache, e.g. draft tokens being verified): [batch, q_len, n_q_heads, D] bf16."""

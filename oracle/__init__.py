@@ -15,7 +15,8 @@ for MQA in CUDA", section "The test that catches what parity misses" (an FP64
 host reference over the same bf16-rounded inputs) and section "One KV head
 breaks the textbook" (the live band of a decode query); vllm-project/
 flash-attention PR #199, review item F4 (an empty row has LSE = -inf);
-pegainfer issue #1051, "Proposed Plan" (a varlen prefill over the paged pool).
+pegainfer issue #1051, "Proposed Plan" (a varlen prefill over the paged pool);
+vllm-project/flash-attention PR #199, "Summary" (an FP8 paged KV cache).
 """
 from __future__ import annotations
 
@@ -64,6 +65,12 @@ def _load():
             lib.oracle_decode_paged_q.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, i, i,
                                                   ctypes.c_double, i, i]
             lib.oracle_decode_paged_q.restype = i
+            lib.oracle_decode_paged_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, i, i,
+                                                    ctypes.c_double, ctypes.c_double,
+                                                    ctypes.c_double, i, i]
+            lib.oracle_decode_paged_fp8.restype = i
+            lib.oracle_e4m3_table.argtypes = [P]
+            lib.oracle_e4m3_table.restype = None
             _lib = lib
     return _lib
 
@@ -247,4 +254,61 @@ def prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, seqused_k, *,
                            causal=causal, window=window, threads=threads)
         out[r0:r1] = o_b
         lse[:, r0:r1] = l_b
+    return out, lse
+
+
+def _u8(x) -> np.ndarray:
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous().view(torch.uint8).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.asarray(x)
+    if a.dtype != np.uint8:
+        raise TypeError("expected e4m3 bytes as uint8, got %s" % a.dtype)
+    return np.ascontiguousarray(a)
+
+
+def e4m3_table() -> np.ndarray:
+    """The 256 E4M3 codes decoded by the oracle (fp64; code 0x7F and 0xFF are NaN)."""
+    out = np.zeros(256, dtype=np.float64)
+    _load().oracle_e4m3_table(_ptr(out))
+    return out
+
+
+def decode_paged_fp8(q, k_pages, v_pages, page_table, kv_lens, *, k_scale: float = 1.0,
+                     v_scale: float = 1.0, scale: float | None = None, window: int = 0,
+                     threads: int | None = None):
+    """Reference decode over an FP8 E4M3 paged cache.
+
+    q [batch, n_q_heads, D] (one token) or [batch, q_len, n_q_heads, D] bf16;
+    k_pages/v_pages [num_pages, page_size, n_kv_heads, D] e4m3 bytes (uint8 or
+    torch.float8_e4m3fn); a key element is k_scale * e4m3(byte), a value
+    element v_scale * e4m3(byte).  Returns ``(out, lse)`` shaped like q
+    (lse without the head-dim axis), fp64.
+    """
+    qb, kb, vb = _bits(q), _u8(k_pages), _u8(v_pages)
+    pt, kl = _i32(page_table), _i32(kv_lens)
+    single = qb.ndim == 3
+    if single:
+        qb = qb[:, None]
+    bsz, qlen, hq, d = qb.shape
+    npages, psz, hk, d2 = kb.shape
+    if d2 != d or vb.shape != kb.shape or pt.ndim != 2 or pt.shape[0] != bsz:
+        raise ValueError("bad shapes")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    qb = np.ascontiguousarray(qb)
+    out = np.zeros((bsz, qlen, hq, d), dtype=np.float64)
+    lse = np.zeros((bsz, qlen, hq), dtype=np.float64)
+    rc = _load().oracle_decode_paged_fp8(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pt), _ptr(kl),
+                                         _ptr(out), _ptr(lse), bsz, qlen, hq, hk, d, psz,
+                                         pt.shape[1], npages, float(scale), float(k_scale),
+                                         float(v_scale), int(window),
+                                         threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_decode_paged_fp8 rejected its arguments")
+    if single:
+        return out[:, 0], lse[:, 0]
     return out, lse

@@ -96,6 +96,66 @@ static void attend_one(const uint16_t *q, const uint16_t *const *key_rows,
     }
 }
 
+/*
+ * One OCP FP8 E4M3 value (the "e4m3fn" encoding): 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; exponent field 0 holds the subnormals
+ * m/8 * 2^-6; there are no infinities and S.1111.111 is NaN, so the largest
+ * finite value is 1.75 * 2^8 = 448.
+ */
+static double e4m3_to_double(uint8_t x)
+{
+    const int sign = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * attend_one over an FP8 cache: key and value element d of a row are
+ * k_scale * e4m3(k[d]) and v_scale * e4m3(v[d]) (per-tensor scales), widened
+ * to double before use; everything else is attend_one, term for term.
+ */
+static void attend_one_fp8(const uint16_t *q, const uint8_t *const *key_rows,
+                           const uint8_t *const *val_rows, int n_keys, int head_dim,
+                           double scale, double k_scale, double v_scale, double *o,
+                           double *lse, double *s)
+{
+    int d, j;
+    if (n_keys == 0) {
+        for (d = 0; d < head_dim; ++d) o[d] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (j = 0; j < n_keys; ++j) {
+        double acc = 0.0;
+        for (d = 0; d < head_dim; ++d)
+            acc += bf16_to_double(q[d]) * (k_scale * e4m3_to_double(key_rows[j][d]));
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+    }
+    double sum = 0.0;
+    for (j = 0; j < n_keys; ++j) sum += exp(s[j] - m);
+    double l = m + log(sum);
+    *lse = l;
+    for (d = 0; d < head_dim; ++d) o[d] = 0.0;
+    for (j = 0; j < n_keys; ++j) {
+        double p = exp(s[j] - l);
+        const uint8_t *vr = val_rows[j];
+        for (d = 0; d < head_dim; ++d) o[d] += p * (v_scale * e4m3_to_double(vr[d]));
+    }
+}
+
+/* All 256 E4M3 codes decoded, for the tests that pin the decoding itself. */
+void oracle_e4m3_table(double *out)
+{
+    for (int i = 0; i < 256; ++i) out[i] = e4m3_to_double((uint8_t)i);
+}
+
 /* ------------------------------------------------------------------ prefill */
 
 typedef struct {
@@ -200,6 +260,9 @@ typedef struct {
     int n_threads, tid;
     int max_len;
     int q_len;
+    /* FP8 cache (kp, vp unused): e4m3 bytes and their per-tensor scales */
+    const uint8_t *kp8, *vp8;
+    double k_scale, v_scale;
 } decode_job;
 
 static void *decode_worker(void *arg)
@@ -209,6 +272,8 @@ static void *decode_worker(void *arg)
     const int G = J->n_q_heads / J->n_kv_heads;
     const uint16_t **krows = (const uint16_t **)malloc(sizeof(void *) * (size_t)(J->max_len + 1));
     const uint16_t **vrows = (const uint16_t **)malloc(sizeof(void *) * (size_t)(J->max_len + 1));
+    const uint8_t **krows8 = (const uint8_t **)malloc(sizeof(void *) * (size_t)(J->max_len + 1));
+    const uint8_t **vrows8 = (const uint8_t **)malloc(sizeof(void *) * (size_t)(J->max_len + 1));
     double *s = (double *)malloc(sizeof(double) * (size_t)(J->max_len + 1));
     long total = (long)J->batch * J->q_len * J->n_q_heads;
     for (long w = J->tid; w < total; w += J->n_threads) {
@@ -231,16 +296,26 @@ static void *decode_worker(void *arg)
             int page = J->page_table[(size_t)b * J->max_pages + j / J->page_size];
             int slot = (int)(j % J->page_size);
             size_t row = ((size_t)page * J->page_size + slot) * J->n_kv_heads + hk;
-            krows[n] = J->kp + row * D;
-            vrows[n] = J->vp + row * D;
+            if (J->kp8) {
+                krows8[n] = J->kp8 + row * D;
+                vrows8[n] = J->vp8 + row * D;
+            } else {
+                krows[n] = J->kp + row * D;
+                vrows[n] = J->vp + row * D;
+            }
         }
         const uint16_t *qr = J->q + ((size_t)bt * J->n_q_heads + h) * D;
         double *o = J->out + ((size_t)bt * J->n_q_heads + h) * D;
         double *l = J->lse + (size_t)bt * J->n_q_heads + h;
-        attend_one(qr, krows, vrows, n, D, J->scale, o, l, s);
+        if (J->kp8)
+            attend_one_fp8(qr, krows8, vrows8, n, D, J->scale, J->k_scale, J->v_scale, o, l, s);
+        else
+            attend_one(qr, krows, vrows, n, D, J->scale, o, l, s);
     }
     free(krows);
     free(vrows);
+    free(krows8);
+    free(vrows8);
     free(s);
     return NULL;
 }
@@ -281,11 +356,49 @@ int oracle_decode_paged(const uint16_t *q, const uint16_t *k_pages, const uint16
  * out [batch, q_len, n_q_heads, head_dim] fp64;  lse [batch, q_len, n_q_heads] fp64.
  * Other arguments as oracle_decode_paged; q_len = 1 is that function.
  */
+static int run_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                      const uint8_t *k_pages8, const uint8_t *v_pages8, double k_scale,
+                      double v_scale, const int *page_table, const int *kv_lens, double *out,
+                      double *lse, int batch, int q_len, int n_q_heads, int n_kv_heads,
+                      int head_dim, int page_size, int max_pages_per_seq, int num_pages,
+                      double scale, int window, int n_threads);
+
 int oracle_decode_paged_q(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                           const int *page_table, const int *kv_lens, double *out, double *lse,
                           int batch, int q_len, int n_q_heads, int n_kv_heads, int head_dim,
                           int page_size, int max_pages_per_seq, int num_pages, double scale,
                           int window, int n_threads)
+{
+    return run_decode(q, k_pages, v_pages, NULL, NULL, 1.0, 1.0, page_table, kv_lens, out, lse,
+                      batch, q_len, n_q_heads, n_kv_heads, head_dim, page_size,
+                      max_pages_per_seq, num_pages, scale, window, n_threads);
+}
+
+/*
+ * Decode of q_len query tokens per sequence over an FP8 E4M3 paged cache
+ * (vllm-project/flash-attention PR #199, "Summary": the paged KV cache in
+ * FP8).  k_pages / v_pages hold one e4m3 byte per element in the layout of
+ * oracle_decode_paged; a key element is k_scale * e4m3(byte), a value
+ * element v_scale * e4m3(byte).  Other arguments as oracle_decode_paged_q.
+ */
+int oracle_decode_paged_fp8(const uint16_t *q, const uint8_t *k_pages, const uint8_t *v_pages,
+                            const int *page_table, const int *kv_lens, double *out, double *lse,
+                            int batch, int q_len, int n_q_heads, int n_kv_heads, int head_dim,
+                            int page_size, int max_pages_per_seq, int num_pages, double scale,
+                            double k_scale, double v_scale, int window, int n_threads)
+{
+    if (!k_pages || !v_pages) return -1;
+    return run_decode(q, NULL, NULL, k_pages, v_pages, k_scale, v_scale, page_table, kv_lens,
+                      out, lse, batch, q_len, n_q_heads, n_kv_heads, head_dim, page_size,
+                      max_pages_per_seq, num_pages, scale, window, n_threads);
+}
+
+static int run_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                      const uint8_t *k_pages8, const uint8_t *v_pages8, double k_scale,
+                      double v_scale, const int *page_table, const int *kv_lens, double *out,
+                      double *lse, int batch, int q_len, int n_q_heads, int n_kv_heads,
+                      int head_dim, int page_size, int max_pages_per_seq, int num_pages,
+                      double scale, int window, int n_threads)
 {
     if (batch < 0 || q_len < 1 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
         page_size <= 0)
@@ -308,7 +421,8 @@ int oracle_decode_paged_q(const uint16_t *q, const uint16_t *k_pages, const uint
     for (int t = 0; t < n_threads; ++t) {
         decode_job J = {q, k_pages, v_pages, page_table, kv_lens, out, lse, batch,
                         n_q_heads, n_kv_heads, head_dim, page_size, max_pages_per_seq,
-                        scale, window, n_threads, t, max_len, q_len};
+                        scale, window, n_threads, t, max_len, q_len,
+                        k_pages8, v_pages8, k_scale, v_scale};
         jobs[t] = J;
         pthread_create(&th[t], NULL, decode_worker, &jobs[t]);
     }

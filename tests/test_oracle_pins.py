@@ -586,3 +586,94 @@ def test_d256_head_mapping_and_last_channel():
     for h in range(hq):
         np.testing.assert_allclose(out[:, h, :], np.broadcast_to(vr[0, h // (hq // hk)], (3, D256)),
                                    atol=1e-14)
+
+
+# ------------------------------------------------------------- FP8 E4M3 cache
+
+def test_e4m3_decoding_fixed_points_and_torch_agreement():
+    """The oracle's E4M3 decoding against the format's fixed points (the
+    largest finite value is 448: vllm-project/flash-attention PR #199, review
+    F1, "256 < 448") and against torch's float8_e4m3fn for all 256 codes."""
+    t = oracle.e4m3_table()
+    fixed = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0x7E: 448.0, 0x08: 2.0 ** -6,
+             0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0xFE: -448.0, 0xB8: -1.0}
+    for code, val in fixed.items():
+        assert t[code] == val, hex(code)
+    assert np.signbit(t[0x80]) and t[0x80] == 0.0
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    assert np.all(np.diff(t[:0x7F]) > 0)                        # monotone over the positive codes
+    np.testing.assert_array_equal(t[0x80:0xFF], -t[0x00:0x7F])   # sign bit
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(np.isnan(t), np.isnan(ref))
+    np.testing.assert_array_equal(t[~np.isnan(t)], ref[~np.isnan(ref)])
+
+
+def _fp8_to_bf16_cache(pages_u8, scale):
+    """The dequantised cache in bf16: scale * e4m3 is exact in bf16 when the
+    scale is a power of two."""
+    return (pages_u8.view(torch.float8_e4m3fn).float() * scale).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("scale_pow2", [1.0, 1 / 32])
+def test_fp8_decode_equals_bf16_decode_on_the_same_values(scale_pow2):
+    """With power-of-two scales every dequantised element is a bf16 value, so
+    the FP8 decode must equal the (pinned) bf16 decode bit for bit, including
+    the poisoned slots it must not read."""
+    lens = [1, 63, 64, 130, 300]
+    pc, _, _ = workloads.paged_fp8_inputs(len(lens), lens, 8, 4, 64, seed=61)
+    kb = _fp8_to_bf16_cache(pc.k_pages, scale_pow2)
+    vb = _fp8_to_bf16_cache(pc.v_pages, scale_pow2)
+    o8, l8 = oracle.decode_paged_fp8(pc.q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
+                                     k_scale=scale_pow2, v_scale=scale_pow2)
+    o16, l16 = oracle.decode_paged(pc.q, kb, vb, pc.page_table, pc.kv_lens)
+    np.testing.assert_array_equal(o8, o16)
+    np.testing.assert_array_equal(l8, l16)
+    # several query tokens and a window take the same path
+    q4 = workloads.draft_queries(len(lens), 3, 8, seed=61)
+    o8, l8 = oracle.decode_paged_fp8(q4, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
+                                     k_scale=scale_pow2, v_scale=scale_pow2, window=50)
+    o16, l16 = oracle.decode_paged_q(q4, kb, vb, pc.page_table, pc.kv_lens, window=50)
+    np.testing.assert_array_equal(o8, o16)
+    np.testing.assert_array_equal(l8, l16)
+
+
+def test_fp8_scale_laws():
+    """k_scale multiplies every logit (the same as scaling the softmax scale);
+    v_scale multiplies O and leaves LSE alone."""
+    pc, _, _ = workloads.paged_fp8_inputs(2, [100, 37], 4, 2, 64, seed=62)
+    base_o, base_l = oracle.decode_paged_fp8(pc.q, pc.k_pages, pc.v_pages, pc.page_table,
+                                             pc.kv_lens, k_scale=0.03, v_scale=0.05)
+    o, l = oracle.decode_paged_fp8(pc.q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
+                                   k_scale=1.0, v_scale=0.05, scale=D ** -0.5 * 0.03)
+    np.testing.assert_allclose(o, base_o, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l, base_l, rtol=1e-12, atol=1e-12)
+    o, l = oracle.decode_paged_fp8(pc.q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
+                                   k_scale=0.03, v_scale=0.15)
+    np.testing.assert_allclose(o, 3 * base_o, rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(l, base_l)
+
+
+def test_fp8_q0_v1_and_softmax_tail_closed_forms():
+    """PR #199 review: q = 0 and V = 1 give exactly 1 (here v_scale) at every
+    length; review F1: one late key ahead by 12 among n keys carries the
+    weight e^12 / (e^12 + n - 1)."""
+    n = 32768
+    pc, _, _ = workloads.paged_fp8_inputs(1, [n], 2, 1, 64, seed=63, spare_pages=1)
+    q = torch.zeros_like(pc.q)
+    ones = torch.full_like(pc.v_pages, 0x38)        # e4m3 1.0
+    o, _ = oracle.decode_paged_fp8(q, pc.k_pages, ones, pc.page_table, pc.kv_lens, v_scale=0.5)
+    np.testing.assert_allclose(o, 0.5, rtol=1e-12)
+    # the tail case: K = 0 except k[n-1][0] = 4 (code 0x48), q[0] = 3, scale 1
+    k = torch.zeros_like(pc.k_pages)
+    v = torch.zeros_like(pc.v_pages)
+    last = int(pc.page_table[0, (n - 1) // 64])
+    k[last, (n - 1) % 64, 0, 0] = 0x48
+    v[:, :, 0, 1] = 0x38
+    v[last, (n - 1) % 64, 0, 0] = 0x38
+    q = torch.zeros_like(pc.q)
+    q[0, :, 0] = 3.0
+    o, l = oracle.decode_paged_fp8(q, k, v, pc.page_table, pc.kv_lens, scale=1.0)
+    w = math.exp(12) / (math.exp(12) + n - 1)
+    np.testing.assert_allclose(o[0, :, 0], w, rtol=1e-12)
+    np.testing.assert_allclose(o[0, :, 1], 1.0, rtol=1e-12)
+    np.testing.assert_allclose(l[0], math.log(math.exp(12) + n - 1), rtol=1e-13)
