@@ -43,6 +43,8 @@ DECODE_Q_SHAPE = {"batch": 64, "kv_len": 16384, "q_len": 4}
 PAGE = 64
 # prefill over a paged cache: (chunk rows, cached positions incl. the chunk) per sequence.
 # "chunked": the headline chunk through shuffled 64-key pages; "varlen": a mixed batch.
+# FP8 E4M3 cache: per-tensor scales of the synthetic cache (N(0,1) / scale -> e4m3)
+FP8_SCALES = (1 / 32, 1 / 32)
 # the sliding-window local layers: heads of 256 dimensions over the last 1,024 tokens
 LOCAL256 = {"seqlen": 20480, "window": 1024, "n_q_heads": 32, "n_kv_heads": 4}
 PAGED_PREFILL = {
@@ -75,10 +77,12 @@ def prefill_flops(seqlen_q, seqlen_k, q_offset, n_q_heads, causal=True, window=0
     return 4 * head_dim * n_q_heads * visible_pairs(seqlen_q, seqlen_k, q_offset, causal, window)
 
 
-def decode_bytes(batch: int, kv_len: int, n_q_heads: int, n_kv_heads: int, q_len: int = 1) -> int:
-    """Algorithmic HBM bytes of one decode call: live K and V rows, q, out, lse,
-    page table and lengths (the split partials are not counted)."""
-    kv = batch * kv_len * n_kv_heads * HEAD_DIM * 2 * 2
+def decode_bytes(batch: int, kv_len: int, n_q_heads: int, n_kv_heads: int, q_len: int = 1,
+                 kv_elem_bytes: int = 2) -> int:
+    """Algorithmic HBM bytes of one decode call: live K and V rows (2 bytes an
+    element in bf16, 1 in FP8 E4M3), q, out, lse, page table and lengths (the
+    split partials are not counted)."""
+    kv = batch * kv_len * n_kv_heads * HEAD_DIM * kv_elem_bytes * 2
     qo = q_len * (batch * n_q_heads * HEAD_DIM * 2 * 2 + batch * n_q_heads * 4)
     pt = batch * ((kv_len + PAGE - 1) // PAGE) * 4 + batch * 4
     return kv + qo + pt
@@ -255,6 +259,66 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU arm
 
+def time_decode_fp8(args, fa, g, dev, stream, shapes, flush, world, peaks):
+    """The decode shapes (q_len 1, 8/4 heads, page 64, num_splits auto) over an
+    FP8 E4M3 cache: every step flushes L2, then calls each shape once."""
+    import torch
+
+    hq, hk = DECODE_HEADS
+    ks, vs = FP8_SCALES
+    gcpu = torch.Generator()
+    gcpu.manual_seed(0x5EED + 8)
+    legs = []
+    for b, n in shapes:
+        npg = (n + PAGE - 1) // PAGE
+        shape = (b * npg, PAGE, hk, HEAD_DIM)
+        kp = (torch.randn(shape, generator=g, device=dev) / ks).to(torch.float8_e4m3fn)
+        vp = (torch.randn(shape, generator=g, device=dev) / vs).to(torch.float8_e4m3fn)
+        pt = torch.randperm(b * npg, generator=gcpu).to(torch.int32).view(b, npg).to(dev)
+        legs.append(dict(b=b, n=n, kp=kp, vp=vp, pt=pt,
+                         kl=torch.full((b,), n, dtype=torch.int32, device=dev),
+                         q=torch.randn((b, hq, HEAD_DIM), generator=g, device=dev).to(torch.bfloat16),
+                         out=torch.empty((b, hq, HEAD_DIM), dtype=torch.bfloat16, device=dev),
+                         lse=torch.empty((b, hq), dtype=torch.float32, device=dev),
+                         ws=torch.empty(fa.fa512_decode_workspace_bytes(b, hq, hk, PAGE, n, 0),
+                                        dtype=torch.uint8, device=dev),
+                         bytes=decode_bytes(b, n, hq, hk, kv_elem_bytes=1)))
+
+    def call(d):
+        fa.fa512_decode_paged_fp8(d["q"], d["kp"], d["vp"], d["pt"], d["kl"], d["out"], d["lse"],
+                                  k_scale=ks, v_scale=vs, max_kv_len=d["n"], workspace=d["ws"],
+                                  stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        for d in legs:
+            call(d)
+    torch.cuda.synchronize()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in legs] for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.zero_()
+        for i, d in enumerate(legs):
+            evs[s][i][0].record(stream)
+            call(d)
+            evs[s][i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)) / args.steps
+          for i in range(len(legs))]
+    ms = max_over_ranks(ms, dev)
+    total_bytes = sum(d["bytes"] for d in legs)
+    gbs = job_rate(total_bytes, args.steps, world, sum(ms) * args.steps / 1e3) / 1e9
+    per = {"b%d_kv%d" % (d["b"], d["n"]): {"ms": m, "GB/s": d["bytes"] / m / 1e6}
+           for d, m in zip(legs, ms)}
+    return {"workload": "paged decode b{1,16,64} x kv{4096,16384,28672}, 8/4 heads, page 64, "
+                        "num_splits auto, FP8 E4M3 K/V cache (per-tensor scales 1/32)",
+            "value": gbs, "unit": "GB/s", "ms": sum(ms), "bytes_per_step": total_bytes,
+            "frac_of_measured_hbm": gbs / world / peaks["hbm_gbs"],
+            "kernel": "fa512::decode::stream::decode_stream_kernel<2, true> + merge",
+            "l2": "flushed before every step (each shape called once per step)",
+            "per_shape": per}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -390,7 +454,10 @@ def run_ours(args):
                            "achieved": dec_gbs / world, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": dec_gbs / world / peaks["hbm_gbs"],
                            "frac_of_8000": dec_gbs / world / 8000.0,
-                           "traffic": recorded_traffic("decode_split_kernel", dec_src),
+                           # DRAM bytes of the largest shape's split kernel (b64 x kv28672:
+                           # q_len 1 and two query heads per KV head run the streaming kernel)
+                           "traffic": recorded_traffic("decode_stream_kernel", dec_src),
+                           "traffic_shape": "b64_kv28672",
                            "src": dec_src, "per_shape": per}
 
     # ---- end to end through the public API with host buffers.  Every step
@@ -551,6 +618,12 @@ def run_ours(args):
         del lq, lk, lv, lout
         assert fa.fa512_device_status() == 0
 
+    # ---- the decode shapes over an FP8 E4M3 cache, timed on their own
+    decode_fp8 = None
+    if not args.no_decode and not args.no_fp8:
+        decode_fp8 = time_decode_fp8(args, fa, g, dev, stream, shapes, flush, world, peaks)
+        assert fa.fa512_device_status() == 0
+
     # ---- paged decode of q_len tokens per sequence, timed on its own
     decode_q = None
     if not args.no_decode and not args.decode_shapes:
@@ -616,6 +689,7 @@ def run_ours(args):
             "roofline": roofline,
             "decode_roofline": decode_roofline,
             "decode_q": decode_q,
+            "decode_fp8": decode_fp8,
             "prefill_paged": prefill_paged,
             "local256": local256,
             "cpu_baseline": cpu,
@@ -644,6 +718,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-paged", action="store_true", help="skip the paged-prefill legs")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-cache decode leg")
     ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling)")
     ap.add_argument("--decode-shapes", default="", help="comma list such as b64_kv28672")
     args = ap.parse_args()

@@ -68,6 +68,9 @@ def load_library():
         lib.fa512_decode_paged_q.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I,
                                              P, Z, P]
         lib.fa512_decode_paged_q.restype = I
+        lib.fa512_decode_paged_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, F,
+                                               F, I, I, P, Z, P]
+        lib.fa512_decode_paged_fp8.restype = I
         lib.fa512_decode_workspace_bytes_q.argtypes = [I, I, I, I, I, I, I]
         lib.fa512_decode_workspace_bytes_q.restype = Z
         lib.fa512_decode_auto_splits.argtypes = [I, I, I, I]
@@ -307,6 +310,62 @@ def fa512_decode_paged_q(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.
         _dptr(lse, "lse", torch.float32), bsz, qlen, hq, hk, psz, npages, mpps, int(max_kv_len),
         float(scale), int(window), int(num_splits), _dptr(workspace, "workspace"), ws_bytes,
         _stream(stream)))
+    return out, lse
+
+
+def _e4m3_bytes(t: torch.Tensor, name: str) -> int | None:
+    """Device pointer of an E4M3 cache given as uint8 codes or torch.float8_e4m3fn."""
+    if isinstance(t, torch.Tensor) and t.dtype == torch.float8_e4m3fn:
+        return _dptr(t, name)
+    return _dptr(t, name, torch.uint8)
+
+
+def fa512_decode_paged_fp8(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                           page_table: torch.Tensor, kv_lens: torch.Tensor,
+                           out: torch.Tensor | None = None, lse: torch.Tensor | None = None, *,
+                           k_scale: float = 1.0, v_scale: float = 1.0,
+                           max_kv_len: int | None = None, scale: float | None = None,
+                           window: int = 0, num_splits: int = 0,
+                           workspace: torch.Tensor | None = None, return_lse: bool = True,
+                           stream=None):
+    """Decode over a paged KV cache stored in FP8 E4M3; returns ``(out, lse)``.
+
+    q [batch, n_q_heads, 512] (one token) or [batch, q_len, n_q_heads, 512] bf16;
+    k_pages / v_pages [num_pages, page_size, n_kv_heads, 512] as uint8 codes or
+    torch.float8_e4m3fn; a key element is k_scale * e4m3, a value element
+    v_scale * e4m3.  out / lse are shaped like q (lse without the head dim).
+    Other arguments as :func:`fa512_decode_paged_q`.
+    """
+    single = q.dim() == 3
+    q4 = q.unsqueeze(1) if single else q
+    if q4.dim() != 4 or k_pages.dim() != 4 or k_pages.shape != v_pages.shape:
+        raise Fa512Error(1, "q must be [batch, (q_len,) heads, 512], pages [n, page, heads, 512]")
+    bsz, qlen, hq, d = q4.shape
+    npages, psz, hk, _ = k_pages.shape
+    if page_table.dim() != 2:
+        raise Fa512Error(1, "page_table must be [batch, max_pages_per_seq]")
+    mpps = page_table.shape[1]
+    if max_kv_len is None:
+        max_kv_len = mpps * psz
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = d ** -0.5
+    lib = load_library()
+    need = int(lib.fa512_decode_workspace_bytes_q(bsz, qlen, hq, hk, psz, int(max_kv_len),
+                                                  int(num_splits)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.fa512_decode_paged_fp8(
+        _dptr(q, "q", torch.bfloat16), _e4m3_bytes(k_pages, "k_pages"),
+        _e4m3_bytes(v_pages, "v_pages"), _dptr(page_table, "page_table", torch.int32),
+        _dptr(kv_lens, "kv_lens", torch.int32), _dptr(out, "out", torch.bfloat16),
+        _dptr(lse, "lse", torch.float32), bsz, qlen, hq, hk, psz, npages, mpps, int(max_kv_len),
+        float(scale), float(k_scale), float(v_scale), int(window), int(num_splits),
+        _dptr(workspace, "workspace"), ws_bytes, _stream(stream)))
     return out, lse
 
 

@@ -82,10 +82,11 @@ fa512_status get_encoder(EncodeTiledFn* fn) {
     return FA512_OK;
 }
 
-// bf16 tensor map with 128-byte swizzle; dims/strides innermost first,
-// strides in bytes for dims 1..rank-1.
-fa512_status encode_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                         const uint64_t* strides_bytes, const uint32_t* box) {
+// Tensor map; dims/strides innermost first, strides in bytes for dims
+// 1..rank-1.
+fa512_status encode_map(CUtensorMap* m, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle,
+                        const void* base, int rank, const uint64_t* dims,
+                        const uint64_t* strides_bytes, const uint32_t* box) {
     EncodeTiledFn enc;
     fa512_status st = get_encoder(&enc);
     if (st != FA512_OK) return st;
@@ -97,12 +98,19 @@ fa512_status encode_bf16(CUtensorMap* m, const void* base, int rank, const uint6
         es[i] = 1;
     }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+    CUresult r = enc(m, dtype, static_cast<cuuint32_t>(rank),
                      const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(FA512_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return FA512_OK;
+}
+
+// bf16 tensor map with 128-byte swizzle.
+fa512_status encode_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides_bytes, const uint32_t* box) {
+    return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, base, rank,
+                      dims, strides_bytes, box);
 }
 
 int sm_count() {
@@ -458,13 +466,18 @@ size_t fa512_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, in
                                           num_splits);
 }
 
-fa512_status fa512_decode_paged_q(const void* q, const void* k_pages, const void* v_pages,
-                                  const int32_t* page_table, const int32_t* kv_lens, void* out,
-                                  float* lse, int batch, int q_len, int n_q_heads, int n_kv_heads,
-                                  int page_size, int num_pages, int max_pages_per_seq,
-                                  int max_kv_len, float scale, int window, int num_splits,
-                                  void* workspace, size_t workspace_bytes,
-                                  fa512_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Body of the decode entry points.  fp8: k_pages / v_pages hold e4m3 bytes
+// and a key (value) element is k_scale (v_scale) times its e4m3 value.
+fa512_status decode_call(const void* q, const void* k_pages, const void* v_pages,
+                         const int32_t* page_table, const int32_t* kv_lens, void* out, float* lse,
+                         int batch, int q_len, int n_q_heads, int n_kv_heads, int page_size,
+                         int num_pages, int max_pages_per_seq, int max_kv_len, float scale,
+                         int window, int num_splits, void* workspace, size_t workspace_bytes,
+                         bool fp8, float k_scale, float v_scale, fa512_stream_t stream) {
     g_last_error[0] = 0;
     if (batch < 0) return fail(FA512_ERR_INVALID_ARG, "negative batch");
     if (q_len < 1) return fail(FA512_ERR_INVALID_ARG, "q_len must be >= 1");
@@ -485,6 +498,8 @@ fa512_status fa512_decode_paged_q(const void* q, const void* k_pages, const void
         return fail(FA512_ERR_INVALID_ARG, "max_kv_len outside [0, max_pages_per_seq * page_size]");
     if (num_splits < 0 || num_splits > 1024) return fail(FA512_ERR_INVALID_ARG, "num_splits outside [0, 1024]");
     if (!(scale == scale) || isinf(scale)) return fail(FA512_ERR_INVALID_ARG, "scale is not finite");
+    if (fp8 && (!(k_scale == k_scale) || isinf(k_scale) || !(v_scale == v_scale) || isinf(v_scale)))
+        return fail(FA512_ERR_INVALID_ARG, "k_scale and v_scale must be finite");
     if (batch == 0) return FA512_OK;
     if (!q || !k_pages || !v_pages || !page_table || !kv_lens || !out)
         return fail(FA512_ERR_INVALID_ARG, "null tensor pointer");
@@ -512,8 +527,15 @@ fa512_status fa512_decode_paged_q(const void* q, const void* k_pages, const void
     fa512::DecodeParams p;
     memset(&p, 0, sizeof p);
     p.q = static_cast<const __nv_bfloat16*>(q);
-    p.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
-    p.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
+    if (fp8) {
+        p.k8 = static_cast<const uint8_t*>(k_pages);
+        p.v8 = static_cast<const uint8_t*>(v_pages);
+        p.o_scale = v_scale;
+    } else {
+        p.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
+        p.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
+        p.o_scale = 1.f;
+    }
     p.page_table = page_table;
     p.kv_lens = kv_lens;
     const size_t rows = static_cast<size_t>(batch) * q_len * n_q_heads * splits;
@@ -537,20 +559,70 @@ fa512_status fa512_decode_paged_q(const void* q, const void* k_pages, const void
     p.tiles_per_split = static_cast<int>((tiles + splits - 1) / splits);
     if (p.tiles_per_split < 1) p.tiles_per_split = 1;
     p.scale_log2 = scale * 1.4426950408889634f;
+    // FP8: k_scale scales every score; applied after the bf16 path's factor
+    // so that a power-of-two k_scale changes no rounding
+    if (fp8) p.scale_log2 *= k_scale;
     p.err = err;
 
     CUtensorMap tmk, tmv;
     const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(n_kv_heads),
                               static_cast<uint64_t>(num_pages) * page_size};
-    const uint64_t strides[2] = {kHeadDim * 2ull, static_cast<uint64_t>(n_kv_heads) * kHeadDim * 2ull};
-    const uint32_t box[3] = {64u, 1u, static_cast<uint32_t>(p.box_rows)};
-    fa512_status st = encode_bf16(&tmk, k_pages, 3, dims, strides, box);
-    if (st != FA512_OK) return st;
-    st = encode_bf16(&tmv, v_pages, 3, dims, strides, box);
-    if (st != FA512_OK) return st;
-    e = fa512::launch_decode(tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
+    fa512_status st;
+    if (fp8) {
+        // e4m3 bytes: 256-byte boxes, no swizzle (the kernel converts them to
+        // the swizzled bf16 tile itself)
+        const uint64_t strides[2] = {static_cast<uint64_t>(kHeadDim),
+                                     static_cast<uint64_t>(n_kv_heads) * kHeadDim};
+        const uint32_t box[3] = {static_cast<uint32_t>(fa512::decode_fp8_box_bytes()), 1u,
+                                 static_cast<uint32_t>(p.box_rows)};
+        st = encode_map(&tmk, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE, k_pages, 3,
+                        dims, strides, box);
+        if (st != FA512_OK) return st;
+        st = encode_map(&tmv, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE, v_pages, 3,
+                        dims, strides, box);
+        if (st != FA512_OK) return st;
+        e = fa512::launch_decode_fp8(tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
+    } else {
+        const uint64_t strides[2] = {kHeadDim * 2ull, static_cast<uint64_t>(n_kv_heads) * kHeadDim * 2ull};
+        const uint32_t box[3] = {64u, 1u, static_cast<uint32_t>(p.box_rows)};
+        st = encode_bf16(&tmk, k_pages, 3, dims, strides, box);
+        if (st != FA512_OK) return st;
+        st = encode_bf16(&tmv, v_pages, 3, dims, strides, box);
+        if (st != FA512_OK) return st;
+        e = fa512::launch_decode(tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return FA512_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa512_status fa512_decode_paged_q(const void* q, const void* k_pages, const void* v_pages,
+                                  const int32_t* page_table, const int32_t* kv_lens, void* out,
+                                  float* lse, int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                  int page_size, int num_pages, int max_pages_per_seq,
+                                  int max_kv_len, float scale, int window, int num_splits,
+                                  void* workspace, size_t workspace_bytes,
+                                  fa512_stream_t stream) {
+    return decode_call(q, k_pages, v_pages, page_table, kv_lens, out, lse, batch, q_len, n_q_heads,
+                       n_kv_heads, page_size, num_pages, max_pages_per_seq, max_kv_len, scale,
+                       window, num_splits, workspace, workspace_bytes, false, 1.f, 1.f, stream);
+}
+
+fa512_status fa512_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages,
+                                    const int32_t* page_table, const int32_t* kv_lens, void* out,
+                                    float* lse, int batch, int q_len, int n_q_heads,
+                                    int n_kv_heads, int page_size, int num_pages,
+                                    int max_pages_per_seq, int max_kv_len, float scale,
+                                    float k_scale, float v_scale, int window, int num_splits,
+                                    void* workspace, size_t workspace_bytes,
+                                    fa512_stream_t stream) {
+    return decode_call(q, k_pages, v_pages, page_table, kv_lens, out, lse, batch, q_len, n_q_heads,
+                       n_kv_heads, page_size, num_pages, max_pages_per_seq, max_kv_len, scale,
+                       window, num_splits, workspace, workspace_bytes, true, k_scale, v_scale,
+                       stream);
 }
 
 fa512_status fa512_decode_paged(const void* q, const void* k_pages, const void* v_pages,

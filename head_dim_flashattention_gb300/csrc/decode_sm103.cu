@@ -42,10 +42,23 @@ constexpr int Q_BYTES = 16 * D * 2;              // 16 padded query rows
 constexpr int P_STRIDE = 80;                     // bytes per P row (64 + pad)
 constexpr int P_BYTES = 16 * P_STRIDE;
 
+// FP8 E4M3 cache: a stage holds the tile's K and V bytes (32 positions x
+// 512 bytes each) as two 256-byte boxes per row run, [half][position][256];
+// after the stage lands every thread converts its share into one bf16 tile
+// in the layout of a bf16 stage (e4m3 -> bf16 is exact), which the MMA code
+// then reads unchanged.
+constexpr int F8_BOX_BYTES = 256;                // head-dim bytes per FP8 box
+constexpr int F8_TILE_BYTES = TILE_K * D;        // 32 x 512 e4m3 = 16 KiB
+constexpr int F8_STAGE_BYTES = 2 * F8_TILE_BYTES;
+
+template <bool FP8>
 struct Smem {
     // Offsets inside the dynamic shared memory block (1024-byte aligned base).
     static constexpr int stages = 0;
-    static constexpr int q = NUM_STAGES * STAGE_BYTES;
+    static constexpr int stage_bytes = FP8 ? F8_STAGE_BYTES : STAGE_BYTES;
+    // FP8: the converted bf16 tile (K then V); bf16: each stage is read in place
+    static constexpr int tile = NUM_STAGES * stage_bytes;
+    static constexpr int q = tile + (FP8 ? STAGE_BYTES : 0);
     static constexpr int p = q + Q_BYTES;
     static constexpr int xs = p + P_BYTES;                    // 4 warps x 32 lanes x float4
     static constexpr int redm = xs + 4 * 32 * 16;            // [4][16] float
@@ -89,29 +102,86 @@ __device__ __forceinline__ TilePlan plan_tile(const DecodeParams& p, int b, int 
     return plan;
 }
 
+template <bool FP8>
 __device__ __forceinline__ void issue_tile(const DecodeParams& p, const CUtensorMap* tmk,
                                            const CUtensorMap* tmv, uint8_t* stage,
                                            uint64_t* bar, int b, int kvh, int t, int lo, int hi) {
     const TilePlan plan = plan_tile(p, b, t, lo, hi, true);
     const int box_rows = p.box_rows;
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(plan.runs) * 8u * box_rows * 128u * 2u);
+    // K and V rows of every loaded run: 512 elements each
+    const uint32_t row_bytes = FP8 ? static_cast<uint32_t>(D) : static_cast<uint32_t>(D) * 2u;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(plan.runs) * box_rows * row_bytes * 2u);
     for (int r0 = 0; r0 < TILE_K; r0 += box_rows) {
         if (!((plan.loaded >> r0) & 1u)) continue;
         const int pos0 = t * TILE_K + r0;
         const int lp = pos0 / p.page_size;
         const int page = p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
         const int row = page * p.page_size + (pos0 - lp * p.page_size);
-        for (int c = 0; c < 8; ++c) {
-            tma_load_3d(stage + c * CHUNK_BYTES + r0 * 128, tmk, bar, c * 64, kvh, row);
-            tma_load_3d(stage + TILE_BYTES + c * CHUNK_BYTES + r0 * 128, tmv, bar, c * 64, kvh,
-                        row);
+        if constexpr (FP8) {
+            for (int c = 0; c < D / F8_BOX_BYTES; ++c) {
+                const int off = c * (TILE_K * F8_BOX_BYTES) + r0 * F8_BOX_BYTES;
+                tma_load_3d(stage + off, tmk, bar, c * F8_BOX_BYTES, kvh, row);
+                tma_load_3d(stage + F8_TILE_BYTES + off, tmv, bar, c * F8_BOX_BYTES, kvh, row);
+            }
+        } else {
+            for (int c = 0; c < 8; ++c) {
+                tma_load_3d(stage + c * CHUNK_BYTES + r0 * 128, tmk, bar, c * 64, kvh, row);
+                tma_load_3d(stage + TILE_BYTES + c * CHUNK_BYTES + r0 * 128, tmv, bar, c * 64, kvh,
+                            row);
+            }
         }
     }
 }
 
+// Two e4m3 values (low byte first) -> two bf16 (low half first), exactly:
+// the hardware e4m3x2 -> f16x2 conversion, widened through fp32.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two_bytes)));
+    float lo, hi;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(static_cast<unsigned short>(h2 & 0xffffu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(static_cast<unsigned short>(h2 >> 16)));
+    return pack_bf16x2(lo, hi);
+}
+
+// FP8 stage -> bf16 tile in the bf16 stage layout (column group of 64
+// elements at CHUNK_BYTES steps, 128-byte rows under the 128-byte swizzle).
+// V rows of positions outside `valid` are written as zeros, so P = 0 never
+// meets stale or poisoned values; K rows there are masked in the scores.
+// Each thread converts 8-element units: a warp covers 256 contiguous bytes
+// of one row (conflict-free reads) and writes all eight 16-byte chunks of
+// four 128-byte lines (conflict-free writes).
+__device__ __forceinline__ void convert_fp8_stage(const uint8_t* stage, uint8_t* tile,
+                                                  uint32_t valid, int tid) {
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+        const uint8_t* src = stage + kv * F8_TILE_BYTES;
+        uint8_t* dst = tile + kv * TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < (TILE_K * D / 8) / NUM_THREADS; ++k) {
+            const int u = k * NUM_THREADS + tid;     // unit: 8 elements
+            const int r = u >> 6;                    // 64 units per position
+            const int e0 = (u & 63) * 8;             // first element of the unit
+            uint4 out = make_uint4(0u, 0u, 0u, 0u);
+            if (kv == 0 || ((valid >> r) & 1u)) {
+                const uint2 w = *reinterpret_cast<const uint2*>(
+                    src + (e0 / F8_BOX_BYTES) * (TILE_K * F8_BOX_BYTES) + r * F8_BOX_BYTES +
+                    (e0 % F8_BOX_BYTES));
+                out.x = e4m3x2_to_bf16x2(w.x & 0xffffu);
+                out.y = e4m3x2_to_bf16x2(w.x >> 16);
+                out.z = e4m3x2_to_bf16x2(w.y & 0xffffu);
+                out.w = e4m3x2_to_bf16x2(w.y >> 16);
+            }
+            *reinterpret_cast<uint4*>(dst + (e0 >> 6) * CHUNK_BYTES + swz(r, (e0 & 63) >> 3)) = out;
+        }
+    }
+}
+
+template <bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+    using Smem = decode::Smem<FP8>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -171,8 +241,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
     // prologue loads
     if (tid == 0) {
         for (int s = 0; s < NUM_STAGES - 1 && s < n_tiles; ++s)
-            issue_tile(p, &tmk, &tmv, smem + s * STAGE_BYTES, &full_bar[s], b, kvh, t_begin + s,
-                       lo, hi);
+            issue_tile<FP8>(p, &tmk, &tmv, smem + s * Smem::stage_bytes, &full_bar[s], b, kvh,
+                            t_begin + s, lo, hi);
     }
 
     // ---- Q fragments (A operand) for this warp's half of the head dim
@@ -206,12 +276,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
     for (int it = 0; it < n_tiles; ++it) {
         const int t = t_begin + it;
         const int st = it % NUM_STAGES;
-        uint8_t* stage = smem + st * STAGE_BYTES;
+        // the bf16 K/V tile the MMAs read: the stage itself, or the FP8
+        // stage's converted copy
+        uint8_t* stage = FP8 ? smem + Smem::tile : smem + st * Smem::stage_bytes;
         // refill the stage consumed in the previous iteration
         if (tid == 0 && it + NUM_STAGES - 1 < n_tiles) {
             const int nst = (it + NUM_STAGES - 1) % NUM_STAGES;
-            issue_tile(p, &tmk, &tmv, smem + nst * STAGE_BYTES, &full_bar[nst], b, kvh,
-                       t + NUM_STAGES - 1, lo, hi);
+            issue_tile<FP8>(p, &tmk, &tmv, smem + nst * Smem::stage_bytes, &full_bar[nst], b,
+                            kvh, t + NUM_STAGES - 1, lo, hi);
         }
         const TilePlan plan = plan_tile(p, b, t, lo, hi, false);
         // live positions of this tile: loaded and inside [lo, hi)
@@ -227,6 +299,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
         if (!mbar_wait(&full_bar[st], static_cast<uint32_t>((it / NUM_STAGES) & 1), p.err)) {
             ok = false;
         }
+        // FP8: the previous tile's MMAs are past the barrier that ended the
+        // last iteration, so the bf16 tile can be rewritten (after a failed
+        // wait the converted bytes are never used)
+        if constexpr (FP8) convert_fp8_stage(smem + st * Smem::stage_bytes, stage, valid, tid);
         if (__syncthreads_or(!ok)) {
             ok = false;
             failed_it = it;
@@ -234,7 +310,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
         }
 
         // zero V rows that hold no live position (stale or poisoned data)
-        if (valid != 0xffffffffu) {
+        if (!FP8 && valid != 0xffffffffu) {
             uint8_t* vt = stage + TILE_BYTES;
             for (int i = tid; i < TILE_K * 64; i += NUM_THREADS) {
                 const int r = i & 31, cc = i >> 5;   // cc: 0..63 16-byte chunks of the row
@@ -381,12 +457,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
         if (row0 < R) {
             const size_t h = (static_cast<size_t>(b) * p.q_len + row0 / G) * p.n_q_heads + kvh * G + row0 % G;
             *reinterpret_cast<float2*>(p.ws_o + (h * S + split) * D + d) =
-                make_float2(ok ? o[j][0] : 0.f, ok ? o[j][1] : 0.f);
+                FP8 ? make_float2(ok ? o[j][0] * p.o_scale : 0.f, ok ? o[j][1] * p.o_scale : 0.f)
+                    : make_float2(ok ? o[j][0] : 0.f, ok ? o[j][1] : 0.f);
         }
         if (row1 < R) {
             const size_t h = (static_cast<size_t>(b) * p.q_len + row1 / G) * p.n_q_heads + kvh * G + row1 % G;
             *reinterpret_cast<float2*>(p.ws_o + (h * S + split) * D + d) =
-                make_float2(ok ? o[j][2] : 0.f, ok ? o[j][3] : 0.f);
+                FP8 ? make_float2(ok ? o[j][2] * p.o_scale : 0.f, ok ? o[j][3] * p.o_scale : 0.f)
+                    : make_float2(ok ? o[j][2] : 0.f, ok ? o[j][3] : 0.f);
         }
     }
     // every thread holds the running max of rows lane/4 and lane/4 + 8;
@@ -420,10 +498,20 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
 // warps' (m, l, O) are merged once at the end into the split's partial.
 namespace stream {
 
-constexpr int POS = 4;                   // positions per chunk
 constexpr int STAGES = 3;                // chunks in flight per warp
 constexpr int WARPS = 8;
-constexpr int CHUNK_BYTES = 2 * POS * D * 2;          // K and V rows: 8 KiB
+// A chunk is 8 KiB of K and V rows: 4 positions of a bf16 cache, 8 of an
+// FP8 E4M3 cache.  A lane owns 16 head-dim columns of every row: 32 bytes of
+// a bf16 row, 16 bytes of an FP8 row.
+template <bool FP8>
+struct Cfg {
+    static constexpr int POS = FP8 ? 8 : 4;              // positions per chunk
+    static constexpr int ROW_BYTES = FP8 ? D : D * 2;
+    static constexpr int LANE_BYTES = ROW_BYTES / 32;
+};
+constexpr int CHUNK_BYTES = 8192;
+static_assert(2 * Cfg<false>::POS * Cfg<false>::ROW_BYTES == CHUNK_BYTES, "chunk size");
+static_assert(2 * Cfg<true>::POS * Cfg<true>::ROW_BYTES == CHUNK_BYTES, "chunk size");
 constexpr int RING_BYTES = WARPS * STAGES * CHUNK_BYTES;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -445,9 +533,131 @@ __device__ __forceinline__ void unpack8(const uint4 a, const uint4 b, float (&f)
     }
 }
 
+// 16 e4m3 values -> fp32 times 2^-120, exactly, with integer operations
+// only (the conversion units would bound the kernel below the HBM rate).
+// An E4M3 byte s.eeee.mmm placed as fp32 bits s at 31 and eeee.mmm at 26..20
+// is the fp32 number 2^(e-127) (1 + m/8) for e >= 1 and the subnormal
+// (m/8) 2^-126 for e = 0 (zero included), i.e. the E4M3 value (bias 7,
+// subnormals (m/8) 2^-6) times 2^-120.  An arithmetic right shift by 4 of
+// the byte placed at bits 31..24 puts it there; the mask clears the copies
+// of the sign.  (The E4M3 NaN code would read as 480: codes are read only
+// inside the live band, where a cache holds finite values.)
+__device__ __forceinline__ void unpack16_e4m3_scaled(const uint4 a, float (&f)[16]) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    constexpr uint32_t M = 0x87f00000u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[4 * i + 0] = __uint_as_float(static_cast<uint32_t>(static_cast<int32_t>(w[i] << 24) >> 4) & M);
+        f[4 * i + 1] = __uint_as_float(static_cast<uint32_t>(static_cast<int32_t>(w[i] << 16) >> 4) & M);
+        f[4 * i + 2] = __uint_as_float(static_cast<uint32_t>(static_cast<int32_t>(w[i] << 8) >> 4) & M);
+        f[4 * i + 3] = __uint_as_float(static_cast<uint32_t>(static_cast<int32_t>(w[i]) >> 4) & M);
+    }
+}
+
+// One chunk of FP8 positions for the G query rows of this lane's warp.
+//
+// Scores: each lane forms its 16-column partial q.k' (k' = k 2^-120) with
+// f32x2 FMAs; the POS x G partials are summed over the 32 lanes by a
+// transposing butterfly (each step halves the values a lane carries), so
+// that lanes 32/NV apart ... end up holding one total each: value j = i G + g
+// sits in lanes with (lane / (32 / NV)) == j.  The chunk max and sum per row
+// are then reduced over those lanes, each lane evaluates one exp2, and the
+// probabilities are broadcast back for O += p v' (p pre-multiplied by 2^120,
+// so the product is p v in the normal range).
 template <int G>
+__device__ __forceinline__ void fp8_chunk(const uint8_t* st, int lane, int pos0, int pe,
+                                          float sl_hi, const float2 (&qq)[16], float (&m)[G],
+                                          float (&l)[G], float2 (&o)[G][8]) {
+    constexpr int POS = Cfg<true>::POS;
+    constexpr int ROW = Cfg<true>::ROW_BYTES;
+    constexpr int NV = POS * G;                    // 8 or 16 partial scores
+    constexpr int LPV = 32 / NV;                   // lanes that end up holding one value
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < POS; ++i) {
+        float kf[16];
+        unpack16_e4m3_scaled(*reinterpret_cast<const uint4*>(st + i * ROW + lane * 16), kf);
+        if constexpr (G == 2) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int d = 0; d < 16; ++d) acc = ffma2(qq[d], make_float2(kf[d], kf[d]), acc);
+            v[i * 2] = acc.x;
+            v[i * 2 + 1] = acc.y;
+        } else {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int d = 0; d < 8; ++d) acc = ffma2(qq[d], make_float2(kf[2 * d], kf[2 * d + 1]), acc);
+            v[i] = acc.x + acc.y;
+        }
+    }
+    // transposing butterfly: after the step at offset `off` a lane keeps the
+    // upper half of its values when (lane & off) != 0, the lower half otherwise
+#pragma unroll
+    for (int off = 16, cnt = NV; cnt > 1; off >>= 1, cnt >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int t = 0; t < cnt / 2; ++t) {
+            const float send = up ? v[t] : v[t + cnt / 2];
+            const float keep = up ? v[t + cnt / 2] : v[t];
+            v[t] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+#pragma unroll
+    for (int off = LPV / 2; off >= 1; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+
+    const int j = lane / LPV;                      // the value this lane holds
+    const int i = j / G, g = j - i * G;
+    // score in log2 units: v 2^120 scale log2(e), in two steps that cannot overflow
+    const float s = (pos0 + i < pe) ? (v[0] * 0x1p64f) * sl_hi : -INFINITY;
+    // chunk max of row g: over the lanes holding values j' = i' G + g
+    float cm = s;
+#pragma unroll
+    for (int off = LPV * G; off < 32; off <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    float mg[G], ag[G];
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+        // every lane learns both rows' chunk maxima (lane gg * LPV holds row gg's)
+        const float c = __shfl_sync(0xffffffffu, cm, gg * LPV);
+        const float mn = fmaxf(m[gg], c);
+        mg[gg] = mn == -INFINITY ? 0.f : mn;      // a row with no key yet shifts by 0
+        ag[gg] = fast_exp2(m[gg] - mg[gg]);
+        m[gg] = mn;
+    }
+    const float pj = fast_exp2(s - (G == 2 && g == 1 ? mg[G - 1] : mg[0]));
+    float ps = pj;
+#pragma unroll
+    for (int off = LPV * G; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+        l[gg] = l[gg] * ag[gg] + __shfl_sync(0xffffffffu, ps, gg * LPV);
+        if (ag[gg] != 1.f) {                       // the same in every lane
+#pragma unroll
+            for (int d = 0; d < 8; ++d) o[gg][d] = ffma2(o[gg][d], make_float2(ag[gg], ag[gg]),
+                                                         make_float2(0.f, 0.f));
+        }
+    }
+    const float pjs = pj * 0x1p120f;
+#pragma unroll
+    for (int ii = 0; ii < POS; ++ii) {
+        float vf[16];
+        unpack16_e4m3_scaled(*reinterpret_cast<const uint4*>(st + (POS + ii) * ROW + lane * 16), vf);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            const float pv = __shfl_sync(0xffffffffu, pjs, (ii * G + gg) * LPV);
+            const float2 pp = make_float2(pv, pv);
+#pragma unroll
+            for (int d = 0; d < 8; ++d)
+                o[gg][d] = ffma2(pp, make_float2(vf[2 * d], vf[2 * d + 1]), o[gg][d]);
+        }
+    }
+}
+
+template <int G, bool FP8>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 decode_stream_kernel(const DecodeParams p) {
+    constexpr int POS = Cfg<FP8>::POS;
+    constexpr int ROW = Cfg<FP8>::ROW_BYTES;
+    constexpr int LB = Cfg<FP8>::LANE_BYTES;
     extern __shared__ __align__(16) uint8_t smem[];
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -481,6 +691,21 @@ decode_stream_kernel(const DecodeParams p) {
 #pragma unroll
         for (int d = 0; d < 16; ++d) o[g][d] = 0.f;
     }
+    // FP8: q as f32x2 operands (G = 2: the two rows' column d; G = 1: columns
+    // 2e, 2e + 1), O as column pairs, and the score scale times 2^56 (the
+    // decoded keys carry 2^-120: 2^64 is applied to the dot product first)
+    float2 qq[16], o2[G][8];
+    const float sl_hi = p.scale_log2 * 0x1p56f;
+    if constexpr (FP8) {
+#pragma unroll
+        for (int d = 0; d < 16; ++d)
+            qq[d] = G == 2 ? make_float2(q[0][d], q[G - 1][d])
+                           : make_float2(q[0][(2 * d) & 15], q[0][(2 * d + 1) & 15]);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int d = 0; d < 8; ++d) o2[g][d] = make_float2(0.f, 0.f);
+    }
 
     const uint32_t ring = smem_u32(smem) + warp * STAGES * CHUNK_BYTES;
     // chunk k of this warp covers positions pb + (warp + 8k) * POS ...
@@ -503,14 +728,19 @@ decode_stream_kernel(const DecodeParams p) {
                         row = (static_cast<size_t>(page) * p.page_size + (pos & (p.page_size - 1))) * p.n_kv_heads + kvh;
                     }
                 }
-                const __nv_bfloat16* ks = p.k_pages + row * D + lane * 16;
-                const __nv_bfloat16* vs = p.v_pages + row * D + lane * 16;
-                const uint32_t kd = st + i * (D * 2) + lane * 32;
-                const uint32_t vd = st + (POS + i) * (D * 2) + lane * 32;
-                cp_async16(kd, ks, valid);
-                cp_async16(kd + 16, ks + 8, valid);
-                cp_async16(vd, vs, valid);
-                cp_async16(vd + 16, vs + 8, valid);
+                const uint32_t kd = st + i * ROW + lane * LB;
+                const uint32_t vd = st + (POS + i) * ROW + lane * LB;
+                if constexpr (FP8) {
+                    cp_async16(kd, p.k8 + row * D + lane * 16, valid);
+                    cp_async16(vd, p.v8 + row * D + lane * 16, valid);
+                } else {
+                    const __nv_bfloat16* ks = p.k_pages + row * D + lane * 16;
+                    const __nv_bfloat16* vs = p.v_pages + row * D + lane * 16;
+                    cp_async16(kd, ks, valid);
+                    cp_async16(kd + 16, ks + 8, valid);
+                    cp_async16(vd, vs, valid);
+                    cp_async16(vd + 16, vs + 8, valid);
+                }
             }
         }
         cp_async_commit();   // one group per chunk slot, empty past the end
@@ -523,62 +753,75 @@ decode_stream_kernel(const DecodeParams p) {
         cp_async_wait<STAGES - 1>();   // this lane's copies of chunk k have landed
         const uint8_t* st = smem + (warp * STAGES + (k % STAGES)) * CHUNK_BYTES;
         const int pos0 = pb + (warp + WARPS * k) * POS;
-        float s[POS][G];
-#pragma unroll
-        for (int i = 0; i < POS; ++i) {
-            float kf[16];
-            const uint4* kr = reinterpret_cast<const uint4*>(st + i * (D * 2) + lane * 32);
-            unpack8(kr[0], kr[1], kf);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float acc = 0.f;
-#pragma unroll
-                for (int d = 0; d < 16; ++d) acc = fmaf(q[g][d], kf[d], acc);
-                s[i][g] = acc;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < POS; ++i)
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float v = s[i][g];
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                s[i][g] = (pos0 + i < pe) ? v * p.scale_log2 : -INFINITY;
-            }
-        float pr[POS][G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float cm = s[0][g];
-#pragma unroll
-            for (int i = 1; i < POS; ++i) cm = fmaxf(cm, s[i][g]);
-            const float mn = fmaxf(m[g], cm);
-            const float sh = mn == -INFINITY ? 0.f : mn;   // no key seen yet
-            const float a = fast_exp2(m[g] - sh);
-            float ps = 0.f;
-#pragma unroll
+        if constexpr (FP8) {
+            fp8_chunk<G>(st, lane, pos0, pe, sl_hi, qq, m, l, o2);
+        } else {
+            float s[POS][G];
+    #pragma unroll
             for (int i = 0; i < POS; ++i) {
-                pr[i][g] = fast_exp2(s[i][g] - sh);
-                ps += pr[i][g];
+                float kf[16];
+                const uint4* kr = reinterpret_cast<const uint4*>(st + i * ROW + lane * LB);
+                unpack8(kr[0], kr[1], kf);
+    #pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float acc = 0.f;
+    #pragma unroll
+                    for (int d = 0; d < 16; ++d) acc = fmaf(q[g][d], kf[d], acc);
+                    s[i][g] = acc;
+                }
             }
-            l[g] = l[g] * a + ps;
-            m[g] = mn;
-#pragma unroll
-            for (int d = 0; d < 16; ++d) o[g][d] *= a;
-        }
-#pragma unroll
-        for (int i = 0; i < POS; ++i) {
-            float vf[16];
-            const uint4* vr = reinterpret_cast<const uint4*>(st + (POS + i) * (D * 2) + lane * 32);
-            unpack8(vr[0], vr[1], vf);
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int d = 0; d < 16; ++d) o[g][d] = fmaf(pr[i][g], vf[d], o[g][d]);
+    #pragma unroll
+            for (int i = 0; i < POS; ++i)
+    #pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float v = s[i][g];
+    #pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                    s[i][g] = (pos0 + i < pe) ? v * p.scale_log2 : -INFINITY;
+                }
+            float pr[POS][G];
+    #pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float cm = s[0][g];
+    #pragma unroll
+                for (int i = 1; i < POS; ++i) cm = fmaxf(cm, s[i][g]);
+                const float mn = fmaxf(m[g], cm);
+                const float sh = mn == -INFINITY ? 0.f : mn;   // no key seen yet
+                const float a = fast_exp2(m[g] - sh);
+                float ps = 0.f;
+    #pragma unroll
+                for (int i = 0; i < POS; ++i) {
+                    pr[i][g] = fast_exp2(s[i][g] - sh);
+                    ps += pr[i][g];
+                }
+                l[g] = l[g] * a + ps;
+                m[g] = mn;
+    #pragma unroll
+                for (int d = 0; d < 16; ++d) o[g][d] *= a;
+            }
+    #pragma unroll
+            for (int i = 0; i < POS; ++i) {
+                float vf[16];
+                const uint4* vr = reinterpret_cast<const uint4*>(st + (POS + i) * ROW + lane * LB);
+                unpack8(vr[0], vr[1], vf);
+    #pragma unroll
+                for (int g = 0; g < G; ++g)
+    #pragma unroll
+                    for (int d = 0; d < 16; ++d) o[g][d] = fmaf(pr[i][g], vf[d], o[g][d]);
+            }
         }
     }
     cp_async_wait<0>();
     __syncthreads();   // every warp is done with its ring: reuse it for the merge
+    if constexpr (FP8) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int d = 0; d < 8; ++d) {
+                o[g][2 * d] = o2[g][d].x;
+                o[g][2 * d + 1] = o2[g][d].y;
+            }
+    }
 
     float* so = reinterpret_cast<float*>(smem);                 // [WARPS][G][512]
     float* sml = so + WARPS * G * D;                             // [WARPS][G][2]
@@ -610,7 +853,7 @@ decode_stream_kernel(const DecodeParams p) {
             }
         }
         const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + g;
-        p.ws_o[(h * S + split) * D + d] = acc;
+        p.ws_o[(h * S + split) * D + d] = FP8 ? acc * p.o_scale : acc;
         if (d == 0) {
             p.ws_ml[(h * S + split) * 2 + 0] = M;
             p.ws_ml[(h * S + split) * 2 + 1] = M == -INFINITY ? 0.f : L;
@@ -660,43 +903,56 @@ decode_merge_kernel(const DecodeParams p) {
 
 }  // namespace decode
 
-int decode_smem_bytes() { return decode::Smem::total + 1024; }
+int decode_smem_bytes() { return decode::Smem<false>::total + 1024; }
+
+int decode_fp8_box_bytes() { return decode::F8_BOX_BYTES; }
 
 int decode_tile_positions() { return decode::TILE_K; }
 
-template <int G>
+template <int G, bool FP8>
 static cudaError_t launch_stream(const DecodeParams& p, cudaStream_t stream) {
     const int smem = decode::stream::RING_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(decode::stream::decode_stream_kernel<G>,
+    cudaError_t e = cudaFuncSetAttribute(decode::stream::decode_stream_kernel<G, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.num_splits, p.n_kv_heads, p.batch);
-    decode::stream::decode_stream_kernel<G><<<grid, decode::stream::WARPS * 32, smem, stream>>>(p);
+    decode::stream::decode_stream_kernel<G, FP8><<<grid, decode::stream::WARPS * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
-                          cudaStream_t stream) {
+template <bool FP8>
+static cudaError_t launch_split_and_merge(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                          const DecodeParams& p, cudaStream_t stream) {
     cudaError_t e;
     if (p.q_len == 1 && p.group == 1) {
-        e = launch_stream<1>(p, stream);
+        e = launch_stream<1, FP8>(p, stream);
     } else if (p.q_len == 1 && p.group == 2) {
-        e = launch_stream<2>(p, stream);
+        e = launch_stream<2, FP8>(p, stream);
     } else {
         // larger query groups or several tokens: S and PV on the tensor cores
         // (q_len * G rows padded to 16)
-        const int smem = decode_smem_bytes();
-        e = cudaFuncSetAttribute(decode::decode_split_kernel,
+        const int smem = decode::Smem<FP8>::total + 1024;
+        e = cudaFuncSetAttribute(decode::decode_split_kernel<FP8>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         dim3 grid(p.num_splits, p.n_kv_heads, p.batch);
-        decode::decode_split_kernel<<<grid, decode::NUM_THREADS, smem, stream>>>(tmk, tmv, p);
+        decode::decode_split_kernel<FP8><<<grid, decode::NUM_THREADS, smem, stream>>>(tmk, tmv, p);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
     dim3 mgrid(p.n_q_heads, p.batch * p.q_len);
     decode::decode_merge_kernel<<<mgrid, 128, 0, stream>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                          cudaStream_t stream) {
+    return launch_split_and_merge<false>(tmk, tmv, p, stream);
+}
+
+cudaError_t launch_decode_fp8(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const DecodeParams& p, cudaStream_t stream) {
+    return launch_split_and_merge<true>(tmk, tmv, p, stream);
 }
 
 }  // namespace fa512

@@ -13,6 +13,12 @@ struct DecodeParams {
     const __nv_bfloat16* q;        // [batch, q_len, n_q_heads, 512]
     const __nv_bfloat16* k_pages;  // [num_pages, page_size, n_kv_heads, 512]
     const __nv_bfloat16* v_pages;
+    // FP8 E4M3 cache (same layout, one byte per element; null for a bf16
+    // cache): a key element is k_scale * e4m3, a value element v_scale * e4m3.
+    // k_scale is folded into scale_log2, v_scale into o_scale.
+    const uint8_t* k8;
+    const uint8_t* v8;
+    float o_scale;                 // multiplies the split partials O (FP8 cache: v_scale)
     const int32_t* page_table;     // [batch, max_pages_per_seq]
     const int32_t* kv_lens;        // [batch]
     float* ws_o;                   // [batch, q_len, n_q_heads, num_splits, 512] unnormalised O
@@ -33,6 +39,11 @@ int decode_smem_bytes();
 int decode_tile_positions();
 cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
                           cudaStream_t stream);
+// FP8 cache: tmk / tmv map the e4m3 pages as bytes, boxes of
+// decode_fp8_box_bytes() head-dim bytes x box_rows positions, no swizzle.
+int decode_fp8_box_bytes();
+cudaError_t launch_decode_fp8(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const DecodeParams& p, cudaStream_t stream);
 
 struct PrefillParams {
     __nv_bfloat16* out;            // [total_q, n_q_heads, 512]

@@ -23,6 +23,9 @@
  *  fa512_prefill_paged -- the same for a batch of chunks of different
  *    lengths over a paged KV cache (pegainfer issue #1051, "Proposed Plan").
  *
+ *  fa512_decode_paged_fp8 -- the same over a cache stored in FP8 E4M3
+ *    (vllm-project/flash-attention PR #199, "Summary").
+ *
  *  fa512_decode_paged -- one query token per sequence against a paged KV
  *    cache, split over the key sequence (Flash-Decoding): each split writes an
  *    unnormalised (O, m, l) partial and a merge step combines them.
@@ -234,6 +237,38 @@ fa512_status fa512_decode_paged_q(const void *q, const void *k_pages, const void
 /* Workspace bytes fa512_decode_paged_q needs (0 for an invalid shape). */
 size_t fa512_decode_workspace_bytes_q(int batch, int q_len, int n_q_heads, int n_kv_heads,
                                       int page_size, int max_kv_len, int num_splits);
+
+/*
+ * fa512_decode_paged_fp8 -- fa512_decode_paged_q over a paged KV cache
+ * stored in FP8 E4M3 (vllm-project/flash-attention PR #199, "Summary": the
+ * paged KV cache in FP8; its "Performance" table times the decode shapes
+ * with an FP8 cache).
+ *
+ *   k_pages, v_pages [num_pages, page_size, n_kv_heads, 512] uint8, device:
+ *              one OCP E4M3 ("e4m3fn": bias 7, no infinities, S.1111.111
+ *              NaN, largest finite 448) byte per element
+ *   k_scale, v_scale per-tensor dequantisation scales: key element
+ *              k_scale * e4m3(byte), value element v_scale * e4m3(byte)
+ *   q, out, lse, positions, workspace and every other argument as
+ *              fa512_decode_paged_q (q_len >= 1, q_len * G <= 16); the
+ *              workspace size is fa512_decode_workspace_bytes_q.
+ *
+ * The cache is read as bytes: half the HBM traffic of a bf16 cache.  Every
+ * byte is widened exactly (e4m3 -> bf16/fp32) before it meets the bf16
+ * query, so the arithmetic is that of fa512_decode_paged_q on the
+ * dequantised cache: fp32 accumulation, fp32 softmax state, P rounded to
+ * bf16 only on the tensor-core path (q_len * G > 2).  Slots outside the live
+ * band are never read (NaN codes there do not reach the output).
+ * k_scale and v_scale must be finite (FA512_ERR_INVALID_ARG otherwise).
+ */
+fa512_status fa512_decode_paged_fp8(const void *q, const void *k_pages, const void *v_pages,
+                                    const int32_t *page_table, const int32_t *kv_lens, void *out,
+                                    float *lse, int batch, int q_len, int n_q_heads,
+                                    int n_kv_heads, int page_size, int num_pages,
+                                    int max_pages_per_seq, int max_kv_len, float scale,
+                                    float k_scale, float v_scale, int window, int num_splits,
+                                    void *workspace, size_t workspace_bytes,
+                                    fa512_stream_t stream);
 
 /* Split count chosen when num_splits == 0: enough (batch, KV head, split)
  * work items to fill the current device's SMs about twice, each split at
