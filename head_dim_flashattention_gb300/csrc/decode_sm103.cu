@@ -498,20 +498,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
 // warps' (m, l, O) are merged once at the end into the split's partial.
 namespace stream {
 
+constexpr int POS = 4;                   // positions per chunk
 constexpr int STAGES = 3;                // chunks in flight per warp
 constexpr int WARPS = 8;
-// A chunk is 8 KiB of K and V rows: 4 positions of a bf16 cache, 8 of an
-// FP8 E4M3 cache.  A lane owns 16 head-dim columns of every row: 32 bytes of
-// a bf16 row, 16 bytes of an FP8 row.
-template <bool FP8>
-struct Cfg {
-    static constexpr int POS = FP8 ? 8 : 4;              // positions per chunk
-    static constexpr int ROW_BYTES = FP8 ? D : D * 2;
-    static constexpr int LANE_BYTES = ROW_BYTES / 32;
-};
-constexpr int CHUNK_BYTES = 8192;
-static_assert(2 * Cfg<false>::POS * Cfg<false>::ROW_BYTES == CHUNK_BYTES, "chunk size");
-static_assert(2 * Cfg<true>::POS * Cfg<true>::ROW_BYTES == CHUNK_BYTES, "chunk size");
+constexpr int CHUNK_BYTES = 2 * POS * D * 2;          // K and V rows: 8 KiB
 constexpr int RING_BYTES = WARPS * STAGES * CHUNK_BYTES;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -533,131 +523,9 @@ __device__ __forceinline__ void unpack8(const uint4 a, const uint4 b, float (&f)
     }
 }
 
-// 16 e4m3 values -> fp32 times 2^-120, exactly, with integer operations
-// only (the conversion units would bound the kernel below the HBM rate).
-// An E4M3 byte s.eeee.mmm placed as fp32 bits s at 31 and eeee.mmm at 26..20
-// is the fp32 number 2^(e-127) (1 + m/8) for e >= 1 and the subnormal
-// (m/8) 2^-126 for e = 0 (zero included), i.e. the E4M3 value (bias 7,
-// subnormals (m/8) 2^-6) times 2^-120.  An arithmetic right shift by 4 of
-// the byte placed at bits 31..24 puts it there; the mask clears the copies
-// of the sign.  (The E4M3 NaN code would read as 480: codes are read only
-// inside the live band, where a cache holds finite values.)
-__device__ __forceinline__ void unpack16_e4m3_scaled(const uint4 a, float (&f)[16]) {
-    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-    constexpr uint32_t M = 0x87f00000u;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[4 * i + 0] = __uint_as_float(static_cast<uint32_t>(static_cast<int32_t>(w[i] << 24) >> 4) & M);
-        f[4 * i + 1] = __uint_as_float(static_cast<uint32_t>(static_cast<int32_t>(w[i] << 16) >> 4) & M);
-        f[4 * i + 2] = __uint_as_float(static_cast<uint32_t>(static_cast<int32_t>(w[i] << 8) >> 4) & M);
-        f[4 * i + 3] = __uint_as_float(static_cast<uint32_t>(static_cast<int32_t>(w[i]) >> 4) & M);
-    }
-}
-
-// One chunk of FP8 positions for the G query rows of this lane's warp.
-//
-// Scores: each lane forms its 16-column partial q.k' (k' = k 2^-120) with
-// f32x2 FMAs; the POS x G partials are summed over the 32 lanes by a
-// transposing butterfly (each step halves the values a lane carries), so
-// that lanes 32/NV apart ... end up holding one total each: value j = i G + g
-// sits in lanes with (lane / (32 / NV)) == j.  The chunk max and sum per row
-// are then reduced over those lanes, each lane evaluates one exp2, and the
-// probabilities are broadcast back for O += p v' (p pre-multiplied by 2^120,
-// so the product is p v in the normal range).
 template <int G>
-__device__ __forceinline__ void fp8_chunk(const uint8_t* st, int lane, int pos0, int pe,
-                                          float sl_hi, const float2 (&qq)[16], float (&m)[G],
-                                          float (&l)[G], float2 (&o)[G][8]) {
-    constexpr int POS = Cfg<true>::POS;
-    constexpr int ROW = Cfg<true>::ROW_BYTES;
-    constexpr int NV = POS * G;                    // 8 or 16 partial scores
-    constexpr int LPV = 32 / NV;                   // lanes that end up holding one value
-    float v[NV];
-#pragma unroll
-    for (int i = 0; i < POS; ++i) {
-        float kf[16];
-        unpack16_e4m3_scaled(*reinterpret_cast<const uint4*>(st + i * ROW + lane * 16), kf);
-        if constexpr (G == 2) {
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int d = 0; d < 16; ++d) acc = ffma2(qq[d], make_float2(kf[d], kf[d]), acc);
-            v[i * 2] = acc.x;
-            v[i * 2 + 1] = acc.y;
-        } else {
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int d = 0; d < 8; ++d) acc = ffma2(qq[d], make_float2(kf[2 * d], kf[2 * d + 1]), acc);
-            v[i] = acc.x + acc.y;
-        }
-    }
-    // transposing butterfly: after the step at offset `off` a lane keeps the
-    // upper half of its values when (lane & off) != 0, the lower half otherwise
-#pragma unroll
-    for (int off = 16, cnt = NV; cnt > 1; off >>= 1, cnt >>= 1) {
-        const bool up = (lane & off) != 0;
-#pragma unroll
-        for (int t = 0; t < cnt / 2; ++t) {
-            const float send = up ? v[t] : v[t + cnt / 2];
-            const float keep = up ? v[t + cnt / 2] : v[t];
-            v[t] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-    }
-#pragma unroll
-    for (int off = LPV / 2; off >= 1; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
-
-    const int j = lane / LPV;                      // the value this lane holds
-    const int i = j / G, g = j - i * G;
-    // score in log2 units: v 2^120 scale log2(e), in two steps that cannot overflow
-    const float s = (pos0 + i < pe) ? (v[0] * 0x1p64f) * sl_hi : -INFINITY;
-    // chunk max of row g: over the lanes holding values j' = i' G + g
-    float cm = s;
-#pragma unroll
-    for (int off = LPV * G; off < 32; off <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-    float mg[G], ag[G];
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-        // every lane learns both rows' chunk maxima (lane gg * LPV holds row gg's)
-        const float c = __shfl_sync(0xffffffffu, cm, gg * LPV);
-        const float mn = fmaxf(m[gg], c);
-        mg[gg] = mn == -INFINITY ? 0.f : mn;      // a row with no key yet shifts by 0
-        ag[gg] = fast_exp2(m[gg] - mg[gg]);
-        m[gg] = mn;
-    }
-    const float pj = fast_exp2(s - (G == 2 && g == 1 ? mg[G - 1] : mg[0]));
-    float ps = pj;
-#pragma unroll
-    for (int off = LPV * G; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-        l[gg] = l[gg] * ag[gg] + __shfl_sync(0xffffffffu, ps, gg * LPV);
-        if (ag[gg] != 1.f) {                       // the same in every lane
-#pragma unroll
-            for (int d = 0; d < 8; ++d) o[gg][d] = ffma2(o[gg][d], make_float2(ag[gg], ag[gg]),
-                                                         make_float2(0.f, 0.f));
-        }
-    }
-    const float pjs = pj * 0x1p120f;
-#pragma unroll
-    for (int ii = 0; ii < POS; ++ii) {
-        float vf[16];
-        unpack16_e4m3_scaled(*reinterpret_cast<const uint4*>(st + (POS + ii) * ROW + lane * 16), vf);
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-            const float pv = __shfl_sync(0xffffffffu, pjs, (ii * G + gg) * LPV);
-            const float2 pp = make_float2(pv, pv);
-#pragma unroll
-            for (int d = 0; d < 8; ++d)
-                o[gg][d] = ffma2(pp, make_float2(vf[2 * d], vf[2 * d + 1]), o[gg][d]);
-        }
-    }
-}
-
-template <int G, bool FP8>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 decode_stream_kernel(const DecodeParams p) {
-    constexpr int POS = Cfg<FP8>::POS;
-    constexpr int ROW = Cfg<FP8>::ROW_BYTES;
-    constexpr int LB = Cfg<FP8>::LANE_BYTES;
     extern __shared__ __align__(16) uint8_t smem[];
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -691,21 +559,6 @@ decode_stream_kernel(const DecodeParams p) {
 #pragma unroll
         for (int d = 0; d < 16; ++d) o[g][d] = 0.f;
     }
-    // FP8: q as f32x2 operands (G = 2: the two rows' column d; G = 1: columns
-    // 2e, 2e + 1), O as column pairs, and the score scale times 2^56 (the
-    // decoded keys carry 2^-120: 2^64 is applied to the dot product first)
-    float2 qq[16], o2[G][8];
-    const float sl_hi = p.scale_log2 * 0x1p56f;
-    if constexpr (FP8) {
-#pragma unroll
-        for (int d = 0; d < 16; ++d)
-            qq[d] = G == 2 ? make_float2(q[0][d], q[G - 1][d])
-                           : make_float2(q[0][(2 * d) & 15], q[0][(2 * d + 1) & 15]);
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int d = 0; d < 8; ++d) o2[g][d] = make_float2(0.f, 0.f);
-    }
 
     const uint32_t ring = smem_u32(smem) + warp * STAGES * CHUNK_BYTES;
     // chunk k of this warp covers positions pb + (warp + 8k) * POS ...
@@ -728,19 +581,14 @@ decode_stream_kernel(const DecodeParams p) {
                         row = (static_cast<size_t>(page) * p.page_size + (pos & (p.page_size - 1))) * p.n_kv_heads + kvh;
                     }
                 }
-                const uint32_t kd = st + i * ROW + lane * LB;
-                const uint32_t vd = st + (POS + i) * ROW + lane * LB;
-                if constexpr (FP8) {
-                    cp_async16(kd, p.k8 + row * D + lane * 16, valid);
-                    cp_async16(vd, p.v8 + row * D + lane * 16, valid);
-                } else {
-                    const __nv_bfloat16* ks = p.k_pages + row * D + lane * 16;
-                    const __nv_bfloat16* vs = p.v_pages + row * D + lane * 16;
-                    cp_async16(kd, ks, valid);
-                    cp_async16(kd + 16, ks + 8, valid);
-                    cp_async16(vd, vs, valid);
-                    cp_async16(vd + 16, vs + 8, valid);
-                }
+                const __nv_bfloat16* ks = p.k_pages + row * D + lane * 16;
+                const __nv_bfloat16* vs = p.v_pages + row * D + lane * 16;
+                const uint32_t kd = st + i * (D * 2) + lane * 32;
+                const uint32_t vd = st + (POS + i) * (D * 2) + lane * 32;
+                cp_async16(kd, ks, valid);
+                cp_async16(kd + 16, ks + 8, valid);
+                cp_async16(vd, vs, valid);
+                cp_async16(vd + 16, vs + 8, valid);
             }
         }
         cp_async_commit();   // one group per chunk slot, empty past the end
@@ -753,75 +601,62 @@ decode_stream_kernel(const DecodeParams p) {
         cp_async_wait<STAGES - 1>();   // this lane's copies of chunk k have landed
         const uint8_t* st = smem + (warp * STAGES + (k % STAGES)) * CHUNK_BYTES;
         const int pos0 = pb + (warp + WARPS * k) * POS;
-        if constexpr (FP8) {
-            fp8_chunk<G>(st, lane, pos0, pe, sl_hi, qq, m, l, o2);
-        } else {
-            float s[POS][G];
-    #pragma unroll
-            for (int i = 0; i < POS; ++i) {
-                float kf[16];
-                const uint4* kr = reinterpret_cast<const uint4*>(st + i * ROW + lane * LB);
-                unpack8(kr[0], kr[1], kf);
-    #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float acc = 0.f;
-    #pragma unroll
-                    for (int d = 0; d < 16; ++d) acc = fmaf(q[g][d], kf[d], acc);
-                    s[i][g] = acc;
-                }
-            }
-    #pragma unroll
-            for (int i = 0; i < POS; ++i)
-    #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float v = s[i][g];
-    #pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                    s[i][g] = (pos0 + i < pe) ? v * p.scale_log2 : -INFINITY;
-                }
-            float pr[POS][G];
-    #pragma unroll
+        float s[POS][G];
+#pragma unroll
+        for (int i = 0; i < POS; ++i) {
+            float kf[16];
+            const uint4* kr = reinterpret_cast<const uint4*>(st + i * (D * 2) + lane * 32);
+            unpack8(kr[0], kr[1], kf);
+#pragma unroll
             for (int g = 0; g < G; ++g) {
-                float cm = s[0][g];
-    #pragma unroll
-                for (int i = 1; i < POS; ++i) cm = fmaxf(cm, s[i][g]);
-                const float mn = fmaxf(m[g], cm);
-                const float sh = mn == -INFINITY ? 0.f : mn;   // no key seen yet
-                const float a = fast_exp2(m[g] - sh);
-                float ps = 0.f;
-    #pragma unroll
-                for (int i = 0; i < POS; ++i) {
-                    pr[i][g] = fast_exp2(s[i][g] - sh);
-                    ps += pr[i][g];
-                }
-                l[g] = l[g] * a + ps;
-                m[g] = mn;
-    #pragma unroll
-                for (int d = 0; d < 16; ++d) o[g][d] *= a;
+                float acc = 0.f;
+#pragma unroll
+                for (int d = 0; d < 16; ++d) acc = fmaf(q[g][d], kf[d], acc);
+                s[i][g] = acc;
             }
-    #pragma unroll
+        }
+#pragma unroll
+        for (int i = 0; i < POS; ++i)
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float v = s[i][g];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                s[i][g] = (pos0 + i < pe) ? v * p.scale_log2 : -INFINITY;
+            }
+        float pr[POS][G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float cm = s[0][g];
+#pragma unroll
+            for (int i = 1; i < POS; ++i) cm = fmaxf(cm, s[i][g]);
+            const float mn = fmaxf(m[g], cm);
+            const float sh = mn == -INFINITY ? 0.f : mn;   // no key seen yet
+            const float a = fast_exp2(m[g] - sh);
+            float ps = 0.f;
+#pragma unroll
             for (int i = 0; i < POS; ++i) {
-                float vf[16];
-                const uint4* vr = reinterpret_cast<const uint4*>(st + (POS + i) * ROW + lane * LB);
-                unpack8(vr[0], vr[1], vf);
-    #pragma unroll
-                for (int g = 0; g < G; ++g)
-    #pragma unroll
-                    for (int d = 0; d < 16; ++d) o[g][d] = fmaf(pr[i][g], vf[d], o[g][d]);
+                pr[i][g] = fast_exp2(s[i][g] - sh);
+                ps += pr[i][g];
             }
+            l[g] = l[g] * a + ps;
+            m[g] = mn;
+#pragma unroll
+            for (int d = 0; d < 16; ++d) o[g][d] *= a;
+        }
+#pragma unroll
+        for (int i = 0; i < POS; ++i) {
+            float vf[16];
+            const uint4* vr = reinterpret_cast<const uint4*>(st + (POS + i) * (D * 2) + lane * 32);
+            unpack8(vr[0], vr[1], vf);
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int d = 0; d < 16; ++d) o[g][d] = fmaf(pr[i][g], vf[d], o[g][d]);
         }
     }
     cp_async_wait<0>();
     __syncthreads();   // every warp is done with its ring: reuse it for the merge
-    if constexpr (FP8) {
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int d = 0; d < 8; ++d) {
-                o[g][2 * d] = o2[g][d].x;
-                o[g][2 * d + 1] = o2[g][d].y;
-            }
-    }
 
     float* so = reinterpret_cast<float*>(smem);                 // [WARPS][G][512]
     float* sml = so + WARPS * G * D;                             // [WARPS][G][2]
@@ -853,7 +688,7 @@ decode_stream_kernel(const DecodeParams p) {
             }
         }
         const size_t h = static_cast<size_t>(b) * p.n_q_heads + kvh * G + g;
-        p.ws_o[(h * S + split) * D + d] = FP8 ? acc * p.o_scale : acc;
+        p.ws_o[(h * S + split) * D + d] = acc;
         if (d == 0) {
             p.ws_ml[(h * S + split) * 2 + 0] = M;
             p.ws_ml[(h * S + split) * 2 + 1] = M == -INFINITY ? 0.f : L;
@@ -862,6 +697,412 @@ decode_stream_kernel(const DecodeParams p) {
 }
 
 }  // namespace stream
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 cache, up to 8 query rows (q_len * G <= 8): streaming warps on the
+// tensor cores.
+//
+// Decoding every cache byte to fp32 for FMA dot products costs more issue
+// slots per position than HBM takes to deliver it, so here the products run
+// on mma.sync (f16 operands, fp32 accumulation) with the query rows in the N
+// dimension: S^T = K Q^T (M = 16 positions, K = head dims) and O^T = V^T P^T
+// (M = 16 head-dim columns, K = 16 positions).  E4M3 -> f16 is exact: K through
+// the hardware e4m3x2 -> f16x2 conversion, V through an integer form (below)
+// that assembles each operand pair from two positions in one byte permute.
+//
+// Sixteen warps = four position groups x four head-dim slices of 128.  The
+// four warps of a group (same positions, one slice each) stream chunks of 16
+// positions: each copies its slice of the chunk's K and V rows (128 + 128
+// bytes a position) into a private cp.async ring, forms its slice of S^T,
+// and the four swap their partial scores through shared memory at a
+// 128-thread named barrier, so all hold the same scores, softmax state and
+// P; each then accumulates its own 128 columns of O^T.  No CTA-wide barrier
+// runs until the final merge of the four position groups.
+namespace mma8 {
+
+constexpr int GROUPS = 4;                        // position groups
+constexpr int SLICES = 4;                        // head-dim slices
+constexpr int WARPS = GROUPS * SLICES;
+constexpr int CPOS = 16;                         // positions per chunk
+constexpr int SLICE = D / SLICES;                // head-dim bytes (elements) per warp: 128
+constexpr int PIECES = SLICE / 16;               // 16-byte pieces per row: 8
+constexpr int KSTEPS = SLICE / 16;               // k-steps of 16 per slice: 8
+constexpr int MTILES = SLICE / 16;               // m-tiles of 16 columns per slice: 8
+constexpr int STAGES = 3;
+constexpr int CHUNK_BYTES = 2 * CPOS * SLICE;    // this warp's K and V slices: 4 KiB
+constexpr int RING_BYTES = WARPS * STAGES * CHUNK_BYTES;
+constexpr int XCH_BYTES = 2 * GROUPS * SLICES * 32 * 16;   // [parity][group][slice][lane] float4
+constexpr int SMEM_BYTES = RING_BYTES + XCH_BYTES;
+static_assert(WARPS * 8 * SLICE * 4 + WARPS * 8 * 2 * 4 <= RING_BYTES, "merge buffer fits the ring");
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// 16-byte piece c of row r (a chunk position, K or V) sits at piece
+// (c + 4r + 2 (r / 2)) & 7 of the row: the async copies (lane pairs fill one
+// row each), the K reads (lanes of a quarter warp read pieces t of rows g,
+// g + 1) and the V reads (piece g of rows 2t, 2t + 1) then touch eight
+// different bank groups per quarter warp.
+__device__ __forceinline__ int swz(int r) { return 4 * r + 2 * (r >> 1); }
+
+__device__ __forceinline__ void bar_group(int id) {
+    asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 values (low byte first) -> f16x2, exactly (hardware conversion).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two)));
+    return h2;
+}
+
+// Byte k of word x and byte k of word y -> f16x2 {x_k, y_k} times 2^-8,
+// exactly.  An E4M3 byte s.eeee.mmm placed as f16 bits s at 15 and
+// eeee.mmm at 13..7 is the f16 number 2^(e-15) (1 + m/8) (e >= 1) or the
+// subnormal (m/8) 2^-14 (e = 0, zero included): the E4M3 value times 2^-8.
+// One permute puts [sign(y_k)][y_k][sign(x_k)][x_k] in the four bytes (the
+// selector's bit 3 replicates a byte's sign bit), a shift by 7 moves each
+// byte's sign copy to bit 15 / 31 and its eeee.mmm to 13..7 / 29..23, and
+// the mask clears what the shift carried in.  (The E4M3 NaN code would read
+// as 480: codes are read only inside the live band.)
+template <int K>
+__device__ __forceinline__ uint32_t e4m3_pair_f16x2_scaled(uint32_t x, uint32_t y) {
+    constexpr uint32_t sel = K | ((8 | K) << 4) | ((4 + K) << 8) | ((12 + K) << 12);
+    uint32_t t;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(y), "n"(sel));
+    return (t << 7) & 0xbf80bf80u;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__global__ void __launch_bounds__(WARPS * 32, 1)
+decode_fp8_mma_kernel(const DecodeParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pg = warp & (GROUPS - 1);      // position group
+    const int sl = warp / GROUPS;            // head-dim slice
+    const int g = lane >> 2, t = lane & 3;   // mma fragment coordinates
+    const int G = p.group;
+    const int R = p.q_len * G;               // query rows, <= 8
+
+    int len = p.kv_lens[b];
+    if (len < 0 || len > p.len_cap) {
+        if (threadIdx.x == 0 && split == 0 && kvh == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+        len = len < 0 ? 0 : p.len_cap;
+    }
+    // union of the rows' bands (the row of token t sees [pos - window + 1, pos])
+    const int hi = len;
+    const int w_lo = len - p.q_len + 1 - p.window;
+    const int lo = (p.window > 0 && w_lo > 0) ? w_lo : 0;
+    const int t_begin = lo / TILE_K + split * p.tiles_per_split;
+    const int pb = max(lo, t_begin * TILE_K);
+    const int pe = min(hi, (t_begin + p.tiles_per_split) * TILE_K);
+    const int n_chunks = pe > pb ? (pe - pb + CPOS - 1) / CPOS : 0;
+    const int my_chunks = n_chunks > pg ? (n_chunks - pg + GROUPS - 1) / GROUPS : 0;
+
+    // ---- Q^T fragments of this warp's slice: b0/b1 of k-step (j, s) hold
+    // row g's elements 64 j + 16 t + 4 s + {0, 1} / {2, 3}, in f16 after a
+    // power-of-two scale per row and slice that keeps the largest element
+    // below 2^15 (exact; every partial score is unscaled before the swap)
+    uint32_t qb[KSTEPS][2];
+    float rs[2];                              // 1 / (this slice's scale) of rows 2t, 2t + 1
+    {
+        float qmax = 0.f;
+        float qv[KSTEPS][4];
+        const bool row_ok = g < R;
+        const size_t qrow = (static_cast<size_t>(b) * p.q_len + (row_ok ? g / G : 0)) * p.n_q_heads +
+                            kvh * G + (row_ok ? g % G : 0);
+#pragma unroll
+        for (int j = 0; j < KSTEPS / 4; ++j) {
+            // 16 elements: 64 j + 16 t .. + 15 of this slice
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * D + sl * SLICE + 64 * j + 16 * t);
+            const uint4 a = row_ok ? src[0] : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 c = row_ok ? src[1] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                qv[4 * j + s][0] = __uint_as_float(w[2 * s] << 16);
+                qv[4 * j + s][1] = __uint_as_float(w[2 * s] & 0xffff0000u);
+                qv[4 * j + s][2] = __uint_as_float(w[2 * s + 1] << 16);
+                qv[4 * j + s][3] = __uint_as_float(w[2 * s + 1] & 0xffff0000u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) qmax = fmaxf(qmax, fabsf(qv[4 * j + s][e]));
+            }
+        }
+        // the row's maximum over its four lanes (t) of this slice
+        qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+        qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+        // qscale = 2^(14 - E), E = exponent of qmax (qmax = 0 or not finite: 1)
+        const int E = (__float_as_uint(qmax) >> 23) & 0xff;
+        const int biased = min(127 + 14 + 127 - E, 254);     // 2^(14 - (E - 127)), at most 2^127
+        const float qscale = (qmax > 0.f && E < 255) ? __uint_as_float(static_cast<uint32_t>(biased) << 23) : 1.f;
+#pragma unroll
+        for (int k = 0; k < KSTEPS; ++k) {
+            qb[k][0] = pack_f16x2(qv[k][0] * qscale, qv[k][1] * qscale);
+            qb[k][1] = pack_f16x2(qv[k][2] * qscale, qv[k][3] * qscale);
+        }
+        // rows 2t, 2t + 1 are held by lanes with g = 2t, 2t + 1
+        rs[0] = 1.f / __shfl_sync(0xffffffffu, qscale, 4 * (2 * t));
+        rs[1] = 1.f / __shfl_sync(0xffffffffu, qscale, 4 * (2 * t + 1));
+    }
+    // positions of rows 2t and 2t + 1 (-1: padding row, sees nothing)
+    int qpos[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int r = 2 * t + i;
+        qpos[i] = r < R ? len - p.q_len + r / G : -1;
+    }
+
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[MTILES][4];                       // O^T: m-tile i = columns 16 g + 2 i, 16 g + 2 i + 1
+#pragma unroll
+    for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    const uint32_t ring = smem_u32(smem) + warp * STAGES * CHUNK_BYTES;
+    float4* xch = reinterpret_cast<float4*>(smem + RING_BYTES);
+
+    // copy plan: lane l fetches position l / 2 of the chunk; at step s it
+    // copies 16-byte piece (l & 1) + 2 (s % 4) of that position's K slice
+    // (s < 4) or V slice (s >= 4), so every instruction covers whole 32-byte
+    // sectors.
+    auto issue = [&](int k) {
+        if (k < my_chunks) {
+            const int pos = pb + (pg + GROUPS * k) * CPOS + (lane >> 1);
+            bool valid = pos < pe;
+            size_t row = 0;
+            if (valid) {
+                const int page = p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size];
+                if (page < 0 || page >= p.num_pages) {
+                    report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                    valid = false;
+                } else {
+                    row = (static_cast<size_t>(page) * p.page_size + (pos & (p.page_size - 1))) * p.n_kv_heads + kvh;
+                }
+            }
+            const uint8_t* ksrc = p.k8 + row * D + sl * SLICE;
+            const uint8_t* vsrc = p.v8 + row * D + sl * SLICE;
+            const uint32_t st = ring + (k % STAGES) * CHUNK_BYTES;
+            const int r = lane >> 1;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int c = (lane & 1) + 2 * (s & 3);
+                const uint32_t dst = st + (s >> 2) * (CPOS * SLICE) + r * SLICE + (((c + swz(r)) & 7) << 4);
+                cp_async16(dst, (s < 4 ? ksrc : vsrc) + c * 16, valid);
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < STAGES - 1; ++k) issue(k);
+
+    for (int k = 0; k < my_chunks; ++k) {
+        issue(k + STAGES - 1);
+        cp_async_wait<STAGES - 1>();
+        __syncwarp();                         // every lane's copies of chunk k are visible
+        const uint8_t* kst = smem + (warp * STAGES + (k % STAGES)) * CHUNK_BYTES;
+        const uint8_t* vst = kst + CPOS * SLICE;
+        const int pos0 = pb + (pg + GROUPS * k) * CPOS;
+
+        // ---- S^T slice = K_slice Q_slice^T, one accumulator chain per 64
+        // head-dim elements, summed at the end
+        float sc[4];
+        {
+            float acc[KSTEPS / 4][4];
+#pragma unroll
+            for (int j = 0; j < KSTEPS / 4; ++j) {
+                acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+                const uint4 ka = *reinterpret_cast<const uint4*>(kst + g * SLICE + (((4 * j + t + swz(g)) & 7) << 4));
+                const uint4 kb = *reinterpret_cast<const uint4*>(kst + (g + 8) * SLICE + (((4 * j + t + swz(g + 8)) & 7) << 4));
+                const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16_16816(acc[j], e4m3x2_f16x2(wa[s] & 0xffffu), e4m3x2_f16x2(wb[s] & 0xffffu),
+                                  e4m3x2_f16x2(wa[s] >> 16), e4m3x2_f16x2(wb[s] >> 16),
+                                  qb[4 * j + s][0], qb[4 * j + s][1]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[e] = (acc[0][e] + acc[1][e]) * (e & 1 ? rs[1] : rs[0]);
+        }
+        // ---- swap slices with the group's other warps: S = (S_0 + S_1) + (S_2 + S_3),
+        // each slice unscaled by its own row scale first (a power of two,
+        // exact); the same sum, in the same order, in all four warps
+        {
+            float4* base = xch + ((k & 1) * GROUPS + pg) * SLICES * 32 + lane;
+            base[sl * 32] = make_float4(sc[0], sc[1], sc[2], sc[3]);
+            bar_group(1 + pg);
+            const float4 x0 = base[0], x1 = base[32], x2 = base[64], x3 = base[96];
+            sc[0] = (x0.x + x1.x) + (x2.x + x3.x);
+            sc[1] = (x0.y + x1.y) + (x2.y + x3.y);
+            sc[2] = (x0.z + x1.z) + (x2.z + x3.z);
+            sc[3] = (x0.w + x1.w) + (x2.w + x3.w);
+        }
+        // ---- online softmax: this thread holds positions g, g + 8 of rows
+        // 2t, 2t + 1; both rows step together (independent shuffle chains)
+        float pr[4], sv[2][2], cm[2], al[2], ps[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            auto sees = [&](int kp) {
+                return kp < pe && kp <= qpos[i] && (p.window <= 0 || kp > qpos[i] - p.window);
+            };
+            sv[i][0] = sees(pos0 + g) ? sc[i] * p.scale_log2 : -INFINITY;
+            sv[i][1] = sees(pos0 + g + 8) ? sc[2 + i] * p.scale_log2 : -INFINITY;
+            cm[i] = fmaxf(sv[i][0], sv[i][1]);
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            const float x0 = __shfl_xor_sync(0xffffffffu, cm[0], off);
+            const float x1 = __shfl_xor_sync(0xffffffffu, cm[1], off);
+            cm[0] = fmaxf(cm[0], x0);
+            cm[1] = fmaxf(cm[1], x1);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float mn = fmaxf(m[i], cm[i]);
+            const float sh = mn == -INFINITY ? 0.f : mn;
+            // a row that has still seen no key has nothing to rescale
+            al[i] = mn == -INFINITY ? 1.f : fast_exp2(m[i] - sh);
+            pr[i] = fast_exp2(sv[i][0] - sh);
+            pr[2 + i] = fast_exp2(sv[i][1] - sh);
+            ps[i] = pr[i] + pr[2 + i];
+            m[i] = mn;
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            const float x0 = __shfl_xor_sync(0xffffffffu, ps[0], off);
+            const float x1 = __shfl_xor_sync(0xffffffffu, ps[1], off);
+            ps[0] += x0;
+            ps[1] += x1;
+        }
+        l[0] = l[0] * al[0] + ps[0];
+        l[1] = l[1] * al[1] + ps[1];
+        if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < MTILES; ++c) {
+                o[c][0] *= al[0];
+                o[c][1] *= al[1];
+                o[c][2] *= al[0];
+                o[c][3] *= al[1];
+            }
+        }
+        // ---- P^T fragments: b0 = P[row g][pos 2t, 2t + 1], b1 = P[g][2t + 8, 2t + 9];
+        // P[r][q] sits in lane 4 (q & 7) + r / 2, register (q >= 8 ? 2 : 0) + (r & 1)
+        uint32_t pb0, pb1;
+        {
+            const int src0 = 4 * (2 * t) + (g >> 1), src1 = 4 * (2 * t + 1) + (g >> 1);
+            const float e00 = __shfl_sync(0xffffffffu, pr[0], src0), e01 = __shfl_sync(0xffffffffu, pr[1], src0);
+            const float e10 = __shfl_sync(0xffffffffu, pr[0], src1), e11 = __shfl_sync(0xffffffffu, pr[1], src1);
+            const float f00 = __shfl_sync(0xffffffffu, pr[2], src0), f01 = __shfl_sync(0xffffffffu, pr[3], src0);
+            const float f10 = __shfl_sync(0xffffffffu, pr[2], src1), f11 = __shfl_sync(0xffffffffu, pr[3], src1);
+            const bool odd = g & 1;
+            pb0 = pack_f16x2(odd ? e01 : e00, odd ? e11 : e10);
+            pb1 = pack_f16x2(odd ? f01 : f00, odd ? f11 : f10);
+        }
+        // ---- O^T slice += V_slice^T P^T: thread g's columns are bytes
+        // 16 g .. 16 g + 15 of each row (column pair i at bytes 2i, 2i + 1);
+        // rows 2t, 2t + 1, 2t + 8, 2t + 9
+        uint32_t vw[4][4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int r = 2 * t + (rr & 1) + 8 * (rr >> 1);
+            const uint4 x = *reinterpret_cast<const uint4*>(vst + r * SLICE + (((g + swz(r)) & 7) << 4));
+            vw[rr][0] = x.x;
+            vw[rr][1] = x.y;
+            vw[rr][2] = x.z;
+            vw[rr][3] = x.w;
+        }
+#pragma unroll
+        for (int i = 0; i < MTILES; ++i) {
+            const int wi = i >> 1;
+            uint32_t a0, a1, a2, a3;
+            if (i & 1) {
+                a0 = e4m3_pair_f16x2_scaled<2>(vw[0][wi], vw[1][wi]);
+                a1 = e4m3_pair_f16x2_scaled<3>(vw[0][wi], vw[1][wi]);
+                a2 = e4m3_pair_f16x2_scaled<2>(vw[2][wi], vw[3][wi]);
+                a3 = e4m3_pair_f16x2_scaled<3>(vw[2][wi], vw[3][wi]);
+            } else {
+                a0 = e4m3_pair_f16x2_scaled<0>(vw[0][wi], vw[1][wi]);
+                a1 = e4m3_pair_f16x2_scaled<1>(vw[0][wi], vw[1][wi]);
+                a2 = e4m3_pair_f16x2_scaled<0>(vw[2][wi], vw[3][wi]);
+                a3 = e4m3_pair_f16x2_scaled<1>(vw[2][wi], vw[3][wi]);
+            }
+            mma_f16_16816(o[i], a0, a1, a2, a3, pb0, pb1);
+        }
+        __syncwarp();                         // the stage may be refilled
+    }
+    cp_async_wait<0>();
+    __syncthreads();   // every warp is done with its ring: reuse it for the merge
+
+    // ---- merge the four position groups: O^T rows 2t, 2t + 1 of slice
+    // columns 16 g + 2 i (M row g of m-tile i) and 16 g + 2 i + 1 (M row
+    // g + 8) -> smem [warp][row 8][128], m and l [warp][row][2]
+    float* so = reinterpret_cast<float*>(smem);
+    float* sml = so + WARPS * 8 * SLICE;
+    // the V operand carried 2^-8: undo it with the value scale
+    const float osc = p.o_scale * 256.f;
+#pragma unroll
+    for (int i = 0; i < MTILES; ++i) {
+        const int c0 = 16 * g + 2 * i, c1 = c0 + 1;
+        so[(warp * 8 + 2 * t) * SLICE + c0] = o[i][0];
+        so[(warp * 8 + 2 * t + 1) * SLICE + c0] = o[i][1];
+        so[(warp * 8 + 2 * t) * SLICE + c1] = o[i][2];
+        so[(warp * 8 + 2 * t + 1) * SLICE + c1] = o[i][3];
+    }
+    if (g == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            sml[(warp * 8 + 2 * t + i) * 2] = m[i];
+            sml[(warp * 8 + 2 * t + i) * 2 + 1] = l[i];
+        }
+    }
+    __syncthreads();
+    const size_t S = static_cast<size_t>(p.num_splits);
+    for (int idx = threadIdx.x; idx < R * D; idx += WARPS * 32) {
+        const int r = idx / D, d = idx - r * D;
+        const int h = d / SLICE, c = d - h * SLICE;   // slice and column within it
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < GROUPS; ++q) M = fmaxf(M, sml[((h * GROUPS + q) * 8 + r) * 2]);
+        float acc = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int q = 0; q < GROUPS; ++q) {
+                const int w = h * GROUPS + q;
+                const float wt = fast_exp2(sml[(w * 8 + r) * 2] - M);
+                acc += wt * so[(w * 8 + r) * SLICE + c];
+                L += wt * sml[(w * 8 + r) * 2 + 1];
+            }
+        }
+        const size_t hq = (static_cast<size_t>(b) * p.q_len + r / G) * p.n_q_heads + kvh * G + r % G;
+        p.ws_o[(hq * S + split) * D + d] = acc * osc;
+        if (d == 0) {
+            p.ws_ml[(hq * S + split) * 2 + 0] = M;
+            p.ws_ml[(hq * S + split) * 2 + 1] = M == -INFINITY ? 0.f : L;
+        }
+    }
+}
+
+}  // namespace mma8
+
 
 // One block per (sequence, query token, query head): merges the splits' (O, m, l).
 __global__ void __launch_bounds__(128)
@@ -909,14 +1150,24 @@ int decode_fp8_box_bytes() { return decode::F8_BOX_BYTES; }
 
 int decode_tile_positions() { return decode::TILE_K; }
 
-template <int G, bool FP8>
+template <int G>
 static cudaError_t launch_stream(const DecodeParams& p, cudaStream_t stream) {
     const int smem = decode::stream::RING_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(decode::stream::decode_stream_kernel<G, FP8>,
+    cudaError_t e = cudaFuncSetAttribute(decode::stream::decode_stream_kernel<G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.num_splits, p.n_kv_heads, p.batch);
-    decode::stream::decode_stream_kernel<G, FP8><<<grid, decode::stream::WARPS * 32, smem, stream>>>(p);
+    decode::stream::decode_stream_kernel<G><<<grid, decode::stream::WARPS * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+static cudaError_t launch_fp8_mma(const DecodeParams& p, cudaStream_t stream) {
+    const int smem = decode::mma8::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(decode::mma8::decode_fp8_mma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.num_splits, p.n_kv_heads, p.batch);
+    decode::mma8::decode_fp8_mma_kernel<<<grid, decode::mma8::WARPS * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -924,10 +1175,12 @@ template <bool FP8>
 static cudaError_t launch_split_and_merge(const CUtensorMap& tmk, const CUtensorMap& tmv,
                                           const DecodeParams& p, cudaStream_t stream) {
     cudaError_t e;
-    if (p.q_len == 1 && p.group == 1) {
-        e = launch_stream<1, FP8>(p, stream);
-    } else if (p.q_len == 1 && p.group == 2) {
-        e = launch_stream<2, FP8>(p, stream);
+    if (FP8 && p.q_len * p.group <= 8) {
+        e = launch_fp8_mma(p, stream);
+    } else if (!FP8 && p.q_len == 1 && p.group == 1) {
+        e = launch_stream<1>(p, stream);
+    } else if (!FP8 && p.q_len == 1 && p.group == 2) {
+        e = launch_stream<2>(p, stream);
     } else {
         // larger query groups or several tokens: S and PV on the tensor cores
         // (q_len * G rows padded to 16)

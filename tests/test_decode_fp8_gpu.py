@@ -40,13 +40,14 @@ def run(fa, pc, q=None, k_pages=None, v_pages=None, k_scale=K_SCALE, v_scale=V_S
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-def check(fa, pc, q=None, k_scale=K_SCALE, v_scale=V_SCALE, num_splits=0, window=0):
+def check(fa, pc, q=None, k_scale=K_SCALE, v_scale=V_SCALE, num_splits=0, window=0, scale=None):
     q = pc.q if q is None else q
     o, l = run(fa, pc, q=q, k_scale=k_scale, v_scale=v_scale, num_splits=num_splits,
-               window=window)
+               window=window, scale=scale)
     assert fa.fa512_device_status() == 0
     ro, rl = oracle.decode_paged_fp8(q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
-                                     k_scale=k_scale, v_scale=v_scale, window=window)
+                                     k_scale=k_scale, v_scale=v_scale, window=window,
+                                     scale=scale)
     compare_o(o, ro)
     compare_lse(l, rl)
     return o, l
@@ -69,8 +70,9 @@ def test_decode_shapes(fa, batch, kv_len):
 @pytest.mark.parametrize("hq,hk,q_len", [(4, 4, 1), (8, 4, 1), (8, 4, 3), (16, 2, 2),
                                          (16, 1, 1), (12, 4, 5)])
 def test_groupings_and_tokens(fa, hq, hk, q_len):
-    """One or two query heads per KV head and one token take the streaming
-    kernel; larger groups or several tokens the tensor-core kernel."""
+    """Up to 8 (token, head) rows take the streaming tensor-core kernel
+    (f16 products of the exactly widened bytes); more rows take the split
+    kernel that converts each FP8 tile into a bf16 tile."""
     pc = fp8_cache(3, [513, 100, 1], hq, hk, seed=71)
     q = workloads.draft_queries(3, q_len, hq, seed=71) if q_len > 1 else pc.q
     check(fa, pc, q=q)
@@ -113,11 +115,11 @@ def _dequant_bf16(pages_u8, scale):
     return (pages_u8.view(torch.float8_e4m3fn).float() * scale).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("hq,hk,q_len", [(8, 4, 3), (16, 2, 1), (8, 4, 2)])
-def test_tensor_core_path_equals_bf16_decode_bitwise(fa, hq, hk, q_len):
-    """With power-of-two scales the dequantised cache is a bf16 cache; the
-    tensor-core kernel converts each FP8 tile exactly into the bf16 tile the
-    bf16 kernel reads, so the two calls agree bit for bit."""
+@pytest.mark.parametrize("hq,hk,q_len", [(16, 2, 2), (16, 1, 1), (12, 4, 3)])
+def test_split_path_equals_bf16_decode_bitwise(fa, hq, hk, q_len):
+    """More than 8 rows: with power-of-two scales the dequantised cache is a
+    bf16 cache, and the split kernel converts each FP8 tile exactly into the
+    bf16 tile the bf16 split kernel reads, so the two calls agree bit for bit."""
     s = 1.0 / 32
     pc = fp8_cache(3, [3000, 129, 64], hq, hk, seed=76)
     q = workloads.draft_queries(3, q_len, hq, seed=76)
@@ -131,20 +133,39 @@ def test_tensor_core_path_equals_bf16_decode_bitwise(fa, hq, hk, q_len):
     assert torch.equal(o8, o16) and torch.equal(l8, l16)
 
 
-def test_streaming_path_agrees_with_bf16_decode(fa):
-    """The streaming kernel walks FP8 rows in chunks of 8 positions (bf16: 4),
-    so the rescale points differ; on the same values the two agree within
-    the rounding of the output."""
+@pytest.mark.parametrize("hq,hk,q_len", [(8, 4, 1), (4, 4, 1), (8, 4, 4), (16, 4, 2), (8, 1, 1)])
+def test_streaming_path_agrees_with_bf16_decode(fa, hq, hk, q_len):
+    """Up to 8 rows: the FP8 kernel's f16 tensor-core products of the exactly
+    widened cache against the bf16 decode of the same values (power-of-two
+    scales): the scores are the same exact products summed in another order,
+    P is rounded to f16 instead of kept in fp32 or rounded to bf16, so the two
+    agree within the rounding of the output."""
     s = 1.0 / 16
-    pc = fp8_cache(4, [4096, 777, 64, 1], seed=77)
-    o8, l8 = run(fa, pc, k_scale=s, v_scale=s)
-    o16, l16 = fa.fa512_decode_paged(pc.q.cuda(), _dequant_bf16(pc.k_pages, s).cuda(),
-                                     _dequant_bf16(pc.v_pages, s).cuda(), pc.page_table.cuda(),
-                                     pc.kv_lens.cuda(), max_kv_len=pc.max_kv_len)
+    pc = fp8_cache(4, [4096, 777, 64, 1], hq, hk, seed=77)
+    q = workloads.draft_queries(4, q_len, hq, seed=77)
+    o8, l8 = run(fa, pc, q=q, k_scale=s, v_scale=s)
+    o16, l16 = fa.fa512_decode_paged_q(q.cuda(), _dequant_bf16(pc.k_pages, s).cuda(),
+                                       _dequant_bf16(pc.v_pages, s).cuda(), pc.page_table.cuda(),
+                                       pc.kv_lens.cuda(), max_kv_len=pc.max_kv_len)
     torch.cuda.synchronize()
     # two bf16 spacings relative, plus the fp32 rounding of small values
     np.testing.assert_allclose(o8, o16.float().cpu().numpy(), atol=2e-3, rtol=8e-3)
-    np.testing.assert_allclose(l8, l16.cpu().numpy(), atol=1e-5, rtol=0)
+    fin = np.isfinite(l8)
+    assert np.array_equal(fin, np.isfinite(l16.cpu().numpy()))
+    np.testing.assert_allclose(l8[fin], l16.cpu().numpy()[fin], atol=1e-5, rtol=0)
+
+
+def test_large_and_small_query_rows(fa):
+    """The tensor-core kernel scales each query row by a power of two before
+    the f16 products, so rows far outside the f16 range keep their scores:
+    one head's query times 2^20 (elements up to ~2^22, beyond f16's 65504)
+    with the softmax scale times 2^-20, and one head's query times 2^-50
+    (below f16's subnormals; its attention is uniform)."""
+    pc = fp8_cache(2, [300, 4097], 8, 4, seed=83)
+    q = pc.q.clone()
+    q[:, 0] *= 2.0 ** 20
+    q[1, 5] *= 2.0 ** -50
+    check(fa, pc, q=q, scale=D ** -0.5 * 2.0 ** -20)
 
 
 @pytest.mark.parametrize("q_len", [1, 4])
