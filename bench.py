@@ -314,7 +314,7 @@ def time_decode_fp8(args, fa, g, dev, stream, shapes, flush, world, peaks):
                         "num_splits auto, FP8 E4M3 K/V cache (per-tensor scales 1/32)",
             "value": gbs, "unit": "GB/s", "ms": sum(ms), "bytes_per_step": total_bytes,
             "frac_of_measured_hbm": gbs / world / peaks["hbm_gbs"],
-            "kernel": "fa512::decode::stream::decode_stream_kernel<2, true> + merge",
+            "kernel": "fa512::decode::mma8::decode_fp8_mma_kernel + merge",
             "l2": "flushed before every step (each shape called once per step)",
             "per_shape": per}
 
