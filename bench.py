@@ -626,8 +626,11 @@ def run_ours(args):
 
     # ---- paged decode of q_len tokens per sequence, timed on its own
     decode_q = None
-    if not args.no_decode and not args.decode_shapes:
-        b, n, ql = DECODE_Q_SHAPE["batch"], DECODE_Q_SHAPE["kv_len"], DECODE_Q_SHAPE["q_len"]
+    # (--decode-shapes selects main-loop shapes for profiling and skips this
+    # leg unless --decode-q-batch asks for it)
+    if not args.no_decode and (not args.decode_shapes or args.decode_q_batch is not None):
+        b = args.decode_q_batch if args.decode_q_batch is not None else DECODE_Q_SHAPE["batch"]
+        n, ql = DECODE_Q_SHAPE["kv_len"], DECODE_Q_SHAPE["q_len"]
         npg = (n + PAGE - 1) // PAGE
         gcpu = torch.Generator()
         gcpu.manual_seed(0x5EED + 6)
@@ -719,6 +722,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-paged", action="store_true", help="skip the paged-prefill legs")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-cache decode leg")
+    ap.add_argument("--decode-q-batch", type=int, default=None,
+                    help="batch of the several-token decode leg (default 64; profiling a smaller case)")
     ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling)")
     ap.add_argument("--decode-shapes", default="", help="comma list such as b64_kv28672")
     args = ap.parse_args()

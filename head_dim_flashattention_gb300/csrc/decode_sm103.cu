@@ -1103,6 +1103,292 @@ decode_fp8_mma_kernel(const DecodeParams p) {
 
 }  // namespace mma8
 
+// ---------------------------------------------------------------------------
+// bf16 cache, 3 to 8 query rows (several tokens, or 3-8 query heads per KV
+// head): the same streaming tensor-core design as the FP8 kernel above, for
+// the rows the FMA streaming kernel cannot take.  A bf16 position carries
+// 2 KiB, so the design's per-position instruction cost fits twice the HBM
+// time it has at FP8; its operands need no widening (K pairs are the A
+// operand as stored; each V operand pair is one 16-bit permute of two
+// positions' words).  Shared memory (16 warps x 3 stages) holds chunks of 8
+// positions: S^T runs with M = 16 over 8 positions (the other 8 rows zero)
+// and O^T = V^T P^T with K = 16 over them (the other 8 zero).
+namespace mma16 {
+
+using mma8::GROUPS;
+using mma8::SLICES;
+using mma8::WARPS;
+constexpr int CPOS = 8;                          // positions per chunk
+constexpr int SLICE = D / SLICES;                // head-dim elements per warp: 128
+constexpr int ROW = SLICE * 2;                   // bytes of a row slice: 256
+constexpr int KGROUPS = SLICE / 32;              // 16-byte loads per K row: 4 (2 k-steps each)
+constexpr int MTILES = SLICE / 16;               // m-tiles of 16 columns: 8
+constexpr int STAGES = 3;
+constexpr int CHUNK_BYTES = 2 * CPOS * ROW;      // 4 KiB
+constexpr int RING_BYTES = WARPS * STAGES * CHUNK_BYTES;
+constexpr int XCH_BYTES = mma8::XCH_BYTES;
+constexpr int SMEM_BYTES = RING_BYTES + XCH_BYTES;
+static_assert(WARPS * 8 * SLICE * 4 + WARPS * 8 * 2 * 4 <= RING_BYTES, "merge buffer fits the ring");
+
+// 16-byte piece c of a K row r sits at piece (c + 4r) & 15, of a V row at
+// (c + 4r + r/2 + 2 (r/4)) & 15: the async copies (four lanes per row), the K
+// reads (pieces 4j + t of row g) and the V reads (pieces 2g, 2g + 1 of rows
+// 2t, 2t + 1) then touch eight different bank groups per quarter warp.
+__device__ __forceinline__ int swz_k(int r) { return 4 * r; }
+__device__ __forceinline__ int swz_v(int r) { return 4 * r + (r >> 1) + 2 * (r >> 2); }
+
+__device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {
+    uint32_t t;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(y), "r"(sel));
+    return t;
+}
+
+__global__ void __launch_bounds__(WARPS * 32, 1)
+decode_bf16_mma_kernel(const DecodeParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pg = warp & (GROUPS - 1);      // position group
+    const int sl = warp / GROUPS;            // head-dim slice
+    const int g = lane >> 2, t = lane & 3;   // mma fragment coordinates
+    const int G = p.group;
+    const int R = p.q_len * G;               // query rows, <= 8
+
+    int len = p.kv_lens[b];
+    if (len < 0 || len > p.len_cap) {
+        if (threadIdx.x == 0 && split == 0 && kvh == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+        len = len < 0 ? 0 : p.len_cap;
+    }
+    const int hi = len;
+    const int w_lo = len - p.q_len + 1 - p.window;
+    const int lo = (p.window > 0 && w_lo > 0) ? w_lo : 0;
+    const int t_begin = lo / TILE_K + split * p.tiles_per_split;
+    const int pb = max(lo, t_begin * TILE_K);
+    const int pe = min(hi, (t_begin + p.tiles_per_split) * TILE_K);
+    const int n_chunks = pe > pb ? (pe - pb + CPOS - 1) / CPOS : 0;
+    const int my_chunks = n_chunks > pg ? (n_chunks - pg + GROUPS - 1) / GROUPS : 0;
+
+    // ---- Q^T fragments (bf16, as stored): b0/b1 of k-step (j, s) hold row
+    // g's elements 32 j + 8 t + 4 s + {0, 1} / {2, 3} of this slice
+    uint32_t qb[2 * KGROUPS][2];
+    {
+        const bool row_ok = g < R;
+        const size_t qrow = (static_cast<size_t>(b) * p.q_len + (row_ok ? g / G : 0)) * p.n_q_heads +
+                            kvh * G + (row_ok ? g % G : 0);
+#pragma unroll
+        for (int j = 0; j < KGROUPS; ++j) {
+            const uint4 a = row_ok ? *reinterpret_cast<const uint4*>(p.q + qrow * D + sl * SLICE + 32 * j + 8 * t)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            qb[2 * j][0] = a.x;
+            qb[2 * j][1] = a.y;
+            qb[2 * j + 1][0] = a.z;
+            qb[2 * j + 1][1] = a.w;
+        }
+    }
+    int qpos[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int r = 2 * t + i;
+        qpos[i] = r < R ? len - p.q_len + r / G : -1;
+    }
+
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[MTILES][4];                       // O^T: m-tile i = columns 16 g + 2 i, 16 g + 2 i + 1
+#pragma unroll
+    for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    const uint32_t ring = smem_u32(smem) + warp * STAGES * CHUNK_BYTES;
+    float4* xch = reinterpret_cast<float4*>(smem + RING_BYTES);
+
+    // copy plan: lane l fetches position l / 4 of the chunk; at step s it
+    // copies piece (l & 3) + 4 (s % 4) of that position's K slice (s < 4) or
+    // V slice (s >= 4): four lanes cover 64 contiguous bytes of a row
+    auto issue = [&](int k) {
+        if (k < my_chunks) {
+            const int pos = pb + (pg + GROUPS * k) * CPOS + (lane >> 2);
+            bool valid = pos < pe;
+            size_t row = 0;
+            if (valid) {
+                const int page = p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size];
+                if (page < 0 || page >= p.num_pages) {
+                    report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                    valid = false;
+                } else {
+                    row = (static_cast<size_t>(page) * p.page_size + (pos & (p.page_size - 1))) * p.n_kv_heads + kvh;
+                }
+            }
+            const uint8_t* ksrc = reinterpret_cast<const uint8_t*>(p.k_pages + row * D + sl * SLICE);
+            const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(p.v_pages + row * D + sl * SLICE);
+            const uint32_t st = ring + (k % STAGES) * CHUNK_BYTES;
+            const int r = lane >> 2;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int c = (lane & 3) + 4 * (s & 3);
+                const int f = s < 4 ? swz_k(r) : swz_v(r);
+                const uint32_t dst = st + (s >> 2) * (CPOS * ROW) + r * ROW + (((c + f) & 15) << 4);
+                mma8::cp_async16(dst, (s < 4 ? ksrc : vsrc) + c * 16, valid);
+            }
+        }
+        mma8::cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < STAGES - 1; ++k) issue(k);
+
+    for (int k = 0; k < my_chunks; ++k) {
+        issue(k + STAGES - 1);
+        mma8::cp_async_wait<STAGES - 1>();
+        __syncwarp();                         // every lane's copies of chunk k are visible
+        const uint8_t* kst = smem + (warp * STAGES + (k % STAGES)) * CHUNK_BYTES;
+        const uint8_t* vst = kst + CPOS * ROW;
+        const int pos0 = pb + (pg + GROUPS * k) * CPOS;
+
+        // ---- S^T slice = K_slice Q_slice^T over positions g (rows g + 8 are zero);
+        // one accumulator chain per 32 head-dim elements, summed at the end
+        float sc[2];
+        {
+            float acc[KGROUPS][4];
+#pragma unroll
+            for (int j = 0; j < KGROUPS; ++j) {
+                acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+                const uint4 ka = *reinterpret_cast<const uint4*>(kst + g * ROW + (((4 * j + t + swz_k(g)) & 15) << 4));
+                mma_bf16_16816(acc[j], {ka.x, 0u, ka.y, 0u}, qb[2 * j][0], qb[2 * j][1]);
+                mma_bf16_16816(acc[j], {ka.z, 0u, ka.w, 0u}, qb[2 * j + 1][0], qb[2 * j + 1][1]);
+            }
+            sc[0] = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
+            sc[1] = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
+        }
+        // ---- swap slices with the group's other warps: S = (S_0 + S_1) + (S_2 + S_3)
+        {
+            float2* base = reinterpret_cast<float2*>(xch) + ((k & 1) * GROUPS + pg) * SLICES * 32 + lane;
+            base[sl * 32] = make_float2(sc[0], sc[1]);
+            mma8::bar_group(1 + pg);
+            const float2 x0 = base[0], x1 = base[32], x2 = base[64], x3 = base[96];
+            sc[0] = (x0.x + x1.x) + (x2.x + x3.x);
+            sc[1] = (x0.y + x1.y) + (x2.y + x3.y);
+        }
+        // ---- online softmax: this thread holds position g of rows 2t, 2t + 1
+        float pr[2], cm[2], al[2], ps[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int kp = pos0 + g;
+            const bool sees = kp < pe && kp <= qpos[i] && (p.window <= 0 || kp > qpos[i] - p.window);
+            pr[i] = sees ? sc[i] * p.scale_log2 : -INFINITY;
+            cm[i] = pr[i];
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            const float x0 = __shfl_xor_sync(0xffffffffu, cm[0], off);
+            const float x1 = __shfl_xor_sync(0xffffffffu, cm[1], off);
+            cm[0] = fmaxf(cm[0], x0);
+            cm[1] = fmaxf(cm[1], x1);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float mn = fmaxf(m[i], cm[i]);
+            const float sh = mn == -INFINITY ? 0.f : mn;
+            al[i] = mn == -INFINITY ? 1.f : fast_exp2(m[i] - sh);
+            pr[i] = fast_exp2(pr[i] - sh);
+            ps[i] = pr[i];
+            m[i] = mn;
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            const float x0 = __shfl_xor_sync(0xffffffffu, ps[0], off);
+            const float x1 = __shfl_xor_sync(0xffffffffu, ps[1], off);
+            ps[0] += x0;
+            ps[1] += x1;
+        }
+        l[0] = l[0] * al[0] + ps[0];
+        l[1] = l[1] * al[1] + ps[1];
+        if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < MTILES; ++c) {
+                o[c][0] *= al[0];
+                o[c][1] *= al[1];
+                o[c][2] *= al[0];
+                o[c][3] *= al[1];
+            }
+        }
+        // ---- P^T fragment b0 = P[row g][pos 2t, 2t + 1] (bf16; b1, positions
+        // 2t + 8 and 2t + 9, is zero); P[r][q] sits in lane 4 q + r / 2, register r & 1
+        uint32_t pb0;
+        {
+            const int src0 = 4 * (2 * t) + (g >> 1), src1 = 4 * (2 * t + 1) + (g >> 1);
+            const float e00 = __shfl_sync(0xffffffffu, pr[0], src0), e01 = __shfl_sync(0xffffffffu, pr[1], src0);
+            const float e10 = __shfl_sync(0xffffffffu, pr[0], src1), e11 = __shfl_sync(0xffffffffu, pr[1], src1);
+            const bool odd = g & 1;
+            pb0 = pack_bf16x2(odd ? e01 : e00, odd ? e11 : e10);
+        }
+        // ---- O^T slice += V_slice^T P^T: thread g's columns are elements
+        // 16 g .. 16 g + 15 (bytes 32 g .. 32 g + 31) of rows 2t, 2t + 1;
+        // M rows g / g + 8 of m-tile i are columns 16 g + 2 i / + 1
+        uint32_t v0[8], v1[8];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const uint4 x = *reinterpret_cast<const uint4*>(vst + (2 * t) * ROW + (((2 * g + h2 + swz_v(2 * t)) & 15) << 4));
+            const uint4 y = *reinterpret_cast<const uint4*>(vst + (2 * t + 1) * ROW + (((2 * g + h2 + swz_v(2 * t + 1)) & 15) << 4));
+            v0[4 * h2 + 0] = x.x; v0[4 * h2 + 1] = x.y; v0[4 * h2 + 2] = x.z; v0[4 * h2 + 3] = x.w;
+            v1[4 * h2 + 0] = y.x; v1[4 * h2 + 1] = y.y; v1[4 * h2 + 2] = y.z; v1[4 * h2 + 3] = y.w;
+        }
+#pragma unroll
+        for (int i = 0; i < MTILES; ++i) {
+            // a0 = {V[2t][col 16g + 2i], V[2t + 1][same]}, a1 = the next column
+            const uint32_t a0 = prmt(v0[i], v1[i], 0x5410u);
+            const uint32_t a1 = prmt(v0[i], v1[i], 0x7632u);
+            mma_bf16_16816(o[i], {a0, a1, 0u, 0u}, pb0, 0u);
+        }
+        __syncwarp();                         // the stage may be refilled
+    }
+    mma8::cp_async_wait<0>();
+    __syncthreads();   // every warp is done with its ring: reuse it for the merge
+
+    float* so = reinterpret_cast<float*>(smem);
+    float* sml = so + WARPS * 8 * SLICE;
+#pragma unroll
+    for (int i = 0; i < MTILES; ++i) {
+        const int c0 = 16 * g + 2 * i, c1 = c0 + 1;
+        so[(warp * 8 + 2 * t) * SLICE + c0] = o[i][0];
+        so[(warp * 8 + 2 * t + 1) * SLICE + c0] = o[i][1];
+        so[(warp * 8 + 2 * t) * SLICE + c1] = o[i][2];
+        so[(warp * 8 + 2 * t + 1) * SLICE + c1] = o[i][3];
+    }
+    if (g == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            sml[(warp * 8 + 2 * t + i) * 2] = m[i];
+            sml[(warp * 8 + 2 * t + i) * 2 + 1] = l[i];
+        }
+    }
+    __syncthreads();
+    const size_t S = static_cast<size_t>(p.num_splits);
+    for (int idx = threadIdx.x; idx < R * D; idx += WARPS * 32) {
+        const int r = idx / D, d = idx - r * D;
+        const int h = d / SLICE, c = d - h * SLICE;
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < GROUPS; ++q) M = fmaxf(M, sml[((h * GROUPS + q) * 8 + r) * 2]);
+        float acc = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int q = 0; q < GROUPS; ++q) {
+                const int w = h * GROUPS + q;
+                const float wt = fast_exp2(sml[(w * 8 + r) * 2] - M);
+                acc += wt * so[(w * 8 + r) * SLICE + c];
+                L += wt * sml[(w * 8 + r) * 2 + 1];
+            }
+        }
+        const size_t hq = (static_cast<size_t>(b) * p.q_len + r / G) * p.n_q_heads + kvh * G + r % G;
+        p.ws_o[(hq * S + split) * D + d] = acc;
+        if (d == 0) {
+            p.ws_ml[(hq * S + split) * 2 + 0] = M;
+            p.ws_ml[(hq * S + split) * 2 + 1] = M == -INFINITY ? 0.f : L;
+        }
+    }
+}
+
+}  // namespace mma16
+
+
 
 // One block per (sequence, query token, query head): merges the splits' (O, m, l).
 __global__ void __launch_bounds__(128)
@@ -1161,6 +1447,16 @@ static cudaError_t launch_stream(const DecodeParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+static cudaError_t launch_bf16_mma(const DecodeParams& p, cudaStream_t stream) {
+    const int smem = decode::mma16::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(decode::mma16::decode_bf16_mma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.num_splits, p.n_kv_heads, p.batch);
+    decode::mma16::decode_bf16_mma_kernel<<<grid, decode::mma8::WARPS * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 static cudaError_t launch_fp8_mma(const DecodeParams& p, cudaStream_t stream) {
     const int smem = decode::mma8::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(decode::mma8::decode_fp8_mma_kernel,
@@ -1181,6 +1477,8 @@ static cudaError_t launch_split_and_merge(const CUtensorMap& tmk, const CUtensor
         e = launch_stream<1>(p, stream);
     } else if (!FP8 && p.q_len == 1 && p.group == 2) {
         e = launch_stream<2>(p, stream);
+    } else if (!FP8 && p.q_len * p.group <= 8) {
+        e = launch_bf16_mma(p, stream);
     } else {
         // larger query groups or several tokens: S and PV on the tensor cores
         // (q_len * G rows padded to 16)
