@@ -1436,6 +1436,8 @@ int decode_fp8_box_bytes() { return decode::F8_BOX_BYTES; }
 
 int decode_tile_positions() { return decode::TILE_K; }
 
+constexpr int TILE_POSITIONS = decode::TILE_K;
+
 template <int G>
 static cudaError_t launch_stream(const DecodeParams& p, cudaStream_t stream) {
     const int smem = decode::stream::RING_BYTES;
@@ -1473,10 +1475,10 @@ static cudaError_t launch_split_and_merge(const CUtensorMap& tmk, const CUtensor
     cudaError_t e;
     if (FP8 && p.q_len * p.group <= 8) {
         e = launch_fp8_mma(p, stream);
-    } else if (!FP8 && p.q_len == 1 && p.group == 1) {
-        e = launch_stream<1>(p, stream);
-    } else if (!FP8 && p.q_len == 1 && p.group == 2) {
-        e = launch_stream<2>(p, stream);
+    } else if (!FP8 && p.q_len == 1 && p.group <= 2 && p.tiles_per_split * TILE_POSITIONS < 1024) {
+        // short splits (small batches): the FMA streaming kernel's lighter
+        // set-up wins; from 1024 positions a split on, the tensor-core one
+        e = p.group == 1 ? launch_stream<1>(p, stream) : launch_stream<2>(p, stream);
     } else if (!FP8 && p.q_len * p.group <= 8) {
         e = launch_bf16_mma(p, stream);
     } else {
