@@ -315,6 +315,9 @@ def time_decode_fp8(args, fa, g, dev, stream, shapes, flush, world, peaks):
             "value": gbs, "unit": "GB/s", "ms": sum(ms), "bytes_per_step": total_bytes,
             "frac_of_measured_hbm": gbs / world / peaks["hbm_gbs"],
             "kernel": "fa512::decode::mma8::decode_fp8_mma_kernel + merge",
+            "traffic_b64_kv28672": recorded_traffic(
+                "decode_fp8_mma_kernel", source_digest(["decode_sm103.cu", "fa512_device.cuh",
+                                                        "fa512_internal.h"])),
             "l2": "flushed before every step (each shape called once per step)",
             "per_shape": per}
 
@@ -454,9 +457,9 @@ def run_ours(args):
                            "achieved": dec_gbs / world, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": dec_gbs / world / peaks["hbm_gbs"],
                            "frac_of_8000": dec_gbs / world / 8000.0,
-                           # DRAM bytes of the largest shape's split kernel (b64 x kv28672:
-                           # q_len 1 and two query heads per KV head run the streaming kernel)
-                           "traffic": recorded_traffic("decode_stream_kernel", dec_src),
+                           # DRAM bytes of the largest shape's split kernel (b64 x kv28672
+                           # runs the tensor-core streaming kernel)
+                           "traffic": recorded_traffic("decode_bf16_mma_kernel", dec_src),
                            "traffic_shape": "b64_kv28672",
                            "src": dec_src, "per_shape": per}
 
