@@ -706,9 +706,10 @@ decode_stream_kernel(const DecodeParams p) {
 // slots per position than HBM takes to deliver it, so here the products run
 // on mma.sync (f16 operands, fp32 accumulation) with the query rows in the N
 // dimension: S^T = K Q^T (M = 16 positions, K = head dims) and O^T = V^T P^T
-// (M = 16 head-dim columns, K = 16 positions).  E4M3 -> f16 is exact: K through
-// the hardware e4m3x2 -> f16x2 conversion, V through an integer form (below)
-// that assembles each operand pair from two positions in one byte permute.
+// (M = 16 head-dim columns, K = 16 positions).  E4M3 -> f16 is exact, through
+// the hardware e4m3x2 -> f16x2 conversion: a K operand pair is two
+// neighbouring bytes of one row, a V pair two positions' bytes of one column,
+// gathered by one byte permute.
 //
 // Sixteen warps = four position groups x four head-dim slices of 128.  The
 // four warps of a group (same positions, one slice each) stream chunks of 16
@@ -725,7 +726,6 @@ constexpr int SLICES = 4;                        // head-dim slices
 constexpr int WARPS = GROUPS * SLICES;
 constexpr int CPOS = 16;                         // positions per chunk
 constexpr int SLICE = D / SLICES;                // head-dim bytes (elements) per warp: 128
-constexpr int PIECES = SLICE / 16;               // 16-byte pieces per row: 8
 constexpr int KSTEPS = SLICE / 16;               // k-steps of 16 per slice: 8
 constexpr int MTILES = SLICE / 16;               // m-tiles of 16 columns per slice: 8
 constexpr int STAGES = 3;
@@ -771,21 +771,14 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
     return h2;
 }
 
-// Byte k of word x and byte k of word y -> f16x2 {x_k, y_k} times 2^-8,
-// exactly.  An E4M3 byte s.eeee.mmm placed as f16 bits s at 15 and
-// eeee.mmm at 13..7 is the f16 number 2^(e-15) (1 + m/8) (e >= 1) or the
-// subnormal (m/8) 2^-14 (e = 0, zero included): the E4M3 value times 2^-8.
-// One permute puts [sign(y_k)][y_k][sign(x_k)][x_k] in the four bytes (the
-// selector's bit 3 replicates a byte's sign bit), a shift by 7 moves each
-// byte's sign copy to bit 15 / 31 and its eeee.mmm to 13..7 / 29..23, and
-// the mask clears what the shift carried in.  (The E4M3 NaN code would read
-// as 480: codes are read only inside the live band.)
+// Byte k of word x and byte k of word y -> f16x2 {x_k, y_k}, exactly: one
+// permute gathers the two bytes, the hardware conversion widens them.
 template <int K>
-__device__ __forceinline__ uint32_t e4m3_pair_f16x2_scaled(uint32_t x, uint32_t y) {
-    constexpr uint32_t sel = K | ((8 | K) << 4) | ((4 + K) << 8) | ((12 + K) << 12);
+__device__ __forceinline__ uint32_t e4m3_pair_f16x2(uint32_t x, uint32_t y) {
+    constexpr uint32_t sel = K | ((4 + K) << 4);
     uint32_t t;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(y), "n"(sel));
-    return (t << 7) & 0xbf80bf80u;
+    return e4m3x2_f16x2(t & 0xffffu);
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -1036,15 +1029,15 @@ decode_fp8_mma_kernel(const DecodeParams p) {
             const int wi = i >> 1;
             uint32_t a0, a1, a2, a3;
             if (i & 1) {
-                a0 = e4m3_pair_f16x2_scaled<2>(vw[0][wi], vw[1][wi]);
-                a1 = e4m3_pair_f16x2_scaled<3>(vw[0][wi], vw[1][wi]);
-                a2 = e4m3_pair_f16x2_scaled<2>(vw[2][wi], vw[3][wi]);
-                a3 = e4m3_pair_f16x2_scaled<3>(vw[2][wi], vw[3][wi]);
+                a0 = e4m3_pair_f16x2<2>(vw[0][wi], vw[1][wi]);
+                a1 = e4m3_pair_f16x2<3>(vw[0][wi], vw[1][wi]);
+                a2 = e4m3_pair_f16x2<2>(vw[2][wi], vw[3][wi]);
+                a3 = e4m3_pair_f16x2<3>(vw[2][wi], vw[3][wi]);
             } else {
-                a0 = e4m3_pair_f16x2_scaled<0>(vw[0][wi], vw[1][wi]);
-                a1 = e4m3_pair_f16x2_scaled<1>(vw[0][wi], vw[1][wi]);
-                a2 = e4m3_pair_f16x2_scaled<0>(vw[2][wi], vw[3][wi]);
-                a3 = e4m3_pair_f16x2_scaled<1>(vw[2][wi], vw[3][wi]);
+                a0 = e4m3_pair_f16x2<0>(vw[0][wi], vw[1][wi]);
+                a1 = e4m3_pair_f16x2<1>(vw[0][wi], vw[1][wi]);
+                a2 = e4m3_pair_f16x2<0>(vw[2][wi], vw[3][wi]);
+                a3 = e4m3_pair_f16x2<1>(vw[2][wi], vw[3][wi]);
             }
             mma_f16_16816(o[i], a0, a1, a2, a3, pb0, pb1);
         }
@@ -1058,8 +1051,7 @@ decode_fp8_mma_kernel(const DecodeParams p) {
     // g + 8) -> smem [warp][row 8][128], m and l [warp][row][2]
     float* so = reinterpret_cast<float*>(smem);
     float* sml = so + WARPS * 8 * SLICE;
-    // the V operand carried 2^-8: undo it with the value scale
-    const float osc = p.o_scale * 256.f;
+    const float osc = p.o_scale;              // v_scale of the FP8 cache
 #pragma unroll
     for (int i = 0; i < MTILES; ++i) {
         const int c0 = 16 * g + 2 * i, c1 = c0 + 1;
