@@ -174,3 +174,39 @@ def test_prefill_d256_rejects_bad_arguments_before_any_launch(lib):
     assert call(scale=float("nan")) == 1
     assert call(hq=256, hk=1) == 2
     assert call(sq=0, q=None) == 0
+
+
+def _decode_fp8(lib, **kw):
+    a = dict(q=16, kp=16, vp=16, pt=16, kl=16, out=16, lse=None, b=2, ql=1, hq=8, hk=4, ps=64,
+             npages=10, mpps=4, maxlen=200, scale=0.05, ks=0.03, vs=0.04, window=0, splits=0,
+             ws=256, wsb=1 << 30)
+    a.update(kw)
+    return lib.fa512_decode_paged_fp8(a["q"], a["kp"], a["vp"], a["pt"], a["kl"], a["out"],
+                                      a["lse"], a["b"], a["ql"], a["hq"], a["hk"], a["ps"],
+                                      a["npages"], a["mpps"], a["maxlen"], a["scale"], a["ks"],
+                                      a["vs"], a["window"], a["splits"], a["ws"], a["wsb"], None)
+
+
+def test_fp8_decode_rejects_bad_arguments_before_any_launch(lib):
+    inf, nan = float("inf"), float("nan")
+    assert _decode_fp8(lib, ks=inf) == 1             # scales must be finite
+    assert _decode_fp8(lib, vs=nan) == 1
+    assert _decode_fp8(lib, scale=nan) == 1
+    assert _decode_fp8(lib, ql=0) == 1
+    assert _decode_fp8(lib, ql=9, hq=8, hk=4) == 2   # 18 rows > 16
+    assert _decode_fp8(lib, ps=48) == 2
+    assert _decode_fp8(lib, maxlen=300) == 1         # beyond the page table
+    assert _decode_fp8(lib, ws=None) == 5
+    assert _decode_fp8(lib, wsb=16) == 5
+    assert _decode_fp8(lib, kp=8) == 1               # pages not 16-byte aligned
+    assert _decode_fp8(lib, b=0, q=None) == 0        # empty batch: no-op
+    assert _decode_fp8(lib, ks=inf) == 1 and b"finite" in lib.fa512_last_error_message()
+
+
+def test_fp8_binding_rejects_a_bf16_cache_before_the_library():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros((1, 8, 512), dtype=torch.bfloat16)
+    pages = torch.zeros((1, 64, 4, 512), dtype=torch.bfloat16)
+    with pytest.raises(fa.Fa512Error):
+        fa.fa512_decode_paged_fp8(q, pages, pages, torch.zeros((1, 1), dtype=torch.int32),
+                                  torch.ones(1, dtype=torch.int32))
