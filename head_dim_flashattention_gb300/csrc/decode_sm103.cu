@@ -987,13 +987,8 @@ decode_fp8_mma_kernel(const DecodeParams p) {
             ps[i] = pr[i] + pr[2 + i];
             m[i] = mn;
         }
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            const float x0 = __shfl_xor_sync(0xffffffffu, ps[0], off);
-            const float x1 = __shfl_xor_sync(0xffffffffu, ps[1], off);
-            ps[0] += x0;
-            ps[1] += x1;
-        }
+        // l stays a per-lane partial (every lane of a row rescales by the
+        // same alpha); the lanes are summed once, after the last chunk
         l[0] = l[0] * al[0] + ps[0];
         l[1] = l[1] * al[1] + ps[1];
         if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
@@ -1044,6 +1039,10 @@ decode_fp8_mma_kernel(const DecodeParams p) {
         __syncwarp();                         // the stage may be refilled
     }
     cp_async_wait<0>();
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) l[i] += __shfl_xor_sync(0xffffffffu, l[i], off);
     __syncthreads();   // every warp is done with its ring: reuse it for the merge
 
     // ---- merge the four position groups: O^T rows 2t, 2t + 1 of slice
@@ -1284,13 +1283,8 @@ decode_bf16_mma_kernel(const DecodeParams p) {
             ps[i] = pr[i];
             m[i] = mn;
         }
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            const float x0 = __shfl_xor_sync(0xffffffffu, ps[0], off);
-            const float x1 = __shfl_xor_sync(0xffffffffu, ps[1], off);
-            ps[0] += x0;
-            ps[1] += x1;
-        }
+        // l stays a per-lane partial (every lane of a row rescales by the
+        // same alpha); the lanes are summed once, after the last chunk
         l[0] = l[0] * al[0] + ps[0];
         l[1] = l[1] * al[1] + ps[1];
         if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
@@ -1335,6 +1329,10 @@ decode_bf16_mma_kernel(const DecodeParams p) {
         __syncwarp();                         // the stage may be refilled
     }
     mma8::cp_async_wait<0>();
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) l[i] += __shfl_xor_sync(0xffffffffu, l[i], off);
     __syncthreads();   // every warp is done with its ring: reuse it for the merge
 
     float* so = reinterpret_cast<float*>(smem);
