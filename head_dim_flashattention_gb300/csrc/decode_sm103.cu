@@ -7,17 +7,25 @@
 // walk absolute positions, read only the live band [max(0, len - window),
 // len), keep K/V tiles double-buffered and rescale once per tile.
 // vllm-project/flash-attention PR #199, "Performance": the cache is paged
-// (page size 64), 8 query heads over 4 KV heads, q_len 1.
+// (page size 64), 8 query heads over 4 KV heads, q_len 1; "Summary": the
+// cache may be stored in FP8 E4M3.
 //
-// Work item = (split, KV head, sequence).  One CTA streams its split's key
-// tiles of TILE_K = 32 positions through a NUM_STAGES-deep ring in shared
-// memory filled by TMA (one 64-column box per page run), computes
-// S = Q K^T and O += P V for the G query heads of its KV head with bf16
-// mma.sync (rows padded to 16), and keeps the softmax state in the log2
-// domain.  HBM traffic per position and KV head: 1 KiB of K + 1 KiB of V.
-// With q_len query tokens per sequence (the last q_len positions of its
-// cache) the rows are (token, head) pairs, q_len * G <= 16, each masked at
-// its own position.
+// Work item = (split, KV head, sequence); the rows of a work item are the
+// (token, head) pairs of the KV head's query group, q_len * G <= 16, each
+// masked at its own position (the last q_len positions of the cache).  Which
+// kernel runs:
+//   decode_stream_kernel<G>   one token, G <= 2, splits shorter than 1,024
+//                             positions (bf16): FMA streaming warps;
+//   decode_bf16_mma_kernel    up to 8 rows otherwise (bf16): streaming warps
+//                             on mma.sync with the rows in N;
+//   decode_fp8_mma_kernel     up to 8 rows over an FP8 cache: the same design
+//                             with every byte widened exactly to f16;
+//   decode_split_kernel<FP8>  9 to 16 rows: a CTA's warps share TMA-loaded
+//                             tiles of 32 positions (FP8 tiles converted
+//                             exactly to bf16), S and PV on mma.sync;
+//   decode_merge_kernel       combines the splits' (O, m, l) partials.
+// HBM traffic per position and KV head: 1 KiB of K + 1 KiB of V (bf16) or
+// 512 + 512 bytes (FP8).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -177,6 +185,10 @@ __device__ __forceinline__ void convert_fp8_stage(const uint8_t* stage, uint8_t*
     }
 }
 
+// One CTA streams its split's key tiles of TILE_K = 32 positions through a
+// NUM_STAGES-deep ring in shared memory filled by TMA (one box per page run),
+// computes S = Q K^T and O += P V for its rows with bf16 mma.sync (rows padded
+// to 16), and keeps the softmax state in the log2 domain.
 template <bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
