@@ -981,12 +981,19 @@ decode_fp8_mma_kernel(const DecodeParams p) {
             sv[i][1] = sees(pos0 + g + 8) ? sc[2 + i] * p.scale_log2 : -INFINITY;
             cm[i] = fmaxf(sv[i][0], sv[i][1]);
         }
+        // the chunk maxima of both rows in one packed bf16x2 reduction: the
+        // running max is only the softmax's reference and needs to be the
+        // same in every lane of a row, not exact (bf16 keeps fp32's range;
+        // rounding moves it by < 0.4 %, so p stays below 2^(0.004 |s|))
+        {
+            uint32_t c2 = pack_bf16x2(cm[0], cm[1]);
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            const float x0 = __shfl_xor_sync(0xffffffffu, cm[0], off);
-            const float x1 = __shfl_xor_sync(0xffffffffu, cm[1], off);
-            cm[0] = fmaxf(cm[0], x0);
-            cm[1] = fmaxf(cm[1], x1);
+            for (int off = 4; off < 32; off <<= 1) {
+                const uint32_t x = __shfl_xor_sync(0xffffffffu, c2, off);
+                asm("max.bf16x2 %0, %0, %1;" : "+r"(c2) : "r"(x));
+            }
+            cm[0] = __uint_as_float(c2 << 16);
+            cm[1] = __uint_as_float(c2 & 0xffff0000u);
         }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
