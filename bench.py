@@ -14,6 +14,16 @@ pairs) / prefill time (the FLOP convention that reproduces the 131 TFLOP the
 RTX PRO 6000 page states for 10 global layers of a 19,985-token prompt).
 Decode is reported as HBM GB/s of live K/V bytes.
 
+Further legs, each timed on its own with L2 flushed before every call (keys
+of the JSON line): `e2e` (the prefill with its inputs copied in from pinned
+host memory and its outputs copied back every step), `prefill_paged` (the
+chunked config and a mixed batch through a paged cache), `local256` (head dim
+256 under a 1,024-key window), `decode_fp8` (the nine decode shapes over an
+FP8 E4M3 cache), `decode_q` (4 query tokens per sequence, batch 64 x kv
+16384), `cpu_baseline` (the fp64 oracle on a bounded row sample).  The
+`roofline` objects carry DRAM traffic per launch from `profiles/
+dram_traffic.txt` when it was captured on the current source.
+
 `--impl reference` times the fp64 CPU oracle on a bounded row sample of the
 same workload (the reference arm of this benchmark).
 """
