@@ -54,3 +54,34 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_decode_bytes_fp8_cache_is_half_the_kv_bytes():
+    b, n, hq, hk = 64, 28672, 8, 4
+    kv16 = b * n * hk * 512 * 2 * 2
+    kv8 = b * n * hk * 512 * 1 * 2
+    other = bench.decode_bytes(b, n, hq, hk) - kv16
+    assert bench.decode_bytes(b, n, hq, hk, kv_elem_bytes=1) == kv8 + other
+    # several tokens add their q / out / lse rows, not K/V bytes
+    assert (bench.decode_bytes(b, n, hq, hk, q_len=4) - bench.decode_bytes(b, n, hq, hk)
+            == 3 * (b * hq * 512 * 2 * 2 + b * hq * 4))
+
+
+def test_recorded_traffic_needs_the_current_source_digest():
+    dec = bench.source_digest(["decode_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
+    pf = bench.source_digest(["prefill_sm103.cu", "fa512_pair.cuh", "fa512_device.cuh",
+                              "fa512_internal.h"])
+    # a stale digest finds nothing; an unknown kernel finds nothing
+    assert bench.recorded_traffic("decode_bf16_mma_kernel", "0" * 16) is None
+    assert bench.recorded_traffic("no_such_kernel", dec) is None
+    # a record taken on the current source holds at least the algorithmic
+    # bytes of the shape it names (a source edited since has no record: None)
+    pf_bytes = bench.recorded_traffic("prefill_kernel", pf)
+    d_bytes = bench.recorded_traffic("decode_bf16_mma_kernel", dec)
+    f_bytes = bench.recorded_traffic("decode_fp8_mma_kernel", dec)
+    if pf_bytes is not None:
+        assert pf_bytes >= 0.9 * 8192 * 32 * 512 * 2 * 2    # Q and O of the chunked config
+    if d_bytes is not None:
+        assert d_bytes >= 64 * 28672 * 4 * 512 * 2 * 2
+    if f_bytes is not None:
+        assert f_bytes >= 64 * 28672 * 4 * 512 * 2
