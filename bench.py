@@ -20,7 +20,13 @@ host memory and its outputs copied back every step), `prefill_paged` (the
 chunked config and a mixed batch through a paged cache), `local256` (head dim
 256 under a 1,024-key window), `decode_fp8` (the nine decode shapes over an
 FP8 E4M3 cache), `decode_q` (4 query tokens per sequence, batch 64 x kv
-16384), `cpu_baseline` (the fp64 oracle on a bounded row sample).  The
+16384), `prefill_full`, `prefill_full_stress` (20480 x 20480 causal, 32/4
+heads; the stress variant multiplies every 64th key row by 8) and
+`prefill_mqa` (49152 x 49152 causal, 16 query heads over 1 KV head), each
+with its own `roofline`; `cpu_baseline` (the fp64 oracle on a bounded row
+sample of the chunked config, and under `plan` the oracle in full on the
+tiny and batch-1 decode configs and per-row on stratified samples of the
+large configs, with a labelled extrapolation).  The
 `roofline` objects carry DRAM traffic per launch from `profiles/
 dram_traffic.txt` when it was captured on the current source.
 
@@ -38,6 +44,8 @@ import subprocess
 import sys
 import tempfile
 import time
+
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -57,6 +65,15 @@ PAGE = 64
 FP8_SCALES = (1 / 32, 1 / 32)
 # the sliding-window local layers: heads of 256 dimensions over the last 1,024 tokens
 LOCAL256 = {"seqlen": 20480, "window": 1024, "n_q_heads": 32, "n_kv_heads": 4}
+# the large prefill configs, each timed as a leg of its own
+PREFILL_LEGS = {
+    "prefill_full": dict(seqlen_q=20480, seqlen_k=20480, q_offset=0, n_q_heads=32, n_kv_heads=4,
+                         stress=False),
+    "prefill_full_stress": dict(seqlen_q=20480, seqlen_k=20480, q_offset=0, n_q_heads=32,
+                                n_kv_heads=4, stress=True),
+    "prefill_mqa": dict(seqlen_q=49152, seqlen_k=49152, q_offset=0, n_q_heads=16, n_kv_heads=1,
+                        stress=False),
+}
 PAGED_PREFILL = {
     "chunked": [(8192, 16384)],
     "varlen": [(8192, 8192), (4096, 12288), (2048, 20480), (1024, 1024), (3000, 7000)],
@@ -213,10 +230,30 @@ class ClockSampler:
 _ORACLE_INPUTS = {}
 
 
+def _stratified_rows(seqlen_q: int, q_offset: int, tokens_per_tile: int, stress: bool,
+                     budget: int) -> list:
+    """A bounded stratified row sample: the first and last rows, rows on both
+    sides of q-tile boundaries near the start, middle and end, the rows just
+    after two stressed keys (stress variant), and evenly spaced rows up to
+    `budget` rows in all."""
+    n = seqlen_q
+    rows = {0, 1, n - 2, n - 1}
+    for t in (tokens_per_tile, (n // (2 * tokens_per_tile)) * tokens_per_tile,
+              (n // tokens_per_tile - 1) * tokens_per_tile):
+        rows.update(x for x in (t - 1, t) if 0 <= x < n)
+    if stress:
+        for j in (64 * 3, 64 * (n // 128)):
+            i = j - q_offset
+            rows.update(x for x in (i, i + 1) if 0 <= x < n)
+    spare = max(0, budget - len(rows))
+    if spare:
+        rows.update(int(x) for x in np.linspace(0, n - 1, spare + 2)[1:-1])
+    return sorted(rows)
+
+
 def oracle_sample(budget_rows: int = 24, decode_batch: int = 1, decode_len: int = 4096):
-    """Times the fp64 oracle on a bounded sample of the same workload.
-    Returns (flops, seconds, threads, description)."""
-    import numpy as np  # noqa: F401
+    """Times the fp64 oracle on a bounded sample of the chunked prefill
+    workload.  Returns (flops, seconds, threads, description)."""
     import oracle
     from head_dim_flashattention_gb300 import workloads
 
@@ -234,6 +271,76 @@ def oracle_sample(budget_rows: int = 24, decode_batch: int = 1, decode_len: int 
     desc = ("oracle_prefill on %d evenly spaced query rows (all 32 heads) of the chunked "
             "config: %.3g GFLOP" % (len(rows), flops / 1e9))
     return flops, dt, threads, desc
+
+
+def oracle_plan(rows_per_config: int = 16):
+    """The fp64 oracle on the host cores, as the CPU baseline plan asks:
+    in full on the tiny prefill config and on the batch-1 decode configs;
+    on a stratified row sample of the chunked, full (and stress) and MQA
+    prefill configs, as seconds per row and a labelled extrapolation to the
+    whole config (the cost of a row grows with its visible keys)."""
+    import torch
+
+    import oracle
+    from head_dim_flashattention_gb300 import workloads
+
+    threads = oracle.default_threads()
+    res = {"cores": threads, "kind": "oracle"}
+    # tiny prefill in full
+    cfg = workloads.PREFILL_CONFIGS["tiny"]
+    q, k, v = workloads.prefill_inputs(cfg)
+    t0 = time.perf_counter()
+    oracle.prefill(q, k, v, q_offset=cfg.q_offset, scale=cfg.scale, causal=cfg.causal,
+                   threads=threads)
+    dt = time.perf_counter() - t0
+    fl = prefill_flops(cfg.seqlen_q, cfg.seqlen_k, cfg.q_offset, cfg.n_q_heads)
+    res["tiny_full"] = {"seconds": dt, "TFLOP/s": fl / dt / 1e12, "flops": fl,
+                        "what": "tiny prefill 256x256, 8/1 heads, every row (full config)"}
+    # batch-1 decode configs in full (GB/s of live K/V, as the GPU leg)
+    dec = {}
+    for n in (4096, 16384, 28672):
+        dc = workloads.DECODE_CONFIGS["b1_kv%d" % n]
+        pc = workloads.decode_inputs(dc)
+        t0 = time.perf_counter()
+        oracle.decode_paged(pc.q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
+                            threads=threads)
+        dt = time.perf_counter() - t0
+        by = decode_bytes(1, n, dc.n_q_heads, dc.n_kv_heads)
+        dec["b1_kv%d" % n] = {"seconds": dt, "GB/s": by / dt / 1e9, "bytes": by}
+    res["decode_full"] = dec
+    # large prefill configs: stratified rows, seconds per row, extrapolation
+    big = {}
+    for name, cname in (("chunked", "chunked"), ("full", "full"), ("full_stress", "full_stress"),
+                        ("mqa", "mqa")):
+        c = workloads.PREFILL_CONFIGS[cname]
+        g = c.n_q_heads // c.n_kv_heads
+        rows = _stratified_rows(c.seqlen_q, c.q_offset, 128 // g, c.stress, rows_per_config)
+        # Q only for the sampled rows (the same distribution); every key
+        qs = workloads.randn_bf16((len(rows), c.n_q_heads, HEAD_DIM), c.seed * 3 + 7)
+        key = ("kv", c.seqlen_k, c.n_kv_heads, c.stress)
+        if key not in _ORACLE_INPUTS:
+            kk = workloads.randn_bf16((c.seqlen_k, c.n_kv_heads, HEAD_DIM), c.seed * 3 + 1)
+            vv = workloads.randn_bf16((c.seqlen_k, c.n_kv_heads, HEAD_DIM), c.seed * 3 + 2)
+            if c.stress:
+                kk[::64] *= 8
+            _ORACLE_INPUTS[key] = (kk, vv)
+        kk, vv = _ORACLE_INPUTS[key]
+        t0 = time.perf_counter()
+        for i, r in enumerate(rows):
+            oracle.prefill(qs[i:i + 1], kk, vv, q_offset=c.q_offset + r, scale=c.scale,
+                           causal=True, threads=threads)
+        dt = time.perf_counter() - t0
+        fl_sample = sum(4 * HEAD_DIM * c.n_q_heads * min(c.seqlen_k, c.q_offset + r + 1)
+                        for r in rows)
+        fl_all = prefill_flops(c.seqlen_q, c.seqlen_k, c.q_offset, c.n_q_heads)
+        big[name] = {"rows": len(rows), "seconds": dt, "seconds_per_row": dt / len(rows),
+                     "TFLOP/s": fl_sample / dt / 1e12,
+                     "extrapolated_seconds_whole_config": dt * fl_all / fl_sample,
+                     "extrapolation": "measured seconds x (config FLOP / sample FLOP); "
+                                      "not measured"}
+        del qs
+    res["prefill_sampled"] = big
+    return res
 
 
 def run_reference(args):
@@ -631,6 +738,60 @@ def run_ours(args):
         del lq, lk, lv, lout
         assert fa.fa512_device_status() == 0
 
+    # ---- the full and MQA prefill configs (and the stress variant), each
+    # timed on its own: one call per step, L2 flushed before every call
+    prefill_legs = {}
+    if not args.no_prefill and not args.no_big:
+        for name, L in PREFILL_LEGS.items():
+            if args.only_big and name not in args.only_big.split(","):
+                continue
+            bq = torch.randn((L["seqlen_q"], L["n_q_heads"], HEAD_DIM), generator=g, device=dev,
+                             dtype=torch.float32).to(torch.bfloat16)
+            bk = torch.randn((L["seqlen_k"], L["n_kv_heads"], HEAD_DIM), generator=g, device=dev,
+                             dtype=torch.float32).to(torch.bfloat16)
+            bv = torch.randn(bk.shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            if L["stress"]:
+                bk[::64] *= 8          # every 64th key row x8 (exact in bf16)
+            bout = torch.empty_like(bq)
+            blse = torch.empty((L["n_q_heads"], L["seqlen_q"]), dtype=torch.float32, device=dev)
+            flops = prefill_flops(L["seqlen_q"], L["seqlen_k"], L["q_offset"], L["n_q_heads"])
+
+            def b_call():
+                fa.fa512_prefill(bq, bk, bv, bout, blse, q_offset=L["q_offset"], causal=True,
+                                 stream=stream)
+
+            for _ in range(max(3, args.warmup)):
+                flush.zero_()
+                b_call()
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for e0, e1 in evs:
+                flush.zero_()
+                e0.record(stream)
+                b_call()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            (t_b,) = max_over_ranks([sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3], dev)
+            tf = job_rate(flops, args.steps, world, t_b) / 1e12
+            ach = flops / (t_b / args.steps) / 1e12
+            prefill_legs[name] = {
+                "workload": "%d x %d causal prefill, %d/%d heads, d512, bf16 N(0,1)%s"
+                            % (L["seqlen_q"], L["seqlen_k"], L["n_q_heads"], L["n_kv_heads"],
+                               "; every 64th K row x8" if L["stress"] else ""),
+                "value": tf, "unit": "TFLOP/s", "ms": t_b / args.steps * 1e3,
+                "flops_per_call": flops,
+                "target_ms_at_50pct_of_measured_burst": flops / (0.5 * peaks["bf16_tflops"] * 1e12) * 1e3,
+                "roofline": {"kernel": "fa512::prefill::prefill_kernel", "bound": "tensor",
+                             "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": ach / peaks["bf16_tflops"],
+                             "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
+                             "peak_kind": "%s burst bf16 (MEASURED_PEAKS.json)" % peak_kind,
+                             "traffic": recorded_traffic("prefill_kernel_" + name, pf_src)},
+                "l2": "flushed before every call"}
+            del bq, bk, bv, bout, blse
+        assert fa.fa512_device_status() == 0
+
     # ---- the decode shapes over an FP8 E4M3 cache, timed on their own
     decode_fp8 = None
     if not args.no_decode and not args.no_fp8:
@@ -688,7 +849,7 @@ def run_ours(args):
     if rank == 0 and world >= 1 and not args.no_cpu:
         f, dt, threads, desc = oracle_sample(budget_rows=args.ref_rows)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": desc, "seconds": dt}
+               "sample": desc, "seconds": dt, "plan": oracle_plan()}
 
     if rank == 0:
         line = {
@@ -708,6 +869,9 @@ def run_ours(args):
             "decode_fp8": decode_fp8,
             "prefill_paged": prefill_paged,
             "local256": local256,
+            "prefill_full": prefill_legs.get("prefill_full"),
+            "prefill_full_stress": prefill_legs.get("prefill_full_stress"),
+            "prefill_mqa": prefill_legs.get("prefill_mqa"),
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": ((0 if args.no_prefill else 1) + 2 * len(dec)) * args.steps,
@@ -735,6 +899,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-paged", action="store_true", help="skip the paged-prefill legs")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-cache decode leg")
+    ap.add_argument("--no-big", action="store_true",
+                    help="skip the full (20480^2, + stress) and MQA (49152^2) prefill legs")
+    ap.add_argument("--only-big", default="",
+                    help="comma list of big prefill legs to run (profiling), e.g. prefill_mqa")
     ap.add_argument("--decode-q-batch", type=int, default=None,
                     help="batch of the several-token decode leg (default 64; profiling a smaller case)")
     ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling)")

@@ -9,6 +9,7 @@ from ._binding import (  # noqa: F401
     Fa512Error,
     fa512_decode_auto_splits,
     fa512_decode_paged,
+    fa512_decode_paged_noalloc,
     fa512_decode_paged_fp8,
     fa512_decode_paged_q,
     fa512_decode_workspace_bytes,

@@ -63,6 +63,9 @@ def load_library():
         lib.fa512_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I,
                                            P, Z, P]
         lib.fa512_decode_paged.restype = I
+        lib.fa512_decode_paged_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I,
+                                                   I, P]
+        lib.fa512_decode_paged_noalloc.restype = I
         lib.fa512_decode_workspace_bytes.argtypes = [I, I, I, I, I, I]
         lib.fa512_decode_workspace_bytes.restype = Z
         lib.fa512_decode_paged_q.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I,
@@ -266,6 +269,35 @@ def fa512_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Te
         _dptr(lse, "lse", torch.float32), bsz, hq, hk, psz, npages, mpps, int(max_kv_len),
         float(scale), int(window), int(num_splits), _dptr(workspace, "workspace"), ws_bytes,
         _stream(stream)))
+    return out, lse
+
+
+def fa512_decode_paged_noalloc(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                               page_table: torch.Tensor, kv_lens: torch.Tensor,
+                               out: torch.Tensor, lse: torch.Tensor | None = None, *,
+                               max_kv_len: int | None = None, scale: float | None = None,
+                               window: int = 0, num_splits: int = 0, stream=None):
+    """fa512_decode_paged without a workspace: the split partials go to the
+    library's static device array (for callers that cannot allocate).  The
+    caller passes ``out`` (and ``lse``, or None); nothing is allocated here
+    either.  Arguments as for :func:`fa512_decode_paged`."""
+    if q.dim() != 3 or k_pages.dim() != 4 or k_pages.shape != v_pages.shape:
+        raise Fa512Error(1, "q must be [batch, heads, 512], pages [n, page, heads, 512]")
+    bsz, hq, d = q.shape
+    npages, psz, hk, _ = k_pages.shape
+    if page_table.dim() != 2:
+        raise Fa512Error(1, "page_table must be [batch, max_pages_per_seq]")
+    mpps = page_table.shape[1]
+    if max_kv_len is None:
+        max_kv_len = mpps * psz
+    if scale is None:
+        scale = d ** -0.5
+    _check(load_library().fa512_decode_paged_noalloc(
+        _dptr(q, "q", torch.bfloat16), _dptr(k_pages, "k_pages", torch.bfloat16),
+        _dptr(v_pages, "v_pages", torch.bfloat16), _dptr(page_table, "page_table", torch.int32),
+        _dptr(kv_lens, "kv_lens", torch.int32), _dptr(out, "out", torch.bfloat16),
+        _dptr(lse, "lse", torch.float32), bsz, hq, hk, psz, npages, mpps, int(max_kv_len),
+        float(scale), int(window), int(num_splits), _stream(stream)))
     return out, lse
 
 

@@ -21,6 +21,7 @@ __device__ unsigned fa512_device_error_word;
 namespace {
 
 constexpr int kHeadDim = FA512_HEAD_DIM;
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;   // the kernels' own default
 thread_local char g_last_error[512];
 
 fa512_status fail(fa512_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -184,10 +185,16 @@ const char* fa512_status_string(fa512_status s) {
 
 const char* fa512_last_error_message(void) { return g_last_error; }
 
-fa512_status fa512_prefill(const void* q, const void* k, const void* v, void* out, float* lse,
-                           int seqlen_q, int seqlen_k, int q_offset, int n_q_heads,
-                           int n_kv_heads, float scale, int causal, int window,
-                           fa512_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Body of fa512_prefill; the test hook below reaches it with a short wait
+// bound and one K load left out.
+fa512_status prefill_call(const void* q, const void* k, const void* v, void* out, float* lse,
+                          int seqlen_q, int seqlen_k, int q_offset, int n_q_heads, int n_kv_heads,
+                          float scale, int causal, int window, fa512_stream_t stream,
+                          unsigned long long wait_limit_ns, int skip_first_k_load) {
     g_last_error[0] = 0;
     if (seqlen_q < 0 || seqlen_k < 0 || q_offset < 0)
         return fail(FA512_ERR_INVALID_ARG, "negative length or offset");
@@ -229,6 +236,8 @@ fa512_status fa512_prefill(const void* q, const void* k, const void* v, void* ou
     p.window = window > 0 ? window : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
+    p.wait_limit_ns = wait_limit_ns;
+    p.test_skip_first_k_load = skip_first_k_load;
     if (static_cast<long long>(p.num_q_tiles) * n_kv_heads * 2 > 0x7fffffffLL)
         return fail(FA512_ERR_UNSUPPORTED, "grid too large");
 
@@ -261,6 +270,30 @@ fa512_status fa512_prefill(const void* q, const void* k, const void* v, void* ou
     e = fa512::launch_prefill(tmq, tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return FA512_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa512_status fa512_prefill(const void* q, const void* k, const void* v, void* out, float* lse,
+                           int seqlen_q, int seqlen_k, int q_offset, int n_q_heads,
+                           int n_kv_heads, float scale, int causal, int window,
+                           fa512_stream_t stream) {
+    return prefill_call(q, k, v, out, lse, seqlen_q, seqlen_k, q_offset, n_q_heads, n_kv_heads,
+                        scale, causal, window, stream, kDefaultWaitLimitNs, 0);
+}
+
+fa512_status fa512_test_prefill_missing_load(const void* q, const void* k, const void* v, void* out,
+                                             float* lse, int seqlen_q, int seqlen_k, int q_offset,
+                                             int n_q_heads, int n_kv_heads, float scale, int causal,
+                                             int window, uint64_t wait_limit_ns,
+                                             fa512_stream_t stream) {
+    if (wait_limit_ns < 1000000ull || wait_limit_ns > kDefaultWaitLimitNs)
+        return fail(FA512_ERR_INVALID_ARG, "wait_limit_ns must lie in [1 ms, 2 s]");
+    if (seqlen_k < 1) return fail(FA512_ERR_INVALID_ARG, "the hook needs at least one key");
+    return prefill_call(q, k, v, out, lse, seqlen_q, seqlen_k, q_offset, n_q_heads, n_kv_heads,
+                        scale, causal, window, stream, wait_limit_ns, 1);
 }
 
 fa512_status fa512_prefill_d256(const void* q, const void* k, const void* v, void* out, float* lse,

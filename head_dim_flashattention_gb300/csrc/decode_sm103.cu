@@ -31,12 +31,23 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "fa512_device.cuh"
 #include "fa512_internal.h"
 
 namespace fa512 {
 namespace decode {
+
+// Programmatic dependent launch: a split kernel lets the merge kernel that
+// follows it on the stream be scheduled while it still runs; the merge waits
+// for the split kernel's completion (and its memory) before reading.
+__device__ __forceinline__ void allow_merge_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_splits() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 constexpr int D = 512;
 constexpr int TILE_K = 32;                       // key positions per tile
@@ -193,6 +204,7 @@ template <bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+    allow_merge_launch();
     using Smem = decode::Smem<FP8>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -538,6 +550,7 @@ __device__ __forceinline__ void unpack8(const uint4 a, const uint4 b, float (&f)
 template <int G>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 decode_stream_kernel(const DecodeParams p) {
+    allow_merge_launch();
     extern __shared__ __align__(16) uint8_t smem[];
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -809,6 +822,7 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t a) {
 
 __global__ void __launch_bounds__(WARPS * 32, 1)
 decode_fp8_mma_kernel(const DecodeParams p) {
+    allow_merge_launch();
     extern __shared__ __align__(16) uint8_t smem[];
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1156,6 +1170,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {
 
 __global__ void __launch_bounds__(WARPS * 32, 1)
 decode_bf16_mma_kernel(const DecodeParams p) {
+    allow_merge_launch();
     extern __shared__ __align__(16) uint8_t smem[];
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1402,42 +1417,88 @@ decode_bf16_mma_kernel(const DecodeParams p) {
 
 
 
-// One block per (sequence, query token, query head): merges the splits' (O, m, l).
-__global__ void __launch_bounds__(128)
+// One block of 128 threads per (sequence, query token, query head): merges
+// the splits' (O, m, l) -- M = max m_s, w_s = 2^(m_s - M), O = sum w_s O_s /
+// sum w_s l_s ("Flash-Decoding for MQA in CUDA", "One KV head breaks the
+// textbook").  Threads first read the splits' (m, l) side by side, then each
+// thread streams its 4 columns of every split's O with 8 loads in flight.
+constexpr int MERGE_THREADS = 128;
+constexpr int MAX_SPLITS = 1024;
+
+__global__ void __launch_bounds__(MERGE_THREADS)
 decode_merge_kernel(const DecodeParams p) {
+    __shared__ float sw[MAX_SPLITS];      // w_s
+    __shared__ float smax[MERGE_THREADS / 32], ssum[MERGE_THREADS / 32];
+    wait_for_splits();
     const int h = blockIdx.x;
     const int bt = blockIdx.y;      // sequence * q_len + token
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t bh = static_cast<size_t>(bt) * p.n_q_heads + h;
     const int S = p.num_splits;
-    const float* ml = p.ws_ml + bh * S * 2;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, ml[2 * s]);
-    const int d = threadIdx.x * 4;
+    const float2* ml = reinterpret_cast<const float2*>(p.ws_ml + bh * S * 2);
+    float mloc = -INFINITY;
+    for (int s = tid; s < S; s += MERGE_THREADS) mloc = fmaxf(mloc, ml[s].x);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+    if (lane == 0) smax[warp] = mloc;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(smax[0], smax[1]), fmaxf(smax[2], smax[3]));
+    float lloc = 0.f;
+    for (int s = tid; s < S; s += MERGE_THREADS) {
+        const float2 x = ml[s];
+        // 0 for an empty split (m = -inf), and for every split when all are empty
+        const float w = M == -INFINITY ? 0.f : fast_exp2(x.x - M);
+        sw[s] = w;
+        lloc += w * x.y;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
+    if (lane == 0) ssum[warp] = lloc;
+    __syncthreads();
+    const float L = (ssum[0] + ssum[1]) + (ssum[2] + ssum[3]);
+    const int d = tid * 4;
     __nv_bfloat16* out = p.out + bh * D + d;
     if (M == -INFINITY) {
         *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
-        if (p.lse && threadIdx.x == 0) p.lse[bh] = -INFINITY;
+        if (p.lse && tid == 0) p.lse[bh] = -INFINITY;
         return;
     }
-    float L = 0.f, acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float* ob = p.ws_o + bh * S * D + d;
-    for (int s = 0; s < S; ++s) {
-        const float w = fast_exp2(ml[2 * s] - M);   // 0 for an empty split (m = -inf)
-        L += w * ml[2 * s + 1];
+    constexpr int U = 8;
+    int s = 0;
+    for (; s + U <= S; s += U) {
+        float4 x[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i) x[i] = *reinterpret_cast<const float4*>(ob + static_cast<size_t>(s + i) * D);
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            // a split whose weight underflowed contributes nothing, whatever it holds
+            const float w = sw[s + i];
+            if (w != 0.f) {
+                acc.x = fmaf(w, x[i].x, acc.x);
+                acc.y = fmaf(w, x[i].y, acc.y);
+                acc.z = fmaf(w, x[i].z, acc.z);
+                acc.w = fmaf(w, x[i].w, acc.w);
+            }
+        }
+    }
+    for (; s < S; ++s) {
+        const float w = sw[s];
         if (w != 0.f) {
             const float4 x = *reinterpret_cast<const float4*>(ob + static_cast<size_t>(s) * D);
-            acc0 += w * x.x;
-            acc1 += w * x.y;
-            acc2 += w * x.z;
-            acc3 += w * x.w;
+            acc.x = fmaf(w, x.x, acc.x);
+            acc.y = fmaf(w, x.y, acc.y);
+            acc.z = fmaf(w, x.z, acc.z);
+            acc.w = fmaf(w, x.w, acc.w);
         }
     }
     const float inv = 1.f / L;
     uint2 packed;
-    packed.x = pack_bf16x2(acc0 * inv, acc1 * inv);
-    packed.y = pack_bf16x2(acc2 * inv, acc3 * inv);
+    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
     *reinterpret_cast<uint2*>(out) = packed;
-    if (p.lse && threadIdx.x == 0) p.lse[bh] = (M + log2f(L)) * 0.69314718055994530942f;
+    if (p.lse && tid == 0) p.lse[bh] = (M + log2f(L)) * 0.69314718055994530942f;
 }
 
 }  // namespace decode
@@ -1505,9 +1566,19 @@ static cudaError_t launch_split_and_merge(const CUtensorMap& tmk, const CUtensor
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    dim3 mgrid(p.n_q_heads, p.batch * p.q_len);
-    decode::decode_merge_kernel<<<mgrid, 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    // the merge may be scheduled while the split kernel runs (it waits for it)
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(p.n_q_heads, p.batch * p.q_len);
+    cfg.blockDim = dim3(decode::MERGE_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode::decode_merge_kernel, p);
 }
 
 cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,

@@ -74,14 +74,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// records a timeout) when the wait exceeds kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+// records a timeout) when the wait exceeds limit_ns (default kWaitLimitNs).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
             report_error(err, FA512_DEVICE_ERR_TIMEOUT);
             return false;
         }

@@ -63,6 +63,8 @@ struct PrefillParams {
     int batch, max_seqlen_q, max_pairs;
     int page_shift, num_pages, max_pages_per_seq;
     int oob_row;                   // num_pages * page_size: a row past the pool (TMA fills zeros)
+    unsigned long long wait_limit_ns;  // bound of each pipeline wait (0: the default, 2 s)
+    int test_skip_first_k_load;    // test hook: CTA 0 does not issue its first K load
 };
 
 int prefill_smem_bytes();

@@ -76,7 +76,8 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
 
 // Bounded wait that also gives up when another role of this CTA has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, unsigned* err,
-                                              volatile int* abort) {
+                                              volatile int* abort,
+                                              unsigned long long limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
@@ -84,7 +85,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, un
         if (mbar_try_wait(a, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 report_error(err, FA512_DEVICE_ERR_TIMEOUT);
                 *abort = 1;
                 return false;

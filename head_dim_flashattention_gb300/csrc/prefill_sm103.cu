@@ -139,6 +139,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    // bound of every pipeline wait (the host may shorten it)
+    const unsigned long long wait_ns = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
 
     // ---- work item: (q-tile pair, KV head, O half, rank in the pair), and in
     // varlen mode the sequence.  KV heads run one after the other so that
@@ -364,7 +366,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 mbar_arrive_expect_tx(&bars[Smem::FULL_KA], 2 * SLOT);
                 mbar_arrive_expect_tx(&bars[Smem::FULL_KB], 2 * SLOT);
             }
-            load_k(rank ? row_hi : row_lo, SLOT_KA, 0, leader_bar(Smem::FULL_KA));
+            // (test hook: the first pair's even CTA leaves out its first K
+            // load, so that pair's waits run into their bound)
+            if (!(p.test_skip_first_k_load && blockIdx.x == 0))
+                load_k(rank ? row_hi : row_lo, SLOT_KA, 0, leader_bar(Smem::FULL_KA));
             load_k(rank ? row_hi : row_lo, SLOT_KB, 1, leader_bar(Smem::FULL_KB));
             bool ok = true;
             for (int j = 0; ok && j < n_kt; ++j) {
@@ -373,15 +378,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     next_lo = half_row((kt_begin + j + 1) * BN);
                     next_hi = half_row((kt_begin + j + 1) * BN + K_BOX_ROWS);
                     // slot KA once the first half of S(j) is done, slot KB once S(j) is
-                    if (!(ok = wait_or_abort(&bars[Smem::EMPTY_KA], ph, p.err, abort))) break;
+                    if (!(ok = wait_or_abort(&bars[Smem::EMPTY_KA], ph, p.err, abort, wait_ns))) break;
                     if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::FULL_KA], 2 * SLOT);
                     load_k(rank ? next_hi : next_lo, SLOT_KA, 0, leader_bar(Smem::FULL_KA));
-                    if (!(ok = wait_or_abort(&bars[Smem::S_FULL + (j & 1)], (j >> 1) & 1, p.err, abort))) break;
+                    if (!(ok = wait_or_abort(&bars[Smem::S_FULL + (j & 1)], (j >> 1) & 1, p.err, abort, wait_ns))) break;
                     if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::FULL_KB], 2 * SLOT);
                     load_k(rank ? next_hi : next_lo, SLOT_KB, 1, leader_bar(Smem::FULL_KB));
                 }
                 // V(j) once O += P(j-1) V(j-1) is done; counted on P ready of tile j
-                if (j > 0 && !(ok = wait_or_abort(&bars[Smem::O_DONE], (j - 1) & 1, p.err, abort))) break;
+                if (j > 0 && !(ok = wait_or_abort(&bars[Smem::O_DONE], (j - 1) & 1, p.err, abort, wait_ns))) break;
                 if constexpr (PAGED) {
                     // Each V box is one half tile (one page or part of one).
                     // The tail tile's V lands on this CTA's own barrier: the
@@ -415,13 +420,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ------------------------------------------------------------ MMA issue (both SMs)
-            bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort);
+            bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort, wait_ns);
             const uint32_t ring_base = smem_u32(smem + Smem::ring);
             const uint32_t q_base = smem_u32(smem + Smem::q);
             auto issue_qk = [&](int j) -> bool {
                 const uint32_t sb = tmem + TM_S + static_cast<uint32_t>(j & 1) * BN;
                 for (int c = 0; c < 2; ++c) {
-                    if (!wait_or_abort(&bars[c == 0 ? Smem::FULL_KA : Smem::FULL_KB], j & 1, p.err, abort))
+                    if (!wait_or_abort(&bars[c == 0 ? Smem::FULL_KA : Smem::FULL_KB], j & 1, p.err, abort, wait_ns))
                         return false;
                     tc_fence_after_sync();
                     const uint32_t kb = ring_base + (c == 0 ? SLOT_KA : SLOT_KB) * SLOT;
@@ -459,14 +464,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 // held P(j-1), consumed by O += P(j-1) V(j-1) issued before it
                 if (j + 1 < n_kt && !(ok = issue_qk(j + 1))) break;
                 // P(j) from both CTAs' softmax and V(j) in both CTAs' V slot
-                if (!(ok = wait_or_abort(&bars[Smem::P_FULL + (j & 1)], (j >> 1) & 1, p.err, abort))) break;
+                if (!(ok = wait_or_abort(&bars[Smem::P_FULL + (j & 1)], (j >> 1) & 1, p.err, abort, wait_ns))) break;
                 tc_fence_after_sync();
                 issue_pv(j);
             }
             if (ok) commit2_both(&bars[Smem::O_FINAL]);
             // let every issued MMA finish before TMEM can be released
             commit2_local(&bars[Smem::DRAIN]);
-            (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err);
+            (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err, wait_ns);
         }
     } else {
         // ---------------------------------------------- softmax + correction + epilogue
@@ -483,7 +488,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
             // (every wait of a softmax warp is made warp-uniform: the warp
             // synchronises below and must leave the loop as one)
-            if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::S_FULL + b], ph, p.err, abort)))) break;
+            if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::S_FULL + b], ph, p.err, abort, wait_ns)))) break;
             tc_fence_after_sync();
             uint32_t sr[2][32];
             const uint32_t s_col = TM_S + static_cast<uint32_t>(b) * BN + kh * BH;
@@ -529,7 +534,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const float own_max = mx[0] * p.scale_log2;
             xmax[(b * 2 + kh) * BM + row] = own_max;
             mbar_arrive(&bars[Smem::XCHG + b]);
-            if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::XCHG + b], ph, p.err, abort)))) break;
+            if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::XCHG + b], ph, p.err, abort, wait_ns)))) break;
             const float tmax = fmaxf(own_max, xmax[(b * 2 + (kh ^ 1)) * BM + row]);
 
             float m_use = m_ref, alpha = 1.f;
@@ -564,7 +569,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 // PV of the previous tile must be done before O is corrected;
                 // each key half corrects its own 128 O columns
                 if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::O_DONE],
-                                                                 static_cast<uint32_t>((j - 1) & 1), p.err, abort))))
+                                                                 static_cast<uint32_t>((j - 1) & 1), p.err, abort, wait_ns))))
                     break;
                 tc_fence_after_sync();
                 for (int c = 0; c < 4; ++c) {
@@ -584,7 +589,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     // the tile holding the cache's end: zero this CTA's V rows
                     // from the end to the end of its half tile, then hand them
                     // to the tensor core (async proxy)
-                    if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::V_TAIL], 0, p.err, abort)))) break;
+                    if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::V_TAIL], 0, p.err, abort, wait_ns)))) break;
                     const int r0 = seqlen_k - tail_tile * BN;       // 1 .. 127, not 64
                     const int n16 = (((r0 + K_BOX_ROWS - 1) & ~(K_BOX_ROWS - 1)) - r0) * 8;   // 16-byte chunks per box
                     uint8_t* vs = smem + Smem::ring + SLOT_V * SLOT + r0 * 128;
@@ -607,14 +612,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         }
         // O is final once PV(n_kt - 1) has completed: a barrier of its own,
         // committed once after the last PV, so no phase can be mistaken
-        if (ok) ok = wait_or_abort(&bars[Smem::O_FINAL], 0, p.err, abort);
+        if (ok) ok = wait_or_abort(&bars[Smem::O_FINAL], 0, p.err, abort, wait_ns);
         // Swap the halves' row sums through the Q area, idle once every MMA
         // has completed.  Each thread arrives exactly once, so the wait ends.
         float* lsum = reinterpret_cast<float*>(smem + Smem::q);
         lsum[(kh * BM + row) * 2 + 0] = l;
         lsum[(kh * BM + row) * 2 + 1] = l_b;
         mbar_arrive(&bars[Smem::L_XCHG]);
-        if (ok) ok = wait_or_abort(&bars[Smem::L_XCHG], 0, p.err, abort);
+        if (ok) ok = wait_or_abort(&bars[Smem::L_XCHG], 0, p.err, abort, wait_ns);
         if (ok) {
             tc_fence_after_sync();
             const float l_all = l + lsum[((kh ^ 1) * BM + row) * 2 + 0];

@@ -2,8 +2,13 @@
  * fa512 -- head-dim-512 FlashAttention forward for GB300 (sm_103a).
  *
  * C ABI of the library.  Plain pointers and sizes only; every device pointer
- * is owned by the caller, the library allocates nothing and never
+ * is owned by the caller, the library calls no allocator and never
  * synchronises the stream it is given.  All work is enqueued on `stream`.
+ * The library's own device memory is static: a 4-byte error word and the
+ * FA512_DECODE_STATIC_SCRATCH_BYTES array of fa512_decode_paged_noalloc,
+ * held on every GPU that loads the library until the process exits.  Their
+ * device addresses are looked up once per device and kept, so the library
+ * must not be used across a device reset (cudaDeviceReset).
  *
  * Operations (page title, then the part of the page that states them):
  *
@@ -295,8 +300,10 @@ int fa512_decode_auto_splits(int batch, int n_kv_heads, int page_size, int max_k
  * anything is enqueued; lower num_splits or the batch to fit.
  *
  * The first call on a device looks up the array's device address on that
- * device (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.  All calls share the one array and it
+ * device (cudaGetSymbolAddress, with that device current) and keeps it for
+ * the life of the process; make that first call before any stream capture.
+ * The kept address does not survive a device reset (cudaDeviceReset or a
+ * reset of the primary context): do not use the library across one.  All calls share the one array and it
  * keeps the last call's contents; nothing in it has to start at zero, since
  * every split writes its whole partial before the merge reads it.  Calls
  * whose kernels overlap on the GPU (different streams, or different host
@@ -311,6 +318,30 @@ fa512_status fa512_decode_paged_noalloc(const void *q, const void *k_pages,
                                         int num_pages, int max_pages_per_seq, int max_kv_len,
                                         float scale, int window, int num_splits,
                                         fa512_stream_t stream);
+
+/*
+ * fa512_test_prefill_missing_load -- test hook, not a step of the method.
+ * (The pages have no counterpart: it exists so that tests can drive the
+ * kernels' bounded waits, which ordinary inputs never exhaust.)
+ *
+ * The same launch as fa512_prefill with the same arguments, except that
+ * (a) every pipeline wait of the kernel is bounded by wait_limit_ns instead
+ * of the default 2 s, and (b) the first CTA pair's even CTA does not issue
+ * its first K tile load, so that pair's waits for it run into the bound.
+ * The pair then records FA512_ERR_TIMEOUT in the device error word, drains
+ * the MMAs it issued, frees its tensor memory and returns; CTAs that start
+ * after the record skip their work.  The rows of the pair (and of skipped
+ * CTAs) are left unwritten.  The device stays usable: read the status with
+ * fa512_device_status(stream, 1) (which also clears it) before the next call.
+ *
+ * wait_limit_ns must lie in [1e6, 2e9] and seqlen_k must be >= 1
+ * (FA512_ERR_INVALID_ARG otherwise); other errors as for fa512_prefill.
+ */
+fa512_status fa512_test_prefill_missing_load(const void *q, const void *k, const void *v,
+                                             void *out, float *lse, int seqlen_q, int seqlen_k,
+                                             int q_offset, int n_q_heads, int n_kv_heads,
+                                             float scale, int causal, int window,
+                                             uint64_t wait_limit_ns, fa512_stream_t stream);
 
 /* Reads and optionally clears the device-side error word after
  * synchronising `stream`.  Returns FA512_OK, FA512_ERR_TIMEOUT,

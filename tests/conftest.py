@@ -19,3 +19,15 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.fail("this test needs a CUDA device; run it with -m gpu on a GPU host")
     return torch.device("cuda", 0)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    try:
+        import parity
+    except ImportError:
+        return
+    path = os.environ.get("FA512_PARITY_LOG")
+    if path and parity.RECORDS:
+        parity.write_log(path)
+    for line in parity.summary_lines():
+        terminalreporter.write_line(line)

@@ -1,27 +1,43 @@
 """Comparison of GPU results with the fp64 oracle, and the tolerance used.
 
-Tolerance (stated for this path): O is bf16, compared with the fp64 oracle at
-max-abs 1e-2 and mean-abs 1e-3; LSE is fp32, max-abs 1e-3.  A bf16 output
-cannot be closer to an fp64 value than half a bf16 spacing, which exceeds
-1e-2 once |O| >= 4 (spacing 2^-5); the max-abs bound is therefore applied to
-the excess over that rounding floor, element by element:
-    |o_gpu - o_ref| <= 1e-2 + ulp_bf16(o_ref) / 2.
-For |O| < 2 (almost every element) the floor adds less than 0.004.  The
-mean-abs bound is read the same way: the mean over elements of the error in
-excess of the rounding floor, max(0, |o_gpu - o_ref| - ulp_bf16(o_ref) / 2),
-is at most 1e-3.  (Rounding alone leaves a mean error of about 1.2e-3 when
-each output is a single value of size ~1 that bf16 cannot hold, as with a
-one-key window over a cache whose dequantised values are not bf16 values;
-an output averaged over many keys is smaller and its floor far below 1e-3.)
-The raw mean-abs error is reported alongside.
+Tolerance stated for this path: O is bf16, compared with the fp64 oracle at
+max-abs 1e-2 and mean-abs 1e-3; LSE is fp32, max-abs 1e-3.  These bounds are
+asserted on the raw error |o_gpu - o_ref| wherever a bf16 value can meet
+them:
+
+* max-abs 1e-2 on every element with |o_ref| < 4.  There bf16 spacing is at
+  most 2^-6, so a correctly rounded output is within 0.0078 and the kernel's
+  own error has at least 0.002 of room.
+* For |o_ref| >= 4 (only where one scaled key dominates a row, as in the
+  stress rows) bf16 spacing is 2^-5 or more: the nearest bf16 value can be
+  0.0156 away, beyond 1e-2.  There the bound applies to the error in excess
+  of half a bf16 spacing of o_ref: |o_gpu - o_ref| - ulp(o_ref)/2 <= 1e-2.
+* mean-abs 1e-3 on the raw error of every case, with one named exception:
+  a one-key window over an FP8 cache (`one_key_fp8=True`).  Each output
+  there is a single dequantised value v_scale * e4m3(v), which bf16 cannot
+  hold; correct rounding alone leaves a mean error of about 0.0013 * mean|O|
+  ~ 1.05e-3 for N(0,1) values.  That case asserts the mean of the error in
+  excess of the rounding floor instead, max(0, err - ulp(o_ref)/2).
+
+Every comparison is recorded (raw max and mean, worst element, how many
+elements fell under the rounding floor rule); `tests/conftest.py` prints the
+worst records at the end of the run and writes all of them to the file named
+by FA512_PARITY_LOG when that variable is set.
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 
 O_MAX_ABS = 1e-2
 O_MEAN_ABS = 1e-3
 LSE_MAX_ABS = 1e-3
+# |O| from which the nearest bf16 value can be more than O_MAX_ABS away
+BF16_FLOOR_FROM = 4.0
+
+RECORDS: list[dict] = []
 
 
 def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
@@ -31,17 +47,42 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
     return np.where(a > 0, 2.0 ** (e - 7) / 2.0, 0.0)
 
 
-def compare_o(o_gpu: np.ndarray, o_ref: np.ndarray, what: str = "O") -> dict:
+def _case_name(what: str) -> str:
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    return "%s [%s]" % (test, what) if test else what
+
+
+def compare_o(o_gpu: np.ndarray, o_ref: np.ndarray, what: str = "O",
+              one_key_fp8: bool = False) -> dict:
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
     assert o_gpu.shape == o_ref.shape, (o_gpu.shape, o_ref.shape)
     assert np.all(np.isfinite(o_gpu)), "%s has non-finite values" % what
     err = np.abs(o_gpu - o_ref)
+    big = np.abs(o_ref) >= BF16_FLOOR_FROM
     excess = err - bf16_half_ulp(o_ref)
-    stats = {"max_abs": float(err.max(initial=0.0)), "mean_abs": float(err.mean()) if err.size else 0.0,
-             "max_excess": float(excess.max(initial=-1.0)),
-             "mean_excess": float(np.maximum(excess, 0.0).mean()) if err.size else 0.0}
-    assert stats["max_excess"] <= O_MAX_ABS, (what, stats)
-    assert stats["mean_excess"] <= O_MEAN_ABS, (what, stats)
+    n = err.size
+    stats = {
+        "case": _case_name(what), "elements": int(n),
+        "max_abs": float(err.max(initial=0.0)),
+        "mean_abs": float(err.mean()) if n else 0.0,
+        "max_abs_below_4": float(err[~big].max(initial=0.0)),
+        "elements_at_or_above_4": int(big.sum()),
+        "max_excess_at_or_above_4": float(excess[big].max(initial=-1.0)),
+        "mean_excess": float(np.maximum(excess, 0.0).mean()) if n else 0.0,
+        "one_key_fp8": bool(one_key_fp8),
+    }
+    if n:
+        i = int(np.argmax(err))
+        stats["worst_ref"] = float(o_ref.reshape(-1)[i])
+        stats["worst_gpu"] = float(o_gpu.reshape(-1)[i])
+    RECORDS.append(stats)
+    assert stats["max_abs_below_4"] <= O_MAX_ABS, (what, "max-abs where |O| < 4", stats)
+    assert stats["max_excess_at_or_above_4"] <= O_MAX_ABS, (what, "excess where |O| >= 4", stats)
+    if one_key_fp8:
+        assert stats["mean_excess"] <= O_MEAN_ABS, (what, "mean excess (one-key FP8 window)", stats)
+    else:
+        assert stats["mean_abs"] <= O_MEAN_ABS, (what, "mean-abs", stats)
     return stats
 
 
@@ -53,5 +94,30 @@ def compare_lse(l_gpu: np.ndarray, l_ref: np.ndarray, what: str = "LSE") -> floa
     fin = ~ninf_ref
     assert np.all(np.isfinite(l_gpu[fin])), "%s has non-finite values" % what
     err = float(np.abs(l_gpu[fin] - l_ref[fin]).max(initial=0.0))
+    RECORDS.append({"case": _case_name(what), "lse_max_abs": err, "elements": int(fin.sum())})
     assert err <= LSE_MAX_ABS, (what, err)
     return err
+
+
+def write_log(path: str) -> None:
+    with open(path, "w") as f:
+        for r in RECORDS:
+            f.write(json.dumps(r) + "\n")
+
+
+def summary_lines(top: int = 8) -> list[str]:
+    o = [r for r in RECORDS if "max_abs" in r]
+    l = [r for r in RECORDS if "lse_max_abs" in r]
+    if not o and not l:
+        return []
+    out = ["parity vs the fp64 oracle: %d O comparisons, %d LSE comparisons" % (len(o), len(l))]
+    if o:
+        out.append("  O: worst raw max-abs %.3e, worst raw mean-abs %.3e, elements with |O| >= 4: %d"
+                   % (max(r["max_abs"] for r in o), max(r["mean_abs"] for r in o),
+                      sum(r["elements_at_or_above_4"] for r in o)))
+        for r in sorted(o, key=lambda r: -r["max_abs_below_4"])[:top]:
+            out.append("    max %.3e (|O|<4 %.3e) mean %.3e  %s"
+                       % (r["max_abs"], r["max_abs_below_4"], r["mean_abs"], r["case"]))
+    if l:
+        out.append("  LSE: worst max-abs %.3e" % max(r["lse_max_abs"] for r in l))
+    return out

@@ -210,3 +210,16 @@ def test_fp8_binding_rejects_a_bf16_cache_before_the_library():
     with pytest.raises(fa.Fa512Error):
         fa.fa512_decode_paged_fp8(q, pages, pages, torch.zeros((1, 1), dtype=torch.int32),
                                   torch.ones(1, dtype=torch.int32))
+
+
+def test_timeout_hook_rejects_bad_bounds_before_any_launch(lib):
+    """The test hook that exhausts a prefill wait refuses bounds outside
+    [1 ms, 2 s] and an empty key sequence on the host."""
+    f = lib.fa512_test_prefill_missing_load
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int,
+                                                                ctypes.c_int, ctypes.c_uint64,
+                                                                ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(16, 16, 16, 16, None, 4, 4, 0, 8, 2, 0.05, 1, 0, 10, None) == 1
+    assert f(16, 16, 16, 16, None, 4, 4, 0, 8, 2, 0.05, 1, 0, 3_000_000_000, None) == 1
+    assert f(16, 16, 16, 16, None, 4, 0, 0, 8, 2, 0.05, 1, 0, 5_000_000, None) == 1

@@ -41,6 +41,9 @@ def run(fa, pc, q=None, k_pages=None, v_pages=None, k_scale=K_SCALE, v_scale=V_S
 
 
 def check(fa, pc, q=None, k_scale=K_SCALE, v_scale=V_SCALE, num_splits=0, window=0, scale=None):
+    """GPU vs oracle.  A one-key window (window 1) makes every output a single
+    dequantised value that bf16 cannot hold: that case is compared with the
+    mean of the error beyond the bf16 rounding floor (tests/parity.py)."""
     q = pc.q if q is None else q
     o, l = run(fa, pc, q=q, k_scale=k_scale, v_scale=v_scale, num_splits=num_splits,
                window=window, scale=scale)
@@ -48,7 +51,7 @@ def check(fa, pc, q=None, k_scale=K_SCALE, v_scale=V_SCALE, num_splits=0, window
     ro, rl = oracle.decode_paged_fp8(q, pc.k_pages, pc.v_pages, pc.page_table, pc.kv_lens,
                                      k_scale=k_scale, v_scale=v_scale, window=window,
                                      scale=scale)
-    compare_o(o, ro)
+    compare_o(o, ro, one_key_fp8=(window == 1))
     compare_lse(l, rl)
     return o, l
 
