@@ -588,17 +588,26 @@ decode_stream_kernel(const DecodeParams p) {
     const uint32_t ring = smem_u32(smem) + warp * STAGES * CHUNK_BYTES;
     // chunk k of this warp covers positions pb + (warp + 8k) * POS ...
     const int my_chunks = n_chunks > warp ? (n_chunks - warp + WARPS - 1) / WARPS : 0;
-    auto issue = [&](int k) {
+    // Page of position pos0 + (lane % POS) of chunk k.  Each chunk's pages are
+    // loaded one chunk before its copies are issued, so the copies never wait
+    // on a page-table load.
+    auto page_of = [&](int k) -> int {
+        const int pos = pb + (warp + WARPS * k) * POS + (lane & (POS - 1));
+        return (k < my_chunks && pos < pe)
+                   ? p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size]
+                   : 0;
+    };
+    auto issue = [&](int k, int page_lane) {
         if (k < my_chunks) {
             const int pos0 = pb + (warp + WARPS * k) * POS;
             const uint32_t st = ring + (k % STAGES) * CHUNK_BYTES;
 #pragma unroll
             for (int i = 0; i < POS; ++i) {
                 const int pos = pos0 + i;
+                const int page = __shfl_sync(0xffffffffu, page_lane, i);
                 bool valid = pos < pe;
                 size_t row = 0;
                 if (valid) {
-                    const int page = p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size];
                     if (page < 0 || page >= p.num_pages) {
                         report_error(p.err, FA512_DEVICE_ERR_INDEX);
                         valid = false;
@@ -618,11 +627,14 @@ decode_stream_kernel(const DecodeParams p) {
         }
         cp_async_commit();   // one group per chunk slot, empty past the end
     };
+    int page_next = page_of(STAGES - 1);
 #pragma unroll
-    for (int k = 0; k < STAGES - 1; ++k) issue(k);
+    for (int k = 0; k < STAGES - 1; ++k) issue(k, page_of(k));
 
     for (int k = 0; k < my_chunks; ++k) {
-        issue(k + STAGES - 1);
+        const int page_now = page_next;
+        page_next = page_of(k + STAGES);
+        issue(k + STAGES - 1, page_now);
         cp_async_wait<STAGES - 1>();   // this lane's copies of chunk k have landed
         const uint8_t* st = smem + (warp * STAGES + (k % STAGES)) * CHUNK_BYTES;
         const int pos0 = pb + (warp + WARPS * k) * POS;
@@ -912,13 +924,20 @@ decode_fp8_mma_kernel(const DecodeParams p) {
     // copies 16-byte piece (l & 1) + 2 (s % 4) of that position's K slice
     // (s < 4) or V slice (s >= 4), so every instruction covers whole 32-byte
     // sectors.
-    auto issue = [&](int k) {
+    // page of this lane's position in chunk k, loaded one chunk before the
+    // chunk's copies are issued (the copies never wait on the page table)
+    auto page_of = [&](int k) -> int {
+        const int pos = pb + (pg + GROUPS * k) * CPOS + (lane >> 1);
+        return (k < my_chunks && pos < pe)
+                   ? p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size]
+                   : 0;
+    };
+    auto issue = [&](int k, int page) {
         if (k < my_chunks) {
             const int pos = pb + (pg + GROUPS * k) * CPOS + (lane >> 1);
             bool valid = pos < pe;
             size_t row = 0;
             if (valid) {
-                const int page = p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size];
                 if (page < 0 || page >= p.num_pages) {
                     report_error(p.err, FA512_DEVICE_ERR_INDEX);
                     valid = false;
@@ -939,11 +958,14 @@ decode_fp8_mma_kernel(const DecodeParams p) {
         }
         cp_async_commit();
     };
+    int page_next = page_of(STAGES - 1);
 #pragma unroll
-    for (int k = 0; k < STAGES - 1; ++k) issue(k);
+    for (int k = 0; k < STAGES - 1; ++k) issue(k, page_of(k));
 
     for (int k = 0; k < my_chunks; ++k) {
-        issue(k + STAGES - 1);
+        const int page_now = page_next;
+        page_next = page_of(k + STAGES);
+        issue(k + STAGES - 1, page_now);
         cp_async_wait<STAGES - 1>();
         __syncwarp();                         // every lane's copies of chunk k are visible
         const uint8_t* kst = smem + (warp * STAGES + (k % STAGES)) * CHUNK_BYTES;
@@ -1229,13 +1251,20 @@ decode_bf16_mma_kernel(const DecodeParams p) {
     // copy plan: lane l fetches position l / 4 of the chunk; at step s it
     // copies piece (l & 3) + 4 (s % 4) of that position's K slice (s < 4) or
     // V slice (s >= 4): four lanes cover 64 contiguous bytes of a row
-    auto issue = [&](int k) {
+    // page of this lane's position in chunk k, loaded one chunk before the
+    // chunk's copies are issued (the copies never wait on the page table)
+    auto page_of = [&](int k) -> int {
+        const int pos = pb + (pg + GROUPS * k) * CPOS + (lane >> 2);
+        return (k < my_chunks && pos < pe)
+                   ? p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size]
+                   : 0;
+    };
+    auto issue = [&](int k, int page) {
         if (k < my_chunks) {
             const int pos = pb + (pg + GROUPS * k) * CPOS + (lane >> 2);
             bool valid = pos < pe;
             size_t row = 0;
             if (valid) {
-                const int page = p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size];
                 if (page < 0 || page >= p.num_pages) {
                     report_error(p.err, FA512_DEVICE_ERR_INDEX);
                     valid = false;
@@ -1257,11 +1286,14 @@ decode_bf16_mma_kernel(const DecodeParams p) {
         }
         mma8::cp_async_commit();
     };
+    int page_next = page_of(STAGES - 1);
 #pragma unroll
-    for (int k = 0; k < STAGES - 1; ++k) issue(k);
+    for (int k = 0; k < STAGES - 1; ++k) issue(k, page_of(k));
 
     for (int k = 0; k < my_chunks; ++k) {
-        issue(k + STAGES - 1);
+        const int page_now = page_next;
+        page_next = page_of(k + STAGES);
+        issue(k + STAGES - 1, page_now);
         mma8::cp_async_wait<STAGES - 1>();
         __syncwarp();                         // every lane's copies of chunk k are visible
         const uint8_t* kst = smem + (warp * STAGES + (k % STAGES)) * CHUNK_BYTES;

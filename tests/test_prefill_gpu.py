@@ -30,12 +30,12 @@ def run(fa, q, k, v, q_offset=0, causal=True, window=0, scale=None, dev="cuda"):
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-def check(fa, q, k, v, rows=None, **kw):
+def check(fa, q, k, v, rows=None, stress=False, **kw):
     o, l = run(fa, q, k, v, **kw)
     ro, rl = oracle.prefill(q, k, v, rows=rows, **kw)
     if rows is not None:
         o, l = o[rows], l[:, rows]
-    st = compare_o(o, ro)
+    st = compare_o(o, ro, stress=stress)
     compare_lse(l, rl)
     return st
 
@@ -126,7 +126,7 @@ def test_large_logits_stress_rows(fa):
     """Every 64th K row x8 forces large max rescales (the stress variant)."""
     cfg = workloads.PrefillConfig("s", 512, 512, 0, 8, 2, stress=True, seed=77)
     q, k, v = workloads.prefill_inputs(cfg)
-    check(fa, q, k, v, causal=True)
+    check(fa, q, k, v, causal=True, stress=True)
 
 
 @pytest.mark.parametrize("name", ["chunked", "full_stress"])
@@ -135,7 +135,8 @@ def test_full_size_configs_sampled_rows(fa, name):
     q, k, v = workloads.prefill_inputs(cfg)
     rows = workloads.sample_rows(cfg, tokens_per_tile=128 // (cfg.n_q_heads // cfg.n_kv_heads),
                                  every=997)
-    check(fa, q, k, v, rows=rows, q_offset=cfg.q_offset, scale=cfg.scale, causal=cfg.causal)
+    check(fa, q, k, v, rows=rows, q_offset=cfg.q_offset, scale=cfg.scale, causal=cfg.causal,
+          stress=cfg.stress)
 
 
 def test_mqa_long_context_sampled_rows(fa):
