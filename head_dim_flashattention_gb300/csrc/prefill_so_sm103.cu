@@ -12,9 +12,9 @@
 // for Gemma 4 on the RTX PRO 6000", "The kernel in three steps", step 1):
 //
 //   * the score pair (cluster ranks 0, 1; one q tile each) keeps its Q tile
-//     resident in shared memory, computes S = Q K^T with 2-SM MMAs
-//     (tcgen05 cta_group::2, M256 x N128, each CTA holding 64 of a tile's
-//     128 keys) into four S buffers in TMEM, and runs the online softmax;
+//     resident, computes S = Q K^T with 2-SM MMAs (tcgen05 cta_group::2,
+//     M256 x N128, each CTA holding 64 of a tile's 128 keys) into S buffers
+//     in TMEM, and runs the online softmax;
 //   * the output pair (ranks 2, 3) keeps the whole fp32 O of its q tile in
 //     TMEM and computes O += P V with 2-SM MMAs (M256 x N256 per O half,
 //     each CTA holding 128 of the half's 256 V columns), P read from its
@@ -22,32 +22,43 @@
 //
 // Every score CTA sends the bf16 P of each tile (and the per-row rescale
 // factor alpha) to the output CTA with the same q tile through distributed
-// shared memory (st.async with mbarrier completion), double-buffered.  S is
-// computed once, so the tensor pipes execute the algorithmic FLOP only: the
-// score pair 2 x 128 x 128 x 512 and the output pair 2 x 128 x 128 x 512
-// multiply-adds per key tile.  (The pages split the head dimension across
-// warps of one SM, "Head dim 512 breaks the textbook" and step 2 of the RTX
-// PRO 6000 page; here the split is between the two products.)
+// shared memory.  S is computed once, so the tensor pipes execute the
+// algorithmic FLOP only: the score pair 2 x 128 x 128 x 512 and the output
+// pair 2 x 128 x 128 x 512 multiply-adds per key tile.  (The pages split the
+// head dimension across warps of one SM, "Head dim 512 breaks the textbook"
+// and step 2 of the RTX PRO 6000 page; here the split is between the two
+// products.)
 //
-// Score pair: K streams through three 32 KiB slots (a half tile: this CTA's
-// 64 keys x 256 head-dim columns), each released by the commit after its 16
-// MMAs; an S buffer is released when every softmax warp has read it, and the
-// producer holds back a tile's first K half until its S buffer is free, so
-// the MMA thread waits only for K.  Eight softmax warps: TMEM lane quadrant
-// (warp % 4) gives a warp its 32 rows, warps 2-5 take keys 0-63 of each tile
-// and warps 6-9 keys 64-127; the two warps of a quadrant swap row maxima
-// through shared memory.  The row max is lazy: O is rescaled only when a
-// row's max grows by more than 2^8.
+// Score pair (per CTA: Q head-dim columns 0-255 in shared memory, 256-511 in
+// TMEM as the A operand of the second half of every QK^T; three S buffers in
+// TMEM): K streams through three 32 KiB slots (a half tile: this CTA's 64
+// keys x 256 head-dim columns), each released by the commit after its 16
+// MMAs; the producer holds back a tile's first K half until its S buffer has
+// been read.  Eight softmax warps: TMEM lane quadrant (warp % 4) gives a warp
+// its 32 rows, warps 2-5 take keys 0-63 of each tile and warps 6-9 keys
+// 64-127; they swap row maxima (rounded up to bf16, so both take the same
+// decision) through shared memory.  The row max is lazy: O is rescaled only
+// when a row's max grows by more than 2^8.  P goes to one of two staging
+// buffers; a copy warp moves each staged tile with one bulk copy (the copy
+// engine) into the output CTA, where it completes on that CTA's mbarrier;
+// alpha follows by remote stores on the same barrier.
 //
-// Output pair: V streams through four 32 KiB slots (two tiles x two O
-// halves); the commit after a tile's 16 MMAs is multicast to all four CTAs
-// and frees that tile's V slots, its P buffer, and lets O be corrected for
-// the tile after it.  Eight correction warps apply alpha to O in TMEM
-// (tcgen05.ld / st) when a row's max moved, then mark the tile ready; at the
-// end they normalise O by the sum of the bf16 P values and write bf16 rows.
+// Output pair (per CTA: the whole 128 x 512 fp32 O in TMEM): V streams
+// through four 32 KiB slots (two tiles x two O halves), P lands in three
+// buffers; the commit after a tile's 16 MMAs (M256 x N256 per O half, P and
+// V from shared memory) is multicast to all four CTAs and frees that tile's
+// V slots and P buffer and lets O be corrected for the next tile.  Eight
+// correction warps apply alpha to O in TMEM (tcgen05.ld / st) when a row's
+// max moved, then mark the tile ready; at the end they normalise O by the
+// sum of the bf16 P values and write bf16 rows.
+//
+// A cluster-scope mbarrier arrival stalls the thread that makes it for about
+// a microsecond, so no softmax or correction warp makes one per tile: they
+// arrive on barriers of their own CTA, and an otherwise idle thread forwards
+// one arrival per tile to the other CTA.
 //
 // Causal / sliding-window tile skipping over the pair's visible band; only
-// the 64-key halves that cross a row's band edge are masked element by
+// the key parts that cross a row's band edge are masked element by
 // element.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -66,22 +77,29 @@ using namespace pair;
 constexpr int D = 512;
 constexpr int BM = 128;                  // packed rows per CTA tile
 constexpr int BN = 128;                  // keys per KV tile
-constexpr int BH = BN / 2;               // keys per softmax warp
-constexpr int NUM_THREADS = 320;
 constexpr int N_WORK_WARPS = 8;          // warps 2-9
+constexpr int COPY_WARP = 2 + N_WORK_WARPS;   // score CTAs: moves each staged P tile to the output CTA
+constexpr int NUM_THREADS = (3 + N_WORK_WARPS) * 32;
+constexpr int PARTS = N_WORK_WARPS / 4;  // warps per TMEM lane quadrant
+constexpr int KP = BN / PARTS;           // score CTAs: keys of a tile per softmax warp (32)
+constexpr int OP = D / PARTS;            // output CTAs: O columns per correction warp (128)
 constexpr int Q_CHUNK = BM * 128;        // one 64-column box of Q: 16 KiB
 constexpr int SLOT = 32768;
 constexpr int K_SLOTS = 3;               // score CTAs: K half tiles
 constexpr int K_BOX_ROWS = BN / 2;       // {64 columns, 64 keys} boxes
 constexpr int K_BOX = K_BOX_ROWS * 128;  // 8 KiB
-constexpr int S_BUFS = 4;                // S buffers of 128 TMEM columns
+constexpr int S_BUFS = 3;                // S buffers of 128 TMEM columns
+constexpr uint32_t TM_QHI = S_BUFS * BN; // Q head-dim columns 256-511 (128 TMEM columns)
 constexpr int V_SLOTS = 4;               // output CTAs: 2 tiles x 2 O halves
 constexpr int V_BOX_ROWS = BN;           // {64 columns, 128 keys} boxes
 constexpr int V_BOX = V_BOX_ROWS * 128;  // 16 KiB
 constexpr int P_CHUNK = BM * 128;        // P of 64 keys for 128 rows, bf16: 16 KiB
 constexpr int P_BUF = 2 * P_CHUNK;       // one tile's P: 32 KiB
+constexpr int P_BUFS = 3;                // output CTAs: P buffers
+constexpr int STAGES = 2;                // score CTAs: P staging buffers
 constexpr uint32_t P_TX = P_BUF + BM * 4;   // bytes landing per tile: P and alpha
 constexpr uint32_t L_TX = BM * 4;           // the final row sums
+static_assert((PARTS == 2 || PARTS == 4) && KP % 32 == 0, "two or four work warps per lane quadrant");
 
 // Rescale O only when the row max grows by more than this (log2 units);
 // until then the stale max stays the reference and p <= 2^8.
@@ -90,32 +108,42 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr uint16_t MASK_SCORE = 0x3, MASK_OUTPUT = 0xC, MASK_ALL = 0xF;
 
 struct Smem {
-    // score CTAs
-    static constexpr int q = 0;                                 // 8 x 16 KiB
-    static constexpr int kring = q + 8 * Q_CHUNK;               // 3 x 32 KiB
-    static constexpr int role_end = kring + K_SLOTS * SLOT;     // 224 KiB
+    // score CTAs: Q head-dim columns 0-255 stay here; columns 256-511 land in
+    // the staging area first and move to TMEM, after which the area stages P
+    static constexpr int q = 0;                                 // 4 x 16 KiB
+    static constexpr int kring = q + 4 * Q_CHUNK;               // 3 x 32 KiB
+    static constexpr int stage = kring + K_SLOTS * SLOT;        // 2 x 32 KiB
+    static constexpr int xmax = stage + STAGES * P_BUF;         // [2 buffers][4 parts][128] bf16
     // output CTAs
     static constexpr int vring = 0;                             // 4 x 32 KiB
-    static constexpr int precv = vring + V_SLOTS * SLOT;        // 2 x 32 KiB
-    static constexpr int alpha = precv + 2 * P_BUF;             // [2][128] f32
-    static constexpr int lrecv = alpha + 2 * BM * 4;            // [128] f32
+    static constexpr int precv = vring + V_SLOTS * SLOT;        // 3 x 32 KiB
+    static constexpr int alpha = precv + P_BUFS * P_BUF;        // [3][128] f32
+    static constexpr int lrecv = alpha + P_BUFS * BM * 4;       // [128] f32
     // both
-    static constexpr int xmax = role_end;                       // [2 buffers][2 halves][128] f32
-    static constexpr int bars = xmax + 2 * 2 * BM * 4;
+    // (2 KiB after the staging / P buffers: the score CTAs' row-max swap, the
+    // output CTAs' alpha and row sums)
+    static constexpr int bars = xmax + 2048;
     enum {
         K_FULL = 0,                      // [3] score leader: both CTAs' half tile landed
         K_EMPTY = K_FULL + K_SLOTS,      // [3] score CTAs: the slot's MMAs completed
-        S_FULL = K_EMPTY + K_SLOTS,      // [4] score CTAs: S of the tile is in TMEM
-        S_FREE = S_FULL + S_BUFS,        // [4] score leader: both CTAs' softmax warps read S
-        XCHG = S_FREE + S_BUFS,          // [2] score CTAs: row-max swap of the key halves
-        Q_FULL = XCHG + 2,               // score leader: both Q tiles landed
-        L_XCHG = Q_FULL + 1,             // score CTAs: row-sum swap
-        PV_DONE = L_XCHG + 1,            // [2] all four: O += P V of the buffer's last tile completed
-        PV_READY = PV_DONE + 2,          // [2] output leader: P landed and O corrected in both, V landed
-        P_LANDED = PV_READY + 2,         // [2] output CTAs: P and alpha of the tile arrived
-        O_FINAL = P_LANDED + 2,          // output CTAs: the last O += P V completed
+        S_FULL = K_EMPTY + K_SLOTS,      // [3] score CTAs: S of the tile is in TMEM
+        S_FREE = S_FULL + S_BUFS,        // [3] score leader: both CTAs' softmax warps read S
+        XCHG = S_FREE + S_BUFS,          // [2] score CTAs: row-max swap of the four key parts
+        Q_FULL = XCHG + 2,               // score leader: head-dim columns 0-255 of both Q tiles landed
+        Q_HI = Q_FULL + 1,               // score CTAs: this CTA's columns 256-511 landed (staging area)
+        Q_TMEM = Q_HI + 1,               // score leader: both CTAs' columns 256-511 are in TMEM
+        P_STAGED = Q_TMEM + 1,           // [2] score CTAs: all softmax warps staged the tile's P
+        STAGE_FREE = P_STAGED + STAGES,  // [2] score CTAs: the buffer's last copy landed, its alpha read
+        S_READ = STAGE_FREE + STAGES,    // [3] score CTA 1: its softmax warps read S (forwarded to S_FREE)
+        L_XCHG = S_READ + S_BUFS,        // score CTAs: row-sum swap
+        PV_DONE = L_XCHG + 1,            // [3] all four: O += P V of the P buffer's last tile completed
+        PV_READY = PV_DONE + P_BUFS,     // [3] output leader: P landed and O corrected in both, V landed
+        P_LANDED = PV_READY + P_BUFS,    // [3] output CTAs: P and alpha of the tile arrived
+        O_FINAL = P_LANDED + P_BUFS,     // output CTAs: the last O += P V completed
         L_READY = O_FINAL + 1,           // output CTAs: the row sums arrived
-        DRAIN = L_READY + 1,             // every MMA this CTA issued has completed
+        ALPHA_READ = L_READY + 1,        // [3] output CTAs: correction warps read the tile's alpha
+        CORR_DONE = ALPHA_READ + P_BUFS, // [3] output CTA 3: its correction warps are done with the tile
+        DRAIN = CORR_DONE + P_BUFS,      // every MMA this CTA issued has completed
         N_BARS = DRAIN + 1
     };
     static constexpr int tmem_addr = bars + N_BARS * 8;
@@ -123,7 +151,8 @@ struct Smem {
     static constexpr int skip_flag = abort_flag + 4;             // written by rank 0 into all four
     static constexpr int total = skip_flag + 4;
 };
-static_assert(Smem::lrecv + BM * 4 <= Smem::role_end, "output CTA layout");
+static_assert(Smem::lrecv + BM * 4 <= Smem::bars && Smem::xmax + 2 * PARTS * BM * 2 <= Smem::bars, "layout");
+static_assert(Smem::kring % 1024 == 0 && Smem::precv % 1024 == 0, "swizzled buffers on 1 KiB");
 // The dynamic shared-memory window starts 1 KiB aligned (checked at run
 // time), which the 128-byte swizzle atoms need.
 static_assert(Smem::total <= 232448, "shared memory budget");
@@ -144,17 +173,20 @@ __device__ __forceinline__ void commit2_mask(uint64_t* bar, uint16_t mask) {
         : "memory");
 }
 
-// 16 bytes into another CTA's shared memory; the bytes complete_tx on that
+// 4 bytes into another CTA's shared memory; the bytes complete_tx on that
 // CTA's mbarrier (both addresses shared::cluster, in the same CTA).
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-                 ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
-                 : "memory");
-}
 __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t a, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                  ::"r"(addr), "r"(a), "r"(bar)
+                 : "memory");
+}
+
+// Bulk copy of `bytes` from this CTA's shared memory to another CTA's (copy
+// engine); the bytes complete_tx on the destination CTA's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst_cluster), "r"(src_cta), "r"(bytes), "r"(bar_cluster)
                  : "memory");
 }
 
@@ -221,11 +253,12 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     const int kt_begin = j_lo / BN;
     const int n_kt = j_hi > j_lo ? (j_hi + BN - 1) / BN - kt_begin : 0;
 
-    // this thread's packed row and half (warps 2-9): key half in the score
-    // CTAs, O column half in the output CTAs
-    const bool work_warp = warp >= 2;
+    // this thread's packed row and part (warps 2-17): TMEM lane quadrant
+    // warp % 4; part = 32 keys of a tile in the score CTAs, 128 O columns in
+    // the output CTAs
+    const bool work_warp = warp >= 2 && warp < COPY_WARP;
     const int row = (warp & 3) * 32 + lane;
-    const int kh = warp >= 6 ? 1 : 0;
+    const int part = (warp - 2) >> 2;
     const int tok = row / G;
     const int g = row - tok * G;
     const bool valid_row = work_warp && row < p.rows_per_tile && tok < ntok;
@@ -237,9 +270,9 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         if (valid_row) {
             if (!scorer) {
                 uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D +
-                                                      kh * 256);
-                for (int i = 0; i < 256 / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-            } else if (kh == 0 && p.lse) {
+                                                      part * OP);
+                for (int i = 0; i < OP / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            } else if (part == 0 && p.lse) {
                 p.lse[static_cast<size_t>(hq) * p.total_q + t0 + tok] = -INFINITY;
             }
         }
@@ -250,9 +283,17 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         for (int i = 0; i < Smem::N_BARS; ++i) {
             uint32_t count = 1;
             if (i == Smem::XCHG || i == Smem::XCHG + 1 || i == Smem::L_XCHG) count = N_WORK_WARPS * 32;
-            if (i >= Smem::S_FREE && i < Smem::S_FREE + S_BUFS) count = 2 * N_WORK_WARPS;
-            // one lane per correction warp of both output CTAs, plus the V load
-            if (i == Smem::PV_READY || i == Smem::PV_READY + 1) count = 2 * N_WORK_WARPS + 1;
+            if (i == Smem::Q_TMEM) count = 2 * N_WORK_WARPS;
+            // the leader's softmax warps, plus one forwarded arrival for the other CTA's
+            if (i >= Smem::S_FREE && i < Smem::S_FREE + S_BUFS) count = N_WORK_WARPS + 1;
+            if ((i >= Smem::S_READ && i < Smem::S_READ + S_BUFS) ||
+                (i >= Smem::ALPHA_READ && i < Smem::ALPHA_READ + P_BUFS) ||
+                (i >= Smem::CORR_DONE && i < Smem::CORR_DONE + P_BUFS))
+                count = N_WORK_WARPS;
+            if (i >= Smem::P_STAGED && i < Smem::P_STAGED + STAGES) count = N_WORK_WARPS;
+            // the leader's correction warps, one forwarded arrival for the other
+            // output CTA's, plus the V load
+            if (i >= Smem::PV_READY && i < Smem::PV_READY + P_BUFS) count = N_WORK_WARPS + 2;
             mbar_init(&bars[i], count);
         }
         *abort = 0;
@@ -291,10 +332,14 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         if (warp == 0) {
             if (lane == 0) {
                 // -------------------------------------------------- Q and K loads
-                const uint32_t q_bytes = static_cast<uint32_t>(8 * 128 * p.rows_per_tile);
+                const uint32_t q_bytes = static_cast<uint32_t>(4 * 128 * p.rows_per_tile);   // 4 boxes
                 if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::Q_FULL], 2 * q_bytes);
-                for (int c = 0; c < 8; ++c)
+                mbar_arrive_expect_tx(&bars[Smem::Q_HI], q_bytes);
+                for (int c = 0; c < 4; ++c)
                     tma2_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, bar_of(Smem::Q_FULL, 0), c * 64, 0, kvh, t0);
+                for (int c = 4; c < 8; ++c)
+                    tma2_load_4d(smem + Smem::stage + (c - 4) * Q_CHUNK, &tmq, bar_of(Smem::Q_HI, rank), c * 64, 0,
+                                 kvh, t0);
                 // half tile h: tile h / 2, head-dim columns 256 (h % 2) .. +256, this CTA's 64 keys
                 for (int h = 0; h < 2 * n_kt; ++h) {
                     const int j = h >> 1, c = h & 1, s = h % K_SLOTS;
@@ -316,10 +361,22 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                                      (c * 4 + b) * 64, kvh, key);
                 }
             }
+        } else if (warp == 1 && rank == 1) {
+            if (lane == 0) {
+                // -------------------------------------------------- forward "S read" to the leader
+                // (one cluster-scope arrival per tile from an idle thread: such an
+                // arrival stalls the thread that makes it)
+                for (int j = 0; j < n_kt; ++j) {
+                    if (!wait_or_abort(&bars[Smem::S_READ + (j % S_BUFS)], (j / S_BUFS) & 1, p.err, abort, wait_ns))
+                        break;
+                    mbar_arrive_remote(bar_of(Smem::S_FREE + (j % S_BUFS), 0));
+                }
+            }
         } else if (warp == 1) {
             if (lane == 0 && rank == 0) {
                 // -------------------------------------------------- S = Q K^T (both SMs)
-                bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort, wait_ns);
+                bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort, wait_ns) &&
+                          wait_or_abort(&bars[Smem::Q_TMEM], 0, p.err, abort, wait_ns);
                 const uint64_t q_desc = make_sdesc_sw128(smem_u32(smem + Smem::q), 16, 1024);
                 const uint64_t k_desc = make_sdesc_sw128(smem_u32(smem + Smem::kring), 16, 1024);
                 for (int j = 0; ok && j < n_kt; ++j) {
@@ -329,15 +386,25 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                         if (!(ok = wait_or_abort(&bars[Smem::K_FULL + s], (h / K_SLOTS) & 1, p.err, abort, wait_ns)))
                             break;
                         tc_fence_after_sync();
-                        const uint64_t ad0 = q_desc + static_cast<uint64_t>(c * 4 * (Q_CHUNK >> 4));
                         const uint64_t bd0 = k_desc + static_cast<uint64_t>(s * (SLOT >> 4));
+                        if (c == 0) {
 #pragma unroll
-                        for (int k16 = 0; k16 < 16; ++k16) {
-                            // head-dim chunk 4c + (k16 >> 2), 16 columns at a time (start field in 16 B units)
-                            const uint64_t off = static_cast<uint64_t>((k16 & 3) * 2);
-                            mma2_ss(sb, ad0 + static_cast<uint64_t>((k16 >> 2) * (Q_CHUNK >> 4)) + off,
-                                    bd0 + static_cast<uint64_t>((k16 >> 2) * (K_BOX >> 4)) + off, IDESC_QK,
-                                    (c | k16) ? 1u : 0u);
+                            for (int k16 = 0; k16 < 16; ++k16) {
+                                // head-dim chunk k16 >> 2 of Q in shared memory, 16 columns at a
+                                // time (start field in 16 B units)
+                                const uint64_t off = static_cast<uint64_t>((k16 & 3) * 2);
+                                mma2_ss(sb, q_desc + static_cast<uint64_t>((k16 >> 2) * (Q_CHUNK >> 4)) + off,
+                                        bd0 + static_cast<uint64_t>((k16 >> 2) * (K_BOX >> 4)) + off, IDESC_QK,
+                                        k16 ? 1u : 0u);
+                            }
+                        } else {
+#pragma unroll
+                            for (int k16 = 0; k16 < 16; ++k16) {
+                                // head-dim columns 256 + 16 k16 .. from TMEM (two bf16 a column)
+                                const uint64_t off = static_cast<uint64_t>((k16 & 3) * 2);
+                                mma2_ts(sb, tmem + TM_QHI + static_cast<uint32_t>(k16 * 8),
+                                        bd0 + static_cast<uint64_t>((k16 >> 2) * (K_BOX >> 4)) + off, IDESC_QK, 1u);
+                            }
                         }
                         commit2_mask(&bars[Smem::K_EMPTY + s], MASK_SCORE);
                     }
@@ -347,82 +414,126 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 commit2_mask(&bars[Smem::DRAIN], static_cast<uint16_t>(1u << rank));
                 (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err, wait_ns);
             }
+        } else if (warp == COPY_WARP) {
+            if (lane == 0) {
+                // -------------------------------------------------- P tiles to the output CTA
+                const uint32_t out_rank = rank + 2;
+                for (int j = 0; j < n_kt; ++j) {
+                    const int b2 = j & 1, pb = j % P_BUFS;
+                    // all softmax warps staged tile j, and the output CTA's P
+                    // buffer pb is free (O += P V of tile j - 3 completed)
+                    if (!wait_or_abort(&bars[Smem::P_STAGED + b2], (j >> 1) & 1, p.err, abort, wait_ns)) break;
+                    if (j >= P_BUFS &&
+                        !wait_or_abort(&bars[Smem::PV_DONE + pb], ((j / P_BUFS) - 1) & 1, p.err, abort, wait_ns))
+                        break;
+                    bulk_copy_to_cluster(map_to_cta(smem_u32(smem + Smem::precv + pb * P_BUF), out_rank),
+                                         smem_u32(smem + Smem::stage + b2 * P_BUF), P_BUF,
+                                         bar_of(Smem::P_LANDED + pb, out_rank));
+                }
+            }
         } else {
             // ------------------------------------------------------ softmax
-            float* xmax = reinterpret_cast<float*>(smem + Smem::xmax);
-            float m_ref = -INFINITY;   // log2 units, the same in both key halves
-            float l = 0.f;             // this half's sum of the fp32 probabilities (for LSE)
-            float l_b = 0.f;           // this half's sum of the bf16-rounded probabilities
+            __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + Smem::xmax);
+            float m_ref = -INFINITY;   // log2 units, the same in all four parts
+            float l = 0.f;             // this part's sum of the fp32 probabilities (for LSE)
+            float l_b = 0.f;           // this part's sum of the bf16-rounded probabilities
             bool ok = true;
             const bool neg_scale = p.scale_log2 < 0.f;
             const uint32_t out_rank = rank + 2;
-            // this row's place in the output CTA's P buffers and alpha array
-            const uint32_t p_dst = map_to_cta(smem_u32(smem + Smem::precv + kh * P_CHUNK + row * 128), out_rank);
             const uint32_t a_dst = map_to_cta(smem_u32(smem + Smem::alpha + row * 4), out_rank);
 
+            // Q head-dim columns 256-511 to TMEM (the operand of the second half
+            // of every QK^T): this warp's 64-column chunk of its rows, undoing
+            // the 128-byte swizzle
+            ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::Q_HI], 0, p.err, abort, wait_ns));
+            if (ok) {
+                for (int cc = 0; cc < 4 / PARTS; ++cc) {
+                    const int c4 = part * (4 / PARTS) + cc;     // chunk 4 + c4 of Q
+                    const uint8_t* src = smem + Smem::stage + c4 * Q_CHUNK + row * 128;
+                    uint32_t w[32];
+#pragma unroll
+                    for (int pc = 0; pc < 8; ++pc) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(src + ((pc ^ (row & 7)) << 4));
+                        w[4 * pc] = x.x;
+                        w[4 * pc + 1] = x.y;
+                        w[4 * pc + 2] = x.z;
+                        w[4 * pc + 3] = x.w;
+                    }
+                    tmem_st32(tmem + lane_base + TM_QHI + static_cast<uint32_t>(c4 * 32), w);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 0) mbar_arrive(&bars[Smem::Q_TMEM]);
+                else mbar_arrive_remote(bar_of(Smem::Q_TMEM, 0));
+            }
+
             for (int j = 0; ok && j < n_kt; ++j) {
-                const int b4 = j % S_BUFS, b2 = j & 1;
+                const int b3 = j % S_BUFS, b2 = j & 1, pb = j % P_BUFS;
                 // (every wait of a softmax warp is made warp-uniform: the warp
                 // synchronises below and must leave the loop as one)
-                if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::S_FULL + b4], (j / S_BUFS) & 1, p.err,
+                if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::S_FULL + b3], (j / S_BUFS) & 1, p.err,
                                                                  abort, wait_ns))))
                     break;
                 tc_fence_after_sync();
-                uint32_t sr[2][32];
-                const uint32_t s_col = static_cast<uint32_t>(b4 * BN + kh * BH);
-                tmem_ld32(tmem + lane_base + s_col, sr[0]);
-                tmem_ld32(tmem + lane_base + s_col + 32, sr[1]);
+                uint32_t sr[KP];
+#pragma unroll
+                for (int c = 0; c < KP / 32; ++c)
+                    tmem_ld32(tmem + lane_base + static_cast<uint32_t>(b3 * BN + part * KP + 32 * c),
+                              *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
                 tmem_ld_wait();
-                // the S buffer may take the QK^T four tiles on
+                // the S buffer may take the QK^T three tiles on
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) {
-                    if (rank == 0) mbar_arrive(&bars[Smem::S_FREE + b4]);
-                    else mbar_arrive_remote(bar_of(Smem::S_FREE + b4, 0));
-                }
-                float s[64];
+                if (lane == 0) mbar_arrive(&bars[rank == 0 ? Smem::S_FREE + b3 : Smem::S_READ + b3]);
+                float s[KP];
 #pragma unroll
-                for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                for (int c = 0; c < KP; ++c) s[c] = __uint_as_float(sr[c]);
 
-                const int key0 = (kt_begin + j) * BN + kh * BH;
-                const bool half_full = ntok > 0 && key0 + BH <= p.seqlen_k &&
-                                       (!p.causal || key0 + BH - 1 <= p_first) &&
+                const int key0 = (kt_begin + j) * BN + part * KP;
+                const bool part_full = ntok > 0 && key0 + KP <= p.seqlen_k &&
+                                       (!p.causal || key0 + KP - 1 <= p_first) &&
                                        (p.window <= 0 || key0 > p_last - p.window);
                 // scores stay unscaled until the exponent; a hidden key gets the
                 // value that scales to -inf whatever the sign of the scale
-                if (!half_full) {
+                if (!part_full) {
                     const float hidden = neg_scale ? INFINITY : -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
+                    for (int c = 0; c < KP; ++c)
                         if (!key_visible(key0 + c, qpos, p)) s[c] = hidden;
                 }
-                float mx[16];
+                float mx[KP / 4];
                 if (!neg_scale) {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
+                    for (int c = 0; c < KP / 4; ++c)
                         mx[c] = fmaxf(fmaxf(s[4 * c], s[4 * c + 1]), fmaxf(s[4 * c + 2], s[4 * c + 3]));
 #pragma unroll
-                    for (int w = 8; w >= 1; w >>= 1)
+                    for (int w = KP / 8; w >= 1; w >>= 1)
 #pragma unroll
                         for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
+                    for (int c = 0; c < KP / 4; ++c)
                         mx[c] = fminf(fminf(s[4 * c], s[4 * c + 1]), fminf(s[4 * c + 2], s[4 * c + 3]));
 #pragma unroll
-                    for (int w = 8; w >= 1; w >>= 1)
+                    for (int w = KP / 8; w >= 1; w >>= 1)
 #pragma unroll
                         for (int c = 0; c < w; ++c) mx[c] = fminf(mx[c], mx[c + w]);
                 }
-                // row max over the whole tile: swap the halves' maxima (log2
-                // units); both halves then take the same decision on the same numbers
-                const float own_max = mx[0] * p.scale_log2;
-                xmax[(b2 * 2 + kh) * BM + row] = own_max;
+                // row max over the whole tile: the four parts swap their maxima
+                // (log2 units, rounded up to bf16 so that all four take the same
+                // decision on the same numbers)
+                xmax[(b2 * PARTS + part) * BM + row] = __float2bfloat16_ru(mx[0] * p.scale_log2);
                 mbar_arrive(&bars[Smem::XCHG + b2]);
                 if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::XCHG + b2], (j >> 1) & 1, p.err, abort,
                                                                  wait_ns))))
                     break;
-                const float tmax = fmaxf(own_max, xmax[(b2 * 2 + (kh ^ 1)) * BM + row]);
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int q4 = 0; q4 < PARTS; ++q4)
+                    tmax = fmaxf(tmax, __bfloat162float(xmax[(b2 * PARTS + q4) * BM + row]));
 
                 float m_use = m_ref, alpha = 1.f;
                 if (tmax > m_ref + RESCALE_THRESHOLD) {
@@ -430,55 +541,70 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     alpha = fast_exp2(m_ref - m_use);   // 0 when m_ref = -inf
                 }
                 const float shift = m_use == -INFINITY ? 0.f : m_use;
-                uint32_t pk[32];
-                float2 ps[4], pb[4];
+                uint32_t pk[KP / 2];
+                float2 ps[2], pbs[2];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) ps[c] = pb[c] = make_float2(0.f, 0.f);
+                for (int c = 0; c < 2; ++c) ps[c] = pbs[c] = make_float2(0.f, 0.f);
                 const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
                 const float2 nsh = make_float2(-shift, -shift);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
+                for (int c = 0; c < KP / 2; ++c) {
                     // p = 2^(s * scale * log2(e) - shift), two lanes per instruction
                     const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2, nsh);
                     const float2 pr2 = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                    ps[c & 3] = fadd2(ps[c & 3], pr2);
+                    ps[c & 1] = fadd2(ps[c & 1], pr2);
                     pk[c] = pack_bf16x2(pr2.x, pr2.y);
                     // the bf16 values the PV product actually uses
-                    pb[c & 3] = fadd2(pb[c & 3], make_float2(__uint_as_float(pk[c] << 16),
-                                                             __uint_as_float(pk[c] & 0xffff0000u)));
+                    pbs[c & 1] = fadd2(pbs[c & 1], make_float2(__uint_as_float(pk[c] << 16),
+                                                               __uint_as_float(pk[c] & 0xffff0000u)));
                 }
-                const float2 ps01 = fadd2(fadd2(ps[0], ps[1]), fadd2(ps[2], ps[3]));
-                const float2 pb01 = fadd2(fadd2(pb[0], pb[1]), fadd2(pb[2], pb[3]));
+                const float2 ps01 = fadd2(ps[0], ps[1]);
+                const float2 pb01 = fadd2(pbs[0], pbs[1]);
                 l = l * alpha + (ps01.x + ps01.y);
                 l_b = l_b * alpha + (pb01.x + pb01.y);
                 m_ref = m_use;
 
-                // the output CTA's P buffer b2 is free once O += P V of tile j - 2 completed
-                if (j >= 2 && !(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::PV_DONE + b2],
-                                                                           ((j >> 1) - 1) & 1, p.err, abort,
-                                                                           wait_ns))))
+                // staging buffer b2: its copy of tile j - 2 has landed and the
+                // output CTA has read that tile's alpha (which also means its
+                // barrier phase for tile j - 3 has completed)
+                if (j >= STAGES && !(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::STAGE_FREE + b2],
+                                                                               ((j >> 1) - 1) & 1, p.err, abort,
+                                                                               wait_ns))))
                     break;
-                // P of this row's 64 keys: eight 16-byte pieces in the 128-byte
-                // swizzle the MMA descriptor expects (piece c at c ^ (row % 8))
-                const uint32_t dst = p_dst + static_cast<uint32_t>(b2 * P_BUF);
-                const uint32_t xbar = bar_of(Smem::P_LANDED + b2, out_rank);
+                // P of this row's KP keys: KP / 8 16-byte pieces of the row's
+                // 128-byte line in its 64-key chunk, in the 128-byte swizzle the
+                // MMA descriptor expects (piece c at c ^ (row % 8))
+                uint8_t* stg = smem + Smem::stage + b2 * P_BUF + ((part * KP) >> 6) * P_CHUNK + row * 128;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    st_async_v4(dst + static_cast<uint32_t>(((c8 ^ (row & 7)) << 4)), pk[4 * c8], pk[4 * c8 + 1],
-                                pk[4 * c8 + 2], pk[4 * c8 + 3], xbar);
-                if (kh == 0) st_async_b32(a_dst + static_cast<uint32_t>(b2 * BM * 4), __float_as_uint(alpha), xbar);
+                for (int c4 = 0; c4 < KP / 8; ++c4) {
+                    const int pc = ((part * KP) & 63) / 8 + c4;
+                    *reinterpret_cast<uint4*>(stg + ((pc ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+                }
+                const uint32_t xbar = bar_of(Smem::P_LANDED + pb, out_rank);
+                if (part == 0) st_async_b32(a_dst + static_cast<uint32_t>(pb * BM * 4), __float_as_uint(alpha), xbar);
+                // the copy engine reads the staged tile: order these writes
+                // before it; the copy warp moves the whole tile once all
+                // sixteen warps have staged
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[Smem::P_STAGED + b2]);
             }
-            // Swap the halves' row sums through the Q area, idle once every
-            // QK^T has completed (the last S_FULL was seen).  Each thread
-            // arrives exactly once, so the wait ends.
+            // Sum the parts' row sums through the Q area, idle once every QK^T
+            // has completed (the last S_FULL was seen).  Each thread arrives
+            // exactly once, so the wait ends.
             float* lsum = reinterpret_cast<float*>(smem + Smem::q);
-            lsum[(kh * BM + row) * 2 + 0] = l;
-            lsum[(kh * BM + row) * 2 + 1] = l_b;
+            lsum[(part * BM + row) * 2 + 0] = l;
+            lsum[(part * BM + row) * 2 + 1] = l_b;
             mbar_arrive(&bars[Smem::L_XCHG]);
             if (ok) ok = wait_or_abort(&bars[Smem::L_XCHG], 0, p.err, abort, wait_ns);
-            if (ok && kh == 0) {
-                const float l_all = l + lsum[(BM + row) * 2 + 0];
-                const float lb_all = l_b + lsum[(BM + row) * 2 + 1];
+            if (ok && part == 0) {
+                float l_all = 0.f, lb_all = 0.f;
+#pragma unroll
+                for (int q4 = 0; q4 < PARTS; ++q4) {
+                    l_all += lsum[(q4 * BM + row) * 2 + 0];
+                    lb_all += lsum[(q4 * BM + row) * 2 + 1];
+                }
                 // O / sum(p~) with p~ the rounded weights PV used: O stays an
                 // exact convex combination of V rows whatever the rounding of P
                 st_async_b32(map_to_cta(smem_u32(smem + Smem::lrecv + row * 4), out_rank), __float_as_uint(lb_all),
@@ -493,17 +619,42 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (lane == 0) {
                 // -------------------------------------------------- V loads
                 for (int j = 0; j < n_kt; ++j) {
-                    const int b2 = j & 1;
-                    // V slots of buffer b2 once O += P V of tile j - 2 completed
-                    if (j >= 2 && !wait_or_abort(&bars[Smem::PV_DONE + b2], ((j >> 1) - 1) & 1, p.err, abort, wait_ns))
+                    const int vb = j & 1;
+                    // V buffer vb once O += P V of tile j - 2 completed
+                    if (j >= 2 && !wait_or_abort(&bars[Smem::PV_DONE + (j - 2) % P_BUFS], ((j - 2) / P_BUFS) & 1,
+                                                 p.err, abort, wait_ns))
                         break;
-                    if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + b2], 2 * 2 * SLOT);
+                    // (the tile's ready barrier goes with its P buffer: the
+                    // correction warps may run three tiles ahead of the MMAs)
+                    const int rb = j % P_BUFS;
+                    if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
                     const int key = (kt_begin + j) * BN;
                     for (int hh = 0; hh < 2; ++hh)
                         for (int bx = 0; bx < 2; ++bx)
-                            tma2_load_3d(smem + Smem::vring + (2 * b2 + hh) * SLOT + bx * V_BOX, &tmv,
-                                         bar_of(Smem::PV_READY + b2, 2),
+                            tma2_load_3d(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX, &tmv,
+                                         bar_of(Smem::PV_READY + rb, 2),
                                          (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh, key);
+                }
+            }
+        } else if (warp == 1 && rank == 3) {
+            if (lane == 0) {
+                // -------------------------------------------------- forward "tile ready" to the leader
+                for (int j = 0; j < n_kt; ++j) {
+                    if (!wait_or_abort(&bars[Smem::CORR_DONE + (j % P_BUFS)], (j / P_BUFS) & 1, p.err, abort, wait_ns))
+                        break;
+                    tc_fence_after_sync();
+                    tc_fence_before_sync();
+                    mbar_arrive_remote(bar_of(Smem::PV_READY + (j % P_BUFS), 2));
+                }
+            }
+        } else if (warp == COPY_WARP) {
+            if (lane == 0) {
+                // -------------------------------------------------- forward "copy landed, alpha read"
+                for (int j = 0; j < n_kt; ++j) {
+                    if (!wait_or_abort(&bars[Smem::ALPHA_READ + (j % P_BUFS)], (j / P_BUFS) & 1, p.err, abort,
+                                       wait_ns))
+                        break;
+                    mbar_arrive_remote(bar_of(Smem::STAGE_FREE + (j & 1), rank - 2));
                 }
             }
         } else if (warp == 1) {
@@ -513,12 +664,12 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 const uint64_t p_desc = make_sdesc_sw128(smem_u32(smem + Smem::precv), 16, 1024);
                 const uint64_t v_desc = make_sdesc_sw128(smem_u32(smem + Smem::vring), V_BOX, 1024);
                 for (int j = 0; ok && j < n_kt; ++j) {
-                    const int b2 = j & 1;
-                    if (!(ok = wait_or_abort(&bars[Smem::PV_READY + b2], (j >> 1) & 1, p.err, abort, wait_ns)))
+                    const int vb = j & 1, pb = j % P_BUFS;
+                    if (!(ok = wait_or_abort(&bars[Smem::PV_READY + pb], (j / P_BUFS) & 1, p.err, abort, wait_ns)))
                         break;
                     tc_fence_after_sync();
-                    const uint64_t ad0 = p_desc + static_cast<uint64_t>(b2 * (P_BUF >> 4));
-                    const uint64_t bd0 = v_desc + static_cast<uint64_t>(2 * b2 * (SLOT >> 4));
+                    const uint64_t ad0 = p_desc + static_cast<uint64_t>(pb * (P_BUF >> 4));
+                    const uint64_t bd0 = v_desc + static_cast<uint64_t>(2 * vb * (SLOT >> 4));
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
                         // P keys 16 kk .. 16 kk + 15: chunk kk / 4, 32 bytes per step within it;
@@ -530,36 +681,41 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                                 (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     // frees the tile's V slots and P buffer; O may be corrected for the next tile
-                    commit2_mask(&bars[Smem::PV_DONE + b2], MASK_ALL);
+                    commit2_mask(&bars[Smem::PV_DONE + pb], MASK_ALL);
                 }
                 if (ok) commit2_mask(&bars[Smem::O_FINAL], MASK_OUTPUT);
                 commit2_mask(&bars[Smem::DRAIN], static_cast<uint16_t>(1u << rank));
                 (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err, wait_ns);
             }
-        } else {
+        } else if (work_warp) {
             // -------------------------------------------------- O correction + epilogue
             const float* alpha_s = reinterpret_cast<const float*>(smem + Smem::alpha);
+            const uint32_t o_col = static_cast<uint32_t>(part * OP);
             bool ok = true;
             if (warp == 2 && lane == 0) mbar_arrive_expect_tx(&bars[Smem::L_READY], L_TX);
             for (int j = 0; ok && j < n_kt; ++j) {
-                const int b2 = j & 1;
-                // P_LANDED[b2]'s phase for tile j - 2 completed before this point
-                if (warp == 2 && lane == 0) mbar_arrive_expect_tx(&bars[Smem::P_LANDED + b2], P_TX);
-                if (!(ok = __all_sync(0xffffffffu, wait_cluster_or_abort(&bars[Smem::P_LANDED + b2], (j >> 1) & 1,
-                                                                         p.err, abort, wait_ns))))
+                const int pb = j % P_BUFS;
+                // P_LANDED[pb]'s phase for tile j - 3 completed before this point
+                if (warp == 2 && lane == 0) mbar_arrive_expect_tx(&bars[Smem::P_LANDED + pb], P_TX);
+                if (!(ok = __all_sync(0xffffffffu, wait_cluster_or_abort(&bars[Smem::P_LANDED + pb],
+                                                                         (j / P_BUFS) & 1, p.err, abort, wait_ns))))
                     break;
-                // P arrived through the generic proxy; the MMA reads it through the async proxy
+                // P arrived through the copy engine and alpha through remote
+                // stores; the MMA reads P through the async proxy
                 fence_proxy_async_smem();
-                const float a = alpha_s[b2 * BM + row];
-                if (j > 0 && __any_sync(0xffffffffu, a != 1.f)) {
+                const float a = alpha_s[pb * BM + row];
+                const bool rescale = j > 0 && __any_sync(0xffffffffu, a != 1.f);
+                // this tile's copy landed and its alpha was read (forwarded to the score CTA)
+                if (lane == 0) mbar_arrive(&bars[Smem::ALPHA_READ + pb]);
+                if (rescale) {
                     // O += P V of the previous tile must be done before O is corrected
-                    if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::PV_DONE + ((j - 1) & 1)],
-                                                                     ((j - 1) >> 1) & 1, p.err, abort, wait_ns))))
+                    if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::PV_DONE + (j - 1) % P_BUFS],
+                                                                     ((j - 1) / P_BUFS) & 1, p.err, abort, wait_ns))))
                         break;
                     tc_fence_after_sync();
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < OP / 32; ++c) {
                         uint32_t o[32];
-                        const uint32_t oc = static_cast<uint32_t>(kh * 256 + c * 32);
+                        const uint32_t oc = o_col + static_cast<uint32_t>(c * 32);
                         tmem_ld32(tmem + lane_base + oc, o);
                         tmem_ld_wait();
 #pragma unroll
@@ -570,10 +726,7 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) {
-                    if (rank == 2) mbar_arrive(&bars[Smem::PV_READY + b2]);
-                    else mbar_arrive_remote(bar_of(Smem::PV_READY + b2, 2));
-                }
+                if (lane == 0) mbar_arrive(&bars[rank == 2 ? Smem::PV_READY + pb : Smem::CORR_DONE + pb]);
             }
             if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::O_FINAL], 0, p.err, abort, wait_ns));
             if (ok) ok = __all_sync(0xffffffffu, wait_cluster_or_abort(&bars[Smem::L_READY], 0, p.err, abort, wait_ns));
@@ -581,10 +734,10 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 tc_fence_after_sync();
                 const float lb = reinterpret_cast<const float*>(smem + Smem::lrecv)[row];
                 const float inv_l = lb > 0.f ? 1.f / lb : 0.f;
-                __nv_bfloat16* dst = p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + kh * 256;
-                for (int c = 0; c < 8; ++c) {
+                __nv_bfloat16* dst = p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + o_col;
+                for (int c = 0; c < OP / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + static_cast<uint32_t>(kh * 256 + c * 32), o);
+                    tmem_ld32(tmem + lane_base + o_col + static_cast<uint32_t>(c * 32), o);
                     tmem_ld_wait();
                     if (valid_row) {
                         uint32_t pk[16];
