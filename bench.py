@@ -554,7 +554,7 @@ def run_ours(args):
 
     peaks, peak_kind = read_peaks()
     pf_avg_s = t_pf / args.steps if not args.no_prefill else float("nan")
-    pf_src = source_digest(["prefill_sm103.cu", "fa512_pair.cuh", "fa512_device.cuh", "fa512_internal.h"])
+    pf_src = source_digest(["prefill_so_sm103.cu", "fa512_pair.cuh", "fa512_device.cuh", "fa512_internal.h"])
     dec_src = source_digest(["decode_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
     roofline = {"kernel": "fa512::prefill::prefill_kernel", "bound": "tensor",
                 "achieved": pf_flops / pf_avg_s / 1e12, "peak": peaks["bf16_tflops"],

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(CSRC, "_build")
 OUT = os.path.join(HERE, "libfa512.so")
-SOURCES = ["api.cu", "prefill_sm103.cu", "prefill_so_sm103.cu", "prefill256_sm103.cu", "decode_sm103.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "prefill_so_sm103.cu", "prefill256_sm103.cu", "decode_sm103.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -267,7 +267,7 @@ fa512_status prefill_call(const void* q, const void* k, const void* v, void* out
         st = encode_bf16(&tmv, v, 3, dims, strides, vbox);
         if (st != FA512_OK) return st;
     }
-    e = fa512::launch_prefill_so(tmq, tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
+    e = fa512::launch_prefill(tmq, tmk, tmv, p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return FA512_OK;
 }

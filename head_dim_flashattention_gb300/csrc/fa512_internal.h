@@ -99,11 +99,6 @@ cudaError_t launch_prefill256(const CUtensorMap& tmq, const CUtensorMap& tmk, co
 void set_last_error_message(const char* msg);
 cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                            const PrefillParams& p, cudaStream_t stream);
-// Contiguous prefill with the score and output work on different SM pairs
-// of a 4-CTA cluster (the same tensor maps and parameters as launch_prefill).
-int prefill_so_smem_bytes();
-cudaError_t launch_prefill_so(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                              const PrefillParams& p, cudaStream_t stream);
 int prefill_paged_v_box_rows();   // keys per V box over a paged cache (one page-aligned half tile)
 cudaError_t launch_prefill_paged(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                                  const PrefillParams& p, cudaStream_t stream);

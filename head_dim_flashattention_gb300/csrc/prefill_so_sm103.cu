@@ -36,8 +36,7 @@
 // MMAs; the producer holds back a tile's first K half until its S buffer has
 // been read.  Eight softmax warps: TMEM lane quadrant (warp % 4) gives a warp
 // its 32 rows, warps 2-5 take keys 0-63 of each tile and warps 6-9 keys
-// 64-127; they swap row maxima (rounded up to bf16, so both take the same
-// decision) through shared memory.  The row max is lazy: O is rescaled only
+// 64-127; they swap row maxima through shared memory.  The row max is lazy: O is rescaled only
 // when a row's max grows by more than 2^8.  P goes to one of two staging
 // buffers; a copy warp moves each staged tile with one bulk copy (the copy
 // engine) into the output CTA, where it completes on that CTA's mbarrier;
@@ -65,6 +64,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "fa512_device.cuh"
 #include "fa512_internal.h"
@@ -113,7 +114,7 @@ struct Smem {
     static constexpr int q = 0;                                 // 4 x 16 KiB
     static constexpr int kring = q + 4 * Q_CHUNK;               // 3 x 32 KiB
     static constexpr int stage = kring + K_SLOTS * SLOT;        // 2 x 32 KiB
-    static constexpr int xmax = stage + STAGES * P_BUF;         // [2 buffers][4 parts][128] bf16
+    static constexpr int xmax = stage + STAGES * P_BUF;         // [2 buffers][PARTS][128] f32
     // output CTAs
     static constexpr int vring = 0;                             // 4 x 32 KiB
     static constexpr int precv = vring + V_SLOTS * SLOT;        // 3 x 32 KiB
@@ -143,7 +144,8 @@ struct Smem {
         L_READY = O_FINAL + 1,           // output CTAs: the row sums arrived
         ALPHA_READ = L_READY + 1,        // [3] output CTAs: correction warps read the tile's alpha
         CORR_DONE = ALPHA_READ + P_BUFS, // [3] output CTA 3: its correction warps are done with the tile
-        DRAIN = CORR_DONE + P_BUFS,      // every MMA this CTA issued has completed
+        V_TAIL = CORR_DONE + P_BUFS,     // paged, output CTAs: this CTA's V of the tile holding the cache's end landed
+        DRAIN = V_TAIL + 1,              // every MMA this CTA issued has completed
         N_BARS = DRAIN + 1
     };
     static constexpr int tmem_addr = bars + N_BARS * 8;
@@ -151,7 +153,7 @@ struct Smem {
     static constexpr int skip_flag = abort_flag + 4;             // written by rank 0 into all four
     static constexpr int total = skip_flag + 4;
 };
-static_assert(Smem::lrecv + BM * 4 <= Smem::bars && Smem::xmax + 2 * PARTS * BM * 2 <= Smem::bars, "layout");
+static_assert(Smem::lrecv + BM * 4 <= Smem::bars && Smem::xmax + 2 * PARTS * BM * 4 <= Smem::bars, "layout");
 static_assert(Smem::kring % 1024 == 0 && Smem::precv % 1024 == 0, "swizzled buffers on 1 KiB");
 // The dynamic shared-memory window starts 1 KiB aligned (checked at run
 // time), which the 128-byte swizzle atoms need.
@@ -160,8 +162,8 @@ static_assert(Smem::total <= 232448, "shared memory budget");
 constexpr uint32_t IDESC_QK = make_idesc_bf16(2 * BM, BN, 0);
 constexpr uint32_t IDESC_PV = make_idesc_bf16(2 * BM, 256, 1);
 
-__device__ __forceinline__ bool key_visible(int j, int qpos, const PrefillParams& p) {
-    return j < p.seqlen_k && (!p.causal || j <= qpos) && (p.window <= 0 || j > qpos - p.window);
+__device__ __forceinline__ bool key_visible(int j, int qpos, int seqlen_k, const PrefillParams& p) {
+    return j < seqlen_k && (!p.causal || j <= qpos) && (p.window <= 0 || j > qpos - p.window);
 }
 
 // Commit of every MMA issued so far by this thread, arriving on the barrier
@@ -209,6 +211,10 @@ __device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t pa
     }
 }
 
+// PAGED: a batch of chunks (varlen rows through cu_seqlens_q) over a paged
+// cache; K and V rows are found through the page table one 64-key half tile
+// at a time (a page holds a whole number of half tiles).
+template <bool PAGED>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
@@ -235,23 +241,137 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     const uint32_t pr = rank & 1;                       // which q tile of the pair
     const int G = p.group;
     const int T = p.tokens_per_tile;
-    const int n_pairs = (p.num_q_tiles + 1) / 2;
     const int item = blockIdx.x >> 2;
-    const int kvh = item / n_pairs;
-    const int pair = n_pairs - 1 - item % n_pairs;
+    int kvh, pair, seq = 0, q_start = 0;
+    int seqlen_q = p.seqlen_q, seqlen_k = p.seqlen_k, q_offset = p.q_offset;
+    if constexpr (PAGED) {
+        // Work items are numbered sequence by sequence, KV head by KV head,
+        // heaviest pair first, with no gaps: warp 0 finds this cluster's
+        // sequence by a scan of the chunk lengths (one contiguous block of
+        // sequences per lane), the others wait at the barrier below.
+        int* found = reinterpret_cast<int*>(smem + Smem::xmax);   // idle until the pipeline starts
+        const int two_t = 2 * T;
+        // pairs of a chunk with rows [s0, s1) (0 for a malformed entry; block 0 records those)
+        auto chunk_pairs = [&](int s0, int s1) -> int {
+            int n = s1 - s0;
+            if (s0 < 0 || n < 0 || s0 > p.total_q - n) {
+                if (blockIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                return 0;
+            }
+            if (n > p.max_seqlen_q) {
+                if (blockIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                n = p.max_seqlen_q;
+            }
+            return (n + two_t - 1) / two_t;
+        };
+        if (warp == 0) {
+            const int per = (p.batch + 31) >> 5;
+            const int lo = min(p.batch, lane * per), hi = min(p.batch, lo + per);
+            // up to 32 sequences: one sequence per lane, all loads in flight at once
+            int s0 = 0, s1 = 0, kv = 0;
+            if (per == 1 && lo < hi) {
+                s0 = p.cu_seqlens_q[lo];
+                s1 = p.cu_seqlens_q[lo + 1];
+                kv = p.seqused_k[lo];
+            }
+            int cnt = 0;
+            if (per == 1) {
+                if (lo < hi) cnt = chunk_pairs(s0, s1) * p.n_kv_heads;
+            } else {
+                for (int b = lo; b < hi; ++b)
+                    cnt += chunk_pairs(p.cu_seqlens_q[b], p.cu_seqlens_q[b + 1]) * p.n_kv_heads;
+            }
+            int incl = cnt;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += t;
+            }
+            const int excl = incl - cnt;
+            const unsigned owner_mask = __ballot_sync(0xffffffffu, item >= excl && item < incl);
+            if (owner_mask) {
+                const int owner = __ffs(owner_mask) - 1;
+                if (lane == owner) {
+                    int f_seq = lo, acc = excl;
+                    if (per > 1) {
+                        for (int b = lo; b < hi; ++b) {
+                            s0 = p.cu_seqlens_q[b];
+                            s1 = p.cu_seqlens_q[b + 1];
+                            const int c = chunk_pairs(s0, s1) * p.n_kv_heads;
+                            if (item < acc + c) {
+                                f_seq = b;
+                                break;
+                            }
+                            acc += c;
+                        }
+                        kv = p.seqused_k[f_seq];
+                    }
+                    found[0] = f_seq;
+                    found[1] = item - acc;
+                    found[2] = s0;
+                    found[3] = s1;
+                    found[4] = kv;
+                }
+            } else if (lane == 0) {
+                found[0] = -1;
+            }
+        }
+        __syncthreads();
+        seq = found[0];
+        if (seq < 0) return;                            // past the last item: all four CTAs
+        const int off = found[1];
+        q_start = found[2];
+        seqlen_q = min(found[3] - q_start, p.max_seqlen_q);
+        seqlen_k = found[4];
+        const int n_pairs_seq = (seqlen_q + two_t - 1) / two_t;
+        kvh = off / n_pairs_seq;
+        pair = n_pairs_seq - 1 - (off - kvh * n_pairs_seq);   // 0 = heaviest pair first
+        q_offset = seqlen_k - (found[3] - q_start);    // the chunk is its sequence's tail
+        const int kv_cap = p.max_pages_per_seq << p.page_shift;
+        if (seqlen_k < 0 || seqlen_k > kv_cap) {
+            // recorded once per sequence; read up to the table's capacity
+            if (tid == 0 && off == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+            seqlen_k = seqlen_k < 0 ? 0 : kv_cap;
+        }
+        __syncthreads();                                // the scratch is reused below
+    } else {
+        const int n_pairs = (p.num_q_tiles + 1) / 2;
+        kvh = item / n_pairs;
+        pair = n_pairs - 1 - item % n_pairs;
+    }
     const int qt = 2 * pair + static_cast<int>(pr);    // may be one past the last tile: no rows
     const int t0 = qt * T;
-    const int ntok = min(T, p.seqlen_q - t0);           // <= 0 for a missing second tile
-    const int p_first = p.q_offset + t0;
-    const int p_last = p.q_offset + t0 + ntok - 1;
-    const int pair_first = p.q_offset + 2 * pair * T;
-    const int pair_last = p.q_offset + min(p.seqlen_q, (2 * pair + 2) * T) - 1;
-    int j_lo = 0, j_hi = p.seqlen_k;
+    const int ntok = min(T, seqlen_q - t0);             // <= 0 for a missing second tile
+    const int p_first = q_offset + t0;
+    const int p_last = q_offset + t0 + ntok - 1;
+    const int pair_first = q_offset + 2 * pair * T;
+    const int pair_last = q_offset + min(seqlen_q, (2 * pair + 2) * T) - 1;
+    // paged: the tile that holds the cache's last key when that key does not
+    // end a half tile (its V rows past the end are live pool memory)
+    const int tail_tile = (PAGED && (seqlen_k & (K_BOX_ROWS - 1))) ? (seqlen_k - 1) / BN : -1;
+    int j_lo = 0, j_hi = seqlen_k;
     if (p.causal) j_hi = min(j_hi, pair_last + 1);
     if (p.window > 0) j_lo = max(0, pair_first - p.window + 1);
     if (j_hi < j_lo) j_hi = j_lo;
     const int kt_begin = j_lo / BN;
     const int n_kt = j_hi > j_lo ? (j_hi + BN - 1) / BN - kt_begin : 0;
+    // Row of the tensor map holding the first key of the 64-key half tile
+    // that starts at logical key `key`: the key itself, or in paged mode its
+    // slot in the pool.  Halves past the cache's end (and pages outside the
+    // pool) read a row past the pool, which the TMA unit fills with zeros.
+    auto half_row = [&](int key) -> int {
+        if constexpr (PAGED) {
+            if (key >= seqlen_k) return p.oob_row;
+            const int pg = p.page_table[static_cast<size_t>(seq) * p.max_pages_per_seq + (key >> p.page_shift)];
+            if (static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages)) {
+                report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                return p.oob_row;
+            }
+            return (pg << p.page_shift) + (key & ((1 << p.page_shift) - 1));
+        } else {
+            return key;
+        }
+    };
 
     // this thread's packed row and part (warps 2-17): TMEM lane quadrant
     // warp % 4; part = 32 keys of a tile in the score CTAs, 128 O columns in
@@ -262,18 +382,18 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     const int tok = row / G;
     const int g = row - tok * G;
     const bool valid_row = work_warp && row < p.rows_per_tile && tok < ntok;
-    const int qpos = p.q_offset + t0 + tok;
+    const int qpos = q_offset + t0 + tok;
     const int hq = kvh * G + g;
 
     if (n_kt == 0) {
         // no key is visible to any row of the pair: O = 0, LSE = -inf
         if (valid_row) {
             if (!scorer) {
-                uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D +
-                                                      part * OP);
+                uint4* dst = reinterpret_cast<uint4*>(
+                    p.out + (static_cast<size_t>(q_start + t0 + tok) * p.n_q_heads + hq) * D + part * OP);
                 for (int i = 0; i < OP / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
             } else if (part == 0 && p.lse) {
-                p.lse[static_cast<size_t>(hq) * p.total_q + t0 + tok] = -INFINITY;
+                p.lse[static_cast<size_t>(hq) * p.total_q + q_start + t0 + tok] = -INFINITY;
             }
         }
         return;
@@ -336,10 +456,11 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::Q_FULL], 2 * q_bytes);
                 mbar_arrive_expect_tx(&bars[Smem::Q_HI], q_bytes);
                 for (int c = 0; c < 4; ++c)
-                    tma2_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, bar_of(Smem::Q_FULL, 0), c * 64, 0, kvh, t0);
+                    tma2_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, bar_of(Smem::Q_FULL, 0), c * 64, 0, kvh,
+                                 q_start + t0);
                 for (int c = 4; c < 8; ++c)
                     tma2_load_4d(smem + Smem::stage + (c - 4) * Q_CHUNK, &tmq, bar_of(Smem::Q_HI, rank), c * 64, 0,
-                                 kvh, t0);
+                                 kvh, q_start + t0);
                 // half tile h: tile h / 2, head-dim columns 256 (h % 2) .. +256, this CTA's 64 keys
                 for (int h = 0; h < 2 * n_kt; ++h) {
                     const int j = h >> 1, c = h & 1, s = h % K_SLOTS;
@@ -355,10 +476,10 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     // (test hook: the first cluster's rank 0 leaves out its first
                     // K half tile, so that cluster's waits run into their bound)
                     if (h == 0 && p.test_skip_first_k_load && blockIdx.x == 0) continue;
-                    const int key = (kt_begin + j) * BN + static_cast<int>(pr) * K_BOX_ROWS;
+                    const int krow = half_row((kt_begin + j) * BN + static_cast<int>(pr) * K_BOX_ROWS);
                     for (int b = 0; b < 4; ++b)
                         tma2_load_3d(smem + Smem::kring + s * SLOT + b * K_BOX, &tmk, bar_of(Smem::K_FULL + s, 0),
-                                     (c * 4 + b) * 64, kvh, key);
+                                     (c * 4 + b) * 64, kvh, krow);
                 }
             }
         } else if (warp == 1 && rank == 1) {
@@ -433,7 +554,7 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             }
         } else {
             // ------------------------------------------------------ softmax
-            __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + Smem::xmax);
+            float* xmax = reinterpret_cast<float*>(smem + Smem::xmax);
             float m_ref = -INFINITY;   // log2 units, the same in all four parts
             float l = 0.f;             // this part's sum of the fp32 probabilities (for LSE)
             float l_b = 0.f;           // this part's sum of the bf16-rounded probabilities
@@ -493,7 +614,7 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 for (int c = 0; c < KP; ++c) s[c] = __uint_as_float(sr[c]);
 
                 const int key0 = (kt_begin + j) * BN + part * KP;
-                const bool part_full = ntok > 0 && key0 + KP <= p.seqlen_k &&
+                const bool part_full = ntok > 0 && key0 + KP <= seqlen_k &&
                                        (!p.causal || key0 + KP - 1 <= p_first) &&
                                        (p.window <= 0 || key0 > p_last - p.window);
                 // scores stay unscaled until the exponent; a hidden key gets the
@@ -502,7 +623,7 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     const float hidden = neg_scale ? INFINITY : -INFINITY;
 #pragma unroll
                     for (int c = 0; c < KP; ++c)
-                        if (!key_visible(key0 + c, qpos, p)) s[c] = hidden;
+                        if (!key_visible(key0 + c, qpos, seqlen_k, p)) s[c] = hidden;
                 }
                 float mx[KP / 4];
                 if (!neg_scale) {
@@ -522,18 +643,18 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 #pragma unroll
                         for (int c = 0; c < w; ++c) mx[c] = fminf(mx[c], mx[c + w]);
                 }
-                // row max over the whole tile: the four parts swap their maxima
-                // (log2 units, rounded up to bf16 so that all four take the same
-                // decision on the same numbers)
-                xmax[(b2 * PARTS + part) * BM + row] = __float2bfloat16_ru(mx[0] * p.scale_log2);
+                // row max over the whole tile: the parts swap their maxima (log2
+                // units); all then take the same decision on the same numbers
+                const float own_max = mx[0] * p.scale_log2;
+                xmax[(b2 * PARTS + part) * BM + row] = own_max;
                 mbar_arrive(&bars[Smem::XCHG + b2]);
                 if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::XCHG + b2], (j >> 1) & 1, p.err, abort,
                                                                  wait_ns))))
                     break;
-                float tmax = -INFINITY;
+                float tmax = own_max;
 #pragma unroll
-                for (int q4 = 0; q4 < PARTS; ++q4)
-                    tmax = fmaxf(tmax, __bfloat162float(xmax[(b2 * PARTS + q4) * BM + row]));
+                for (int q4 = 1; q4 < PARTS; ++q4)
+                    tmax = fmaxf(tmax, xmax[(b2 * PARTS + ((part + q4) % PARTS)) * BM + row]);
 
                 float m_use = m_ref, alpha = 1.f;
                 if (tmax > m_ref + RESCALE_THRESHOLD) {
@@ -542,9 +663,9 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 }
                 const float shift = m_use == -INFINITY ? 0.f : m_use;
                 uint32_t pk[KP / 2];
-                float2 ps[2], pbs[2];
+                float2 ps[4], pbs[4];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) ps[c] = pbs[c] = make_float2(0.f, 0.f);
+                for (int c = 0; c < 4; ++c) ps[c] = pbs[c] = make_float2(0.f, 0.f);
                 const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
                 const float2 nsh = make_float2(-shift, -shift);
 #pragma unroll
@@ -552,14 +673,14 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     // p = 2^(s * scale * log2(e) - shift), two lanes per instruction
                     const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2, nsh);
                     const float2 pr2 = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                    ps[c & 1] = fadd2(ps[c & 1], pr2);
+                    ps[c & 3] = fadd2(ps[c & 3], pr2);
                     pk[c] = pack_bf16x2(pr2.x, pr2.y);
                     // the bf16 values the PV product actually uses
-                    pbs[c & 1] = fadd2(pbs[c & 1], make_float2(__uint_as_float(pk[c] << 16),
+                    pbs[c & 3] = fadd2(pbs[c & 3], make_float2(__uint_as_float(pk[c] << 16),
                                                                __uint_as_float(pk[c] & 0xffff0000u)));
                 }
-                const float2 ps01 = fadd2(ps[0], ps[1]);
-                const float2 pb01 = fadd2(pbs[0], pbs[1]);
+                const float2 ps01 = fadd2(fadd2(ps[0], ps[1]), fadd2(ps[2], ps[3]));
+                const float2 pb01 = fadd2(fadd2(pbs[0], pbs[1]), fadd2(pbs[2], pbs[3]));
                 l = l * alpha + (ps01.x + ps01.y);
                 l_b = l_b * alpha + (pb01.x + pb01.y);
                 m_ref = m_use;
@@ -610,7 +731,7 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 st_async_b32(map_to_cta(smem_u32(smem + Smem::lrecv + row * 4), out_rank), __float_as_uint(lb_all),
                              bar_of(Smem::L_READY, out_rank));
                 if (valid_row && p.lse)
-                    p.lse[static_cast<size_t>(hq) * p.total_q + t0 + tok] =
+                    p.lse[static_cast<size_t>(hq) * p.total_q + q_start + t0 + tok] =
                         l_all > 0.f ? (m_ref + log2f(l_all)) * 0.69314718055994530942f : -INFINITY;
             }
         }
@@ -627,13 +748,38 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     // (the tile's ready barrier goes with its P buffer: the
                     // correction warps may run three tiles ahead of the MMAs)
                     const int rb = j % P_BUFS;
-                    if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
                     const int key = (kt_begin + j) * BN;
-                    for (int hh = 0; hh < 2; ++hh)
-                        for (int bx = 0; bx < 2; ++bx)
-                            tma2_load_3d(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX, &tmv,
-                                         bar_of(Smem::PV_READY + rb, 2),
-                                         (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh, key);
+                    if constexpr (PAGED) {
+                        // Each V box is one half tile (one page or part of one).
+                        // The tail tile's V lands on this CTA's own barrier: the
+                        // correction warps clear the rows past the cache's end
+                        // before they mark the tile ready (a NaN there would
+                        // survive a zero weight).
+                        const bool tail = kt_begin + j == tail_tile;
+                        uint32_t vbar;
+                        if (tail) {
+                            if (rank == 2) mbar_arrive(&bars[Smem::PV_READY + rb]);
+                            mbar_arrive_expect_tx(&bars[Smem::V_TAIL], 2 * SLOT);
+                            vbar = bar_of(Smem::V_TAIL, rank);
+                        } else {
+                            if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
+                            vbar = bar_of(Smem::PV_READY + rb, 2);
+                        }
+                        const int rows[2] = {half_row(key), half_row(key + K_BOX_ROWS)};
+                        for (int hh = 0; hh < 2; ++hh)
+                            for (int bx = 0; bx < 2; ++bx)
+                                for (int r = 0; r < 2; ++r)
+                                    tma2_load_3d(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX + r * K_BOX,
+                                                 &tmv, vbar, (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh,
+                                                 rows[r]);
+                    } else {
+                        if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
+                        for (int hh = 0; hh < 2; ++hh)
+                            for (int bx = 0; bx < 2; ++bx)
+                                tma2_load_3d(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX, &tmv,
+                                             bar_of(Smem::PV_READY + rb, 2),
+                                             (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh, key);
+                    }
                 }
             }
         } else if (warp == 1 && rank == 3) {
@@ -724,6 +870,25 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     }
                     tmem_st_wait();
                 }
+                if constexpr (PAGED) {
+                    if (kt_begin + j == tail_tile) {
+                        // the tile holding the cache's end: zero this CTA's V rows
+                        // from the end to the end of its half tile, in both O
+                        // halves' slots, then hand them to the tensor core (async proxy)
+                        if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::V_TAIL], 0, p.err, abort,
+                                                                         wait_ns))))
+                            break;
+                        const int r0 = seqlen_k - tail_tile * BN;       // 1 .. 127, not 64
+                        const int n16 = (((r0 + K_BOX_ROWS - 1) & ~(K_BOX_ROWS - 1)) - r0) * 8;   // per box
+                        uint8_t* vs = smem + Smem::vring + (2 * (j & 1)) * SLOT + r0 * 128;
+                        for (int i = tid - 64; i < 4 * n16; i += N_WORK_WARPS * 32) {
+                            const int bx = i / n16;                   // (O half, 64-column box)
+                            *reinterpret_cast<uint4*>(vs + (bx >> 1) * SLOT + (bx & 1) * V_BOX + (i - bx * n16) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[rank == 2 ? Smem::PV_READY + pb : Smem::CORR_DONE + pb]);
@@ -734,7 +899,8 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 tc_fence_after_sync();
                 const float lb = reinterpret_cast<const float*>(smem + Smem::lrecv)[row];
                 const float inv_l = lb > 0.f ? 1.f / lb : 0.f;
-                __nv_bfloat16* dst = p.out + (static_cast<size_t>(t0 + tok) * p.n_q_heads + hq) * D + o_col;
+                __nv_bfloat16* dst =
+                    p.out + (static_cast<size_t>(q_start + t0 + tok) * p.n_q_heads + hq) * D + o_col;
                 for (int c = 0; c < OP / 32; ++c) {
                     uint32_t o[32];
                     tmem_ld32(tmem + lane_base + o_col + static_cast<uint32_t>(c * 32), o);
@@ -768,18 +934,39 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 
 }  // namespace prefill_so
 
-int prefill_so_smem_bytes() { return prefill_so::Smem::total; }
+int prefill_smem_bytes() { return prefill_so::Smem::total; }
+int prefill_k_box_rows() { return prefill_so::K_BOX_ROWS; }
+int prefill_v_box_rows() { return prefill_so::V_BOX_ROWS; }
+int prefill_paged_v_box_rows() { return prefill_so::K_BOX_ROWS; }
 
-cudaError_t launch_prefill_so(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                              const PrefillParams& p, cudaStream_t stream) {
-    const int smem = prefill_so_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(prefill_so::prefill_so_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem);
+cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                           const PrefillParams& p, cudaStream_t stream) {
+    const int smem = prefill_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(prefill_so::prefill_so_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    // (rank in the cluster) per q-tile pair and KV head
+    // four CTAs (cluster ranks) per q-tile pair and KV head
     const int n_pairs = (p.num_q_tiles + 1) / 2;
     const long long n_blocks = static_cast<long long>(n_pairs) * 4 * p.n_kv_heads;
-    prefill_so::prefill_so_kernel<<<static_cast<unsigned>(n_blocks), prefill_so::NUM_THREADS, smem, stream>>>(
+    prefill_so::prefill_so_kernel<false><<<static_cast<unsigned>(n_blocks), prefill_so::NUM_THREADS, smem, stream>>>(
+        tmq, tmk, tmv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_paged(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                 const PrefillParams& p, cudaStream_t stream) {
+    const int smem = prefill_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(prefill_so::prefill_so_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // (sequence, KV head, q-tile pair) numbered without gaps, four CTAs each;
+    // the chunks hold at most total_q / (2 T) + batch pairs
+    const long long per_head = std::min(static_cast<long long>(p.batch) * p.max_pairs,
+                                        (static_cast<long long>(p.total_q) + 2 * p.tokens_per_tile - 1) /
+                                                (2 * p.tokens_per_tile) + p.batch);
+    const long long n_blocks = per_head * p.n_kv_heads * 4;
+    if (n_blocks == 0) return cudaSuccess;
+    prefill_so::prefill_so_kernel<true><<<static_cast<unsigned>(n_blocks), prefill_so::NUM_THREADS, smem, stream>>>(
         tmq, tmk, tmv, p);
     return cudaGetLastError();
 }

@@ -69,7 +69,7 @@ def test_decode_bytes_fp8_cache_is_half_the_kv_bytes():
 
 def test_recorded_traffic_needs_the_current_source_digest():
     dec = bench.source_digest(["decode_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
-    pf = bench.source_digest(["prefill_sm103.cu", "fa512_pair.cuh", "fa512_device.cuh",
+    pf = bench.source_digest(["prefill_so_sm103.cu", "fa512_pair.cuh", "fa512_device.cuh",
                               "fa512_internal.h"])
     # a stale digest finds nothing; an unknown kernel finds nothing
     assert bench.recorded_traffic("decode_bf16_mma_kernel", "0" * 16) is None
