@@ -1449,88 +1449,106 @@ decode_bf16_mma_kernel(const DecodeParams p) {
 
 
 
-// One block of 128 threads per (sequence, query token, query head): merges
-// the splits' (O, m, l) -- M = max m_s, w_s = 2^(m_s - M), O = sum w_s O_s /
-// sum w_s l_s ("Flash-Decoding for MQA in CUDA", "One KV head breaks the
-// textbook").  Threads first read the splits' (m, l) side by side, then each
-// thread streams its 4 columns of every split's O with 8 loads in flight.
-constexpr int MERGE_THREADS = 128;
+// One block per (sequence, query token, query head): merges the splits'
+// (O, m, l) -- M = max m_s, w_s = 2^(m_s - M), O = sum w_s O_s / sum w_s l_s
+// ("Flash-Decoding for MQA in CUDA", "One KV head breaks the textbook").
+// 256 threads: 128 column quads x 2 groups of splits.  Every thread issues
+// the loads of its splits' O columns first, then the block finds the
+// weights from the (m, l) pairs, so the merge costs about one memory round
+// trip; the two groups' sums meet in shared memory.
+constexpr int MERGE_THREADS = 256;
+constexpr int MERGE_GROUPS = MERGE_THREADS / (D / 4);
+constexpr int MERGE_UNROLL = 16;         // splits a thread loads up front
 constexpr int MAX_SPLITS = 1024;
 
 __global__ void __launch_bounds__(MERGE_THREADS)
 decode_merge_kernel(const DecodeParams p) {
     __shared__ float sw[MAX_SPLITS];      // w_s
+    __shared__ float4 sacc[MERGE_GROUPS - 1][D / 4];
     __shared__ float smax[MERGE_THREADS / 32], ssum[MERGE_THREADS / 32];
     wait_for_splits();
     const int h = blockIdx.x;
     const int bt = blockIdx.y;      // sequence * q_len + token
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cq = tid % (D / 4), grp = tid / (D / 4);
     const size_t bh = static_cast<size_t>(bt) * p.n_q_heads + h;
     const int S = p.num_splits;
+    const float* ob = p.ws_o + bh * S * D + cq * 4;
+    float4 x[MERGE_UNROLL];
+#pragma unroll
+    for (int i = 0; i < MERGE_UNROLL; ++i) {
+        const int sp = grp + i * MERGE_GROUPS;
+        x[i] = sp < S ? *reinterpret_cast<const float4*>(ob + static_cast<size_t>(sp) * D)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const float2* ml = reinterpret_cast<const float2*>(p.ws_ml + bh * S * 2);
-    float mloc = -INFINITY;
-    for (int s = tid; s < S; s += MERGE_THREADS) mloc = fmaxf(mloc, ml[s].x);
+    float2 mine = make_float2(-INFINITY, 0.f);
+    if (tid < S) mine = ml[tid];
+    float mloc = mine.x;
+    for (int sp = tid + MERGE_THREADS; sp < S; sp += MERGE_THREADS) mloc = fmaxf(mloc, ml[sp].x);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
     if (lane == 0) smax[warp] = mloc;
     __syncthreads();
-    const float M = fmaxf(fmaxf(smax[0], smax[1]), fmaxf(smax[2], smax[3]));
+    float M = smax[0];
+#pragma unroll
+    for (int w = 1; w < MERGE_THREADS / 32; ++w) M = fmaxf(M, smax[w]);
     float lloc = 0.f;
-    for (int s = tid; s < S; s += MERGE_THREADS) {
-        const float2 x = ml[s];
+    for (int sp = tid; sp < S; sp += MERGE_THREADS) {
+        const float2 v = sp == tid ? mine : ml[sp];
         // 0 for an empty split (m = -inf), and for every split when all are empty
-        const float w = M == -INFINITY ? 0.f : fast_exp2(x.x - M);
-        sw[s] = w;
-        lloc += w * x.y;
+        const float w = M == -INFINITY ? 0.f : fast_exp2(v.x - M);
+        sw[sp] = w;
+        lloc += w * v.y;
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
     if (lane == 0) ssum[warp] = lloc;
     __syncthreads();
-    const float L = (ssum[0] + ssum[1]) + (ssum[2] + ssum[3]);
-    const int d = tid * 4;
-    __nv_bfloat16* out = p.out + bh * D + d;
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < MERGE_THREADS / 32; ++w) L += ssum[w];
+    __nv_bfloat16* out = p.out + bh * D + cq * 4;
     if (M == -INFINITY) {
-        *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
+        if (grp == 0) *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
         if (p.lse && tid == 0) p.lse[bh] = -INFINITY;
         return;
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* ob = p.ws_o + bh * S * D + d;
-    constexpr int U = 8;
-    int s = 0;
-    for (; s + U <= S; s += U) {
-        float4 x[U];
-#pragma unroll
-        for (int i = 0; i < U; ++i) x[i] = *reinterpret_cast<const float4*>(ob + static_cast<size_t>(s + i) * D);
-#pragma unroll
-        for (int i = 0; i < U; ++i) {
-            // a split whose weight underflowed contributes nothing, whatever it holds
-            const float w = sw[s + i];
-            if (w != 0.f) {
-                acc.x = fmaf(w, x[i].x, acc.x);
-                acc.y = fmaf(w, x[i].y, acc.y);
-                acc.z = fmaf(w, x[i].z, acc.z);
-                acc.w = fmaf(w, x[i].w, acc.w);
-            }
-        }
-    }
-    for (; s < S; ++s) {
-        const float w = sw[s];
+    auto add = [&](float w, const float4& v) {
+        // a split whose weight underflowed contributes nothing, whatever it holds
         if (w != 0.f) {
-            const float4 x = *reinterpret_cast<const float4*>(ob + static_cast<size_t>(s) * D);
-            acc.x = fmaf(w, x.x, acc.x);
-            acc.y = fmaf(w, x.y, acc.y);
-            acc.z = fmaf(w, x.z, acc.z);
-            acc.w = fmaf(w, x.w, acc.w);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
         }
+    };
+#pragma unroll
+    for (int i = 0; i < MERGE_UNROLL; ++i) {
+        const int sp = grp + i * MERGE_GROUPS;
+        if (sp < S) add(sw[sp], x[i]);
     }
-    const float inv = 1.f / L;
-    uint2 packed;
-    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(out) = packed;
-    if (p.lse && tid == 0) p.lse[bh] = (M + log2f(L)) * 0.69314718055994530942f;
+    for (int sp = grp + MERGE_UNROLL * MERGE_GROUPS; sp < S; sp += MERGE_GROUPS)
+        add(sw[sp], *reinterpret_cast<const float4*>(ob + static_cast<size_t>(sp) * D));
+    if (grp > 0) sacc[grp - 1][cq] = acc;
+    __syncthreads();
+    if (grp == 0) {
+#pragma unroll
+        for (int g = 0; g < MERGE_GROUPS - 1; ++g) {
+            const float4 a = sacc[g][cq];
+            acc.x += a.x;
+            acc.y += a.y;
+            acc.z += a.z;
+            acc.w += a.w;
+        }
+        const float inv = 1.f / L;
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(out) = packed;
+        if (p.lse && tid == 0) p.lse[bh] = (M + log2f(L)) * 0.69314718055994530942f;
+    }
 }
 
 }  // namespace decode
