@@ -455,15 +455,17 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         if (warp == 0) {
             if (lane == 0) {
                 // -------------------------------------------------- Q and K loads
+                // Q is read once; K and V are read by every pair of the KV head
+                const uint64_t pol_q = l2_policy_stream(), pol_kv = l2_policy_keep();
                 const uint32_t q_bytes = static_cast<uint32_t>(4 * 128 * p.rows_per_tile);   // 4 boxes
                 if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::Q_FULL], 2 * q_bytes);
                 mbar_arrive_expect_tx(&bars[Smem::Q_HI], q_bytes);
                 for (int c = 0; c < 4; ++c)
-                    tma2_load_4d(smem + Smem::q + c * Q_CHUNK, &tmq, bar_of(Smem::Q_FULL, 0), c * 64, 0, kvh,
-                                 q_start + t0);
+                    tma2_load_4d_hint(smem + Smem::q + c * Q_CHUNK, &tmq, bar_of(Smem::Q_FULL, 0), c * 64, 0, kvh,
+                                      q_start + t0, pol_q);
                 for (int c = 4; c < 8; ++c)
-                    tma2_load_4d(smem + Smem::stage + (c - 4) * Q_CHUNK, &tmq, bar_of(Smem::Q_HI, rank), c * 64, 0,
-                                 kvh, q_start + t0);
+                    tma2_load_4d_hint(smem + Smem::stage + (c - 4) * Q_CHUNK, &tmq, bar_of(Smem::Q_HI, rank), c * 64,
+                                      0, kvh, q_start + t0, pol_q);
                 // half tile h: tile h / 2, head-dim columns 256 (h % 2) .. +256, this CTA's 64 keys
                 for (int h = 0; h < 2 * n_kt; ++h) {
                     const int j = h >> 1, c = h & 1, s = h % K_SLOTS;
@@ -481,8 +483,8 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     if (h == 0 && p.test_skip_first_k_load && blockIdx.x == 0) continue;
                     const int krow = half_row((kt_begin + j) * BN + static_cast<int>(pr) * K_BOX_ROWS);
                     for (int b = 0; b < 4; ++b)
-                        tma2_load_3d(smem + Smem::kring + s * SLOT + b * K_BOX, &tmk, bar_of(Smem::K_FULL + s, 0),
-                                     (c * 4 + b) * 64, kvh, krow);
+                        tma2_load_3d_hint(smem + Smem::kring + s * SLOT + b * K_BOX, &tmk,
+                                          bar_of(Smem::K_FULL + s, 0), (c * 4 + b) * 64, kvh, krow, pol_kv);
                 }
             }
         } else if (warp == 1 && rank == 1) {
@@ -742,6 +744,7 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         if (warp == 0) {
             if (lane == 0) {
                 // -------------------------------------------------- V loads
+                const uint64_t pol_kv = l2_policy_keep();   // read by every pair of the KV head
                 for (int j = 0; j < n_kt; ++j) {
                     const int vb = j & 1;
                     // V buffer vb once O += P V of tile j - 2 completed
@@ -772,16 +775,17 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                         for (int hh = 0; hh < 2; ++hh)
                             for (int bx = 0; bx < 2; ++bx)
                                 for (int r = 0; r < 2; ++r)
-                                    tma2_load_3d(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX + r * K_BOX,
-                                                 &tmv, vbar, (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh,
-                                                 rows[r]);
+                                    tma2_load_3d_hint(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX +
+                                                          r * K_BOX,
+                                                      &tmv, vbar, (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh,
+                                                      rows[r], pol_kv);
                     } else {
                         if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
                         for (int hh = 0; hh < 2; ++hh)
                             for (int bx = 0; bx < 2; ++bx)
-                                tma2_load_3d(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX, &tmv,
-                                             bar_of(Smem::PV_READY + rb, 2),
-                                             (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh, key);
+                                tma2_load_3d_hint(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX, &tmv,
+                                                  bar_of(Smem::PV_READY + rb, 2),
+                                                  (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh, key, pol_kv);
                     }
                 }
             }
@@ -913,10 +917,16 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                        // O is written once: streaming stores (evicted first from L2).
+                        // Measured on one GB300: +1.2 % on the contiguous configs,
+                        // -1.8 % on the paged ones, which keep plain stores.
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 v = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                            if constexpr (PAGED) d4[i] = v;
+                            else __stcs(d4 + i, v);
+                        }
                     }
                 }
             }
