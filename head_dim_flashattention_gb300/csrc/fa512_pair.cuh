@@ -20,6 +20,14 @@ __device__ __forceinline__ void mma2_ss(uint32_t d, uint64_t a, uint64_t b, uint
                  ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
                  : "memory");
 }
+// One lane of a converged warp (the same lane every time): the lane that
+// issues tensor-core work while the whole warp runs the loop around it, so
+// the operands stay warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+    return pred != 0;
+}
 __device__ __forceinline__ void mma2_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"

@@ -29,12 +29,14 @@
 // and step 2 of the RTX PRO 6000 page; here the split is between the two
 // products.)
 //
-// Score pair (per CTA: Q head-dim columns 0-255 in shared memory, 256-511 in
-// TMEM as the A operand of the second half of every QK^T; three S buffers in
-// TMEM): K streams through three 32 KiB slots (a half tile: this CTA's 64
-// keys x 256 head-dim columns), each released by the commit after its 16
-// MMAs; the producer holds back a tile's first K half until its S buffer has
-// been read.  Eight softmax warps: TMEM lane quadrant (warp % 4) gives a warp
+// Score pair (per CTA: the whole 128 x 512 bf16 Q tile in TMEM, 256
+// columns, as the A operand of every QK^T, so that each MMA reads only K from
+// shared memory; two S buffers in the other 256 columns): K streams through
+// five 32 KiB slots (a half tile: this CTA's 64 keys x 256 head-dim columns),
+// each released by the commit after its 16 MMAs; the MMA thread holds back a
+// tile's QK^T until its S buffer has been read (the K loads run ahead).  Q lands in the last
+// two K slots and the P staging area, and the softmax warps move it to TMEM
+// before either is needed.  Eight softmax warps: TMEM lane quadrant (warp % 4) gives a warp
 // its 32 rows, warps 2-5 take keys 0-63 of each tile and warps 6-9 keys
 // 64-127; they swap row maxima through shared memory.  The row max is lazy: O is rescaled only
 // when a row's max grows by more than 2^16.  P goes to one of two staging
@@ -86,11 +88,12 @@ constexpr int KP = BN / PARTS;           // score CTAs: keys of a tile per softm
 constexpr int OP = D / PARTS;            // output CTAs: O columns per correction warp (128)
 constexpr int Q_CHUNK = BM * 128;        // one 64-column box of Q: 16 KiB
 constexpr int SLOT = 32768;
-constexpr int K_SLOTS = 3;               // score CTAs: K half tiles
+constexpr int K_SLOTS = 5;               // score CTAs: K half tiles
 constexpr int K_BOX_ROWS = BN / 2;       // {64 columns, 64 keys} boxes
 constexpr int K_BOX = K_BOX_ROWS * 128;  // 8 KiB
-constexpr int S_BUFS = 3;                // S buffers of 128 TMEM columns
-constexpr uint32_t TM_QHI = S_BUFS * BN; // Q head-dim columns 256-511 (128 TMEM columns)
+constexpr int S_BUFS = 2;                // S buffers of 128 TMEM columns
+constexpr uint32_t TM_Q = S_BUFS * BN;   // the Q tile: head-dim column d in TMEM column TM_Q + d / 2
+constexpr int Q_PARK_SLOT = K_SLOTS - 2; // Q chunks 0-3 land in K slots 3-4, chunks 4-7 in the staging area
 constexpr int V_SLOTS = 4;               // output CTAs: 2 tiles x 2 O halves
 constexpr int V_BOX_ROWS = BN;           // {64 columns, 128 keys} boxes
 constexpr int V_BOX = V_BOX_ROWS * 128;  // 16 KiB
@@ -112,10 +115,9 @@ constexpr float RESCALE_THRESHOLD = 16.0f;
 constexpr uint16_t MASK_SCORE = 0x3, MASK_OUTPUT = 0xC, MASK_ALL = 0xF;
 
 struct Smem {
-    // score CTAs: Q head-dim columns 0-255 stay here; columns 256-511 land in
-    // the staging area first and move to TMEM, after which the area stages P
-    static constexpr int q = 0;                                 // 4 x 16 KiB
-    static constexpr int kring = q + 4 * Q_CHUNK;               // 3 x 32 KiB
+    // score CTAs: the Q tile lands in the last two K slots and the staging
+    // area and moves to TMEM before either is used for K or P
+    static constexpr int kring = 0;                             // 5 x 32 KiB
     static constexpr int stage = kring + K_SLOTS * SLOT;        // 2 x 32 KiB
     static constexpr int xmax = stage + STAGES * P_BUF;         // [2 buffers][PARTS][128] f32
     // output CTAs
@@ -128,17 +130,17 @@ struct Smem {
     // output CTAs' alpha and row sums)
     static constexpr int bars = xmax + 2048;
     enum {
-        K_FULL = 0,                      // [3] score leader: both CTAs' half tile landed
-        K_EMPTY = K_FULL + K_SLOTS,      // [3] score CTAs: the slot's MMAs completed
-        S_FULL = K_EMPTY + K_SLOTS,      // [3] score CTAs: S of the tile is in TMEM
-        S_FREE = S_FULL + S_BUFS,        // [3] score leader: both CTAs' softmax warps read S
-        XCHG = S_FREE + S_BUFS,          // [2] score CTAs: row-max swap of the four key parts
-        Q_FULL = XCHG + 2,               // score leader: head-dim columns 0-255 of both Q tiles landed
-        Q_HI = Q_FULL + 1,               // score CTAs: this CTA's columns 256-511 landed (staging area)
-        Q_TMEM = Q_HI + 1,               // score leader: both CTAs' columns 256-511 are in TMEM
+        K_FULL = 0,                      // [5] score leader: both CTAs' half tile landed
+        K_EMPTY = K_FULL + K_SLOTS,      // [5] score CTAs: the slot's MMAs completed
+        S_FULL = K_EMPTY + K_SLOTS,      // [2] score CTAs: S of the tile is in TMEM
+        S_FREE = S_FULL + S_BUFS,        // [2] score leader: both CTAs' softmax warps read S
+        XCHG = S_FREE + S_BUFS,          // [2] score CTAs: row-max swap of the key parts
+        Q_COPIED = XCHG + 2,             // score CTAs: this CTA's softmax warps moved Q to TMEM
+        Q_HI = Q_COPIED + 1,             // score CTAs: this CTA's Q tile landed (K slots 3-4, staging area)
+        Q_TMEM = Q_HI + 1,               // score leader: both CTAs' Q tiles are in TMEM
         P_STAGED = Q_TMEM + 1,           // [2] score CTAs: all softmax warps staged the tile's P
         STAGE_FREE = P_STAGED + STAGES,  // [2] score CTAs: the buffer's last copy landed, its alpha read
-        S_READ = STAGE_FREE + STAGES,    // [3] score CTA 1: its softmax warps read S (forwarded to S_FREE)
+        S_READ = STAGE_FREE + STAGES,    // [2] score CTA 1: its softmax warps read S (forwarded to S_FREE)
         L_XCHG = S_READ + S_BUFS,        // score CTAs: row-sum swap
         PV_DONE = L_XCHG + 1,            // [3] all four: O += P V of the P buffer's last tile completed
         PV_READY = PV_DONE + P_BUFS,     // [3] output leader: P landed and O corrected in both, V landed
@@ -405,8 +407,9 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < Smem::N_BARS; ++i) {
             uint32_t count = 1;
-            if (i == Smem::XCHG || i == Smem::XCHG + 1 || i == Smem::L_XCHG) count = N_WORK_WARPS * 32;
+            if (i == Smem::XCHG || i == Smem::XCHG + 1 || i == Smem::L_XCHG) count = N_WORK_WARPS;
             if (i == Smem::Q_TMEM) count = 2 * N_WORK_WARPS;
+            if (i == Smem::Q_COPIED) count = N_WORK_WARPS;
             // the leader's softmax warps, plus one forwarded arrival for the other CTA's
             if (i >= Smem::S_FREE && i < Smem::S_FREE + S_BUFS) count = N_WORK_WARPS + 1;
             if ((i >= Smem::S_READ && i < Smem::S_READ + S_BUFS) ||
@@ -457,26 +460,20 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 // -------------------------------------------------- Q and K loads
                 // Q is read once; K and V are read by every pair of the KV head
                 const uint64_t pol_q = l2_policy_stream(), pol_kv = l2_policy_keep();
-                const uint32_t q_bytes = static_cast<uint32_t>(4 * 128 * p.rows_per_tile);   // 4 boxes
-                if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::Q_FULL], 2 * q_bytes);
+                const uint32_t q_bytes = static_cast<uint32_t>(8 * 128 * p.rows_per_tile);   // 8 boxes
                 mbar_arrive_expect_tx(&bars[Smem::Q_HI], q_bytes);
-                for (int c = 0; c < 4; ++c)
-                    tma2_load_4d_hint(smem + Smem::q + c * Q_CHUNK, &tmq, bar_of(Smem::Q_FULL, 0), c * 64, 0, kvh,
-                                      q_start + t0, pol_q);
-                for (int c = 4; c < 8; ++c)
-                    tma2_load_4d_hint(smem + Smem::stage + (c - 4) * Q_CHUNK, &tmq, bar_of(Smem::Q_HI, rank), c * 64,
-                                      0, kvh, q_start + t0, pol_q);
+                for (int c = 0; c < 8; ++c)
+                    tma2_load_4d_hint(smem + (c < 4 ? Smem::kring + Q_PARK_SLOT * SLOT + c * Q_CHUNK
+                                                    : Smem::stage + (c - 4) * Q_CHUNK),
+                                      &tmq, bar_of(Smem::Q_HI, rank), c * 64, 0, kvh, q_start + t0, pol_q);
                 // half tile h: tile h / 2, head-dim columns 256 (h % 2) .. +256, this CTA's 64 keys
                 for (int h = 0; h < 2 * n_kt; ++h) {
                     const int j = h >> 1, c = h & 1, s = h % K_SLOTS;
                     if (h >= K_SLOTS && !wait_or_abort(&bars[Smem::K_EMPTY + s], ((h / K_SLOTS) - 1) & 1, p.err,
                                                        abort, wait_ns))
                         break;
-                    // the tile's S buffer must have been read before its QK^T may start
-                    if (rank == 0 && c == 0 && j >= S_BUFS &&
-                        !wait_or_abort(&bars[Smem::S_FREE + (j % S_BUFS)], ((j / S_BUFS) - 1) & 1, p.err, abort,
-                                       wait_ns))
-                        break;
+                    // the slots that held Q: once this CTA's Q is in TMEM
+                    if (h == Q_PARK_SLOT && !wait_or_abort(&bars[Smem::Q_COPIED], 0, p.err, abort, wait_ns)) break;
                     if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::K_FULL + s], 2 * SLOT);
                     // (test hook: the first cluster's rank 0 leaves out its first
                     // K half tile, so that cluster's waits run into their bound)
@@ -499,45 +496,45 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 }
             }
         } else if (warp == 1) {
-            if (lane == 0 && rank == 0) {
+            if (rank == 0) {
                 // -------------------------------------------------- S = Q K^T (both SMs)
-                bool ok = wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort, wait_ns) &&
-                          wait_or_abort(&bars[Smem::Q_TMEM], 0, p.err, abort, wait_ns);
-                const uint64_t q_desc = make_sdesc_sw128(smem_u32(smem + Smem::q), 16, 1024);
+                // The whole warp runs the loop and its waits (warp-uniform, so
+                // the MMA operands stay uniform); one elected lane issues.
+                bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::Q_TMEM], 0, p.err, abort, wait_ns));
                 const uint64_t k_desc = make_sdesc_sw128(smem_u32(smem + Smem::kring), 16, 1024);
                 for (int j = 0; ok && j < n_kt; ++j) {
                     const uint32_t sb = tmem + static_cast<uint32_t>(j % S_BUFS) * BN;
+                    // the tile's S buffer must have been read before its QK^T may start
+                    if (j >= S_BUFS && !(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::S_FREE + (j % S_BUFS)],
+                                                                                    ((j / S_BUFS) - 1) & 1, p.err,
+                                                                                    abort, wait_ns))))
+                        break;
                     for (int c = 0; c < 2; ++c) {
                         const int h = 2 * j + c, s = h % K_SLOTS;
-                        if (!(ok = wait_or_abort(&bars[Smem::K_FULL + s], (h / K_SLOTS) & 1, p.err, abort, wait_ns)))
+                        if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::K_FULL + s], (h / K_SLOTS) & 1,
+                                                                         p.err, abort, wait_ns))))
                             break;
                         tc_fence_after_sync();
                         const uint64_t bd0 = k_desc + static_cast<uint64_t>(s * (SLOT >> 4));
-                        if (c == 0) {
+                        if (elect_one()) {
 #pragma unroll
                             for (int k16 = 0; k16 < 16; ++k16) {
-                                // head-dim chunk k16 >> 2 of Q in shared memory, 16 columns at a
-                                // time (start field in 16 B units)
+                                // head-dim columns 256 c + 16 k16 .. +16: Q from TMEM (two bf16 a
+                                // column), K from its box k16 / 4 (start field in 16 B units)
                                 const uint64_t off = static_cast<uint64_t>((k16 & 3) * 2);
-                                mma2_ss(sb, q_desc + static_cast<uint64_t>((k16 >> 2) * (Q_CHUNK >> 4)) + off,
+                                mma2_ts(sb, tmem + TM_Q + static_cast<uint32_t>(c * 128 + k16 * 8),
                                         bd0 + static_cast<uint64_t>((k16 >> 2) * (K_BOX >> 4)) + off, IDESC_QK,
-                                        k16 ? 1u : 0u);
+                                        (c | k16) ? 1u : 0u);
                             }
-                        } else {
-#pragma unroll
-                            for (int k16 = 0; k16 < 16; ++k16) {
-                                // head-dim columns 256 + 16 k16 .. from TMEM (two bf16 a column)
-                                const uint64_t off = static_cast<uint64_t>((k16 & 3) * 2);
-                                mma2_ts(sb, tmem + TM_QHI + static_cast<uint32_t>(k16 * 8),
-                                        bd0 + static_cast<uint64_t>((k16 >> 2) * (K_BOX >> 4)) + off, IDESC_QK, 1u);
-                            }
+                            commit2_mask(&bars[Smem::K_EMPTY + s], MASK_SCORE);
+                            if (c == 1) commit2_mask(&bars[Smem::S_FULL + (j % S_BUFS)], MASK_SCORE);
                         }
-                        commit2_mask(&bars[Smem::K_EMPTY + s], MASK_SCORE);
+                        __syncwarp();
                     }
-                    if (ok) commit2_mask(&bars[Smem::S_FULL + (j % S_BUFS)], MASK_SCORE);
                 }
                 // let every issued MMA finish before TMEM can be released
-                commit2_mask(&bars[Smem::DRAIN], static_cast<uint16_t>(1u << rank));
+                if (elect_one()) commit2_mask(&bars[Smem::DRAIN], static_cast<uint16_t>(1u << rank));
+                __syncwarp();
                 (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err, wait_ns);
             }
         } else if (warp == COPY_WARP) {
@@ -568,14 +565,14 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             const uint32_t out_rank = rank + 2;
             const uint32_t a_dst = map_to_cta(smem_u32(smem + Smem::alpha + row * 4), out_rank);
 
-            // Q head-dim columns 256-511 to TMEM (the operand of the second half
-            // of every QK^T): this warp's 64-column chunk of its rows, undoing
-            // the 128-byte swizzle
+            // The Q tile to TMEM (the A operand of every QK^T): this warp's
+            // 64-column chunks of its rows, undoing the 128-byte swizzle
             ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::Q_HI], 0, p.err, abort, wait_ns));
             if (ok) {
-                for (int cc = 0; cc < 4 / PARTS; ++cc) {
-                    const int c4 = part * (4 / PARTS) + cc;     // chunk 4 + c4 of Q
-                    const uint8_t* src = smem + Smem::stage + c4 * Q_CHUNK + row * 128;
+                for (int cc = 0; cc < 8 / PARTS; ++cc) {
+                    const int c8 = part * (8 / PARTS) + cc;     // chunk c8 of Q: head-dim columns 64 c8 ..
+                    const uint8_t* src = smem + (c8 < 4 ? Smem::kring + Q_PARK_SLOT * SLOT + c8 * Q_CHUNK
+                                                        : Smem::stage + (c8 - 4) * Q_CHUNK) + row * 128;
                     uint32_t w[32];
 #pragma unroll
                     for (int pc = 0; pc < 8; ++pc) {
@@ -585,13 +582,14 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                         w[4 * pc + 2] = x.z;
                         w[4 * pc + 3] = x.w;
                     }
-                    tmem_st32(tmem + lane_base + TM_QHI + static_cast<uint32_t>(c4 * 32), w);
+                    tmem_st32(tmem + lane_base + TM_Q + static_cast<uint32_t>(c8 * 32), w);
                 }
                 tmem_st_wait();
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
+                mbar_arrive(&bars[Smem::Q_COPIED]);
                 if (rank == 0) mbar_arrive(&bars[Smem::Q_TMEM]);
                 else mbar_arrive_remote(bar_of(Smem::Q_TMEM, 0));
             }
@@ -652,7 +650,10 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 // units); all then take the same decision on the same numbers
                 const float own_max = mx[0] * p.scale_log2;
                 xmax[(b2 * PARTS + part) * BM + row] = own_max;
-                mbar_arrive(&bars[Smem::XCHG + b2]);
+                // one arrival per warp, after the warp's stores (256 single-thread
+                // arrivals on one barrier would serialise)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[Smem::XCHG + b2]);
                 if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::XCHG + b2], (j >> 1) & 1, p.err, abort,
                                                                  wait_ns))))
                     break;
@@ -711,18 +712,19 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 if (part == 0) st_async_b32(a_dst + static_cast<uint32_t>(pb * BM * 4), __float_as_uint(alpha), xbar);
                 // the copy engine reads the staged tile: order these writes
                 // before it; the copy warp moves the whole tile once all
-                // sixteen warps have staged
+                // softmax warps have staged
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[Smem::P_STAGED + b2]);
             }
-            // Sum the parts' row sums through the Q area, idle once every QK^T
-            // has completed (the last S_FULL was seen).  Each thread arrives
-            // exactly once, so the wait ends.
-            float* lsum = reinterpret_cast<float*>(smem + Smem::q);
+            // Sum the parts' row sums through the K ring, idle once every QK^T
+            // has completed (the last S_FULL was seen).  Each warp arrives
+            // exactly once (its loop exits warp-uniformly), so the wait ends.
+            float* lsum = reinterpret_cast<float*>(smem + Smem::kring);
             lsum[(part * BM + row) * 2 + 0] = l;
             lsum[(part * BM + row) * 2 + 1] = l_b;
-            mbar_arrive(&bars[Smem::L_XCHG]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[Smem::L_XCHG]);
             if (ok) ok = wait_or_abort(&bars[Smem::L_XCHG], 0, p.err, abort, wait_ns);
             if (ok && part == 0) {
                 float l_all = 0.f, lb_all = 0.f;
@@ -811,33 +813,39 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 }
             }
         } else if (warp == 1) {
-            if (lane == 0 && rank == 2) {
+            if (rank == 2) {
                 // -------------------------------------------------- O += P V (both SMs)
+                // (the whole warp runs the loop, one elected lane issues)
                 bool ok = true;
                 const uint64_t p_desc = make_sdesc_sw128(smem_u32(smem + Smem::precv), 16, 1024);
                 const uint64_t v_desc = make_sdesc_sw128(smem_u32(smem + Smem::vring), V_BOX, 1024);
                 for (int j = 0; ok && j < n_kt; ++j) {
                     const int vb = j & 1, pb = j % P_BUFS;
-                    if (!(ok = wait_or_abort(&bars[Smem::PV_READY + pb], (j / P_BUFS) & 1, p.err, abort, wait_ns)))
+                    if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::PV_READY + pb], (j / P_BUFS) & 1,
+                                                                     p.err, abort, wait_ns))))
                         break;
                     tc_fence_after_sync();
                     const uint64_t ad0 = p_desc + static_cast<uint64_t>(pb * (P_BUF >> 4));
                     const uint64_t bd0 = v_desc + static_cast<uint64_t>(2 * vb * (SLOT >> 4));
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        // P keys 16 kk .. 16 kk + 15: chunk kk / 4, 32 bytes per step within it;
-                        // V is MN-major: 8-key groups 1 KiB apart
-                        const uint64_t ad = ad0 + static_cast<uint64_t>((kk >> 2) * (P_CHUNK >> 4) + (kk & 3) * 2);
-                        const uint64_t bd = bd0 + static_cast<uint64_t>(kk * (16 * 128 >> 4));
-                        mma2_ss(tmem, ad, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                        mma2_ss(tmem + 256, ad, bd + static_cast<uint64_t>(SLOT >> 4), IDESC_PV,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            // P keys 16 kk .. 16 kk + 15: chunk kk / 4, 32 bytes per step within it;
+                            // V is MN-major: 8-key groups 1 KiB apart
+                            const uint64_t ad = ad0 + static_cast<uint64_t>((kk >> 2) * (P_CHUNK >> 4) + (kk & 3) * 2);
+                            const uint64_t bd = bd0 + static_cast<uint64_t>(kk * (16 * 128 >> 4));
+                            mma2_ss(tmem, ad, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                            mma2_ss(tmem + 256, ad, bd + static_cast<uint64_t>(SLOT >> 4), IDESC_PV,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        // frees the tile's V slots and P buffer; O may be corrected for the next tile
+                        commit2_mask(&bars[Smem::PV_DONE + pb], MASK_ALL);
+                        if (j == n_kt - 1) commit2_mask(&bars[Smem::O_FINAL], MASK_OUTPUT);
                     }
-                    // frees the tile's V slots and P buffer; O may be corrected for the next tile
-                    commit2_mask(&bars[Smem::PV_DONE + pb], MASK_ALL);
+                    __syncwarp();
                 }
-                if (ok) commit2_mask(&bars[Smem::O_FINAL], MASK_OUTPUT);
-                commit2_mask(&bars[Smem::DRAIN], static_cast<uint16_t>(1u << rank));
+                if (elect_one()) commit2_mask(&bars[Smem::DRAIN], static_cast<uint16_t>(1u << rank));
+                __syncwarp();
                 (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err, wait_ns);
             }
         } else if (work_warp) {
