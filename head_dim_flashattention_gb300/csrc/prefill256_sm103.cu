@@ -29,7 +29,7 @@
 //
 // Roles (320 threads per CTA), as in the head-dim-512 kernel: warp 0 lane 0
 // issues this CTA's TMA loads and stores; warp 1 owns TMEM and, in the even
-// CTA, lane 0 issues every MMA of the pair; warps 2-9 run the softmax, the O
+// CTA, runs the MMA loop (one elected lane issues every MMA of the pair); warps 2-9 run the softmax, the O
 // correction and the epilogue of this CTA's rows (TMEM lane quadrant
 // warp % 4, keys 0-63 of a tile for warps 2-5 and 64-127 for warps 6-9).
 #include <cuda.h>
@@ -196,7 +196,7 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < Smem::N_BARS; ++i) {
             uint32_t count = 1;
-            if (i == Smem::XCHG || i == Smem::XCHG + 1) count = N_SOFTMAX_WARPS * 32;
+            if (i == Smem::XCHG || i == Smem::XCHG + 1) count = N_SOFTMAX_WARPS;
             // one lane per softmax warp of both CTAs (plus the even CTA's V load)
             if (i == Smem::P_FULL || i == Smem::P_FULL + 1) count = 2 * N_SOFTMAX_WARPS + 1;
             if (i == Smem::O_FREE) count = 2 * N_SOFTMAX_WARPS;
@@ -325,51 +325,62 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             bulk_wait_all();
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
+        if (rank == 0) {
             // ------------------------------------------------------------ MMA issue (both SMs)
+            // The whole warp walks the tiles and waits (warp-uniform, so the
+            // MMA operands stay uniform); one elected lane issues and commits.
             const uint32_t ring_base = smem_u32(smem + Smem::ring);
             const uint32_t q_base = smem_u32(smem + Smem::q);
             bool ok = true;
             auto issue_qk = [&](const TileCursor& t) -> bool {
                 const int b = t.g & 1;
-                if (t.j == 0 && !wait_or_abort(&bars[Smem::Q_FULL + (t.qi & 1)], (t.qi >> 1) & 1, p.err, abort))
+                if (t.j == 0 && !__all_sync(0xffffffffu, wait_or_abort(&bars[Smem::Q_FULL + (t.qi & 1)],
+                                                                       (t.qi >> 1) & 1, p.err, abort)))
                     return false;
-                if (!wait_or_abort(&bars[Smem::FULL_K + b], (t.g >> 1) & 1, p.err, abort)) return false;
+                if (!__all_sync(0xffffffffu, wait_or_abort(&bars[Smem::FULL_K + b], (t.g >> 1) & 1, p.err, abort)))
+                    return false;
                 tc_fence_after_sync();
                 const uint32_t sb = tmem + TM_S + static_cast<uint32_t>(b) * S_STRIDE;
                 const uint64_t ad0 = make_sdesc_sw128(q_base + (t.qi & 1) * Q_BUF, 16, 1024);
                 const uint64_t bd0 = make_sdesc_sw128(ring_base + (SLOT_K0 + b) * SLOT, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int k16 = 0; k16 < 16; ++k16) {
-                    // head-dim chunk k16 >> 2, 16 columns at a time (start field in 16 B units)
-                    const uint64_t off = static_cast<uint64_t>((k16 & 3) * 2);
-                    mma2_ss(sb, ad0 + static_cast<uint64_t>((k16 >> 2) * (Q_CHUNK >> 4)) + off,
-                            bd0 + static_cast<uint64_t>((k16 >> 2) * (K_BOX >> 4)) + off, IDESC_QK,
-                            k16 ? 1u : 0u);
+                    for (int k16 = 0; k16 < 16; ++k16) {
+                        // head-dim chunk k16 >> 2, 16 columns at a time (start field in 16 B units)
+                        const uint64_t off = static_cast<uint64_t>((k16 & 3) * 2);
+                        mma2_ss(sb, ad0 + static_cast<uint64_t>((k16 >> 2) * (Q_CHUNK >> 4)) + off,
+                                bd0 + static_cast<uint64_t>((k16 >> 2) * (K_BOX >> 4)) + off, IDESC_QK,
+                                k16 ? 1u : 0u);
+                    }
+                    commit2_both(&bars[Smem::S_FULL + b]);
                 }
-                commit2_both(&bars[Smem::S_FULL + b]);
+                __syncwarp();
                 return true;
             };
             auto issue_pv = [&](const TileCursor& t) -> bool {
                 // an item's first PV overwrites O: the softmax warps must have
                 // read the previous item's O out of TMEM
                 if (t.j == 0 && t.qi >= 1) {
-                    if (!wait_or_abort(&bars[Smem::O_FREE], (t.qi - 1) & 1, p.err, abort)) return false;
+                    if (!__all_sync(0xffffffffu, wait_or_abort(&bars[Smem::O_FREE], (t.qi - 1) & 1, p.err, abort)))
+                        return false;
                     tc_fence_after_sync();
                 }
                 const uint32_t pb = tmem + TM_S + static_cast<uint32_t>(t.g & 1) * S_STRIDE;
                 const uint32_t vb = ring_base + SLOT_V * SLOT;
                 const uint64_t bd0 = make_sdesc_sw128(vb, V_BOX, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // V is MN-major: 64-column boxes V_BOX apart, 8-key groups 1 KiB apart;
-                    // P of keys [64 h, 64 h + 64) sits at S columns [64 h, 64 h + 32)
-                    const uint64_t bd = bd0 + static_cast<uint64_t>(kk * (16 * 128 >> 4));
-                    mma2_ts(tmem + TM_O, pb + (kk >> 2) * BH + (kk & 3) * 8, bd, IDESC_PV,
-                            (t.j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        // V is MN-major: 64-column boxes V_BOX apart, 8-key groups 1 KiB apart;
+                        // P of keys [64 h, 64 h + 64) sits at S columns [64 h, 64 h + 32)
+                        const uint64_t bd = bd0 + static_cast<uint64_t>(kk * (16 * 128 >> 4));
+                        mma2_ts(tmem + TM_O, pb + (kk >> 2) * BH + (kk & 3) * 8, bd, IDESC_PV,
+                                (t.j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    commit2_both(&bars[Smem::O_DONE]);
+                    if (t.last_of_item()) commit2_both(&bars[Smem::O_FINAL]);
                 }
-                commit2_both(&bars[Smem::O_DONE]);
-                if (t.last_of_item()) commit2_both(&bars[Smem::O_FINAL]);
+                __syncwarp();
                 return true;
             };
             TileCursor cur, nxt;
@@ -381,12 +392,15 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 // S of the next tile (of this item or the next) runs while the
                 // softmax works on this one; its buffer last held P(g-1)
                 if (nxt.valid && !(ok = issue_qk(nxt))) break;
-                if (!(ok = wait_or_abort(&bars[Smem::P_FULL + (cur.g & 1)], (cur.g >> 1) & 1, p.err, abort))) break;
+                if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::P_FULL + (cur.g & 1)], (cur.g >> 1) & 1,
+                                                                 p.err, abort))))
+                    break;
                 tc_fence_after_sync();
                 if (!(ok = issue_pv(cur))) break;
                 cur = nxt;
             }
-            commit2_local(&bars[Smem::DRAIN]);
+            if (elect_one()) commit2_local(&bars[Smem::DRAIN]);
+            __syncwarp();
             (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err);
         }
     } else {
@@ -545,7 +559,8 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 }
                 const float own_max = mx[0] * p.scale_log2;
                 xmax[(b * 2 + kh) * BM + row] = own_max;
-                mbar_arrive(&bars[Smem::XCHG + b]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[Smem::XCHG + b]);   // one arrival per warp
                 ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::XCHG + b], ph, p.err, abort));
                 if (ok) {
                     const float tmax = fmaxf(own_max, xmax[(b * 2 + (kh ^ 1)) * BM + row]);
