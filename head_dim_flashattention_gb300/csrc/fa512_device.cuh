@@ -307,6 +307,13 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar_addr) {
                  : "memory");
 }
 
+// The same without release semantics: for a signal that publishes no memory
+// writes (a buffer whose reads have completed may be overwritten).  It does
+// not hold up the arriving thread the way a cluster-scope release does.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
     uint32_t ok;
     asm volatile(

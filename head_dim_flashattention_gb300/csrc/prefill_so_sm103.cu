@@ -492,7 +492,8 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 for (int j = 0; j < n_kt; ++j) {
                     if (!wait_or_abort(&bars[Smem::S_READ + (j % S_BUFS)], (j / S_BUFS) & 1, p.err, abort, wait_ns))
                         break;
-                    mbar_arrive_remote(bar_of(Smem::S_FREE + (j % S_BUFS), 0));
+                    // (the S values are in registers: nothing to publish)
+                    mbar_arrive_remote_relaxed(bar_of(Smem::S_FREE + (j % S_BUFS), 0));
                 }
             }
         } else if (warp == 1) {
@@ -799,7 +800,10 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                         break;
                     tc_fence_after_sync();
                     tc_fence_before_sync();
-                    mbar_arrive_remote(bar_of(Smem::PV_READY + (j % P_BUFS), 2));
+                    // O was corrected (tcgen05.st completed) and P landed: nothing
+                    // to publish, except the cleared V rows of a paged tail tile
+                    if (kt_begin + j == tail_tile) mbar_arrive_remote(bar_of(Smem::PV_READY + (j % P_BUFS), 2));
+                    else mbar_arrive_remote_relaxed(bar_of(Smem::PV_READY + (j % P_BUFS), 2));
                 }
             }
         } else if (warp == COPY_WARP) {
@@ -809,7 +813,8 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     if (!wait_or_abort(&bars[Smem::ALPHA_READ + (j % P_BUFS)], (j / P_BUFS) & 1, p.err, abort,
                                        wait_ns))
                         break;
-                    mbar_arrive_remote(bar_of(Smem::STAGE_FREE + (j & 1), rank - 2));
+                    // (alpha was read and the copy landed: nothing to publish)
+                    mbar_arrive_remote_relaxed(bar_of(Smem::STAGE_FREE + (j & 1), rank - 2));
                 }
             }
         } else if (warp == 1) {
