@@ -53,10 +53,12 @@
 // max moved, then mark the tile ready; at the end they normalise O by the
 // sum of the bf16 P values and write bf16 rows.
 //
-// A cluster-scope mbarrier arrival stalls the thread that makes it for about
-// a microsecond, so no softmax or correction warp makes one per tile: they
-// arrive on barriers of their own CTA, and an otherwise idle thread forwards
-// one arrival per tile to the other CTA.
+// A cluster-scope mbarrier arrival with release semantics stalls the thread
+// that makes it for about a microsecond.  The per-tile signals to another CTA
+// ("S read", "alpha read", "tile ready") publish no memory writes -- the
+// values were loaded into registers, or the tensor-core stores completed --
+// so the warps make them as relaxed arrivals, which cost no such stall; only
+// a paged tail tile, whose cleared V rows the MMA must see, takes a release.
 //
 // Causal / sliding-window tile skipping over the pair's visible band; only
 // the key parts that cross a row's band edge are masked element by
@@ -147,9 +149,7 @@ struct Smem {
         P_LANDED = PV_READY + P_BUFS,    // [3] output CTAs: P and alpha of the tile arrived
         O_FINAL = P_LANDED + P_BUFS,     // output CTAs: the last O += P V completed
         L_READY = O_FINAL + 1,           // output CTAs: the row sums arrived
-        ALPHA_READ = L_READY + 1,        // [3] output CTAs: correction warps read the tile's alpha
-        CORR_DONE = ALPHA_READ + P_BUFS, // [3] output CTA 3: its correction warps are done with the tile
-        V_TAIL = CORR_DONE + P_BUFS,     // paged, output CTAs: this CTA's V of the tile holding the cache's end landed
+        V_TAIL = L_READY + 1,            // paged, output CTAs: this CTA's V of the tile holding the cache's end landed
         DRAIN = V_TAIL + 1,              // every MMA this CTA issued has completed
         N_BARS = DRAIN + 1
     };
@@ -412,14 +412,13 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (i == Smem::Q_COPIED) count = N_WORK_WARPS;
             // the leader's softmax warps, plus one forwarded arrival for the other CTA's
             if (i >= Smem::S_FREE && i < Smem::S_FREE + S_BUFS) count = N_WORK_WARPS + 1;
-            if ((i >= Smem::S_READ && i < Smem::S_READ + S_BUFS) ||
-                (i >= Smem::ALPHA_READ && i < Smem::ALPHA_READ + P_BUFS) ||
-                (i >= Smem::CORR_DONE && i < Smem::CORR_DONE + P_BUFS))
+            // this CTA's softmax warps; the output CTA's correction warps
+            if ((i >= Smem::P_STAGED && i < Smem::P_STAGED + STAGES) ||
+                (i >= Smem::STAGE_FREE && i < Smem::STAGE_FREE + STAGES) ||
+                (i >= Smem::S_READ && i < Smem::S_READ + S_BUFS))
                 count = N_WORK_WARPS;
-            if (i >= Smem::P_STAGED && i < Smem::P_STAGED + STAGES) count = N_WORK_WARPS;
-            // the leader's correction warps, one forwarded arrival for the other
-            // output CTA's, plus the V load
-            if (i >= Smem::PV_READY && i < Smem::PV_READY + P_BUFS) count = N_WORK_WARPS + 2;
+            // the correction warps of both output CTAs, plus the V load
+            if (i >= Smem::PV_READY && i < Smem::PV_READY + P_BUFS) count = 2 * N_WORK_WARPS + 1;
             mbar_init(&bars[i], count);
         }
         *abort = 0;
@@ -487,12 +486,11 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         } else if (warp == 1 && rank == 1) {
             if (lane == 0) {
                 // -------------------------------------------------- forward "S read" to the leader
-                // (one cluster-scope arrival per tile from an idle thread: such an
-                // arrival stalls the thread that makes it)
+                // (the softmax warps arrive locally: a remote arrival, even a
+                // relaxed one, measured slower on their critical path)
                 for (int j = 0; j < n_kt; ++j) {
                     if (!wait_or_abort(&bars[Smem::S_READ + (j % S_BUFS)], (j / S_BUFS) & 1, p.err, abort, wait_ns))
                         break;
-                    // (the S values are in registers: nothing to publish)
                     mbar_arrive_remote_relaxed(bar_of(Smem::S_FREE + (j % S_BUFS), 0));
                 }
             }
@@ -792,31 +790,6 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     }
                 }
             }
-        } else if (warp == 1 && rank == 3) {
-            if (lane == 0) {
-                // -------------------------------------------------- forward "tile ready" to the leader
-                for (int j = 0; j < n_kt; ++j) {
-                    if (!wait_or_abort(&bars[Smem::CORR_DONE + (j % P_BUFS)], (j / P_BUFS) & 1, p.err, abort, wait_ns))
-                        break;
-                    tc_fence_after_sync();
-                    tc_fence_before_sync();
-                    // O was corrected (tcgen05.st completed) and P landed: nothing
-                    // to publish, except the cleared V rows of a paged tail tile
-                    if (kt_begin + j == tail_tile) mbar_arrive_remote(bar_of(Smem::PV_READY + (j % P_BUFS), 2));
-                    else mbar_arrive_remote_relaxed(bar_of(Smem::PV_READY + (j % P_BUFS), 2));
-                }
-            }
-        } else if (warp == COPY_WARP) {
-            if (lane == 0) {
-                // -------------------------------------------------- forward "copy landed, alpha read"
-                for (int j = 0; j < n_kt; ++j) {
-                    if (!wait_or_abort(&bars[Smem::ALPHA_READ + (j % P_BUFS)], (j / P_BUFS) & 1, p.err, abort,
-                                       wait_ns))
-                        break;
-                    // (alpha was read and the copy landed: nothing to publish)
-                    mbar_arrive_remote_relaxed(bar_of(Smem::STAGE_FREE + (j & 1), rank - 2));
-                }
-            }
         } else if (warp == 1) {
             if (rank == 2) {
                 // -------------------------------------------------- O += P V (both SMs)
@@ -871,8 +844,10 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 fence_proxy_async_smem();
                 const float a = alpha_s[pb * BM + row];
                 const bool rescale = j > 0 && __any_sync(0xffffffffu, a != 1.f);
-                // this tile's copy landed and its alpha was read (forwarded to the score CTA)
-                if (lane == 0) mbar_arrive(&bars[Smem::ALPHA_READ + pb]);
+                // this tile's copy landed and its alpha was read: the score CTA's
+                // staging buffer may take the tile after next (relaxed: nothing
+                // to publish)
+                if (lane == 0) mbar_arrive_remote_relaxed(bar_of(Smem::STAGE_FREE + (j & 1), rank - 2));
                 if (rescale) {
                     // O += P V of the previous tile must be done before O is corrected
                     if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::PV_DONE + (j - 1) % P_BUFS],
@@ -911,7 +886,13 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[rank == 2 ? Smem::PV_READY + pb : Smem::CORR_DONE + pb]);
+                // O corrected (tcgen05.st completed) and P landed: relaxed, except
+                // where a paged tail tile's cleared V rows must be published
+                if (lane == 0) {
+                    if (rank == 2) mbar_arrive(&bars[Smem::PV_READY + pb]);
+                    else if (PAGED && kt_begin + j == tail_tile) mbar_arrive_remote(bar_of(Smem::PV_READY + pb, 2));
+                    else mbar_arrive_remote_relaxed(bar_of(Smem::PV_READY + pb, 2));
+                }
             }
             if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::O_FINAL], 0, p.err, abort, wait_ns));
             if (ok) ok = __all_sync(0xffffffffu, wait_cluster_or_abort(&bars[Smem::L_READY], 0, p.err, abort, wait_ns));
