@@ -556,13 +556,13 @@ def run_ours(args):
     pf_avg_s = t_pf / args.steps if not args.no_prefill else float("nan")
     pf_src = source_digest(["prefill_so_sm103.cu", "fa512_pair.cuh", "fa512_device.cuh", "fa512_internal.h"])
     dec_src = source_digest(["decode_sm103.cu", "fa512_device.cuh", "fa512_internal.h"])
-    roofline = {"kernel": "fa512::prefill::prefill_kernel", "bound": "tensor",
+    roofline = {"kernel": "fa512::prefill_so::prefill_so_kernel<false>", "bound": "tensor",
                 "achieved": pf_flops / pf_avg_s / 1e12, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": pf_flops / pf_avg_s / 1e12 / peaks["bf16_tflops"],
                 "peak_kind": "%s burst bf16 (MEASURED_PEAKS.json)" % peak_kind,
                 "frac_of_sustained": pf_flops / pf_avg_s / 1e12 / peaks["bf16_tflops_sustained"],
                 "frac_of_nominal_2250": pf_flops / pf_avg_s / 1e12 / 2250.0,
-                "traffic": recorded_traffic("prefill_kernel", pf_src), "src": pf_src}
+                "traffic": recorded_traffic("prefill_so_kernel", pf_src), "src": pf_src}
     decode_roofline = None
     if dec:
         per = {}
@@ -782,12 +782,12 @@ def run_ours(args):
                 "value": tf, "unit": "TFLOP/s", "ms": t_b / args.steps * 1e3,
                 "flops_per_call": flops,
                 "target_ms_at_50pct_of_measured_burst": flops / (0.5 * peaks["bf16_tflops"] * 1e12) * 1e3,
-                "roofline": {"kernel": "fa512::prefill::prefill_kernel", "bound": "tensor",
+                "roofline": {"kernel": "fa512::prefill_so::prefill_so_kernel<false>", "bound": "tensor",
                              "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                              "frac": ach / peaks["bf16_tflops"],
                              "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                              "peak_kind": "%s burst bf16 (MEASURED_PEAKS.json)" % peak_kind,
-                             "traffic": recorded_traffic("prefill_kernel_" + name, pf_src)},
+                             "traffic": recorded_traffic("prefill_so_kernel_" + name, pf_src)},
                 "l2": "flushed before every call"}
             del bq, bk, bv, bout, blse
         assert fa.fa512_device_status() == 0
