@@ -136,8 +136,8 @@ struct Smem {
         K_EMPTY = K_FULL + K_SLOTS,      // [5] score CTAs: the slot's MMAs completed
         S_FULL = K_EMPTY + K_SLOTS,      // [2] score CTAs: S of the tile is in TMEM
         S_FREE = S_FULL + S_BUFS,        // [2] score leader: both CTAs' softmax warps read S
-        XCHG = S_FREE + S_BUFS,          // [2] score CTAs: row-max swap of the key parts
-        Q_COPIED = XCHG + 2,             // score CTAs: this CTA's softmax warps moved Q to TMEM
+        XCHG = S_FREE + S_BUFS,          // [2][4] score CTAs: row-max swap of one lane quadrant's key parts
+        Q_COPIED = XCHG + 8,             // score CTAs: this CTA's softmax warps moved Q to TMEM
         Q_HI = Q_COPIED + 1,             // score CTAs: this CTA's Q tile landed (K slots 3-4, staging area)
         Q_TMEM = Q_HI + 1,               // score leader: both CTAs' Q tiles are in TMEM
         P_STAGED = Q_TMEM + 1,           // [2] score CTAs: all softmax warps staged the tile's P
@@ -407,7 +407,8 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < Smem::N_BARS; ++i) {
             uint32_t count = 1;
-            if (i == Smem::XCHG || i == Smem::XCHG + 1 || i == Smem::L_XCHG) count = N_WORK_WARPS;
+            if (i == Smem::L_XCHG) count = N_WORK_WARPS;
+            if (i >= Smem::XCHG && i < Smem::XCHG + 8) count = PARTS;   // the warps sharing a lane quadrant
             if (i == Smem::Q_TMEM) count = 2 * N_WORK_WARPS;
             if (i == Smem::Q_COPIED) count = N_WORK_WARPS;
             // the leader's softmax warps, plus one forwarded arrival for the other CTA's
@@ -649,11 +650,12 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 // units); all then take the same decision on the same numbers
                 const float own_max = mx[0] * p.scale_log2;
                 xmax[(b2 * PARTS + part) * BM + row] = own_max;
-                // one arrival per warp, after the warp's stores (256 single-thread
-                // arrivals on one barrier would serialise)
+                // one arrival per warp, after the warp's stores; only the PARTS
+                // warps of this lane quadrant hold parts of these rows
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[Smem::XCHG + b2]);
-                if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::XCHG + b2], (j >> 1) & 1, p.err, abort,
+                const int xb = Smem::XCHG + b2 * 4 + (warp & 3);
+                if (lane == 0) mbar_arrive(&bars[xb]);
+                if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[xb], (j >> 1) & 1, p.err, abort,
                                                                  wait_ns))))
                     break;
                 float tmax = own_max;
