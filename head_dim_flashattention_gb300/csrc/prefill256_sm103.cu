@@ -81,8 +81,8 @@ struct Smem {
         FULL_K = 0,                      // 2, even CTA: both halves of K(g) landed in slot g & 1
         S_FULL = FULL_K + 2,             // 2: S(g) done; also: K slot g & 1 may be refilled
         P_FULL = S_FULL + 2,             // 2, even CTA: P of both CTAs in TMEM and V landed
-        XCHG = P_FULL + 2,               // 2: row-max swap between the two softmax halves
-        Q_FULL = XCHG + 2,               // 2, even CTA: Q of both CTAs landed in buffer i & 1
+        XCHG = P_FULL + 2,               // [2][4]: row-max swap between the two warps of a lane quadrant
+        Q_FULL = XCHG + 8,               // 2, even CTA: Q of both CTAs landed in buffer i & 1
         O_DONE = Q_FULL + 2,             // O += P(g) V(g) done; also: the V slot may be refilled
         O_FINAL = O_DONE + 1,            // the last O += P V of an item has completed
         O_FREE = O_FINAL + 1,            // even CTA: both CTAs' softmax warps have read an item's O
@@ -196,7 +196,7 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < Smem::N_BARS; ++i) {
             uint32_t count = 1;
-            if (i == Smem::XCHG || i == Smem::XCHG + 1) count = N_SOFTMAX_WARPS;
+            if (i >= Smem::XCHG && i < Smem::XCHG + 8) count = 2;   // the two warps sharing the rows
             // one lane per softmax warp of both CTAs (plus the even CTA's V load)
             if (i == Smem::P_FULL || i == Smem::P_FULL + 1) count = 2 * N_SOFTMAX_WARPS + 1;
             if (i == Smem::O_FREE) count = 2 * N_SOFTMAX_WARPS;
@@ -468,8 +468,9 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
+                        // (relaxed: O was read into registers, nothing to publish)
                         if (rank == 0) mbar_arrive(&bars[Smem::O_FREE]);
-                        else mbar_arrive_remote(leader_bar(Smem::O_FREE));
+                        else mbar_arrive_remote_relaxed(leader_bar(Smem::O_FREE));
                     }
                 }
                 // 64 bytes of this row: 16-byte units (c & 1) * 4 .. + 3 of
@@ -560,8 +561,9 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 const float own_max = mx[0] * p.scale_log2;
                 xmax[(b * 2 + kh) * BM + row] = own_max;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[Smem::XCHG + b]);   // one arrival per warp
-                ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::XCHG + b], ph, p.err, abort));
+                const int xb = Smem::XCHG + b * 4 + (warp & 3);      // one arrival per warp
+                if (lane == 0) mbar_arrive(&bars[xb]);
+                ok = __all_sync(0xffffffffu, wait_or_abort(&bars[xb], ph, p.err, abort));
                 if (ok) {
                     const float tmax = fmaxf(own_max, xmax[(b * 2 + (kh ^ 1)) * BM + row]);
                     float m_use = m_ref, alpha = 1.f;
@@ -614,8 +616,11 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                         tc_fence_before_sync();
                         __syncwarp();
                         if (lane == 0) {
+                            // (relaxed: P went to TMEM by completed tensor-core
+                            // stores, nothing to publish; a release here would
+                            // hold the warp about a microsecond every tile)
                             if (rank == 0) mbar_arrive(&bars[Smem::P_FULL + b]);
-                            else mbar_arrive_remote(leader_bar(Smem::P_FULL + b));
+                            else mbar_arrive_remote_relaxed(leader_bar(Smem::P_FULL + b));
                         }
                     }
                 }
