@@ -85,7 +85,9 @@ struct Prefill256Params {
     float scale_log2;
     unsigned* err;
     int n_clusters;
-    int range_start[kMaxPersistentClusters + 1];   // items of cluster c: [range_start[c], range_start[c + 1])
+    // items of cluster c: range_start[c], + item_stride, ... below range_start[c + 1]
+    int item_stride;
+    int range_start[kMaxPersistentClusters + 1];
 };
 
 int prefill256_smem_bytes();

@@ -136,11 +136,12 @@ __device__ __forceinline__ bool key_visible(int j, int qpos, const Prefill256Par
 // Walks the key tiles of a range of items in order, skipping items with no
 // visible key; qi counts the items that have tiles.
 struct TileCursor {
-    int idx, end, qi, j, g;
+    int idx, end, stride, qi, j, g;
     Item it;
     bool valid;
     __device__ __forceinline__ void first(int begin, int end_, const Prefill256Params& p, int rank) {
-        idx = begin - 1;
+        stride = p.item_stride;
+        idx = begin - stride;
         end = end_;
         qi = -1;
         j = 0;
@@ -150,7 +151,7 @@ struct TileCursor {
     }
     __device__ __forceinline__ void next_item(const Prefill256Params& p, int rank) {
         for (;;) {
-            ++idx;
+            idx += stride;
             if (idx >= end) {
                 valid = false;
                 return;
@@ -190,7 +191,7 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     const int irank = static_cast<int>(rank);
     const int cluster = blockIdx.x >> 1;
     const int begin = p.range_start[cluster];
-    const int end = p.range_start[cluster + 1];
+    const int end = p.item_stride == 1 ? p.range_start[cluster + 1] : p.n_items;
     if (begin >= end) return;   // both CTAs of the pair
 
     if (warp == 0 && lane == 0) {
@@ -417,7 +418,7 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         bool ok = true;
 
         // items with no visible key: O = 0, LSE = -inf
-        for (int idx = begin; idx < end; ++idx) {
+        for (int idx = begin; idx < end; idx += p.item_stride) {
             const Item it = item_geometry(idx, p, irank);
             if (it.n_kt != 0 || row >= p.rows_per_tile || tok >= it.ntok) continue;
             const int hq = it.kvh * G + g_in;
@@ -658,26 +659,19 @@ int prefill256_smem_bytes() { return local256::Smem::total; }
 int prefill256_k_box_rows() { return local256::K_BOX_ROWS; }
 int prefill256_v_box_rows() { return local256::V_BOX_ROWS; }
 
-// Splits the items (KV head major, pairs in order) into at most
-// kMaxPersistentClusters contiguous ranges of about equal cost: a pair's key
-// tiles plus one tile's worth for its start and epilogue.
+// Deals the items (KV head major, pairs in order) round-robin to at most
+// kMaxPersistentClusters clusters: cluster c takes items c, c + n, c + 2n, ...
+// At any time the clusters then work on neighbouring q-tile pairs of one KV
+// head, whose key window the L2 holds once for all of them (a contiguous
+// range per cluster spread the clusters over every part of the sequence, and
+// their windows did not fit).  Items cost about the same (a window of
+// tiles), so the deal also balances the work.
 void plan_prefill256(Prefill256Params& p, int n_sm) {
     const int max_clusters = std::min(kMaxPersistentClusters, std::max(1, n_sm / 2));
     const int n_clusters = std::max(1, std::min(max_clusters, p.n_items));
-    std::vector<long long> cum(static_cast<size_t>(p.n_items) + 1, 0);
-    for (int i = 0; i < p.n_items; ++i) {
-        const local256::Item it = local256::item_geometry(i, p, 0);
-        cum[i + 1] = cum[i] + it.n_kt + 1;
-    }
-    const long long total = cum[p.n_items];
     p.n_clusters = n_clusters;
-    p.range_start[0] = 0;
-    int i = 0;
-    for (int c = 1; c < n_clusters; ++c) {
-        const long long target = total * c / n_clusters;
-        while (i < p.n_items && cum[i] < target) ++i;
-        p.range_start[c] = i;
-    }
+    p.item_stride = n_clusters;
+    for (int c = 0; c < n_clusters; ++c) p.range_start[c] = c;
     p.range_start[n_clusters] = p.n_items;
 }
 
