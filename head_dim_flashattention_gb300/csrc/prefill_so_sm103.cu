@@ -364,10 +364,21 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     // that starts at logical key `key`: the key itself, or in paged mode its
     // slot in the pool.  Halves past the cache's end (and pages outside the
     // pool) read a row past the pool, which the TMA unit fills with zeros.
-    auto half_row = [&](int key) -> int {
+    // Paged: the producers load a half tile's page-table entry (page_entry)
+    // several tiles before they need its row (half_row), so the dependent
+    // load is off their critical path.
+    auto page_entry = [&](int key) -> int {
+        if constexpr (PAGED) {
+            return key < seqlen_k
+                       ? p.page_table[static_cast<size_t>(seq) * p.max_pages_per_seq + (key >> p.page_shift)]
+                       : 0;
+        } else {
+            return 0;
+        }
+    };
+    auto half_row = [&](int key, int pg) -> int {
         if constexpr (PAGED) {
             if (key >= seqlen_k) return p.oob_row;
-            const int pg = p.page_table[static_cast<size_t>(seq) * p.max_pages_per_seq + (key >> p.page_shift)];
             if (static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages)) {
                 report_error(p.err, FA512_DEVICE_ERR_INDEX);
                 return p.oob_row;
@@ -377,6 +388,7 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             return key;
         }
     };
+    constexpr int PF = 4;   // paged: tiles whose page-table entries a producer holds ahead
 
     // this thread's packed row and part (warps 2-17): TMEM lane quadrant
     // warp % 4; part = 32 keys of a tile in the score CTAs, 128 O columns in
@@ -467,6 +479,11 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                                                     : Smem::stage + (c - 4) * Q_CHUNK),
                                       &tmq, bar_of(Smem::Q_HI, rank), c * 64, 0, kvh, q_start + t0, pol_q);
                 // half tile h: tile h / 2, head-dim columns 256 (h % 2) .. +256, this CTA's 64 keys
+                auto k_key = [&](int j) { return (kt_begin + j) * BN + static_cast<int>(pr) * K_BOX_ROWS; };
+                int pf[PF];
+#pragma unroll
+                for (int i = 0; i < PF; ++i) pf[i] = i < n_kt ? page_entry(k_key(i)) : 0;
+                int krow = 0;
                 for (int h = 0; h < 2 * n_kt; ++h) {
                     const int j = h >> 1, c = h & 1, s = h % K_SLOTS;
                     if (h >= K_SLOTS && !wait_or_abort(&bars[Smem::K_EMPTY + s], ((h / K_SLOTS) - 1) & 1, p.err,
@@ -475,10 +492,16 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     // the slots that held Q: once this CTA's Q is in TMEM
                     if (h == Q_PARK_SLOT && !wait_or_abort(&bars[Smem::Q_COPIED], 0, p.err, abort, wait_ns)) break;
                     if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::K_FULL + s], 2 * SLOT);
+                    if (c == 0) {
+                        // both head-dim halves of tile j read the same keys
+                        krow = half_row(k_key(j), pf[0]);
+#pragma unroll
+                        for (int i = 0; i < PF - 1; ++i) pf[i] = pf[i + 1];
+                        pf[PF - 1] = j + PF < n_kt ? page_entry(k_key(j + PF)) : 0;
+                    }
                     // (test hook: the first cluster's rank 0 leaves out its first
                     // K half tile, so that cluster's waits run into their bound)
                     if (h == 0 && p.test_skip_first_k_load && blockIdx.x == 0) continue;
-                    const int krow = half_row((kt_begin + j) * BN + static_cast<int>(pr) * K_BOX_ROWS);
                     for (int b = 0; b < 4; ++b)
                         tma2_load_3d_hint(smem + Smem::kring + s * SLOT + b * K_BOX, &tmk,
                                           bar_of(Smem::K_FULL + s, 0), (c * 4 + b) * 64, kvh, krow, pol_kv);
@@ -748,6 +771,12 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (lane == 0) {
                 // -------------------------------------------------- V loads
                 const uint64_t pol_kv = l2_policy_keep();   // read by every pair of the KV head
+                int pf[PF][2];
+#pragma unroll
+                for (int i = 0; i < PF; ++i)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+                        pf[i][r] = i < n_kt ? page_entry((kt_begin + i) * BN + r * K_BOX_ROWS) : 0;
                 for (int j = 0; j < n_kt; ++j) {
                     const int vb = j & 1;
                     // V buffer vb once O += P V of tile j - 2 completed
@@ -774,7 +803,15 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                             if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
                             vbar = bar_of(Smem::PV_READY + rb, 2);
                         }
-                        const int rows[2] = {half_row(key), half_row(key + K_BOX_ROWS)};
+                        const int rows[2] = {half_row(key, pf[0][0]), half_row(key + K_BOX_ROWS, pf[0][1])};
+#pragma unroll
+                        for (int i = 0; i < PF - 1; ++i) {
+                            pf[i][0] = pf[i + 1][0];
+                            pf[i][1] = pf[i + 1][1];
+                        }
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+                            pf[PF - 1][r] = j + PF < n_kt ? page_entry((kt_begin + j + PF) * BN + r * K_BOX_ROWS) : 0;
                         for (int hh = 0; hh < 2; ++hh)
                             for (int bx = 0; bx < 2; ++bx)
                                 for (int r = 0; r < 2; ++r)
