@@ -34,6 +34,14 @@ __device__ __forceinline__ void mma2_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
                  ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
                  : "memory");
 }
+// Copy of a 128-row x 32-byte block from each CTA's shared memory (described
+// like an MMA operand: the rows' 32-byte K slice of a 128-byte-swizzled
+// tile) into the same TMEM columns of each CTA (8 columns, row r in lane r).
+// Runs in the tensor-core pipeline, in issue order with the MMAs of the
+// issuing thread; a commit tracks its completion.
+__device__ __forceinline__ void tmem_cp2_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 // Arrives on the barrier at this offset in both CTAs once every MMA issued so
 // far has completed.
 __device__ __forceinline__ void commit2_both(uint64_t* bar) {

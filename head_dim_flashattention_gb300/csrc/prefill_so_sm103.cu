@@ -35,8 +35,8 @@
 // five 32 KiB slots (a half tile: this CTA's 64 keys x 256 head-dim columns),
 // each released by the commit after its 16 MMAs; the MMA thread holds back a
 // tile's QK^T until its S buffer has been read (the K loads run ahead).  Q lands in the last
-// two K slots and the P staging area, and the softmax warps move it to TMEM
-// before either is needed.  Eight softmax warps: TMEM lane quadrant (warp % 4) gives a warp
+// two K slots and the P staging area, and the MMA thread copies it into TMEM
+// (tcgen05.cp, ahead of its first MMA) before either is needed.  Eight softmax warps: TMEM lane quadrant (warp % 4) gives a warp
 // its 32 rows, warps 2-5 take keys 0-63 of each tile and warps 6-9 keys
 // 64-127; they swap row maxima through shared memory.  The row max is lazy: O is rescaled only
 // when a row's max grows by more than 2^16.  P goes to one of two staging
@@ -137,10 +137,9 @@ struct Smem {
         S_FULL = K_EMPTY + K_SLOTS,      // [2] score CTAs: S of the tile is in TMEM
         S_FREE = S_FULL + S_BUFS,        // [2] score leader: both CTAs' softmax warps read S
         XCHG = S_FREE + S_BUFS,          // [2][4] score CTAs: row-max swap of one lane quadrant's key parts
-        Q_COPIED = XCHG + 8,             // score CTAs: this CTA's softmax warps moved Q to TMEM
-        Q_HI = Q_COPIED + 1,             // score CTAs: this CTA's Q tile landed (K slots 3-4, staging area)
-        Q_TMEM = Q_HI + 1,               // score leader: both CTAs' Q tiles are in TMEM
-        P_STAGED = Q_TMEM + 1,           // [2] score CTAs: all softmax warps staged the tile's P
+        Q_FULL = XCHG + 8,               // score leader: both CTAs' Q tiles landed (K slots 3-4, staging area)
+        Q_COPIED = Q_FULL + 1,           // score CTAs: the Q tile was copied into TMEM (commit of the copies)
+        P_STAGED = Q_COPIED + 1,         // [2] score CTAs: all softmax warps staged the tile's P
         STAGE_FREE = P_STAGED + STAGES,  // [2] score CTAs: the buffer's last copy landed, its alpha read
         S_READ = STAGE_FREE + STAGES,    // [2] score CTA 1: its softmax warps read S (forwarded to S_FREE)
         L_XCHG = S_READ + S_BUFS,        // score CTAs: row-sum swap
@@ -421,8 +420,6 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             uint32_t count = 1;
             if (i == Smem::L_XCHG) count = N_WORK_WARPS;
             if (i >= Smem::XCHG && i < Smem::XCHG + 8) count = PARTS;   // the warps sharing a lane quadrant
-            if (i == Smem::Q_TMEM) count = 2 * N_WORK_WARPS;
-            if (i == Smem::Q_COPIED) count = N_WORK_WARPS;
             // the leader's softmax warps, plus one forwarded arrival for the other CTA's
             if (i >= Smem::S_FREE && i < Smem::S_FREE + S_BUFS) count = N_WORK_WARPS + 1;
             // this CTA's softmax warps; the output CTA's correction warps
@@ -473,11 +470,11 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 // Q is read once; K and V are read by every pair of the KV head
                 const uint64_t pol_q = l2_policy_stream(), pol_kv = l2_policy_keep();
                 const uint32_t q_bytes = static_cast<uint32_t>(8 * 128 * p.rows_per_tile);   // 8 boxes
-                mbar_arrive_expect_tx(&bars[Smem::Q_HI], q_bytes);
+                if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::Q_FULL], 2 * q_bytes);
                 for (int c = 0; c < 8; ++c)
                     tma2_load_4d_hint(smem + (c < 4 ? Smem::kring + Q_PARK_SLOT * SLOT + c * Q_CHUNK
                                                     : Smem::stage + (c - 4) * Q_CHUNK),
-                                      &tmq, bar_of(Smem::Q_HI, rank), c * 64, 0, kvh, q_start + t0, pol_q);
+                                      &tmq, bar_of(Smem::Q_FULL, 0), c * 64, 0, kvh, q_start + t0, pol_q);
                 // half tile h: tile h / 2, head-dim columns 256 (h % 2) .. +256, this CTA's 64 keys
                 auto k_key = [&](int j) { return (kt_begin + j) * BN + static_cast<int>(pr) * K_BOX_ROWS; };
                 int pf[PF];
@@ -489,7 +486,7 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     if (h >= K_SLOTS && !wait_or_abort(&bars[Smem::K_EMPTY + s], ((h / K_SLOTS) - 1) & 1, p.err,
                                                        abort, wait_ns))
                         break;
-                    // the slots that held Q: once this CTA's Q is in TMEM
+                    // the slots that held Q: once Q has been copied into TMEM
                     if (h == Q_PARK_SLOT && !wait_or_abort(&bars[Smem::Q_COPIED], 0, p.err, abort, wait_ns)) break;
                     if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::K_FULL + s], 2 * SLOT);
                     if (c == 0) {
@@ -523,7 +520,28 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 // -------------------------------------------------- S = Q K^T (both SMs)
                 // The whole warp runs the loop and its waits (warp-uniform, so
                 // the MMA operands stay uniform); one elected lane issues.
-                bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::Q_TMEM], 0, p.err, abort, wait_ns));
+                // Q of both CTAs into TMEM (the A operand of every QK^T): 32
+                // copies of a 16-column slice, in the tensor-core pipeline
+                // ahead of the first MMA; their commit frees the parking slots
+                bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort, wait_ns));
+                if (ok) {
+                    tc_fence_after_sync();
+                    if (elect_one()) {
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            const uint64_t qd = make_sdesc_sw128(
+                                smem_u32(smem + (c8 < 4 ? Smem::kring + Q_PARK_SLOT * SLOT + c8 * Q_CHUNK
+                                                        : Smem::stage + (c8 - 4) * Q_CHUNK)),
+                                16, 1024);
+#pragma unroll
+                            for (int piece = 0; piece < 4; ++piece)
+                                tmem_cp2_128x256b(tmem + TM_Q + static_cast<uint32_t>(c8 * 32 + piece * 8),
+                                                  qd + static_cast<uint64_t>(piece * 2));
+                        }
+                        commit2_mask(&bars[Smem::Q_COPIED], MASK_SCORE);
+                    }
+                    __syncwarp();
+                }
                 const uint64_t k_desc = make_sdesc_sw128(smem_u32(smem + Smem::kring), 16, 1024);
                 for (int j = 0; ok && j < n_kt; ++j) {
                     const uint32_t sb = tmem + static_cast<uint32_t>(j % S_BUFS) * BN;
@@ -587,35 +605,6 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             const bool neg_scale = p.scale_log2 < 0.f;
             const uint32_t out_rank = rank + 2;
             const uint32_t a_dst = map_to_cta(smem_u32(smem + Smem::alpha + row * 4), out_rank);
-
-            // The Q tile to TMEM (the A operand of every QK^T): this warp's
-            // 64-column chunks of its rows, undoing the 128-byte swizzle
-            ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::Q_HI], 0, p.err, abort, wait_ns));
-            if (ok) {
-                for (int cc = 0; cc < 8 / PARTS; ++cc) {
-                    const int c8 = part * (8 / PARTS) + cc;     // chunk c8 of Q: head-dim columns 64 c8 ..
-                    const uint8_t* src = smem + (c8 < 4 ? Smem::kring + Q_PARK_SLOT * SLOT + c8 * Q_CHUNK
-                                                        : Smem::stage + (c8 - 4) * Q_CHUNK) + row * 128;
-                    uint32_t w[32];
-#pragma unroll
-                    for (int pc = 0; pc < 8; ++pc) {
-                        const uint4 x = *reinterpret_cast<const uint4*>(src + ((pc ^ (row & 7)) << 4));
-                        w[4 * pc] = x.x;
-                        w[4 * pc + 1] = x.y;
-                        w[4 * pc + 2] = x.z;
-                        w[4 * pc + 3] = x.w;
-                    }
-                    tmem_st32(tmem + lane_base + TM_Q + static_cast<uint32_t>(c8 * 32), w);
-                }
-                tmem_st_wait();
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[Smem::Q_COPIED]);
-                if (rank == 0) mbar_arrive(&bars[Smem::Q_TMEM]);
-                else mbar_arrive_remote(bar_of(Smem::Q_TMEM, 0));
-            }
 
             for (int j = 0; ok && j < n_kt; ++j) {
                 const int b3 = j % S_BUFS, b2 = j & 1, pb = j % P_BUFS;
