@@ -95,7 +95,6 @@ constexpr int K_BOX_ROWS = BN / 2;       // {64 columns, 64 keys} boxes
 constexpr int K_BOX = K_BOX_ROWS * 128;  // 8 KiB
 constexpr int S_BUFS = 2;                // S buffers of 128 TMEM columns
 constexpr uint32_t TM_Q = S_BUFS * BN;   // the Q tile: head-dim column d in TMEM column TM_Q + d / 2
-constexpr int Q_PARK_SLOT = K_SLOTS - 2; // Q chunks 0-3 land in K slots 3-4, chunks 4-7 in the staging area
 constexpr int V_SLOTS = 4;               // output CTAs: 2 tiles x 2 O halves
 constexpr int V_BOX_ROWS = BN;           // {64 columns, 128 keys} boxes
 constexpr int V_BOX = V_BOX_ROWS * 128;  // 16 KiB
@@ -105,7 +104,7 @@ constexpr int P_BUFS = 3;                // output CTAs: P buffers
 constexpr int STAGES = 2;                // score CTAs: P staging buffers
 constexpr uint32_t P_TX = P_BUF + BM * 4;   // bytes landing per tile: P and alpha
 constexpr uint32_t L_TX = BM * 4;           // the final row sums
-static_assert((PARTS == 2 || PARTS == 4) && KP % 32 == 0, "two or four work warps per lane quadrant");
+static_assert(PARTS == 2 && KP % 32 == 0, "two work warps per lane quadrant");
 
 // Rescale O only when the row max grows by more than this (log2 units);
 // until then the stale max stays the reference and p <= 2^16 (bf16 and the
@@ -117,8 +116,7 @@ constexpr float RESCALE_THRESHOLD = 16.0f;
 constexpr uint16_t MASK_SCORE = 0x3, MASK_OUTPUT = 0xC, MASK_ALL = 0xF;
 
 struct Smem {
-    // score CTAs: the Q tile lands in the last two K slots and the staging
-    // area and moves to TMEM before either is used for K or P
+    // score CTAs: Q and K entries of the ring (Q is copied on into TMEM)
     static constexpr int kring = 0;                             // 5 x 32 KiB
     static constexpr int stage = kring + K_SLOTS * SLOT;        // 2 x 32 KiB
     static constexpr int xmax = stage + STAGES * P_BUF;         // [2 buffers][PARTS][128] f32
@@ -132,22 +130,21 @@ struct Smem {
     // output CTAs' alpha and row sums)
     static constexpr int bars = xmax + 2048;
     enum {
-        K_FULL = 0,                      // [5] score leader: both CTAs' half tile landed
-        K_EMPTY = K_FULL + K_SLOTS,      // [5] score CTAs: the slot's MMAs completed
+        K_FULL = 0,                      // [5] score leader: both CTAs' ring entry (Q boxes or K half tile) landed
+        K_EMPTY = K_FULL + K_SLOTS,      // [5] score CTAs: the entry's copies or MMAs completed
         S_FULL = K_EMPTY + K_SLOTS,      // [2] score CTAs: S of the tile is in TMEM
         S_FREE = S_FULL + S_BUFS,        // [2] score leader: both CTAs' softmax warps read S
         XCHG = S_FREE + S_BUFS,          // [2][4] score CTAs: row-max swap of one lane quadrant's key parts
-        Q_FULL = XCHG + 8,               // score leader: both CTAs' Q tiles landed (K slots 3-4, staging area)
-        Q_COPIED = Q_FULL + 1,           // score CTAs: the Q tile was copied into TMEM (commit of the copies)
-        P_STAGED = Q_COPIED + 1,         // [2] score CTAs: all softmax warps staged the tile's P
+        P_STAGED = XCHG + 8,             // [2] score CTAs: all softmax warps staged the tile's P
         STAGE_FREE = P_STAGED + STAGES,  // [2] score CTAs: the buffer's last copy landed, its alpha read
         S_READ = STAGE_FREE + STAGES,    // [2] score CTA 1: its softmax warps read S (forwarded to S_FREE)
-        L_XCHG = S_READ + S_BUFS,        // score CTAs: row-sum swap
-        PV_DONE = L_XCHG + 1,            // [3] all four: O += P V of the P buffer's last tile completed
+        L_XCHG = S_READ + S_BUFS,        // score CTAs: part 1's row sums of the item are staged
+        L_FREE = L_XCHG + 1,             // score CTAs: the output CTA read the item's row sums
+        PV_DONE = L_FREE + 1,            // [3] all four: O += P V of the P buffer's last tile completed
         PV_READY = PV_DONE + P_BUFS,     // [3] output leader: P landed and O corrected in both, V landed
         P_LANDED = PV_READY + P_BUFS,    // [3] output CTAs: P and alpha of the tile arrived
-        O_FINAL = P_LANDED + P_BUFS,     // output CTAs: the last O += P V completed
-        L_READY = O_FINAL + 1,           // output CTAs: the row sums arrived
+        O_FINAL = P_LANDED + P_BUFS,     // output CTAs: the item's last O += P V completed
+        L_READY = O_FINAL + 1,           // output CTAs: the item's row sums arrived
         V_TAIL = L_READY + 1,            // paged, output CTAs: this CTA's V of the tile holding the cache's end landed
         DRAIN = V_TAIL + 1,              // every MMA this CTA issued has completed
         N_BARS = DRAIN + 1
@@ -196,6 +193,20 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint3
                  : "memory");
 }
 
+// 32 bytes (eight 32-bit words) to global memory in one store; STREAM: with
+// the evict-first policy (data written once).  The address is 32-byte aligned.
+template <bool STREAM>
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
+    if constexpr (STREAM)
+        asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]),
+                     "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                     : "memory");
+    else
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]),
+                     "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                     : "memory");
+}
+
 // Bounded wait with cluster-scope acquire (for data another CTA delivered).
 __device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t parity, unsigned* err,
                                                       volatile int* abort, unsigned long long limit_ns) {
@@ -215,9 +226,138 @@ __device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t pa
     }
 }
 
-// PAGED: a batch of chunks (varlen rows through cu_seqlens_q) over a paged
-// cache; K and V rows are found through the page table one 64-key half tile
-// at a time (a page holds a whole number of half tiles).
+// Geometry of one work item (a q-tile pair of one KV head) for the cluster
+// ranks with tile parity pr (which q tile of the pair).
+struct Geo {
+    bool valid;                  // the item exists
+    int kvh, seq, q_start, seqlen_q, seqlen_k, q_offset;
+    int t0, ntok, p_first, p_last;
+    int kt_begin, n_kt, tail_tile;
+};
+
+// Work items are numbered KV head by KV head (contiguous), or sequence by
+// sequence and KV head by KV head (paged), heaviest pair first, with no gaps.
+// Called by a whole warp: in paged mode it finds the item's sequence by a
+// scan of the chunk lengths (one contiguous block of sequences per lane).
+template <bool PAGED>
+__device__ Geo item_geometry(const PrefillParams& p, int item, uint32_t pr, int lane) {
+    Geo g;
+    g.valid = false;
+    const int T = p.tokens_per_tile;
+    int pair;
+    g.seq = 0;
+    g.q_start = 0;
+    g.seqlen_q = p.seqlen_q;
+    g.seqlen_k = p.seqlen_k;
+    g.q_offset = p.q_offset;
+    if constexpr (PAGED) {
+        const int two_t = 2 * T;
+        // pairs of a chunk with rows [s0, s1) (0 for a malformed entry, recorded)
+        auto chunk_pairs = [&](int s0, int s1) -> int {
+            int n = s1 - s0;
+            if (s0 < 0 || n < 0 || s0 > p.total_q - n) {
+                if (blockIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                return 0;
+            }
+            if (n > p.max_seqlen_q) {
+                if (blockIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                n = p.max_seqlen_q;
+            }
+            return (n + two_t - 1) / two_t;
+        };
+        const int per = (p.batch + 31) >> 5;
+        const int lo = min(p.batch, lane * per), hi = min(p.batch, lo + per);
+        // up to 32 sequences: one sequence per lane, all loads in flight at once
+        int s0 = 0, s1 = 0, kv = 0;
+        if (per == 1 && lo < hi) {
+            s0 = p.cu_seqlens_q[lo];
+            s1 = p.cu_seqlens_q[lo + 1];
+            kv = p.seqused_k[lo];
+        }
+        int cnt = 0;
+        if (per == 1) {
+            if (lo < hi) cnt = chunk_pairs(s0, s1) * p.n_kv_heads;
+        } else {
+            for (int b = lo; b < hi; ++b) cnt += chunk_pairs(p.cu_seqlens_q[b], p.cu_seqlens_q[b + 1]) * p.n_kv_heads;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += t;
+        }
+        const int excl = incl - cnt;
+        const unsigned owner_mask = __ballot_sync(0xffffffffu, item >= excl && item < incl);
+        if (!owner_mask) return g;   // past the last item
+        const int owner = __ffs(owner_mask) - 1;
+        int f_seq = lo, acc = excl;
+        if (lane == owner && per > 1) {
+            for (int b = lo; b < hi; ++b) {
+                s0 = p.cu_seqlens_q[b];
+                s1 = p.cu_seqlens_q[b + 1];
+                const int c = chunk_pairs(s0, s1) * p.n_kv_heads;
+                if (item < acc + c) {
+                    f_seq = b;
+                    break;
+                }
+                acc += c;
+            }
+            kv = p.seqused_k[f_seq];
+        }
+        f_seq = __shfl_sync(0xffffffffu, f_seq, owner);
+        acc = __shfl_sync(0xffffffffu, acc, owner);
+        s0 = __shfl_sync(0xffffffffu, s0, owner);
+        s1 = __shfl_sync(0xffffffffu, s1, owner);
+        kv = __shfl_sync(0xffffffffu, kv, owner);
+        const int off = item - acc;
+        g.seq = f_seq;
+        g.q_start = s0;
+        g.seqlen_q = min(s1 - s0, p.max_seqlen_q);
+        g.seqlen_k = kv;
+        const int n_pairs_seq = (g.seqlen_q + two_t - 1) / two_t;
+        g.kvh = off / n_pairs_seq;
+        pair = n_pairs_seq - 1 - (off - g.kvh * n_pairs_seq);   // 0 = heaviest pair first
+        g.q_offset = g.seqlen_k - (s1 - s0);                    // the chunk is its sequence's tail
+        const int kv_cap = p.max_pages_per_seq << p.page_shift;
+        if (g.seqlen_k < 0 || g.seqlen_k > kv_cap) {
+            // recorded (idempotently); read up to the table's capacity
+            if (off == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
+            g.seqlen_k = g.seqlen_k < 0 ? 0 : kv_cap;
+        }
+    } else {
+        const int n_pairs = (p.num_q_tiles + 1) / 2;
+        if (item >= n_pairs * p.n_kv_heads) return g;
+        g.kvh = item / n_pairs;
+        pair = n_pairs - 1 - item % n_pairs;
+    }
+    g.valid = true;
+    const int qt = 2 * pair + static_cast<int>(pr);    // may be one past the last tile: no rows
+    g.t0 = qt * T;
+    g.ntok = min(T, g.seqlen_q - g.t0);                 // <= 0 for a missing second tile
+    g.p_first = g.q_offset + g.t0;
+    g.p_last = g.q_offset + g.t0 + g.ntok - 1;
+    const int pair_first = g.q_offset + 2 * pair * T;
+    const int pair_last = g.q_offset + min(g.seqlen_q, (2 * pair + 2) * T) - 1;
+    // paged: the tile that holds the cache's last key when that key does not
+    // end a half tile (its V rows past the end are live pool memory)
+    g.tail_tile = (PAGED && (g.seqlen_k & (K_BOX_ROWS - 1))) ? (g.seqlen_k - 1) / BN : -1;
+    int j_lo = 0, j_hi = g.seqlen_k;
+    if (p.causal) j_hi = min(j_hi, pair_last + 1);
+    if (p.window > 0) j_lo = max(0, pair_first - p.window + 1);
+    if (j_hi < j_lo) j_hi = j_lo;
+    g.kt_begin = j_lo / BN;
+    g.n_kt = j_hi > j_lo ? (j_hi + BN - 1) / BN - g.kt_begin : 0;
+    return g;
+}
+
+// A persistent cluster of four takes the work items cluster, cluster + n,
+// cluster + 2n, ... (n clusters): every role walks the same item sequence
+// and keeps running counters (K-ring entries, tiles, items), so the barrier
+// phases run on across items and the next item's Q loads, QK^T and P V
+// overlap the end of the current one.  PAGED: a batch of chunks (varlen rows
+// through cu_seqlens_q) over a paged cache; K and V rows are found through
+// the page table one 64-key half tile at a time (a page holds a whole number
+// of half tiles).
 template <bool PAGED>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -237,195 +377,24 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     const int lane = tid & 31;
     const unsigned long long wait_ns = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
 
-    // ---- work item: (q-tile pair, KV head); KV heads one after the other so
-    // that resident clusters share one head's K and V in L2, the heaviest
-    // (latest) q tiles of a head first.
     const uint32_t rank = cluster_ctarank();            // == blockIdx.x & 3
     const bool scorer = rank < 2;
     const uint32_t pr = rank & 1;                       // which q tile of the pair
     const int G = p.group;
-    const int T = p.tokens_per_tile;
-    const int item = blockIdx.x >> 2;
-    int kvh, pair, seq = 0, q_start = 0;
-    int seqlen_q = p.seqlen_q, seqlen_k = p.seqlen_k, q_offset = p.q_offset;
-    if constexpr (PAGED) {
-        // Work items are numbered sequence by sequence, KV head by KV head,
-        // heaviest pair first, with no gaps: warp 0 finds this cluster's
-        // sequence by a scan of the chunk lengths (one contiguous block of
-        // sequences per lane), the others wait at the barrier below.
-        int* found = reinterpret_cast<int*>(smem + Smem::xmax);   // idle until the pipeline starts
-        const int two_t = 2 * T;
-        // pairs of a chunk with rows [s0, s1) (0 for a malformed entry; block 0 records those)
-        auto chunk_pairs = [&](int s0, int s1) -> int {
-            int n = s1 - s0;
-            if (s0 < 0 || n < 0 || s0 > p.total_q - n) {
-                if (blockIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
-                return 0;
-            }
-            if (n > p.max_seqlen_q) {
-                if (blockIdx.x == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
-                n = p.max_seqlen_q;
-            }
-            return (n + two_t - 1) / two_t;
-        };
-        if (warp == 0) {
-            const int per = (p.batch + 31) >> 5;
-            const int lo = min(p.batch, lane * per), hi = min(p.batch, lo + per);
-            // up to 32 sequences: one sequence per lane, all loads in flight at once
-            int s0 = 0, s1 = 0, kv = 0;
-            if (per == 1 && lo < hi) {
-                s0 = p.cu_seqlens_q[lo];
-                s1 = p.cu_seqlens_q[lo + 1];
-                kv = p.seqused_k[lo];
-            }
-            int cnt = 0;
-            if (per == 1) {
-                if (lo < hi) cnt = chunk_pairs(s0, s1) * p.n_kv_heads;
-            } else {
-                for (int b = lo; b < hi; ++b)
-                    cnt += chunk_pairs(p.cu_seqlens_q[b], p.cu_seqlens_q[b + 1]) * p.n_kv_heads;
-            }
-            int incl = cnt;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, incl, d);
-                if (lane >= d) incl += t;
-            }
-            const int excl = incl - cnt;
-            const unsigned owner_mask = __ballot_sync(0xffffffffu, item >= excl && item < incl);
-            if (owner_mask) {
-                const int owner = __ffs(owner_mask) - 1;
-                if (lane == owner) {
-                    int f_seq = lo, acc = excl;
-                    if (per > 1) {
-                        for (int b = lo; b < hi; ++b) {
-                            s0 = p.cu_seqlens_q[b];
-                            s1 = p.cu_seqlens_q[b + 1];
-                            const int c = chunk_pairs(s0, s1) * p.n_kv_heads;
-                            if (item < acc + c) {
-                                f_seq = b;
-                                break;
-                            }
-                            acc += c;
-                        }
-                        kv = p.seqused_k[f_seq];
-                    }
-                    found[0] = f_seq;
-                    found[1] = item - acc;
-                    found[2] = s0;
-                    found[3] = s1;
-                    found[4] = kv;
-                }
-            } else if (lane == 0) {
-                found[0] = -1;
-            }
-        }
-        __syncthreads();
-        seq = found[0];
-        if (seq < 0) return;                            // past the last item: all four CTAs
-        const int off = found[1];
-        q_start = found[2];
-        seqlen_q = min(found[3] - q_start, p.max_seqlen_q);
-        seqlen_k = found[4];
-        const int n_pairs_seq = (seqlen_q + two_t - 1) / two_t;
-        kvh = off / n_pairs_seq;
-        pair = n_pairs_seq - 1 - (off - kvh * n_pairs_seq);   // 0 = heaviest pair first
-        q_offset = seqlen_k - (found[3] - q_start);    // the chunk is its sequence's tail
-        const int kv_cap = p.max_pages_per_seq << p.page_shift;
-        if (seqlen_k < 0 || seqlen_k > kv_cap) {
-            // recorded once per sequence; read up to the table's capacity
-            if (tid == 0 && off == 0) report_error(p.err, FA512_DEVICE_ERR_INDEX);
-            seqlen_k = seqlen_k < 0 ? 0 : kv_cap;
-        }
-        __syncthreads();                                // the scratch is reused below
-    } else {
-        const int n_pairs = (p.num_q_tiles + 1) / 2;
-        kvh = item / n_pairs;
-        pair = n_pairs - 1 - item % n_pairs;
-    }
-    const int qt = 2 * pair + static_cast<int>(pr);    // may be one past the last tile: no rows
-    const int t0 = qt * T;
-    const int ntok = min(T, seqlen_q - t0);             // <= 0 for a missing second tile
-    const int p_first = q_offset + t0;
-    const int p_last = q_offset + t0 + ntok - 1;
-    const int pair_first = q_offset + 2 * pair * T;
-    const int pair_last = q_offset + min(seqlen_q, (2 * pair + 2) * T) - 1;
-    // paged: the tile that holds the cache's last key when that key does not
-    // end a half tile (its V rows past the end are live pool memory)
-    const int tail_tile = (PAGED && (seqlen_k & (K_BOX_ROWS - 1))) ? (seqlen_k - 1) / BN : -1;
-    int j_lo = 0, j_hi = seqlen_k;
-    if (p.causal) j_hi = min(j_hi, pair_last + 1);
-    if (p.window > 0) j_lo = max(0, pair_first - p.window + 1);
-    if (j_hi < j_lo) j_hi = j_lo;
-    const int kt_begin = j_lo / BN;
-    const int n_kt = j_hi > j_lo ? (j_hi + BN - 1) / BN - kt_begin : 0;
-    // Row of the tensor map holding the first key of the 64-key half tile
-    // that starts at logical key `key`: the key itself, or in paged mode its
-    // slot in the pool.  Halves past the cache's end (and pages outside the
-    // pool) read a row past the pool, which the TMA unit fills with zeros.
-    // Paged: the producers load a half tile's page-table entry (page_entry)
-    // several tiles before they need its row (half_row), so the dependent
-    // load is off their critical path.
-    auto page_entry = [&](int key) -> int {
-        if constexpr (PAGED) {
-            return key < seqlen_k
-                       ? p.page_table[static_cast<size_t>(seq) * p.max_pages_per_seq + (key >> p.page_shift)]
-                       : 0;
-        } else {
-            return 0;
-        }
-    };
-    auto half_row = [&](int key, int pg) -> int {
-        if constexpr (PAGED) {
-            if (key >= seqlen_k) return p.oob_row;
-            if (static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages)) {
-                report_error(p.err, FA512_DEVICE_ERR_INDEX);
-                return p.oob_row;
-            }
-            return (pg << p.page_shift) + (key & ((1 << p.page_shift) - 1));
-        } else {
-            return key;
-        }
-    };
-    constexpr int PF = 4;   // paged: tiles whose page-table entries a producer holds ahead
-
-    // this thread's packed row and part (warps 2-17): TMEM lane quadrant
-    // warp % 4; part = 32 keys of a tile in the score CTAs, 128 O columns in
-    // the output CTAs
-    const bool work_warp = warp >= 2 && warp < COPY_WARP;
-    const int row = (warp & 3) * 32 + lane;
-    const int part = (warp - 2) >> 2;
-    const int tok = row / G;
-    const int g = row - tok * G;
-    const bool valid_row = work_warp && row < p.rows_per_tile && tok < ntok;
-    const int qpos = q_offset + t0 + tok;
-    const int hq = kvh * G + g;
-
-    if (n_kt == 0) {
-        // no key is visible to any row of the pair: O = 0, LSE = -inf
-        if (valid_row) {
-            if (!scorer) {
-                uint4* dst = reinterpret_cast<uint4*>(
-                    p.out + (static_cast<size_t>(q_start + t0 + tok) * p.n_q_heads + hq) * D + part * OP);
-                for (int i = 0; i < OP / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-            } else if (part == 0 && p.lse) {
-                p.lse[static_cast<size_t>(hq) * p.total_q + q_start + t0 + tok] = -INFINITY;
-            }
-        }
-        return;
-    }
+    const int cluster = blockIdx.x >> 2;
+    const int n_clusters = gridDim.x >> 2;
 
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < Smem::N_BARS; ++i) {
             uint32_t count = 1;
-            if (i == Smem::L_XCHG) count = N_WORK_WARPS;
+            if (i == Smem::L_XCHG) count = N_WORK_WARPS / PARTS;           // the part-1 softmax warps
             if (i >= Smem::XCHG && i < Smem::XCHG + 8) count = PARTS;   // the warps sharing a lane quadrant
             // the leader's softmax warps, plus one forwarded arrival for the other CTA's
             if (i >= Smem::S_FREE && i < Smem::S_FREE + S_BUFS) count = N_WORK_WARPS + 1;
             // this CTA's softmax warps; the output CTA's correction warps
             if ((i >= Smem::P_STAGED && i < Smem::P_STAGED + STAGES) ||
                 (i >= Smem::STAGE_FREE && i < Smem::STAGE_FREE + STAGES) ||
-                (i >= Smem::S_READ && i < Smem::S_READ + S_BUFS))
+                (i >= Smem::S_READ && i < Smem::S_READ + S_BUFS) || i == Smem::L_FREE)
                 count = N_WORK_WARPS;
             // the correction warps of both output CTAs, plus the V load
             if (i >= Smem::PV_READY && i < Smem::PV_READY + P_BUFS) count = 2 * N_WORK_WARPS + 1;
@@ -462,99 +431,166 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     // barrier i of cluster rank r
     auto bar_of = [&](int i, uint32_t r) -> uint32_t { return map_to_cta(smem_u32(&bars[i]), r); };
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // a wait made by every lane of a warp, with a warp-uniform outcome
+    auto wait_warp = [&](int i, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait_or_abort(&bars[i], parity, p.err, abort, wait_ns));
+    };
+
+    // Row of the tensor map holding the first key of the 64-key half tile
+    // that starts at logical key `key`: the key itself, or in paged mode its
+    // slot in the pool.  Halves past the cache's end (and pages outside the
+    // pool) read a row past the pool, which the TMA unit fills with zeros.
+    // Paged: the producers load a half tile's page-table entry (page_entry)
+    // several tiles before they need its row (half_row), so the dependent
+    // load is off their critical path.
+    auto page_entry = [&](const Geo& gm, int key) -> int {
+        if constexpr (PAGED) {
+            return key < gm.seqlen_k
+                       ? p.page_table[static_cast<size_t>(gm.seq) * p.max_pages_per_seq + (key >> p.page_shift)]
+                       : 0;
+        } else {
+            return 0;
+        }
+    };
+    auto half_row = [&](const Geo& gm, int key, int pg) -> int {
+        if constexpr (PAGED) {
+            if (key >= gm.seqlen_k) return p.oob_row;
+            if (static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages)) {
+                report_error(p.err, FA512_DEVICE_ERR_INDEX);
+                return p.oob_row;
+            }
+            return (pg << p.page_shift) + (key & ((1 << p.page_shift) - 1));
+        } else {
+            return key;
+        }
+    };
+    constexpr int PF = 4;   // paged: tiles whose page-table entries a producer holds ahead
+
+    // this thread's packed row and part (warps 2-9): TMEM lane quadrant
+    // warp % 4; part = 64 keys of a tile in the score CTAs, 256 O columns in
+    // the output CTAs
+    const bool work_warp = warp >= 2 && warp < COPY_WARP;
+    const int row = (warp & 3) * 32 + lane;
+    const int part = (warp - 2) >> 2;
 
     if (scorer) {
         if (warp == 0) {
-            if (lane == 0) {
-                // -------------------------------------------------- Q and K loads
-                // Q is read once; K and V are read by every pair of the KV head
-                const uint64_t pol_q = l2_policy_stream(), pol_kv = l2_policy_keep();
-                const uint32_t q_bytes = static_cast<uint32_t>(8 * 128 * p.rows_per_tile);   // 8 boxes
-                if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::Q_FULL], 2 * q_bytes);
-                for (int c = 0; c < 8; ++c)
-                    tma2_load_4d_hint(smem + (c < 4 ? Smem::kring + Q_PARK_SLOT * SLOT + c * Q_CHUNK
-                                                    : Smem::stage + (c - 4) * Q_CHUNK),
-                                      &tmq, bar_of(Smem::Q_FULL, 0), c * 64, 0, kvh, q_start + t0, pol_q);
-                // half tile h: tile h / 2, head-dim columns 256 (h % 2) .. +256, this CTA's 64 keys
-                auto k_key = [&](int j) { return (kt_begin + j) * BN + static_cast<int>(pr) * K_BOX_ROWS; };
+            // ---------------------------------------------------- Q and K into the ring
+            // Per item: four entries of Q (two 64-column boxes each; the MMA
+            // thread copies them into TMEM), then the item's K half tiles
+            // (tile h / 2, head-dim columns 256 (h % 2) .. +256, this CTA's
+            // 64 keys).  Q is read once; K and V by every pair of the KV head.
+            const uint64_t pol_q = l2_policy_stream(), pol_kv = l2_policy_keep();
+            const uint32_t q_box_bytes = static_cast<uint32_t>(128 * p.rows_per_tile);
+            int e = 0;   // ring entries so far
+            bool ok = true, first_k = true;
+            auto take_slot = [&](int& s) -> bool {
+                s = e % K_SLOTS;
+                return e < K_SLOTS || wait_warp(Smem::K_EMPTY + s, ((e / K_SLOTS) - 1) & 1);
+            };
+            for (int item = cluster; ok; item += n_clusters) {
+                const Geo gm = item_geometry<PAGED>(p, item, pr, lane);
+                if (!gm.valid) break;
+                if (gm.n_kt == 0) continue;
+                for (int qe = 0; qe < 4 && ok; ++qe) {
+                    int s;
+                    if (!(ok = take_slot(s))) break;
+                    if (lane == 0) {
+                        if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::K_FULL + s], 2 * 2 * q_box_bytes);
+                        for (int bx = 0; bx < 2; ++bx)
+                            tma2_load_4d_hint(smem + Smem::kring + s * SLOT + bx * Q_CHUNK, &tmq,
+                                              bar_of(Smem::K_FULL + s, 0), (2 * qe + bx) * 64, 0, gm.kvh,
+                                              gm.q_start + gm.t0, pol_q);
+                    }
+                    ++e;
+                }
+                if (!ok) break;
+                auto k_key = [&](int j) { return (gm.kt_begin + j) * BN + static_cast<int>(pr) * K_BOX_ROWS; };
                 int pf[PF];
 #pragma unroll
-                for (int i = 0; i < PF; ++i) pf[i] = i < n_kt ? page_entry(k_key(i)) : 0;
+                for (int i = 0; i < PF; ++i) pf[i] = i < gm.n_kt ? page_entry(gm, k_key(i)) : 0;
                 int krow = 0;
-                for (int h = 0; h < 2 * n_kt; ++h) {
-                    const int j = h >> 1, c = h & 1, s = h % K_SLOTS;
-                    if (h >= K_SLOTS && !wait_or_abort(&bars[Smem::K_EMPTY + s], ((h / K_SLOTS) - 1) & 1, p.err,
-                                                       abort, wait_ns))
-                        break;
-                    // the slots that held Q: once Q has been copied into TMEM
-                    if (h == Q_PARK_SLOT && !wait_or_abort(&bars[Smem::Q_COPIED], 0, p.err, abort, wait_ns)) break;
-                    if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::K_FULL + s], 2 * SLOT);
+                for (int h = 0; h < 2 * gm.n_kt; ++h) {
+                    const int j = h >> 1, c = h & 1;
+                    int s;
+                    if (!(ok = take_slot(s))) break;
                     if (c == 0) {
                         // both head-dim halves of tile j read the same keys
-                        krow = half_row(k_key(j), pf[0]);
+                        krow = half_row(gm, k_key(j), pf[0]);
 #pragma unroll
                         for (int i = 0; i < PF - 1; ++i) pf[i] = pf[i + 1];
-                        pf[PF - 1] = j + PF < n_kt ? page_entry(k_key(j + PF)) : 0;
+                        pf[PF - 1] = j + PF < gm.n_kt ? page_entry(gm, k_key(j + PF)) : 0;
                     }
                     // (test hook: the first cluster's rank 0 leaves out its first
                     // K half tile, so that cluster's waits run into their bound)
-                    if (h == 0 && p.test_skip_first_k_load && blockIdx.x == 0) continue;
-                    for (int b = 0; b < 4; ++b)
-                        tma2_load_3d_hint(smem + Smem::kring + s * SLOT + b * K_BOX, &tmk,
-                                          bar_of(Smem::K_FULL + s, 0), (c * 4 + b) * 64, kvh, krow, pol_kv);
+                    const bool skip = first_k && p.test_skip_first_k_load && blockIdx.x == 0;
+                    first_k = false;
+                    if (lane == 0) {
+                        if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::K_FULL + s], 2 * SLOT);
+                        if (!skip)
+                            for (int b = 0; b < 4; ++b)
+                                tma2_load_3d_hint(smem + Smem::kring + s * SLOT + b * K_BOX, &tmk,
+                                                  bar_of(Smem::K_FULL + s, 0), (c * 4 + b) * 64, gm.kvh, krow,
+                                                  pol_kv);
+                    }
+                    ++e;
                 }
             }
         } else if (warp == 1 && rank == 1) {
-            if (lane == 0) {
-                // -------------------------------------------------- forward "S read" to the leader
-                // (the softmax warps arrive locally: a remote arrival, even a
-                // relaxed one, measured slower on their critical path)
-                for (int j = 0; j < n_kt; ++j) {
-                    if (!wait_or_abort(&bars[Smem::S_READ + (j % S_BUFS)], (j / S_BUFS) & 1, p.err, abort, wait_ns))
-                        break;
-                    mbar_arrive_remote_relaxed(bar_of(Smem::S_FREE + (j % S_BUFS), 0));
+            // ---------------------------------------------------- forward "S read" to the leader
+            // (the softmax warps arrive locally: a remote arrival, even a
+            // relaxed one, measured slower on their critical path)
+            int t = 0;
+            bool ok = true;
+            for (int item = cluster; ok; item += n_clusters) {
+                const Geo gm = item_geometry<PAGED>(p, item, pr, lane);
+                if (!gm.valid) break;
+                for (int j = 0; j < gm.n_kt; ++j, ++t) {
+                    if (!(ok = wait_warp(Smem::S_READ + (t % S_BUFS), (t / S_BUFS) & 1))) break;
+                    if (lane == 0) mbar_arrive_remote_relaxed(bar_of(Smem::S_FREE + (t % S_BUFS), 0));
                 }
             }
         } else if (warp == 1) {
-            if (rank == 0) {
-                // -------------------------------------------------- S = Q K^T (both SMs)
-                // The whole warp runs the loop and its waits (warp-uniform, so
-                // the MMA operands stay uniform); one elected lane issues.
-                // Q of both CTAs into TMEM (the A operand of every QK^T): 32
-                // copies of a 16-column slice, in the tensor-core pipeline
-                // ahead of the first MMA; their commit frees the parking slots
-                bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::Q_FULL], 0, p.err, abort, wait_ns));
-                if (ok) {
+            // ---------------------------------------------------- S = Q K^T (both SMs)
+            // The whole warp runs the loop and its waits (warp-uniform, so the
+            // MMA operands stay uniform); one elected lane issues.
+            const uint64_t k_desc = make_sdesc_sw128(smem_u32(smem + Smem::kring), 16, 1024);
+            int e = 0, t = 0;
+            bool ok = true;
+            for (int item = cluster; ok; item += n_clusters) {
+                const Geo gm = item_geometry<PAGED>(p, item, pr, lane);
+                if (!gm.valid) break;
+                if (gm.n_kt == 0) continue;
+                // The item's Q overwrites the TMEM the previous item's QK^T
+                // read: wait for the commit of that item's last tile first.
+                if (t > 0 && !(ok = wait_warp(Smem::S_FULL + ((t - 1) % S_BUFS), ((t - 1) / S_BUFS) & 1))) break;
+                for (int qe = 0; qe < 4; ++qe, ++e) {
+                    const int s = e % K_SLOTS;
+                    if (!(ok = wait_warp(Smem::K_FULL + s, (e / K_SLOTS) & 1))) break;
                     tc_fence_after_sync();
                     if (elect_one()) {
+                        // boxes 2 qe, 2 qe + 1 of both CTAs' Q into TMEM: four
+                        // 16-column slices each, ahead of the MMAs that read them
 #pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) {
-                            const uint64_t qd = make_sdesc_sw128(
-                                smem_u32(smem + (c8 < 4 ? Smem::kring + Q_PARK_SLOT * SLOT + c8 * Q_CHUNK
-                                                        : Smem::stage + (c8 - 4) * Q_CHUNK)),
-                                16, 1024);
+                        for (int bx = 0; bx < 2; ++bx) {
+                            const uint64_t qd = make_sdesc_sw128(smem_u32(smem + Smem::kring + s * SLOT + bx * Q_CHUNK),
+                                                                 16, 1024);
 #pragma unroll
                             for (int piece = 0; piece < 4; ++piece)
-                                tmem_cp2_128x256b(tmem + TM_Q + static_cast<uint32_t>(c8 * 32 + piece * 8),
+                                tmem_cp2_128x256b(tmem + TM_Q + static_cast<uint32_t>((2 * qe + bx) * 32 + piece * 8),
                                                   qd + static_cast<uint64_t>(piece * 2));
                         }
-                        commit2_mask(&bars[Smem::Q_COPIED], MASK_SCORE);
+                        commit2_mask(&bars[Smem::K_EMPTY + s], MASK_SCORE);
                     }
                     __syncwarp();
                 }
-                const uint64_t k_desc = make_sdesc_sw128(smem_u32(smem + Smem::kring), 16, 1024);
-                for (int j = 0; ok && j < n_kt; ++j) {
-                    const uint32_t sb = tmem + static_cast<uint32_t>(j % S_BUFS) * BN;
+                for (int j = 0; ok && j < gm.n_kt; ++j, ++t) {
+                    const uint32_t sb = tmem + static_cast<uint32_t>(t % S_BUFS) * BN;
                     // the tile's S buffer must have been read before its QK^T may start
-                    if (j >= S_BUFS && !(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::S_FREE + (j % S_BUFS)],
-                                                                                    ((j / S_BUFS) - 1) & 1, p.err,
-                                                                                    abort, wait_ns))))
-                        break;
-                    for (int c = 0; c < 2; ++c) {
-                        const int h = 2 * j + c, s = h % K_SLOTS;
-                        if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::K_FULL + s], (h / K_SLOTS) & 1,
-                                                                         p.err, abort, wait_ns))))
-                            break;
+                    if (t >= S_BUFS && !(ok = wait_warp(Smem::S_FREE + (t % S_BUFS), ((t / S_BUFS) - 1) & 1))) break;
+                    for (int c = 0; c < 2; ++c, ++e) {
+                        const int s = e % K_SLOTS;
+                        if (!(ok = wait_warp(Smem::K_FULL + s, (e / K_SLOTS) & 1))) break;
                         tc_fence_after_sync();
                         const uint64_t bd0 = k_desc + static_cast<uint64_t>(s * (SLOT >> 4));
                         if (elect_one()) {
@@ -568,231 +604,241 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                                         (c | k16) ? 1u : 0u);
                             }
                             commit2_mask(&bars[Smem::K_EMPTY + s], MASK_SCORE);
-                            if (c == 1) commit2_mask(&bars[Smem::S_FULL + (j % S_BUFS)], MASK_SCORE);
+                            if (c == 1) commit2_mask(&bars[Smem::S_FULL + (t % S_BUFS)], MASK_SCORE);
                         }
                         __syncwarp();
                     }
                 }
-                // let every issued MMA finish before TMEM can be released
-                if (elect_one()) commit2_mask(&bars[Smem::DRAIN], static_cast<uint16_t>(1u << rank));
-                __syncwarp();
-                (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err, wait_ns);
             }
+            // let every issued MMA finish before TMEM can be released
+            if (elect_one()) commit2_mask(&bars[Smem::DRAIN], static_cast<uint16_t>(1u << rank));
+            __syncwarp();
+            (void)mbar_wait(&bars[Smem::DRAIN], 0, p.err, wait_ns);
         } else if (warp == COPY_WARP) {
-            if (lane == 0) {
-                // -------------------------------------------------- P tiles to the output CTA
-                const uint32_t out_rank = rank + 2;
-                for (int j = 0; j < n_kt; ++j) {
-                    const int b2 = j & 1, pb = j % P_BUFS;
-                    // all softmax warps staged tile j, and the output CTA's P
-                    // buffer pb is free (O += P V of tile j - 3 completed)
-                    if (!wait_or_abort(&bars[Smem::P_STAGED + b2], (j >> 1) & 1, p.err, abort, wait_ns)) break;
-                    if (j >= P_BUFS &&
-                        !wait_or_abort(&bars[Smem::PV_DONE + pb], ((j / P_BUFS) - 1) & 1, p.err, abort, wait_ns))
-                        break;
-                    bulk_copy_to_cluster(map_to_cta(smem_u32(smem + Smem::precv + pb * P_BUF), out_rank),
-                                         smem_u32(smem + Smem::stage + b2 * P_BUF), P_BUF,
-                                         bar_of(Smem::P_LANDED + pb, out_rank));
+            // ---------------------------------------------------- P tiles to the output CTA
+            const uint32_t out_rank = rank + 2;
+            int t = 0;
+            bool ok = true;
+            for (int item = cluster; ok; item += n_clusters) {
+                const Geo gm = item_geometry<PAGED>(p, item, pr, lane);
+                if (!gm.valid) break;
+                for (int j = 0; j < gm.n_kt; ++j, ++t) {
+                    const int b2 = t & 1, pb = t % P_BUFS;
+                    // all softmax warps staged tile t, and the output CTA's P
+                    // buffer pb is free (O += P V of tile t - 3 completed)
+                    if (!(ok = wait_warp(Smem::P_STAGED + b2, (t >> 1) & 1))) break;
+                    if (t >= P_BUFS && !(ok = wait_warp(Smem::PV_DONE + pb, ((t / P_BUFS) - 1) & 1))) break;
+                    if (lane == 0)
+                        bulk_copy_to_cluster(map_to_cta(smem_u32(smem + Smem::precv + pb * P_BUF), out_rank),
+                                             smem_u32(smem + Smem::stage + b2 * P_BUF), P_BUF,
+                                             bar_of(Smem::P_LANDED + pb, out_rank));
                 }
             }
         } else {
-            // ------------------------------------------------------ softmax
+            // ---------------------------------------------------- softmax
             float* xmax = reinterpret_cast<float*>(smem + Smem::xmax);
-            float m_ref = -INFINITY;   // log2 units, the same in all four parts
-            float l = 0.f;             // this part's sum of the fp32 probabilities (for LSE)
-            float l_b = 0.f;           // this part's sum of the bf16-rounded probabilities
-            bool ok = true;
             const bool neg_scale = p.scale_log2 < 0.f;
             const uint32_t out_rank = rank + 2;
             const uint32_t a_dst = map_to_cta(smem_u32(smem + Smem::alpha + row * 4), out_rank);
-
-            for (int j = 0; ok && j < n_kt; ++j) {
-                const int b3 = j % S_BUFS, b2 = j & 1, pb = j % P_BUFS;
-                // (every wait of a softmax warp is made warp-uniform: the warp
-                // synchronises below and must leave the loop as one)
-                if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::S_FULL + b3], (j / S_BUFS) & 1, p.err,
-                                                                 abort, wait_ns))))
-                    break;
-                tc_fence_after_sync();
-                uint32_t sr[KP];
-#pragma unroll
-                for (int c = 0; c < KP / 32; ++c)
-                    tmem_ld32(tmem + lane_base + static_cast<uint32_t>(b3 * BN + part * KP + 32 * c),
-                              *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
-                tmem_ld_wait();
-                // the S buffer may take the QK^T three tiles on
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[rank == 0 ? Smem::S_FREE + b3 : Smem::S_READ + b3]);
-                float s[KP];
-#pragma unroll
-                for (int c = 0; c < KP; ++c) s[c] = __uint_as_float(sr[c]);
-
-                const int key0 = (kt_begin + j) * BN + part * KP;
-                const bool part_full = ntok > 0 && key0 + KP <= seqlen_k &&
-                                       (!p.causal || key0 + KP - 1 <= p_first) &&
-                                       (p.window <= 0 || key0 > p_last - p.window);
-                // scores stay unscaled until the exponent; a hidden key gets the
-                // value that scales to -inf whatever the sign of the scale
-                if (!part_full) {
-                    const float hidden = neg_scale ? INFINITY : -INFINITY;
-#pragma unroll
-                    for (int c = 0; c < KP; ++c)
-                        if (!key_visible(key0 + c, qpos, seqlen_k, p)) s[c] = hidden;
+            int t = 0, ic = 0;   // tiles, items with keys
+            bool ok = true;
+            for (int item = cluster; ok; item += n_clusters) {
+                const Geo gm = item_geometry<PAGED>(p, item, pr, lane);
+                if (!gm.valid) break;
+                const int tok = row / G;
+                const int g = row - tok * G;
+                const bool valid_row = row < p.rows_per_tile && tok < gm.ntok;
+                const int qpos = gm.q_offset + gm.t0 + tok;
+                const int hq = gm.kvh * G + g;
+                if (gm.n_kt == 0) {
+                    // no key is visible to any row of the pair: LSE = -inf
+                    if (valid_row && part == 0 && p.lse)
+                        p.lse[static_cast<size_t>(hq) * p.total_q + gm.q_start + gm.t0 + tok] = -INFINITY;
+                    continue;
                 }
-                float mx[KP / 4];
-                if (!neg_scale) {
+                float m_ref = -INFINITY;   // log2 units, the same in all parts
+                float l = 0.f;             // this part's sum of the fp32 probabilities (for LSE)
+                float l_b = 0.f;           // this part's sum of the bf16-rounded probabilities
+                for (int j = 0; j < gm.n_kt; ++j, ++t) {
+                    const int b3 = t % S_BUFS, b2 = t & 1, pb = t % P_BUFS;
+                    // (every wait of a softmax warp is warp-uniform: the warp
+                    // synchronises below and must leave the loop as one)
+                    if (!(ok = wait_warp(Smem::S_FULL + b3, (t / S_BUFS) & 1))) break;
+                    tc_fence_after_sync();
+                    uint32_t sr[KP];
 #pragma unroll
-                    for (int c = 0; c < KP / 4; ++c)
-                        mx[c] = fmaxf(fmaxf(s[4 * c], s[4 * c + 1]), fmaxf(s[4 * c + 2], s[4 * c + 3]));
+                    for (int c = 0; c < KP / 32; ++c)
+                        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(b3 * BN + part * KP + 32 * c),
+                                  *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+                    tmem_ld_wait();
+                    // the S buffer may take the QK^T two tiles on
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[rank == 0 ? Smem::S_FREE + b3 : Smem::S_READ + b3]);
+                    float s[KP];
 #pragma unroll
-                    for (int w = KP / 8; w >= 1; w >>= 1)
+                    for (int c = 0; c < KP; ++c) s[c] = __uint_as_float(sr[c]);
+
+                    const int key0 = (gm.kt_begin + j) * BN + part * KP;
+                    const bool part_full = gm.ntok > 0 && key0 + KP <= gm.seqlen_k &&
+                                           (!p.causal || key0 + KP - 1 <= gm.p_first) &&
+                                           (p.window <= 0 || key0 > gm.p_last - p.window);
+                    // scores stay unscaled until the exponent; a hidden key gets the
+                    // value that scales to -inf whatever the sign of the scale
+                    if (!part_full) {
+                        const float hidden = neg_scale ? INFINITY : -INFINITY;
 #pragma unroll
-                        for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+                        for (int c = 0; c < KP; ++c)
+                            if (!key_visible(key0 + c, qpos, gm.seqlen_k, p)) s[c] = hidden;
+                    }
+                    float mx[KP / 4];
+                    if (!neg_scale) {
+#pragma unroll
+                        for (int c = 0; c < KP / 4; ++c)
+                            mx[c] = fmaxf(fmaxf(s[4 * c], s[4 * c + 1]), fmaxf(s[4 * c + 2], s[4 * c + 3]));
+#pragma unroll
+                        for (int w = KP / 8; w >= 1; w >>= 1)
+#pragma unroll
+                            for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < KP / 4; ++c)
+                            mx[c] = fminf(fminf(s[4 * c], s[4 * c + 1]), fminf(s[4 * c + 2], s[4 * c + 3]));
+#pragma unroll
+                        for (int w = KP / 8; w >= 1; w >>= 1)
+#pragma unroll
+                            for (int c = 0; c < w; ++c) mx[c] = fminf(mx[c], mx[c + w]);
+                    }
+                    // row max over the whole tile: the parts swap their maxima (log2
+                    // units); all then take the same decision on the same numbers
+                    const float own_max = mx[0] * p.scale_log2;
+                    xmax[(b2 * PARTS + part) * BM + row] = own_max;
+                    // one arrival per warp, after the warp's stores; only the PARTS
+                    // warps of this lane quadrant hold parts of these rows
+                    __syncwarp();
+                    const int xb = Smem::XCHG + b2 * 4 + (warp & 3);
+                    if (lane == 0) mbar_arrive(&bars[xb]);
+                    if (!(ok = wait_warp(xb, (t >> 1) & 1))) break;
+                    float tmax = own_max;
+#pragma unroll
+                    for (int q4 = 1; q4 < PARTS; ++q4)
+                        tmax = fmaxf(tmax, xmax[(b2 * PARTS + ((part + q4) % PARTS)) * BM + row]);
+
+                    float m_use = m_ref, alpha = 1.f;
+                    if (tmax > m_ref + RESCALE_THRESHOLD) {
+                        m_use = tmax;
+                        alpha = fast_exp2(m_ref - m_use);   // 0 when m_ref = -inf
+                    }
+                    const float shift = m_use == -INFINITY ? 0.f : m_use;
+                    uint32_t pk[KP / 2];
+                    float2 ps[4], pbs[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) ps[c] = pbs[c] = make_float2(0.f, 0.f);
+                    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+                    const float2 nsh = make_float2(-shift, -shift);
+#pragma unroll
+                    for (int c = 0; c < KP / 2; ++c) {
+                        // p = 2^(s * scale * log2(e) - shift), two lanes per instruction
+                        const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2, nsh);
+                        const float2 pr2 = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        ps[c & 3] = fadd2(ps[c & 3], pr2);
+                        pk[c] = pack_bf16x2(pr2.x, pr2.y);
+                        // the bf16 values the PV product actually uses
+                        pbs[c & 3] = fadd2(pbs[c & 3], make_float2(__uint_as_float(pk[c] << 16),
+                                                                   __uint_as_float(pk[c] & 0xffff0000u)));
+                    }
+                    const float2 ps01 = fadd2(fadd2(ps[0], ps[1]), fadd2(ps[2], ps[3]));
+                    const float2 pb01 = fadd2(fadd2(pbs[0], pbs[1]), fadd2(pbs[2], pbs[3]));
+                    l = l * alpha + (ps01.x + ps01.y);
+                    l_b = l_b * alpha + (pb01.x + pb01.y);
+                    m_ref = m_use;
+
+                    // staging buffer b2: its copy of tile t - 2 has landed and the
+                    // output CTA has read that tile's alpha (which also means its
+                    // barrier phase for tile t - 3 has completed)
+                    if (t >= STAGES && !(ok = wait_warp(Smem::STAGE_FREE + b2, ((t >> 1) - 1) & 1))) break;
+                    // P of this row's KP keys: KP / 8 16-byte pieces of the row's
+                    // 128-byte line in its 64-key chunk, in the 128-byte swizzle the
+                    // MMA descriptor expects (piece c at c ^ (row % 8))
+                    uint8_t* stg = smem + Smem::stage + b2 * P_BUF + ((part * KP) >> 6) * P_CHUNK + row * 128;
+#pragma unroll
+                    for (int c4 = 0; c4 < KP / 8; ++c4) {
+                        const int pc = ((part * KP) & 63) / 8 + c4;
+                        *reinterpret_cast<uint4*>(stg + ((pc ^ (row & 7)) << 4)) =
+                            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+                    }
+                    const uint32_t xbar = bar_of(Smem::P_LANDED + pb, out_rank);
+                    if (part == 0) st_async_b32(a_dst + static_cast<uint32_t>(pb * BM * 4), __float_as_uint(alpha), xbar);
+                    // the copy engine reads the staged tile: order these writes
+                    // before it; the copy warp moves the whole tile once all
+                    // softmax warps have staged
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[Smem::P_STAGED + b2]);
+                }
+                if (!ok) break;
+                // The parts' row sums meet in the staging buffer the next tile
+                // will use, once its last copy has landed: part 1 leaves them
+                // in the first 8 bytes of its rows' lines of the first chunk,
+                // which only this quadrant's part 0 writes next (after it has
+                // read them), and part 0 adds them to its own.
+                const int bn = t & 1;
+                if (t >= STAGES && !(ok = wait_warp(Smem::STAGE_FREE + bn, ((t >> 1) - 1) & 1))) break;
+                float2* lx = reinterpret_cast<float2*>(smem + Smem::stage + bn * P_BUF + row * 128);
+                if (part == 1) {
+                    *lx = make_float2(l, l_b);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[Smem::L_XCHG]);
                 } else {
-#pragma unroll
-                    for (int c = 0; c < KP / 4; ++c)
-                        mx[c] = fminf(fminf(s[4 * c], s[4 * c + 1]), fminf(s[4 * c + 2], s[4 * c + 3]));
-#pragma unroll
-                    for (int w = KP / 8; w >= 1; w >>= 1)
-#pragma unroll
-                        for (int c = 0; c < w; ++c) mx[c] = fminf(mx[c], mx[c + w]);
+                    if (!(ok = wait_warp(Smem::L_XCHG, ic & 1))) break;
+                    const float2 other = *lx;
+                    const float l_all = l + other.x, lb_all = l_b + other.y;
+                    // the output CTA's row-sum slot is free once it has read
+                    // the previous item's sums
+                    if (ic >= 1 && !(ok = wait_warp(Smem::L_FREE, (ic - 1) & 1))) break;
+                    // O / sum(p~) with p~ the rounded weights PV used: O stays an
+                    // exact convex combination of V rows whatever the rounding of P
+                    st_async_b32(map_to_cta(smem_u32(smem + Smem::lrecv + row * 4), out_rank), __float_as_uint(lb_all),
+                                 bar_of(Smem::L_READY, out_rank));
+                    if (valid_row && p.lse)
+                        p.lse[static_cast<size_t>(hq) * p.total_q + gm.q_start + gm.t0 + tok] =
+                            l_all > 0.f ? (m_ref + log2f(l_all)) * 0.69314718055994530942f : -INFINITY;
                 }
-                // row max over the whole tile: the parts swap their maxima (log2
-                // units); all then take the same decision on the same numbers
-                const float own_max = mx[0] * p.scale_log2;
-                xmax[(b2 * PARTS + part) * BM + row] = own_max;
-                // one arrival per warp, after the warp's stores; only the PARTS
-                // warps of this lane quadrant hold parts of these rows
-                __syncwarp();
-                const int xb = Smem::XCHG + b2 * 4 + (warp & 3);
-                if (lane == 0) mbar_arrive(&bars[xb]);
-                if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[xb], (j >> 1) & 1, p.err, abort,
-                                                                 wait_ns))))
-                    break;
-                float tmax = own_max;
-#pragma unroll
-                for (int q4 = 1; q4 < PARTS; ++q4)
-                    tmax = fmaxf(tmax, xmax[(b2 * PARTS + ((part + q4) % PARTS)) * BM + row]);
-
-                float m_use = m_ref, alpha = 1.f;
-                if (tmax > m_ref + RESCALE_THRESHOLD) {
-                    m_use = tmax;
-                    alpha = fast_exp2(m_ref - m_use);   // 0 when m_ref = -inf
-                }
-                const float shift = m_use == -INFINITY ? 0.f : m_use;
-                uint32_t pk[KP / 2];
-                float2 ps[4], pbs[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) ps[c] = pbs[c] = make_float2(0.f, 0.f);
-                const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
-                const float2 nsh = make_float2(-shift, -shift);
-#pragma unroll
-                for (int c = 0; c < KP / 2; ++c) {
-                    // p = 2^(s * scale * log2(e) - shift), two lanes per instruction
-                    const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2, nsh);
-                    const float2 pr2 = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                    ps[c & 3] = fadd2(ps[c & 3], pr2);
-                    pk[c] = pack_bf16x2(pr2.x, pr2.y);
-                    // the bf16 values the PV product actually uses
-                    pbs[c & 3] = fadd2(pbs[c & 3], make_float2(__uint_as_float(pk[c] << 16),
-                                                               __uint_as_float(pk[c] & 0xffff0000u)));
-                }
-                const float2 ps01 = fadd2(fadd2(ps[0], ps[1]), fadd2(ps[2], ps[3]));
-                const float2 pb01 = fadd2(fadd2(pbs[0], pbs[1]), fadd2(pbs[2], pbs[3]));
-                l = l * alpha + (ps01.x + ps01.y);
-                l_b = l_b * alpha + (pb01.x + pb01.y);
-                m_ref = m_use;
-
-                // staging buffer b2: its copy of tile j - 2 has landed and the
-                // output CTA has read that tile's alpha (which also means its
-                // barrier phase for tile j - 3 has completed)
-                if (j >= STAGES && !(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::STAGE_FREE + b2],
-                                                                               ((j >> 1) - 1) & 1, p.err, abort,
-                                                                               wait_ns))))
-                    break;
-                // P of this row's KP keys: KP / 8 16-byte pieces of the row's
-                // 128-byte line in its 64-key chunk, in the 128-byte swizzle the
-                // MMA descriptor expects (piece c at c ^ (row % 8))
-                uint8_t* stg = smem + Smem::stage + b2 * P_BUF + ((part * KP) >> 6) * P_CHUNK + row * 128;
-#pragma unroll
-                for (int c4 = 0; c4 < KP / 8; ++c4) {
-                    const int pc = ((part * KP) & 63) / 8 + c4;
-                    *reinterpret_cast<uint4*>(stg + ((pc ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-                }
-                const uint32_t xbar = bar_of(Smem::P_LANDED + pb, out_rank);
-                if (part == 0) st_async_b32(a_dst + static_cast<uint32_t>(pb * BM * 4), __float_as_uint(alpha), xbar);
-                // the copy engine reads the staged tile: order these writes
-                // before it; the copy warp moves the whole tile once all
-                // softmax warps have staged
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[Smem::P_STAGED + b2]);
-            }
-            // Sum the parts' row sums through the K ring, idle once every QK^T
-            // has completed (the last S_FULL was seen).  Each warp arrives
-            // exactly once (its loop exits warp-uniformly), so the wait ends.
-            float* lsum = reinterpret_cast<float*>(smem + Smem::kring);
-            lsum[(part * BM + row) * 2 + 0] = l;
-            lsum[(part * BM + row) * 2 + 1] = l_b;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[Smem::L_XCHG]);
-            if (ok) ok = wait_or_abort(&bars[Smem::L_XCHG], 0, p.err, abort, wait_ns);
-            if (ok && part == 0) {
-                float l_all = 0.f, lb_all = 0.f;
-#pragma unroll
-                for (int q4 = 0; q4 < PARTS; ++q4) {
-                    l_all += lsum[(q4 * BM + row) * 2 + 0];
-                    lb_all += lsum[(q4 * BM + row) * 2 + 1];
-                }
-                // O / sum(p~) with p~ the rounded weights PV used: O stays an
-                // exact convex combination of V rows whatever the rounding of P
-                st_async_b32(map_to_cta(smem_u32(smem + Smem::lrecv + row * 4), out_rank), __float_as_uint(lb_all),
-                             bar_of(Smem::L_READY, out_rank));
-                if (valid_row && p.lse)
-                    p.lse[static_cast<size_t>(hq) * p.total_q + q_start + t0 + tok] =
-                        l_all > 0.f ? (m_ref + log2f(l_all)) * 0.69314718055994530942f : -INFINITY;
+                ++ic;
             }
         }
     } else {
         if (warp == 0) {
-            if (lane == 0) {
-                // -------------------------------------------------- V loads
-                const uint64_t pol_kv = l2_policy_keep();   // read by every pair of the KV head
+            // ---------------------------------------------------- V loads
+            const uint64_t pol_kv = l2_policy_keep();   // read by every pair of the KV head
+            int t = 0;
+            bool ok = true;
+            for (int item = cluster; ok; item += n_clusters) {
+                const Geo gm = item_geometry<PAGED>(p, item, pr, lane);
+                if (!gm.valid) break;
+                if (gm.n_kt == 0) continue;
                 int pf[PF][2];
 #pragma unroll
                 for (int i = 0; i < PF; ++i)
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
-                        pf[i][r] = i < n_kt ? page_entry((kt_begin + i) * BN + r * K_BOX_ROWS) : 0;
-                for (int j = 0; j < n_kt; ++j) {
-                    const int vb = j & 1;
-                    // V buffer vb once O += P V of tile j - 2 completed
-                    if (j >= 2 && !wait_or_abort(&bars[Smem::PV_DONE + (j - 2) % P_BUFS], ((j - 2) / P_BUFS) & 1,
-                                                 p.err, abort, wait_ns))
-                        break;
+                        pf[i][r] = i < gm.n_kt ? page_entry(gm, (gm.kt_begin + i) * BN + r * K_BOX_ROWS) : 0;
+                for (int j = 0; j < gm.n_kt; ++j, ++t) {
+                    const int vb = t & 1;
+                    // V buffer vb once O += P V of tile t - 2 completed
+                    if (t >= 2 && !(ok = wait_warp(Smem::PV_DONE + (t - 2) % P_BUFS, ((t - 2) / P_BUFS) & 1))) break;
                     // (the tile's ready barrier goes with its P buffer: the
                     // correction warps may run three tiles ahead of the MMAs)
-                    const int rb = j % P_BUFS;
-                    const int key = (kt_begin + j) * BN;
+                    const int rb = t % P_BUFS;
+                    const int key = (gm.kt_begin + j) * BN;
                     if constexpr (PAGED) {
                         // Each V box is one half tile (one page or part of one).
                         // The tail tile's V lands on this CTA's own barrier: the
                         // correction warps clear the rows past the cache's end
                         // before they mark the tile ready (a NaN there would
                         // survive a zero weight).
-                        const bool tail = kt_begin + j == tail_tile;
-                        uint32_t vbar;
-                        if (tail) {
-                            if (rank == 2) mbar_arrive(&bars[Smem::PV_READY + rb]);
-                            mbar_arrive_expect_tx(&bars[Smem::V_TAIL], 2 * SLOT);
-                            vbar = bar_of(Smem::V_TAIL, rank);
-                        } else {
-                            if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
-                            vbar = bar_of(Smem::PV_READY + rb, 2);
-                        }
-                        const int rows[2] = {half_row(key, pf[0][0]), half_row(key + K_BOX_ROWS, pf[0][1])};
+                        const bool tail = gm.kt_begin + j == gm.tail_tile;
+                        const int rows[2] = {half_row(gm, key, pf[0][0]), half_row(gm, key + K_BOX_ROWS, pf[0][1])};
 #pragma unroll
                         for (int i = 0; i < PF - 1; ++i) {
                             pf[i][0] = pf[i + 1][0];
@@ -800,21 +846,37 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                         }
 #pragma unroll
                         for (int r = 0; r < 2; ++r)
-                            pf[PF - 1][r] = j + PF < n_kt ? page_entry((kt_begin + j + PF) * BN + r * K_BOX_ROWS) : 0;
-                        for (int hh = 0; hh < 2; ++hh)
-                            for (int bx = 0; bx < 2; ++bx)
-                                for (int r = 0; r < 2; ++r)
-                                    tma2_load_3d_hint(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX +
-                                                          r * K_BOX,
-                                                      &tmv, vbar, (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh,
-                                                      rows[r], pol_kv);
+                            pf[PF - 1][r] = j + PF < gm.n_kt
+                                                ? page_entry(gm, (gm.kt_begin + j + PF) * BN + r * K_BOX_ROWS)
+                                                : 0;
+                        if (lane == 0) {
+                            uint32_t vbar;
+                            if (tail) {
+                                if (rank == 2) mbar_arrive(&bars[Smem::PV_READY + rb]);
+                                mbar_arrive_expect_tx(&bars[Smem::V_TAIL], 2 * SLOT);
+                                vbar = bar_of(Smem::V_TAIL, rank);
+                            } else {
+                                if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
+                                vbar = bar_of(Smem::PV_READY + rb, 2);
+                            }
+                            for (int hh = 0; hh < 2; ++hh)
+                                for (int bx = 0; bx < 2; ++bx)
+                                    for (int r = 0; r < 2; ++r)
+                                        tma2_load_3d_hint(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX +
+                                                              r * K_BOX,
+                                                          &tmv, vbar, (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64,
+                                                          gm.kvh, rows[r], pol_kv);
+                        }
                     } else {
-                        if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
-                        for (int hh = 0; hh < 2; ++hh)
-                            for (int bx = 0; bx < 2; ++bx)
-                                tma2_load_3d_hint(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX, &tmv,
-                                                  bar_of(Smem::PV_READY + rb, 2),
-                                                  (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, kvh, key, pol_kv);
+                        if (lane == 0) {
+                            if (rank == 2) mbar_arrive_expect_tx(&bars[Smem::PV_READY + rb], 2 * 2 * SLOT);
+                            for (int hh = 0; hh < 2; ++hh)
+                                for (int bx = 0; bx < 2; ++bx)
+                                    tma2_load_3d_hint(smem + Smem::vring + (2 * vb + hh) * SLOT + bx * V_BOX, &tmv,
+                                                      bar_of(Smem::PV_READY + rb, 2),
+                                                      (hh * 4 + static_cast<int>(pr) * 2 + bx) * 64, gm.kvh, key,
+                                                      pol_kv);
+                        }
                     }
                 }
             }
@@ -822,33 +884,38 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             if (rank == 2) {
                 // -------------------------------------------------- O += P V (both SMs)
                 // (the whole warp runs the loop, one elected lane issues)
-                bool ok = true;
                 const uint64_t p_desc = make_sdesc_sw128(smem_u32(smem + Smem::precv), 16, 1024);
                 const uint64_t v_desc = make_sdesc_sw128(smem_u32(smem + Smem::vring), V_BOX, 1024);
-                for (int j = 0; ok && j < n_kt; ++j) {
-                    const int vb = j & 1, pb = j % P_BUFS;
-                    if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::PV_READY + pb], (j / P_BUFS) & 1,
-                                                                     p.err, abort, wait_ns))))
-                        break;
-                    tc_fence_after_sync();
-                    const uint64_t ad0 = p_desc + static_cast<uint64_t>(pb * (P_BUF >> 4));
-                    const uint64_t bd0 = v_desc + static_cast<uint64_t>(2 * vb * (SLOT >> 4));
-                    if (elect_one()) {
+                int t = 0;
+                bool ok = true;
+                for (int item = cluster; ok; item += n_clusters) {
+                    const Geo gm = item_geometry<PAGED>(p, item, pr, lane);
+                    if (!gm.valid) break;
+                    for (int j = 0; j < gm.n_kt; ++j, ++t) {
+                        const int vb = t & 1, pb = t % P_BUFS;
+                        // P landed and O corrected in both CTAs (for an item's
+                        // first tile: the previous item's O read out), V landed
+                        if (!(ok = wait_warp(Smem::PV_READY + pb, (t / P_BUFS) & 1))) break;
+                        tc_fence_after_sync();
+                        const uint64_t ad0 = p_desc + static_cast<uint64_t>(pb * (P_BUF >> 4));
+                        const uint64_t bd0 = v_desc + static_cast<uint64_t>(2 * vb * (SLOT >> 4));
+                        if (elect_one()) {
 #pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            // P keys 16 kk .. 16 kk + 15: chunk kk / 4, 32 bytes per step within it;
-                            // V is MN-major: 8-key groups 1 KiB apart
-                            const uint64_t ad = ad0 + static_cast<uint64_t>((kk >> 2) * (P_CHUNK >> 4) + (kk & 3) * 2);
-                            const uint64_t bd = bd0 + static_cast<uint64_t>(kk * (16 * 128 >> 4));
-                            mma2_ss(tmem, ad, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                            mma2_ss(tmem + 256, ad, bd + static_cast<uint64_t>(SLOT >> 4), IDESC_PV,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < BN / 16; ++kk) {
+                                // P keys 16 kk .. 16 kk + 15: chunk kk / 4, 32 bytes per step within it;
+                                // V is MN-major: 8-key groups 1 KiB apart
+                                const uint64_t ad = ad0 + static_cast<uint64_t>((kk >> 2) * (P_CHUNK >> 4) + (kk & 3) * 2);
+                                const uint64_t bd = bd0 + static_cast<uint64_t>(kk * (16 * 128 >> 4));
+                                mma2_ss(tmem, ad, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                                mma2_ss(tmem + 256, ad, bd + static_cast<uint64_t>(SLOT >> 4), IDESC_PV,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            // frees the tile's V slots and P buffer; O may be corrected for the next tile
+                            commit2_mask(&bars[Smem::PV_DONE + pb], MASK_ALL);
+                            if (j == gm.n_kt - 1) commit2_mask(&bars[Smem::O_FINAL], MASK_OUTPUT);
                         }
-                        // frees the tile's V slots and P buffer; O may be corrected for the next tile
-                        commit2_mask(&bars[Smem::PV_DONE + pb], MASK_ALL);
-                        if (j == n_kt - 1) commit2_mask(&bars[Smem::O_FINAL], MASK_OUTPUT);
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
                 if (elect_one()) commit2_mask(&bars[Smem::DRAIN], static_cast<uint16_t>(1u << rank));
                 __syncwarp();
@@ -858,99 +925,133 @@ prefill_so_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             // -------------------------------------------------- O correction + epilogue
             const float* alpha_s = reinterpret_cast<const float*>(smem + Smem::alpha);
             const uint32_t o_col = static_cast<uint32_t>(part * OP);
+            // 32-byte stores need a 32-byte aligned O (rows are 1 KiB apart)
+            const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+            int t = 0, ic = 0, tails = 0;   // tiles, items with keys, paged tail tiles
             bool ok = true;
-            if (warp == 2 && lane == 0) mbar_arrive_expect_tx(&bars[Smem::L_READY], L_TX);
-            for (int j = 0; ok && j < n_kt; ++j) {
-                const int pb = j % P_BUFS;
-                // P_LANDED[pb]'s phase for tile j - 3 completed before this point
-                if (warp == 2 && lane == 0) mbar_arrive_expect_tx(&bars[Smem::P_LANDED + pb], P_TX);
-                if (!(ok = __all_sync(0xffffffffu, wait_cluster_or_abort(&bars[Smem::P_LANDED + pb],
-                                                                         (j / P_BUFS) & 1, p.err, abort, wait_ns))))
-                    break;
-                // P arrived through the copy engine and alpha through remote
-                // stores; the MMA reads P through the async proxy
-                fence_proxy_async_smem();
-                const float a = alpha_s[pb * BM + row];
-                const bool rescale = j > 0 && __any_sync(0xffffffffu, a != 1.f);
-                // this tile's copy landed and its alpha was read: the score CTA's
-                // staging buffer may take the tile after next (relaxed: nothing
-                // to publish)
-                if (lane == 0) mbar_arrive_remote_relaxed(bar_of(Smem::STAGE_FREE + (j & 1), rank - 2));
-                if (rescale) {
-                    // O += P V of the previous tile must be done before O is corrected
-                    if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::PV_DONE + (j - 1) % P_BUFS],
-                                                                     ((j - 1) / P_BUFS) & 1, p.err, abort, wait_ns))))
+            for (int item = cluster; ok; item += n_clusters) {
+                const Geo gm = item_geometry<PAGED>(p, item, pr, lane);
+                if (!gm.valid) break;
+                const int tok = row / G;
+                const int g = row - tok * G;
+                const bool valid_row = row < p.rows_per_tile && tok < gm.ntok;
+                const int hq = gm.kvh * G + g;
+                __nv_bfloat16* dst = p.out + (static_cast<size_t>(gm.q_start + gm.t0 + tok) * p.n_q_heads + hq) * D + o_col;
+                if (gm.n_kt == 0) {
+                    // no key is visible to any row of the pair: O = 0
+                    if (valid_row) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst);
+                        for (int i = 0; i < OP / 8; ++i) d4[i] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    continue;
+                }
+                if (warp == 2 && lane == 0) mbar_arrive_expect_tx(&bars[Smem::L_READY], L_TX);
+                for (int j = 0; j < gm.n_kt; ++j, ++t) {
+                    const int pb = t % P_BUFS;
+                    // P_LANDED[pb]'s phase for tile t - 3 completed before this point
+                    if (warp == 2 && lane == 0) mbar_arrive_expect_tx(&bars[Smem::P_LANDED + pb], P_TX);
+                    if (!(ok = __all_sync(0xffffffffu, wait_cluster_or_abort(&bars[Smem::P_LANDED + pb],
+                                                                             (t / P_BUFS) & 1, p.err, abort, wait_ns))))
                         break;
-                    tc_fence_after_sync();
-                    for (int c = 0; c < OP / 32; ++c) {
-                        uint32_t o[32];
-                        const uint32_t oc = o_col + static_cast<uint32_t>(c * 32);
-                        tmem_ld32(tmem + lane_base + oc, o);
-                        tmem_ld_wait();
+                    // P arrived through the copy engine and alpha through remote
+                    // stores; the MMA reads P through the async proxy
+                    fence_proxy_async_smem();
+                    const float a = alpha_s[pb * BM + row];
+                    const bool rescale = j > 0 && __any_sync(0xffffffffu, a != 1.f);
+                    // this tile's copy landed and its alpha was read: the score CTA's
+                    // staging buffer may take the tile after next (relaxed: nothing
+                    // to publish)
+                    if (lane == 0) mbar_arrive_remote_relaxed(bar_of(Smem::STAGE_FREE + (t & 1), rank - 2));
+                    if (rescale) {
+                        // O += P V of the previous tile must be done before O is corrected
+                        if (!(ok = wait_warp(Smem::PV_DONE + (t - 1) % P_BUFS, ((t - 1) / P_BUFS) & 1))) break;
+                        tc_fence_after_sync();
+                        for (int c = 0; c < OP / 32; ++c) {
+                            uint32_t o[32];
+                            const uint32_t oc = o_col + static_cast<uint32_t>(c * 32);
+                            tmem_ld32(tmem + lane_base + oc, o);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-                        tmem_st32(tmem + lane_base + oc, o);
-                    }
-                    tmem_st_wait();
-                }
-                if constexpr (PAGED) {
-                    if (kt_begin + j == tail_tile) {
-                        // the tile holding the cache's end: zero this CTA's V rows
-                        // from the end to the end of its half tile, in both O
-                        // halves' slots, then hand them to the tensor core (async proxy)
-                        if (!(ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::V_TAIL], 0, p.err, abort,
-                                                                         wait_ns))))
-                            break;
-                        const int r0 = seqlen_k - tail_tile * BN;       // 1 .. 127, not 64
-                        const int n16 = (((r0 + K_BOX_ROWS - 1) & ~(K_BOX_ROWS - 1)) - r0) * 8;   // per box
-                        uint8_t* vs = smem + Smem::vring + (2 * (j & 1)) * SLOT + r0 * 128;
-                        for (int i = tid - 64; i < 4 * n16; i += N_WORK_WARPS * 32) {
-                            const int bx = i / n16;                   // (O half, 64-column box)
-                            *reinterpret_cast<uint4*>(vs + (bx >> 1) * SLOT + (bx & 1) * V_BOX + (i - bx * n16) * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                            tmem_st32(tmem + lane_base + oc, o);
                         }
-                        fence_proxy_async_smem();
+                        tmem_st_wait();
+                    }
+                    bool tail = false;
+                    if constexpr (PAGED) {
+                        if (gm.kt_begin + j == gm.tail_tile) {
+                            // the tile holding the cache's end: zero this CTA's V rows
+                            // from the end to the end of its half tile, in both O
+                            // halves' slots, then hand them to the tensor core (async proxy)
+                            tail = true;
+                            if (!(ok = wait_warp(Smem::V_TAIL, tails & 1))) break;
+                            ++tails;
+                            const int r0 = gm.seqlen_k - gm.tail_tile * BN;   // 1 .. 127, not 64
+                            const int n16 = (((r0 + K_BOX_ROWS - 1) & ~(K_BOX_ROWS - 1)) - r0) * 8;   // per box
+                            uint8_t* vs = smem + Smem::vring + (2 * (t & 1)) * SLOT + r0 * 128;
+                            for (int i = tid - 64; i < 4 * n16; i += N_WORK_WARPS * 32) {
+                                const int bx = i / n16;                   // (O half, 64-column box)
+                                *reinterpret_cast<uint4*>(vs + (bx >> 1) * SLOT + (bx & 1) * V_BOX + (i - bx * n16) * 16) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            fence_proxy_async_smem();
+                        }
+                    }
+                    // O corrected (tcgen05.st completed) and P landed: relaxed, except
+                    // where a paged tail tile's cleared V rows must be published
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (rank == 2) mbar_arrive(&bars[Smem::PV_READY + pb]);
+                        else if (tail) mbar_arrive_remote(bar_of(Smem::PV_READY + pb, 2));
+                        else mbar_arrive_remote_relaxed(bar_of(Smem::PV_READY + pb, 2));
                     }
                 }
-                tc_fence_before_sync();
-                __syncwarp();
-                // O corrected (tcgen05.st completed) and P landed: relaxed, except
-                // where a paged tail tile's cleared V rows must be published
-                if (lane == 0) {
-                    if (rank == 2) mbar_arrive(&bars[Smem::PV_READY + pb]);
-                    else if (PAGED && kt_begin + j == tail_tile) mbar_arrive_remote(bar_of(Smem::PV_READY + pb, 2));
-                    else mbar_arrive_remote_relaxed(bar_of(Smem::PV_READY + pb, 2));
-                }
-            }
-            if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&bars[Smem::O_FINAL], 0, p.err, abort, wait_ns));
-            if (ok) ok = __all_sync(0xffffffffu, wait_cluster_or_abort(&bars[Smem::L_READY], 0, p.err, abort, wait_ns));
-            if (ok) {
+                if (!ok) break;
+                // ---- epilogue: O / sum(p~) as bf16 rows
+                if (!(ok = wait_warp(Smem::O_FINAL, ic & 1))) break;
+                if (!(ok = __all_sync(0xffffffffu, wait_cluster_or_abort(&bars[Smem::L_READY], ic & 1, p.err, abort,
+                                                                         wait_ns))))
+                    break;
                 tc_fence_after_sync();
                 const float lb = reinterpret_cast<const float*>(smem + Smem::lrecv)[row];
                 const float inv_l = lb > 0.f ? 1.f / lb : 0.f;
-                __nv_bfloat16* dst =
-                    p.out + (static_cast<size_t>(q_start + t0 + tok) * p.n_q_heads + hq) * D + o_col;
-                for (int c = 0; c < OP / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + o_col + static_cast<uint32_t>(c * 32), o);
+                // the row-sum slot may take the next item's sums (relaxed: the
+                // value is in a register)
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote_relaxed(bar_of(Smem::L_FREE, rank - 2));
+                // O is read out of TMEM before the next item's first tile is
+                // marked ready (its O += P V overwrites O), 64 columns at a
+                // time; each row's 128 bytes leave as four 32-byte stores, so
+                // every store writes whole sectors and the store queue holds
+                // up the next TMEM load less (the stores drain while the next
+                // item's first O += P V runs)
+                for (int c = 0; c < OP / 64; ++c) {
+                    uint32_t o[64];
+                    tmem_ld32(tmem + lane_base + o_col + static_cast<uint32_t>(c * 64),
+                              *reinterpret_cast<uint32_t(*)[32]>(o));
+                    tmem_ld32(tmem + lane_base + o_col + static_cast<uint32_t>(c * 64 + 32),
+                              *reinterpret_cast<uint32_t(*)[32]>(o + 32));
                     tmem_ld_wait();
                     if (valid_row) {
-                        uint32_t pk[16];
+                        uint32_t pk[32];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
+                        for (int i = 0; i < 32; ++i)
                             pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-                        // O is written once: streaming stores (evicted first from L2).
-                        // Measured on one GB300: +1.2 % on the contiguous configs,
-                        // -1.8 % on the paged ones, which keep plain stores.
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+                        __nv_bfloat16* d = dst + c * 64;
+                        if (out32) {
+                            // O is written once: streaming stores (evicted first from
+                            // L2) on the contiguous configs, plain ones when paged
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint4 v = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                            if constexpr (PAGED) d4[i] = v;
-                            else __stcs(d4 + i, v);
+                            for (int i = 0; i < 4; ++i) st_global_v8<!PAGED>(d + i * 16, pk + 8 * i);
+                        } else {
+                            uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                         }
                     }
                 }
+                ++ic;
             }
         }
     }
@@ -974,36 +1075,51 @@ int prefill_k_box_rows() { return prefill_so::K_BOX_ROWS; }
 int prefill_v_box_rows() { return prefill_so::V_BOX_ROWS; }
 int prefill_paged_v_box_rows() { return prefill_so::K_BOX_ROWS; }
 
-cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                           const PrefillParams& p, cudaStream_t stream) {
+// Persistent clusters: as many as can be resident at once (but no more than
+// the items), each walking its share of the items.
+template <bool PAGED>
+static cudaError_t launch_persistent(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                     const PrefillParams& p, long long n_items, cudaStream_t stream) {
+    if (n_items <= 0) return cudaSuccess;
     const int smem = prefill_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(prefill_so::prefill_so_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kern = prefill_so::prefill_so_kernel<PAGED>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    // four CTAs (cluster ranks) per q-tile pair and KV head
-    const int n_pairs = (p.num_q_tiles + 1) / 2;
-    const long long n_blocks = static_cast<long long>(n_pairs) * 4 * p.n_kv_heads;
-    prefill_so::prefill_so_kernel<false><<<static_cast<unsigned>(n_blocks), prefill_so::NUM_THREADS, smem, stream>>>(
+    int clusters = 0;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(4 * 64);
+    cfg.blockDim = dim3(prefill_so::NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+        (void)cudaGetLastError();
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        clusters = std::max(1, sms / 4);
+    }
+    const long long n = std::min<long long>(clusters, n_items);
+    prefill_so::prefill_so_kernel<PAGED><<<static_cast<unsigned>(4 * n), prefill_so::NUM_THREADS, smem, stream>>>(
         tmq, tmk, tmv, p);
     return cudaGetLastError();
 }
 
+cudaError_t launch_prefill(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                           const PrefillParams& p, cudaStream_t stream) {
+    // (q-tile pair, KV head) items
+    const long long n_items = static_cast<long long>((p.num_q_tiles + 1) / 2) * p.n_kv_heads;
+    return launch_persistent<false>(tmq, tmk, tmv, p, n_items, stream);
+}
+
 cudaError_t launch_prefill_paged(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                                  const PrefillParams& p, cudaStream_t stream) {
-    const int smem = prefill_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(prefill_so::prefill_so_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    // (sequence, KV head, q-tile pair) numbered without gaps, four CTAs each;
-    // the chunks hold at most total_q / (2 T) + batch pairs
+    // (sequence, KV head, q-tile pair) items numbered without gaps; the
+    // chunks hold at most total_q / (2 T) + batch pairs
     const long long per_head = std::min(static_cast<long long>(p.batch) * p.max_pairs,
                                         (static_cast<long long>(p.total_q) + 2 * p.tokens_per_tile - 1) /
                                                 (2 * p.tokens_per_tile) + p.batch);
-    const long long n_blocks = per_head * p.n_kv_heads * 4;
-    if (n_blocks == 0) return cudaSuccess;
-    prefill_so::prefill_so_kernel<true><<<static_cast<unsigned>(n_blocks), prefill_so::NUM_THREADS, smem, stream>>>(
-        tmq, tmk, tmv, p);
-    return cudaGetLastError();
+    return launch_persistent<true>(tmq, tmk, tmv, p, per_head * p.n_kv_heads, stream);
 }
 
 }  // namespace fa512
