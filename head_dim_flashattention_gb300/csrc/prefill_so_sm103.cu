@@ -31,18 +31,21 @@
 //
 // Score pair (per CTA: the whole 128 x 512 bf16 Q tile in TMEM, 256
 // columns, as the A operand of every QK^T, so that each MMA reads only K from
-// shared memory; two S buffers in the other 256 columns): K streams through
-// five 32 KiB slots (a half tile: this CTA's 64 keys x 256 head-dim columns),
-// each released by the commit after its 16 MMAs; the MMA thread holds back a
-// tile's QK^T until its S buffer has been read (the K loads run ahead).  Q lands in the last
-// two K slots and the P staging area, and the MMA thread copies it into TMEM
-// (tcgen05.cp, ahead of its first MMA) before either is needed.  Eight softmax warps: TMEM lane quadrant (warp % 4) gives a warp
-// its 32 rows, warps 2-5 take keys 0-63 of each tile and warps 6-9 keys
-// 64-127; they swap row maxima through shared memory.  The row max is lazy: O is rescaled only
-// when a row's max grows by more than 2^16.  P goes to one of two staging
-// buffers; a copy warp moves each staged tile with one bulk copy (the copy
-// engine) into the output CTA, where it completes on that CTA's mbarrier;
-// alpha follows by remote stores on the same barrier.
+// shared memory; two S buffers in the other 256 columns): a ring of five 32
+// KiB slots carries, per item, four entries of Q (two 64-column boxes each;
+// the MMA thread copies them into TMEM with tcgen05.cp once the previous
+// item's QK^T has completed) and then the item's K half tiles (this CTA's 64
+// keys x 256 head-dim columns), each slot released by the commit after its
+// copies or its 16 MMAs; the MMA thread holds back a tile's QK^T until its S
+// buffer has been read (the loads run ahead).  Eight softmax warps: TMEM lane
+// quadrant (warp % 4) gives a warp its 32 rows, warps 2-5 take keys 0-63 of
+// each tile and warps 6-9 keys 64-127; the two warps of a quadrant swap row
+// maxima through shared memory.  The row max is lazy: O is rescaled only when
+// a row's max grows by more than 2^16.  P goes to one of two staging buffers;
+// a copy warp moves each staged tile with one bulk copy (the copy engine) into
+// the output CTA, where it completes on that CTA's mbarrier; alpha follows by
+// remote stores on the same barrier.  At the end of an item the two parts of a
+// row add up their row sums and the sums go to the output CTA.
 //
 // Output pair (per CTA: the whole 128 x 512 fp32 O in TMEM): V streams
 // through four 32 KiB slots (two tiles x two O halves), P lands in three
@@ -51,7 +54,14 @@
 // V slots and P buffer and lets O be corrected for the next tile.  Eight
 // correction warps apply alpha to O in TMEM (tcgen05.ld / st) when a row's
 // max moved, then mark the tile ready; at the end they normalise O by the
-// sum of the bf16 P values and write bf16 rows.
+// sum of the bf16 P values and write bf16 rows.  The next item's first
+// O += P V, which overwrites O, waits for their tile-ready arrival after O
+// has been read out.
+//
+// The kernel is persistent: as many clusters as can be resident take the
+// work items round-robin, and every role walks the same item sequence with
+// running counters, so the next item's loads and products overlap the end of
+// the current one.
 //
 // A cluster-scope mbarrier arrival with release semantics stalls the thread
 // that makes it for about a microsecond.  The per-tile signals to another CTA
@@ -70,6 +80,8 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
+#include <string.h>
 
 #include "fa512_device.cuh"
 #include "fa512_internal.h"
@@ -1085,19 +1097,27 @@ static cudaError_t launch_persistent(const CUtensorMap& tmq, const CUtensorMap& 
     auto kern = prefill_so::prefill_so_kernel<PAGED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    int clusters = 0;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(4 * 64);
-    cfg.blockDim = dim3(prefill_so::NUM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
-        (void)cudaGetLastError();
-        int dev = 0, sms = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        clusters = std::max(1, sms / 4);
+    // resident clusters of four on this device: queried once per device
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> resident[2][kMaxDev];
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    int clusters = (dev >= 0 && dev < kMaxDev) ? resident[PAGED][dev].load(std::memory_order_relaxed) : 0;
+    if (clusters < 1) {
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(4 * 64);
+        cfg.blockDim = dim3(prefill_so::NUM_THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+            (void)cudaGetLastError();
+            int sms = 0;
+            if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+            clusters = std::max(1, sms / 4);
+        } else if (dev >= 0 && dev < kMaxDev) {
+            resident[PAGED][dev].store(clusters, std::memory_order_relaxed);
+        }
     }
     const long long n = std::min<long long>(clusters, n_items);
     prefill_so::prefill_so_kernel<PAGED><<<static_cast<unsigned>(4 * n), prefill_so::NUM_THREADS, smem, stream>>>(
