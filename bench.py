@@ -397,7 +397,7 @@ def time_decode_fp8(args, fa, g, dev, stream, shapes, flush, world, peaks):
                          q=torch.randn((b, hq, HEAD_DIM), generator=g, device=dev).to(torch.bfloat16),
                          out=torch.empty((b, hq, HEAD_DIM), dtype=torch.bfloat16, device=dev),
                          lse=torch.empty((b, hq), dtype=torch.float32, device=dev),
-                         ws=torch.empty(fa.fa512_decode_workspace_bytes(b, hq, hk, PAGE, n, 0),
+                         ws=torch.empty(fa.fa512_decode_workspace_bytes_fp8(b, 1, hq, hk, PAGE, n, 0),
                                         dtype=torch.uint8, device=dev),
                          bytes=decode_bytes(b, n, hq, hk, kv_elem_bytes=1)))
 

@@ -8,11 +8,13 @@ and it raises if the library has not been built.
 from ._binding import (  # noqa: F401
     Fa512Error,
     fa512_decode_auto_splits,
+    fa512_decode_auto_splits_fp8,
     fa512_decode_paged,
     fa512_decode_paged_noalloc,
     fa512_decode_paged_fp8,
     fa512_decode_paged_q,
     fa512_decode_workspace_bytes,
+    fa512_decode_workspace_bytes_fp8,
     fa512_device_status,
     fa512_prefill,
     fa512_prefill_d256,

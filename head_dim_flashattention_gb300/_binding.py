@@ -78,6 +78,10 @@ def load_library():
         lib.fa512_decode_workspace_bytes_q.restype = Z
         lib.fa512_decode_auto_splits.argtypes = [I, I, I, I]
         lib.fa512_decode_auto_splits.restype = I
+        lib.fa512_decode_auto_splits_fp8.argtypes = [I, I, I, I, I, I]
+        lib.fa512_decode_auto_splits_fp8.restype = I
+        lib.fa512_decode_workspace_bytes_fp8.argtypes = [I, I, I, I, I, I, I]
+        lib.fa512_decode_workspace_bytes_fp8.restype = Z
         lib.fa512_device_status.argtypes = [P, I]
         lib.fa512_device_status.restype = I
         lib.fa512_status_string.argtypes = [I]
@@ -225,6 +229,18 @@ def fa512_decode_workspace_bytes(batch: int, n_q_heads: int, n_kv_heads: int, pa
 
 def fa512_decode_auto_splits(batch: int, n_kv_heads: int, page_size: int, max_kv_len: int) -> int:
     return int(load_library().fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len))
+
+
+def fa512_decode_auto_splits_fp8(batch: int, q_len: int, n_q_heads: int, n_kv_heads: int,
+                                 page_size: int, max_kv_len: int) -> int:
+    return int(load_library().fa512_decode_auto_splits_fp8(batch, q_len, n_q_heads, n_kv_heads,
+                                                           page_size, max_kv_len))
+
+
+def fa512_decode_workspace_bytes_fp8(batch: int, q_len: int, n_q_heads: int, n_kv_heads: int,
+                                     page_size: int, max_kv_len: int, num_splits: int = 0) -> int:
+    return int(load_library().fa512_decode_workspace_bytes_fp8(batch, q_len, n_q_heads, n_kv_heads,
+                                                               page_size, max_kv_len, num_splits))
 
 
 def fa512_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
@@ -386,8 +402,8 @@ def fa512_decode_paged_fp8(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
     if scale is None:
         scale = d ** -0.5
     lib = load_library()
-    need = int(lib.fa512_decode_workspace_bytes_q(bsz, qlen, hq, hk, psz, int(max_kv_len),
-                                                  int(num_splits)))
+    need = int(lib.fa512_decode_workspace_bytes_fp8(bsz, qlen, hq, hk, psz, int(max_kv_len),
+                                                    int(num_splits)))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()

@@ -137,16 +137,18 @@ long long band_tiles(int max_kv_len, int window) {
     return t;
 }
 
-int choose_splits(long long items, long long tiles, int n_sm) {
+// Split count for `items` (sequence, KV head) pairs of `tiles` key tiles on
+// `slots` resident split CTAs: time model waves x (tiles per split + a fixed
+// cost of `fixed` tiles), at most `s_cap` splits.
+int choose_splits(long long items, long long tiles, int slots, int fixed, int s_cap) {
     if (items <= 0 || tiles <= 1) return 1;
     long long best_s = 1;
     double best = 1e300;
-    const long long s_max = tiles < 1024 ? tiles : 1024;
+    const long long s_max = tiles < s_cap ? tiles : s_cap;
     for (long long s = 1; s <= s_max; ++s) {
-        const long long waves = (items * s + n_sm - 1) / n_sm;
+        const long long waves = (items * s + slots - 1) / slots;
         const long long per = (tiles + s - 1) / s;
-        // time model: waves x (tiles per split + fixed cost of ~2 tiles)
-        const double cost = static_cast<double>(waves) * static_cast<double>(per + 2);
+        const double cost = static_cast<double>(waves) * static_cast<double>(per + fixed);
         if (cost < best) {
             best = cost;
             best_s = s;
@@ -479,8 +481,31 @@ fa512_status fa512_prefill_paged(const void* q, const void* k_pages, const void*
 int fa512_decode_auto_splits(int batch, int n_kv_heads, int page_size, int max_kv_len) {
     (void)page_size;
     if (batch <= 0 || n_kv_heads <= 0 || max_kv_len <= 0) return 1;
+    // one 16-warp split CTA per SM
     return choose_splits(static_cast<long long>(batch) * n_kv_heads, band_tiles(max_kv_len, 0),
-                         sm_count());
+                         sm_count(), 2, 1024);
+}
+
+int fa512_decode_auto_splits_fp8(int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                 int page_size, int max_kv_len) {
+    if (batch <= 0 || q_len < 1 || n_kv_heads <= 0 || n_q_heads <= 0 || max_kv_len <= 0) return 1;
+    if (q_len * (n_q_heads / n_kv_heads) > fa512::decode_fp8_mma_rows())
+        return fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len);
+    // four 4-warp split CTAs per SM, each split's partial merged by the
+    // merge kernel (whose cost grows with the split count: at most 64)
+    return choose_splits(static_cast<long long>(batch) * n_kv_heads, band_tiles(max_kv_len, 0),
+                         fa512::decode_fp8_ctas_per_sm() * sm_count(), 1, 64);
+}
+
+size_t fa512_decode_workspace_bytes_fp8(int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                        int page_size, int max_kv_len, int num_splits) {
+    if (batch < 0 || q_len < 1 || n_q_heads <= 0 || n_kv_heads <= 0 || max_kv_len < 0 ||
+        num_splits < 0 || num_splits > 1024)
+        return 0;
+    const int s = num_splits > 0 ? num_splits
+                                 : fa512_decode_auto_splits_fp8(batch, q_len, n_q_heads, n_kv_heads,
+                                                                page_size, max_kv_len);
+    return workspace_for(batch * q_len, n_q_heads, s);
 }
 
 size_t fa512_decode_workspace_bytes_q(int batch, int q_len, int n_q_heads, int n_kv_heads,
@@ -543,7 +568,9 @@ fa512_status decode_call(const void* q, const void* k_pages, const void* v_pages
         return fail(FA512_ERR_INVALID_ARG, "page_table, kv_lens and lse must be 4-byte aligned");
 
     const int splits = num_splits > 0 ? num_splits
-                                      : fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len);
+                       : fp8 ? fa512_decode_auto_splits_fp8(batch, q_len, n_q_heads, n_kv_heads,
+                                                            page_size, max_kv_len)
+                             : fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len);
     const size_t need = workspace_for(batch * q_len, n_q_heads, splits);
     if (!workspace || workspace_bytes < need)
         return fail(FA512_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);

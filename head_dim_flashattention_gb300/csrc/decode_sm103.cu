@@ -748,17 +748,23 @@ decode_stream_kernel(const DecodeParams p) {
 // neighbouring bytes of one row, a V pair two positions' bytes of one column,
 // gathered by one byte permute.
 //
-// Sixteen warps = four position groups x four head-dim slices of 128.  The
-// four warps of a group (same positions, one slice each) stream chunks of 16
-// positions: each copies its slice of the chunk's K and V rows (128 + 128
-// bytes a position) into a private cp.async ring, forms its slice of S^T,
-// and the four swap their partial scores through shared memory at a
-// 128-thread named barrier, so all hold the same scores, softmax state and
-// P; each then accumulates its own 128 columns of O^T.  No CTA-wide barrier
-// runs until the final merge of the four position groups.
+// A CTA is one split of the keys and four warps, one per head-dim slice of
+// 128.  The four stream the split's chunks of 16 positions together: each
+// copies its slice of the chunk's K and V rows (128 + 128 bytes a position)
+// into a private cp.async ring, forms its slice of S^T, and the four swap
+// their partial scores through shared memory at a CTA barrier, so all hold
+// the same scores, softmax state and P; each then accumulates its own 128
+// columns of O^T and, after the split's last chunk, writes them to the
+// split's (O, m, l) partial straight from its registers.  Four such CTAs
+// share an SM (16 warps): while one waits on its first page-table entries
+// and copies, or writes its partial, the other three keep streaming, and a
+// finished CTA's slot takes the next split at once.
+//
+// (The bf16 kernel below groups four such position groups in one CTA of 16
+// warps and merges them in shared memory before writing one partial.)
 namespace mma8 {
 
-constexpr int GROUPS = 4;                        // position groups
+constexpr int GROUPS = 4;                        // position groups of the bf16 kernel's CTA
 constexpr int SLICES = 4;                        // head-dim slices
 constexpr int WARPS = GROUPS * SLICES;
 constexpr int CPOS = 16;                         // positions per chunk
@@ -771,6 +777,14 @@ constexpr int RING_BYTES = WARPS * STAGES * CHUNK_BYTES;
 constexpr int XCH_BYTES = 2 * GROUPS * SLICES * 32 * 16;   // [parity][group][slice][lane] float4
 constexpr int SMEM_BYTES = RING_BYTES + XCH_BYTES;
 static_assert(WARPS * 8 * SLICE * 4 + WARPS * 8 * 2 * 4 <= RING_BYTES, "merge buffer fits the ring");
+
+// the FP8 kernel's CTA: one position group
+constexpr int F8_WARPS = SLICES;
+constexpr int F8_CTAS_PER_SM = 4;
+constexpr int F8_RING_BYTES = F8_WARPS * STAGES * CHUNK_BYTES;    // 48 KiB
+constexpr int F8_XCH_BYTES = 2 * SLICES * 32 * 16;                // [parity][slice][lane] float4
+constexpr int F8_SMEM_BYTES = F8_RING_BYTES + F8_XCH_BYTES;
+static_assert(F8_CTAS_PER_SM * (F8_SMEM_BYTES + 1024) <= 228 * 1024, "four CTAs fit an SM's shared memory");
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -832,16 +846,12 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t a) {
     return d;
 }
 
-__global__ void __launch_bounds__(WARPS * 32, 1)
+__global__ void __launch_bounds__(F8_WARPS * 32, F8_CTAS_PER_SM)
 decode_fp8_mma_kernel(const DecodeParams p) {
     allow_merge_launch();
     extern __shared__ __align__(16) uint8_t smem[];
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int pg = warp & (GROUPS - 1);      // position group
-    const int sl = warp / GROUPS;            // head-dim slice
-    // (a group's four warps share one SM sub-partition: on the large shapes
-    // this measured 2 % faster than spreading them, as the bf16 kernel does)
+    const int sl = threadIdx.x >> 5, lane = threadIdx.x & 31;   // warp = head-dim slice
     const int g = lane >> 2, t = lane & 3;   // mma fragment coordinates
     const int G = p.group;
     const int R = p.q_len * G;               // query rows, <= 8
@@ -859,7 +869,6 @@ decode_fp8_mma_kernel(const DecodeParams p) {
     const int pb = max(lo, t_begin * TILE_K);
     const int pe = min(hi, (t_begin + p.tiles_per_split) * TILE_K);
     const int n_chunks = pe > pb ? (pe - pb + CPOS - 1) / CPOS : 0;
-    const int my_chunks = n_chunks > pg ? (n_chunks - pg + GROUPS - 1) / GROUPS : 0;
 
     // ---- Q^T fragments of this warp's slice: b0/b1 of k-step (j, s) hold
     // row g's elements 64 j + 16 t + 4 s + {0, 1} / {2, 3}, in f16 after a
@@ -919,8 +928,8 @@ decode_fp8_mma_kernel(const DecodeParams p) {
 #pragma unroll
     for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-    const uint32_t ring = smem_u32(smem) + warp * STAGES * CHUNK_BYTES;
-    float4* xch = reinterpret_cast<float4*>(smem + RING_BYTES);
+    const uint32_t ring = smem_u32(smem) + sl * STAGES * CHUNK_BYTES;
+    float4* xch = reinterpret_cast<float4*>(smem + F8_RING_BYTES);
 
     // copy plan: lane l fetches position l / 2 of the chunk; at step s it
     // copies 16-byte piece (l & 1) + 2 (s % 4) of that position's K slice
@@ -929,14 +938,14 @@ decode_fp8_mma_kernel(const DecodeParams p) {
     // page of this lane's position in chunk k, loaded one chunk before the
     // chunk's copies are issued (the copies never wait on the page table)
     auto page_of = [&](int k) -> int {
-        const int pos = pb + (pg + GROUPS * k) * CPOS + (lane >> 1);
-        return (k < my_chunks && pos < pe)
+        const int pos = pb + k * CPOS + (lane >> 1);
+        return (k < n_chunks && pos < pe)
                    ? p.page_table[static_cast<size_t>(b) * p.max_pages_per_seq + pos / p.page_size]
                    : 0;
     };
     auto issue = [&](int k, int page) {
-        if (k < my_chunks) {
-            const int pos = pb + (pg + GROUPS * k) * CPOS + (lane >> 1);
+        if (k < n_chunks) {
+            const int pos = pb + k * CPOS + (lane >> 1);
             bool valid = pos < pe;
             size_t row = 0;
             if (valid) {
@@ -964,15 +973,15 @@ decode_fp8_mma_kernel(const DecodeParams p) {
 #pragma unroll
     for (int k = 0; k < STAGES - 1; ++k) issue(k, page_of(k));
 
-    for (int k = 0; k < my_chunks; ++k) {
+    for (int k = 0; k < n_chunks; ++k) {
         const int page_now = page_next;
         page_next = page_of(k + STAGES);
         issue(k + STAGES - 1, page_now);
         cp_async_wait<STAGES - 1>();
         __syncwarp();                         // every lane's copies of chunk k are visible
-        const uint8_t* kst = smem + (warp * STAGES + (k % STAGES)) * CHUNK_BYTES;
+        const uint8_t* kst = smem + (sl * STAGES + (k % STAGES)) * CHUNK_BYTES;
         const uint8_t* vst = kst + CPOS * SLICE;
-        const int pos0 = pb + (pg + GROUPS * k) * CPOS;
+        const int pos0 = pb + k * CPOS;
 
         // ---- S^T slice = K_slice Q_slice^T, one accumulator chain per 64
         // head-dim elements, summed at the end
@@ -994,13 +1003,13 @@ decode_fp8_mma_kernel(const DecodeParams p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) sc[e] = (acc[0][e] + acc[1][e]) * (e & 1 ? rs[1] : rs[0]);
         }
-        // ---- swap slices with the group's other warps: S = (S_0 + S_1) + (S_2 + S_3),
+        // ---- swap slices with the other three warps: S = (S_0 + S_1) + (S_2 + S_3),
         // each slice unscaled by its own row scale first (a power of two,
         // exact); the same sum, in the same order, in all four warps
         {
-            float4* base = xch + ((k & 1) * GROUPS + pg) * SLICES * 32 + lane;
+            float4* base = xch + (k & 1) * SLICES * 32 + lane;
             base[sl * 32] = make_float4(sc[0], sc[1], sc[2], sc[3]);
-            bar_group(1 + pg);
+            __syncthreads();
             const float4 x0 = base[0], x1 = base[32], x2 = base[64], x3 = base[96];
             sc[0] = (x0.x + x1.x) + (x2.x + x3.x);
             sc[1] = (x0.y + x1.y) + (x2.y + x3.y);
@@ -1100,52 +1109,28 @@ decode_fp8_mma_kernel(const DecodeParams p) {
     for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) l[i] += __shfl_xor_sync(0xffffffffu, l[i], off);
-    __syncthreads();   // every warp is done with its ring: reuse it for the merge
 
-    // ---- merge the four position groups: O^T rows 2t, 2t + 1 of slice
-    // columns 16 g + 2 i (M row g of m-tile i) and 16 g + 2 i + 1 (M row
-    // g + 8) -> smem [warp][row 8][128], m and l [warp][row][2]
-    float* so = reinterpret_cast<float*>(smem);
-    float* sml = so + WARPS * 8 * SLICE;
+    // ---- this split's partial, unnormalised and times v_scale: row 2t + i
+    // holds columns 16 g .. 16 g + 15 of this slice (m-tile j: columns
+    // 16 g + 2 j in o[j][i], 16 g + 2 j + 1 in o[j][2 + i]); m and l are the
+    // same in every slice warp, written by slice 0.  A split that saw no key
+    // has m = -inf and O = 0.
+    const size_t S = static_cast<size_t>(p.num_splits);
     const float osc = p.o_scale;              // v_scale of the FP8 cache
 #pragma unroll
-    for (int i = 0; i < MTILES; ++i) {
-        const int c0 = 16 * g + 2 * i, c1 = c0 + 1;
-        so[(warp * 8 + 2 * t) * SLICE + c0] = o[i][0];
-        so[(warp * 8 + 2 * t + 1) * SLICE + c0] = o[i][1];
-        so[(warp * 8 + 2 * t) * SLICE + c1] = o[i][2];
-        so[(warp * 8 + 2 * t + 1) * SLICE + c1] = o[i][3];
-    }
-    if (g == 0) {
+    for (int i = 0; i < 2; ++i) {
+        const int r = 2 * t + i;
+        if (r < R) {
+            const size_t hq = (static_cast<size_t>(b) * p.q_len + r / G) * p.n_q_heads + kvh * G + r % G;
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + (hq * S + split) * D + sl * SLICE + 16 * g);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            sml[(warp * 8 + 2 * t + i) * 2] = m[i];
-            sml[(warp * 8 + 2 * t + i) * 2 + 1] = l[i];
-        }
-    }
-    __syncthreads();
-    const size_t S = static_cast<size_t>(p.num_splits);
-    for (int idx = threadIdx.x; idx < R * D; idx += WARPS * 32) {
-        const int r = idx / D, d = idx - r * D;
-        const int h = d / SLICE, c = d - h * SLICE;   // slice and column within it
-        float M = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < GROUPS; ++q) M = fmaxf(M, sml[((h * GROUPS + q) * 8 + r) * 2]);
-        float acc = 0.f, L = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int q = 0; q < GROUPS; ++q) {
-                const int w = h * GROUPS + q;   // the warp of group q, slice h
-                const float wt = fast_exp2(sml[(w * 8 + r) * 2] - M);
-                acc += wt * so[(w * 8 + r) * SLICE + c];
-                L += wt * sml[(w * 8 + r) * 2 + 1];
+            for (int j = 0; j < MTILES / 2; ++j)
+                dst[j] = make_float4(o[2 * j][i] * osc, o[2 * j][2 + i] * osc, o[2 * j + 1][i] * osc,
+                                     o[2 * j + 1][2 + i] * osc);
+            if (sl == 0 && g == 0) {
+                p.ws_ml[(hq * S + split) * 2 + 0] = m[i];
+                p.ws_ml[(hq * S + split) * 2 + 1] = m[i] == -INFINITY ? 0.f : l[i];
             }
-        }
-        const size_t hq = (static_cast<size_t>(b) * p.q_len + r / G) * p.n_q_heads + kvh * G + r % G;
-        p.ws_o[(hq * S + split) * D + d] = acc * osc;
-        if (d == 0) {
-            p.ws_ml[(hq * S + split) * 2 + 0] = M;
-            p.ws_ml[(hq * S + split) * 2 + 1] = M == -INFINITY ? 0.f : L;
         }
     }
 }
@@ -1154,10 +1139,12 @@ decode_fp8_mma_kernel(const DecodeParams p) {
 
 // ---------------------------------------------------------------------------
 // bf16 cache, 3 to 8 query rows (several tokens, or 3-8 query heads per KV
-// head): the same streaming tensor-core design as the FP8 kernel above, for
-// the rows the FMA streaming kernel cannot take.  A bf16 position carries
-// 2 KiB, so the design's per-position instruction cost fits twice the HBM
-// time it has at FP8; its operands need no widening (K pairs are the A
+// head): the streaming tensor-core design of the FP8 kernel above, for the
+// rows the FMA streaming kernel cannot take, with four position groups of
+// four slice warps in one CTA (16 warps) that stride over the split's
+// chunks and merge their (O, m, l) in shared memory at the end.  A bf16
+// position carries 2 KiB, so the design's per-position instruction cost fits
+// twice the HBM time it has at FP8; its operands need no widening (K pairs are the A
 // operand as stored; each V operand pair is one 16-bit permute of two
 // positions' words).  Shared memory (16 warps x 3 stages) holds chunks of 8
 // positions: S^T runs with M = 16 over 8 positions (the other 8 rows zero)
@@ -1534,6 +1521,7 @@ decode_merge_kernel(const DecodeParams p) {
         const int sp = grp + i * MERGE_GROUPS;
         if (sp < S) add(sw[sp], x[i]);
     }
+#pragma unroll 4
     for (int sp = grp + MERGE_UNROLL * MERGE_GROUPS; sp < S; sp += MERGE_GROUPS)
         add(sw[sp], *reinterpret_cast<const float4*>(ob + static_cast<size_t>(sp) * D));
     if (grp > 0) sacc[grp - 1][cq] = acc;
@@ -1562,6 +1550,10 @@ int decode_smem_bytes() { return decode::Smem<false>::total + 1024; }
 
 int decode_fp8_box_bytes() { return decode::F8_BOX_BYTES; }
 
+int decode_fp8_mma_rows() { return 8; }
+
+int decode_fp8_ctas_per_sm() { return decode::mma8::F8_CTAS_PER_SM; }
+
 int decode_tile_positions() { return decode::TILE_K; }
 
 constexpr int TILE_POSITIONS = decode::TILE_K;
@@ -1588,12 +1580,12 @@ static cudaError_t launch_bf16_mma(const DecodeParams& p, cudaStream_t stream) {
 }
 
 static cudaError_t launch_fp8_mma(const DecodeParams& p, cudaStream_t stream) {
-    const int smem = decode::mma8::SMEM_BYTES;
+    const int smem = decode::mma8::F8_SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(decode::mma8::decode_fp8_mma_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.num_splits, p.n_kv_heads, p.batch);
-    decode::mma8::decode_fp8_mma_kernel<<<grid, decode::mma8::WARPS * 32, smem, stream>>>(p);
+    decode::mma8::decode_fp8_mma_kernel<<<grid, decode::mma8::F8_WARPS * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -1601,7 +1593,7 @@ template <bool FP8>
 static cudaError_t launch_split_and_merge(const CUtensorMap& tmk, const CUtensorMap& tmv,
                                           const DecodeParams& p, cudaStream_t stream) {
     cudaError_t e;
-    if (FP8 && p.q_len * p.group <= 8) {
+    if (FP8 && p.q_len * p.group <= decode_fp8_mma_rows()) {
         e = launch_fp8_mma(p, stream);
     } else if (!FP8 && p.q_len == 1 && p.group <= 2 && p.tiles_per_split * TILE_POSITIONS < 1024) {
         // short splits (small batches): the FMA streaming kernel's lighter

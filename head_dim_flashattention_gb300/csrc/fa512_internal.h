@@ -42,6 +42,10 @@ cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const 
 // FP8 cache: tmk / tmv map the e4m3 pages as bytes, boxes of
 // decode_fp8_box_bytes() head-dim bytes x box_rows positions, no swizzle.
 int decode_fp8_box_bytes();
+// FP8 cache with q_len * G <= decode_fp8_mma_rows(): the split kernel runs
+// decode_fp8_ctas_per_sm() CTAs per SM, one split each.
+int decode_fp8_mma_rows();
+int decode_fp8_ctas_per_sm();
 cudaError_t launch_decode_fp8(const CUtensorMap& tmk, const CUtensorMap& tmv,
                               const DecodeParams& p, cudaStream_t stream);
 

@@ -254,9 +254,11 @@ size_t fa512_decode_workspace_bytes_q(int batch, int q_len, int n_q_heads, int n
  *              NaN, largest finite 448) byte per element
  *   k_scale, v_scale per-tensor dequantisation scales: key element
  *              k_scale * e4m3(byte), value element v_scale * e4m3(byte)
- *   q, out, lse, positions, workspace and every other argument as
- *              fa512_decode_paged_q (q_len >= 1, q_len * G <= 16); the
- *              workspace size is fa512_decode_workspace_bytes_q.
+ *   q, out, lse, positions and every other argument as
+ *              fa512_decode_paged_q (q_len >= 1, q_len * G <= 16)
+ *   num_splits 0 picks fa512_decode_auto_splits_fp8(); workspace must be
+ *              at least fa512_decode_workspace_bytes_fp8() bytes for the
+ *              split count used (256-byte aligned).
  *
  * The cache is read as bytes: half the HBM traffic of a bf16 cache.  Every
  * byte is widened exactly (e4m3 -> bf16/fp32) before it meets the bf16
@@ -279,6 +281,20 @@ fa512_status fa512_decode_paged_fp8(const void *q, const void *k_pages, const vo
  * work items to fill the current device's SMs about twice, each split at
  * least one page.  Returns 1 when there is nothing to split. */
 int fa512_decode_auto_splits(int batch, int n_kv_heads, int page_size, int max_kv_len);
+
+/* Split count fa512_decode_paged_fp8 uses when num_splits == 0.  With
+ * q_len * G <= 8 its split kernel runs four CTAs of four warps per SM, one
+ * split each, so the choice fills four times as many slots (at most 64
+ * splits); otherwise it is fa512_decode_auto_splits().  Returns 1 when there
+ * is nothing to split. */
+int fa512_decode_auto_splits_fp8(int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                 int page_size, int max_kv_len);
+
+/* Workspace bytes fa512_decode_paged_fp8 needs for this shape and split
+ * count (num_splits 0: fa512_decode_auto_splits_fp8).  0 for an invalid
+ * shape. */
+size_t fa512_decode_workspace_bytes_fp8(int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                        int page_size, int max_kv_len, int num_splits);
 
 /*
  * fa512_decode_paged_noalloc -- fa512_decode_paged without a workspace

@@ -101,6 +101,27 @@ def test_workspace_size_and_auto_splits(lib):
     assert fa.fa512_decode_workspace_bytes(-1, 8, 4, 64, 10, 0) == 0
 
 
+def test_fp8_workspace_and_auto_splits(lib):
+    # an explicit split count: the partial layout of the bf16 calls
+    assert (fa.fa512_decode_workspace_bytes_fp8(4, 1, 8, 4, 64, 4096, 3)
+            == fa.fa512_decode_workspace_bytes(4, 8, 4, 64, 4096, 3))
+    assert (fa.fa512_decode_workspace_bytes_fp8(4, 2, 8, 4, 64, 4096, 3)
+            == lib.fa512_decode_workspace_bytes_q(4, 2, 8, 4, 64, 4096, 3))
+    # the automatic choice of the one-split-per-CTA kernel: at most 64 splits,
+    # at most one per tile, and the workspace query sizes for it
+    for b, n in ((1, 4096), (16, 16384), (64, 28672)):
+        s = fa.fa512_decode_auto_splits_fp8(b, 1, 8, 4, 64, n)
+        assert 1 <= s <= min(64, n // 32)
+        assert (fa.fa512_decode_workspace_bytes_fp8(b, 1, 8, 4, 64, n, 0)
+                == fa.fa512_decode_workspace_bytes_fp8(b, 1, 8, 4, 64, n, s))
+    # more rows than that kernel takes (q_len x G > 8): the bf16 choice
+    assert (fa.fa512_decode_auto_splits_fp8(16, 8, 8, 4, 64, 16384)
+            == fa.fa512_decode_auto_splits(16, 4, 64, 16384))
+    assert fa.fa512_decode_auto_splits_fp8(1, 1, 8, 4, 64, 0) == 1
+    assert fa.fa512_decode_workspace_bytes_fp8(-1, 1, 8, 4, 64, 10, 0) == 0
+    assert fa.fa512_decode_workspace_bytes_fp8(4, 0, 8, 4, 64, 10, 0) == 0
+
+
 def _decode_q(lib, **kw):
     a = dict(q=16, kp=16, vp=16, pt=16, kl=16, out=16, lse=None, b=2, ql=4, hq=8, hk=4, ps=64,
              npages=10, mpps=4, maxlen=200, scale=0.05, window=0, splits=0, ws=256,
