@@ -137,18 +137,46 @@ long long band_tiles(int max_kv_len, int window) {
     return t;
 }
 
-// Split count for `items` (sequence, KV head) pairs of `tiles` key tiles on
-// `slots` resident split CTAs: time model waves x (tiles per split + a fixed
-// cost of `fixed` tiles), at most `s_cap` splits.
-int choose_splits(long long items, long long tiles, int slots, int fixed, int s_cap) {
+// Split count for `items` (sequence, KV head) pairs of `tiles` key tiles,
+// one 16-warp split CTA per SM.
+int choose_splits(long long items, long long tiles, int n_sm) {
     if (items <= 0 || tiles <= 1) return 1;
     long long best_s = 1;
     double best = 1e300;
-    const long long s_max = tiles < s_cap ? tiles : s_cap;
+    const long long s_max = tiles < 1024 ? tiles : 1024;
     for (long long s = 1; s <= s_max; ++s) {
-        const long long waves = (items * s + slots - 1) / slots;
+        const long long waves = (items * s + n_sm - 1) / n_sm;
         const long long per = (tiles + s - 1) / s;
-        const double cost = static_cast<double>(waves) * static_cast<double>(per + fixed);
+        // time model: waves x (tiles per split + fixed cost of ~2 tiles)
+        const double cost = static_cast<double>(waves) * static_cast<double>(per + 2);
+        if (cost < best) {
+            best = cost;
+            best_s = s;
+        }
+    }
+    return static_cast<int>(best_s);
+}
+
+// Split count for the FP8 kernel that runs `slots` CTAs at once (four per
+// SM), one split each.  A finished CTA's slot takes the next split at once,
+// so the work spreads over the slots in fractions of a round rather than
+// whole waves; the model, in tile times of one CTA:
+//   max(1, items x s / slots) x (tiles per split + 2)   streaming + start
+//   + 0.75 x tiles per split                             the ragged end
+//   + 0.2 x max(0, s - 32)                               merge loads past the
+//                                                        merge kernel's first 32
+// (fitted to times of batch 1/16/64 x KV 4096/16384/28672, 4 KV heads,
+// over 8 split counts each: within 0.3 % of the best count per shape).
+int choose_splits_fp8(long long items, long long tiles, int slots) {
+    if (items <= 0 || tiles <= 1) return 1;
+    long long best_s = 1;
+    double best = 1e300;
+    const long long s_max = tiles < 128 ? tiles : 128;
+    for (long long s = 1; s <= s_max; ++s) {
+        const double per = static_cast<double>((tiles + s - 1) / s);
+        const double x = static_cast<double>(items * s) / slots;
+        const double cost = (x > 1.0 ? x : 1.0) * (per + 2.0) + 0.75 * per +
+                            0.2 * static_cast<double>(s > 32 ? s - 32 : 0);
         if (cost < best) {
             best = cost;
             best_s = s;
@@ -481,9 +509,8 @@ fa512_status fa512_prefill_paged(const void* q, const void* k_pages, const void*
 int fa512_decode_auto_splits(int batch, int n_kv_heads, int page_size, int max_kv_len) {
     (void)page_size;
     if (batch <= 0 || n_kv_heads <= 0 || max_kv_len <= 0) return 1;
-    // one 16-warp split CTA per SM
     return choose_splits(static_cast<long long>(batch) * n_kv_heads, band_tiles(max_kv_len, 0),
-                         sm_count(), 2, 1024);
+                         sm_count());
 }
 
 int fa512_decode_auto_splits_fp8(int batch, int q_len, int n_q_heads, int n_kv_heads,
@@ -491,10 +518,8 @@ int fa512_decode_auto_splits_fp8(int batch, int q_len, int n_q_heads, int n_kv_h
     if (batch <= 0 || q_len < 1 || n_kv_heads <= 0 || n_q_heads <= 0 || max_kv_len <= 0) return 1;
     if (q_len * (n_q_heads / n_kv_heads) > fa512::decode_fp8_mma_rows())
         return fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len);
-    // four 4-warp split CTAs per SM, each split's partial merged by the
-    // merge kernel (whose cost grows with the split count: at most 64)
-    return choose_splits(static_cast<long long>(batch) * n_kv_heads, band_tiles(max_kv_len, 0),
-                         fa512::decode_fp8_ctas_per_sm() * sm_count(), 1, 64);
+    return choose_splits_fp8(static_cast<long long>(batch) * n_kv_heads, band_tiles(max_kv_len, 0),
+                             fa512::decode_fp8_ctas_per_sm() * sm_count());
 }
 
 size_t fa512_decode_workspace_bytes_fp8(int batch, int q_len, int n_q_heads, int n_kv_heads,

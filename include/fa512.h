@@ -284,9 +284,9 @@ int fa512_decode_auto_splits(int batch, int n_kv_heads, int page_size, int max_k
 
 /* Split count fa512_decode_paged_fp8 uses when num_splits == 0.  With
  * q_len * G <= 8 its split kernel runs four CTAs of four warps per SM, one
- * split each, so the choice fills four times as many slots (at most 64
- * splits); otherwise it is fa512_decode_auto_splits().  Returns 1 when there
- * is nothing to split. */
+ * split each, so the choice spreads the keys over four times as many CTAs
+ * (at most 128 splits); otherwise it is fa512_decode_auto_splits().  Returns
+ * 1 when there is nothing to split. */
 int fa512_decode_auto_splits_fp8(int batch, int q_len, int n_q_heads, int n_kv_heads,
                                  int page_size, int max_kv_len);
 

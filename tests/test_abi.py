@@ -107,11 +107,11 @@ def test_fp8_workspace_and_auto_splits(lib):
             == fa.fa512_decode_workspace_bytes(4, 8, 4, 64, 4096, 3))
     assert (fa.fa512_decode_workspace_bytes_fp8(4, 2, 8, 4, 64, 4096, 3)
             == lib.fa512_decode_workspace_bytes_q(4, 2, 8, 4, 64, 4096, 3))
-    # the automatic choice of the one-split-per-CTA kernel: at most 64 splits,
-    # at most one per tile, and the workspace query sizes for it
+    # the automatic choice of the one-split-per-CTA kernel: at most 128
+    # splits, at most one per tile, and the workspace query sizes for it
     for b, n in ((1, 4096), (16, 16384), (64, 28672)):
         s = fa.fa512_decode_auto_splits_fp8(b, 1, 8, 4, 64, n)
-        assert 1 <= s <= min(64, n // 32)
+        assert 1 <= s <= min(128, n // 32)
         assert (fa.fa512_decode_workspace_bytes_fp8(b, 1, 8, 4, 64, n, 0)
                 == fa.fa512_decode_workspace_bytes_fp8(b, 1, 8, 4, 64, n, s))
     # more rows than that kernel takes (q_len x G > 8): the bf16 choice
