@@ -157,26 +157,39 @@ int choose_splits(long long items, long long tiles, int n_sm) {
     return static_cast<int>(best_s);
 }
 
-// Split count for the FP8 kernel that runs `slots` CTAs at once (four per
-// SM), one split each.  A finished CTA's slot takes the next split at once,
-// so the work spreads over the slots in fractions of a round rather than
-// whole waves; the model, in tile times of one CTA:
+// Split count for the FP8 kernel, four CTAs per SM, one split each, `rows`
+// (sequence, token, query head) rows to merge.  Times in tile times of one
+// CTA.  Large batches (the merge takes whole rows): a finished CTA's slot
+// takes the next split at once, so the work spreads over the slots in
+// fractions of a round rather than whole waves:
 //   max(1, items x s / slots) x (tiles per split + 2)   streaming + start
 //   + 0.75 x tiles per split                             the ragged end
 //   + 0.2 x max(0, s - 32)                               merge loads past the
 //                                                        merge kernel's first 32
-// (fitted to times of batch 1/16/64 x KV 4096/16384/28672, 4 KV heads,
-// over 8 split counts each: within 0.3 % of the best count per shape).
-int choose_splits_fp8(long long items, long long tiles, int slots) {
+// Small batches (every CTA resident at once, the merge in column slices):
+// an SM's time is its CTAs x tiles per split, and one CTA alone runs no
+// faster than two sharing the SM (it is latency-bound), so
+//   max(2, CTAs on the busiest SM) x tiles per split.
+// Both fitted to times of batch 1/16/64 x KV 4096/16384/28672, 4 KV heads,
+// over 8 split counts each: within 0.5 % of the best count per shape.
+int choose_splits_fp8(long long items, long long tiles, int n_sm, long long rows) {
     if (items <= 0 || tiles <= 1) return 1;
+    const bool small = fa512::decode_merge_sliced(rows);
+    const double slots = static_cast<double>(fa512::decode_fp8_ctas_per_sm()) * n_sm;
     long long best_s = 1;
     double best = 1e300;
     const long long s_max = tiles < 128 ? tiles : 128;
     for (long long s = 1; s <= s_max; ++s) {
         const double per = static_cast<double>((tiles + s - 1) / s);
-        const double x = static_cast<double>(items * s) / slots;
-        const double cost = (x > 1.0 ? x : 1.0) * (per + 2.0) + 0.75 * per +
-                            0.2 * static_cast<double>(s > 32 ? s - 32 : 0);
+        double cost;
+        if (small) {
+            const long long busiest = (items * s + n_sm - 1) / n_sm;
+            cost = static_cast<double>(busiest > 2 ? busiest : 2) * per;
+        } else {
+            const double x = static_cast<double>(items * s) / slots;
+            cost = (x > 1.0 ? x : 1.0) * (per + 2.0) + 0.75 * per +
+                   0.2 * static_cast<double>(s > 32 ? s - 32 : 0);
+        }
         if (cost < best) {
             best = cost;
             best_s = s;
@@ -519,7 +532,7 @@ int fa512_decode_auto_splits_fp8(int batch, int q_len, int n_q_heads, int n_kv_h
     if (q_len * (n_q_heads / n_kv_heads) > fa512::decode_fp8_mma_rows())
         return fa512_decode_auto_splits(batch, n_kv_heads, page_size, max_kv_len);
     return choose_splits_fp8(static_cast<long long>(batch) * n_kv_heads, band_tiles(max_kv_len, 0),
-                             fa512::decode_fp8_ctas_per_sm() * sm_count());
+                             sm_count(), static_cast<long long>(batch) * q_len * n_q_heads);
 }
 
 size_t fa512_decode_workspace_bytes_fp8(int batch, int q_len, int n_q_heads, int n_kv_heads,

@@ -19,11 +19,13 @@
 //   decode_bf16_mma_kernel    up to 8 rows otherwise (bf16): streaming warps
 //                             on mma.sync with the rows in N;
 //   decode_fp8_mma_kernel     up to 8 rows over an FP8 cache: the same design
-//                             with every byte widened exactly to f16;
+//                             with every byte widened exactly to f16, one
+//                             split per 4-warp CTA, four CTAs per SM;
 //   decode_split_kernel<FP8>  9 to 16 rows: a CTA's warps share TMA-loaded
 //                             tiles of 32 positions (FP8 tiles converted
 //                             exactly to bf16), S and PV on mma.sync;
-//   decode_merge_kernel       combines the splits' (O, m, l) partials.
+//   decode_merge_kernel<CS>   combines the splits' (O, m, l) partials, each
+//                             row in CS column slices.
 // HBM traffic per position and KV head: 1 KiB of K + 1 KiB of V (bf16) or
 // 512 + 512 bytes (FP8).
 #include <cuda.h>
@@ -1441,35 +1443,41 @@ decode_bf16_mma_kernel(const DecodeParams p) {
 
 
 
-// One block per (sequence, query token, query head): merges the splits'
-// (O, m, l) -- M = max m_s, w_s = 2^(m_s - M), O = sum w_s O_s / sum w_s l_s
-// ("Flash-Decoding for MQA in CUDA", "One KV head breaks the textbook").
-// 256 threads: 128 column quads x 2 groups of splits.  Every thread issues
-// the loads of its splits' O columns first, then the block finds the
-// weights from the (m, l) pairs, so the merge costs about one memory round
-// trip; the two groups' sums meet in shared memory.
+// One block per (sequence, query token, query head) and slice of CS column
+// slices: merges the splits' (O, m, l) -- M = max m_s, w_s = 2^(m_s - M),
+// O = sum w_s O_s / sum w_s l_s ("Flash-Decoding for MQA in CUDA", "One KV
+// head breaks the textbook").  256 threads: the slice's column quads x
+// groups of splits (CS = 1: 128 quads x 2 groups; CS = 4: 32 quads x 8
+// groups, four blocks per row, for batches whose rows alone leave most SMs
+// idle).  Every thread issues the loads of its splits' O columns first, then
+// the block finds the weights from the (m, l) pairs, so the merge costs about
+// one memory round trip; the groups' sums meet in shared memory.
 constexpr int MERGE_THREADS = 256;
-constexpr int MERGE_GROUPS = MERGE_THREADS / (D / 4);
 constexpr int MERGE_UNROLL = 16;         // splits a thread loads up front
 constexpr int MAX_SPLITS = 1024;
 
+template <int CS>
 __global__ void __launch_bounds__(MERGE_THREADS)
 decode_merge_kernel(const DecodeParams p) {
+    constexpr int QB = D / 4 / CS;                  // column quads of the slice
+    constexpr int NG = MERGE_THREADS / QB;          // groups of splits
+    static_assert(QB * NG == MERGE_THREADS, "threads = quads x groups");
     __shared__ float sw[MAX_SPLITS];      // w_s
-    __shared__ float4 sacc[MERGE_GROUPS - 1][D / 4];
+    __shared__ float4 sacc[NG - 1][QB];
     __shared__ float smax[MERGE_THREADS / 32], ssum[MERGE_THREADS / 32];
     wait_for_splits();
     const int h = blockIdx.x;
     const int bt = blockIdx.y;      // sequence * q_len + token
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cq = tid % (D / 4), grp = tid / (D / 4);
+    const int cq = tid % QB, grp = tid / QB;
+    const int col = blockIdx.z * (D / CS) + cq * 4;
     const size_t bh = static_cast<size_t>(bt) * p.n_q_heads + h;
     const int S = p.num_splits;
-    const float* ob = p.ws_o + bh * S * D + cq * 4;
+    const float* ob = p.ws_o + bh * S * D + col;
     float4 x[MERGE_UNROLL];
 #pragma unroll
     for (int i = 0; i < MERGE_UNROLL; ++i) {
-        const int sp = grp + i * MERGE_GROUPS;
+        const int sp = grp + i * NG;
         x[i] = sp < S ? *reinterpret_cast<const float4*>(ob + static_cast<size_t>(sp) * D)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -1500,10 +1508,11 @@ decode_merge_kernel(const DecodeParams p) {
     float L = 0.f;
 #pragma unroll
     for (int w = 0; w < MERGE_THREADS / 32; ++w) L += ssum[w];
-    __nv_bfloat16* out = p.out + bh * D + cq * 4;
+    __nv_bfloat16* out = p.out + bh * D + col;
+    const bool lse_here = p.lse && tid == 0 && blockIdx.z == 0;
     if (M == -INFINITY) {
         if (grp == 0) *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
-        if (p.lse && tid == 0) p.lse[bh] = -INFINITY;
+        if (lse_here) p.lse[bh] = -INFINITY;
         return;
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1518,17 +1527,17 @@ decode_merge_kernel(const DecodeParams p) {
     };
 #pragma unroll
     for (int i = 0; i < MERGE_UNROLL; ++i) {
-        const int sp = grp + i * MERGE_GROUPS;
+        const int sp = grp + i * NG;
         if (sp < S) add(sw[sp], x[i]);
     }
 #pragma unroll 4
-    for (int sp = grp + MERGE_UNROLL * MERGE_GROUPS; sp < S; sp += MERGE_GROUPS)
+    for (int sp = grp + MERGE_UNROLL * NG; sp < S; sp += NG)
         add(sw[sp], *reinterpret_cast<const float4*>(ob + static_cast<size_t>(sp) * D));
     if (grp > 0) sacc[grp - 1][cq] = acc;
     __syncthreads();
     if (grp == 0) {
 #pragma unroll
-        for (int g = 0; g < MERGE_GROUPS - 1; ++g) {
+        for (int g = 0; g < NG - 1; ++g) {
             const float4 a = sacc[g][cq];
             acc.x += a.x;
             acc.y += a.y;
@@ -1540,7 +1549,7 @@ decode_merge_kernel(const DecodeParams p) {
         packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
         packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
         *reinterpret_cast<uint2*>(out) = packed;
-        if (p.lse && tid == 0) p.lse[bh] = (M + log2f(L)) * 0.69314718055994530942f;
+        if (lse_here) p.lse[bh] = (M + log2f(L)) * 0.69314718055994530942f;
     }
 }
 
@@ -1551,6 +1560,8 @@ int decode_smem_bytes() { return decode::Smem<false>::total + 1024; }
 int decode_fp8_box_bytes() { return decode::F8_BOX_BYTES; }
 
 int decode_fp8_mma_rows() { return 8; }
+
+bool decode_merge_sliced(long long rows) { return rows * 4 <= 152; }
 
 int decode_fp8_ctas_per_sm() { return decode::mma8::F8_CTAS_PER_SM; }
 
@@ -1613,10 +1624,13 @@ static cudaError_t launch_split_and_merge(const CUtensorMap& tmk, const CUtensor
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    // the merge may be scheduled while the split kernel runs (it waits for it)
+    // the merge may be scheduled while the split kernel runs (it waits for
+    // it); rows too few to spread over the SMs are merged in four column
+    // slices each
+    const bool sliced = decode_merge_sliced(static_cast<long long>(p.n_q_heads) * p.batch * p.q_len);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(p.n_q_heads, p.batch * p.q_len);
+    cfg.gridDim = dim3(p.n_q_heads, p.batch * p.q_len, sliced ? 4 : 1);
     cfg.blockDim = dim3(decode::MERGE_THREADS);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -1625,7 +1639,8 @@ static cudaError_t launch_split_and_merge(const CUtensorMap& tmk, const CUtensor
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode::decode_merge_kernel, p);
+    return sliced ? cudaLaunchKernelEx(&cfg, decode::decode_merge_kernel<4>, p)
+                  : cudaLaunchKernelEx(&cfg, decode::decode_merge_kernel<1>, p);
 }
 
 cudaError_t launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,

@@ -46,6 +46,10 @@ int decode_fp8_box_bytes();
 // decode_fp8_ctas_per_sm() CTAs per SM, one split each.
 int decode_fp8_mma_rows();
 int decode_fp8_ctas_per_sm();
+// The merge kernel takes `rows` (sequence, token, query head) rows in four
+// column slices each (128 splits loaded up front) when this is true, else
+// whole (32 splits up front).
+bool decode_merge_sliced(long long rows);
 cudaError_t launch_decode_fp8(const CUtensorMap& tmk, const CUtensorMap& tmv,
                               const DecodeParams& p, cudaStream_t stream);
 
