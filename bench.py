@@ -425,7 +425,8 @@ def time_decode_fp8(args, fa, g, dev, stream, shapes, flush, world, peaks):
     ms = max_over_ranks(ms, dev)
     total_bytes = sum(d["bytes"] for d in legs)
     gbs = job_rate(total_bytes, args.steps, world, sum(ms) * args.steps / 1e3) / 1e9
-    per = {"b%d_kv%d" % (d["b"], d["n"]): {"ms": m, "GB/s": d["bytes"] / m / 1e6}
+    per = {"b%d_kv%d" % (d["b"], d["n"]): {"ms": m, "GB/s": d["bytes"] / m / 1e6,
+                                            "splits": fa.fa512_decode_auto_splits_fp8(d["b"], 1, hq, hk, PAGE, d["n"])}
            for d, m in zip(legs, ms)}
     return {"workload": "paged decode b{1,16,64} x kv{4096,16384,28672}, 8/4 heads, page 64, "
                         "num_splits auto, FP8 E4M3 K/V cache (per-tensor scales 1/32)",
