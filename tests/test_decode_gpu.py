@@ -53,7 +53,17 @@ def test_decode_configs(fa, name):
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 64, 1024])
 def test_split_invariance(fa, splits):
+    # 3 sequences x 8 heads = 24 rows: the merge takes each row in four
+    # column slices (128 splits loaded up front, the rest in its loop)
     pc = workloads.paged_decode_inputs(3, [1000, 64, 4097], 8, 4, 64, seed=31)
+    check(fa, pc, num_splits=splits)
+
+
+@pytest.mark.parametrize("splits", [33, 100, 1024])
+def test_split_invariance_whole_rows(fa, splits):
+    # 6 sequences x 8 heads = 48 rows: the merge takes whole rows (32 splits
+    # loaded up front, the rest in its unrolled loop, with a remainder)
+    pc = workloads.paged_decode_inputs(6, [1000, 64, 4097, 0, 2500, 3333], 8, 4, 64, seed=41)
     check(fa, pc, num_splits=splits)
 
 
