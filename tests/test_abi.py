@@ -122,6 +122,19 @@ def test_fp8_workspace_and_auto_splits(lib):
     assert fa.fa512_decode_workspace_bytes_fp8(4, 0, 8, 4, 64, 10, 0) == 0
 
 
+def test_fp8_auto_splits_on_152_sms(lib):
+    # with no GPU the library plans for 152 SMs: the counts the fitted time
+    # models give on the nine decode shapes (8/4 heads, page 64)
+    import torch
+    if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the counts are for 152 SMs")
+    want = {(1, 4096): 64, (1, 16384): 74, (1, 28672): 75,
+            (16, 4096): 16, (16, 16384): 32, (16, 28672): 39,
+            (64, 4096): 8, (64, 16384): 19, (64, 28672): 28}
+    got = {(b, n): fa.fa512_decode_auto_splits_fp8(b, 1, 8, 4, 64, n) for b, n in want}
+    assert got == want
+
+
 def _decode_q(lib, **kw):
     a = dict(q=16, kp=16, vp=16, pt=16, kl=16, out=16, lse=None, b=2, ql=4, hq=8, hk=4, ps=64,
              npages=10, mpps=4, maxlen=200, scale=0.05, window=0, splits=0, ws=256,
