@@ -225,6 +225,15 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+def leg_sampler(device):
+    """A started ClockSampler for one separately timed leg (its calls run back
+    to back, so its clocks and power reasons can differ from the main step's)."""
+    cs = ClockSampler(device.index if device.index is not None else 0)
+    cs.start()
+    time.sleep(0.2)
+    return cs
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 _ORACLE_INPUTS = {}
@@ -413,6 +422,7 @@ def time_decode_fp8(args, fa, g, dev, stream, shapes, flush, world, peaks):
     torch.cuda.synchronize()
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in legs] for _ in range(args.steps)]
+    cs = leg_sampler(dev)
     for s in range(args.steps):
         flush.zero_()
         for i, d in enumerate(legs):
@@ -420,6 +430,7 @@ def time_decode_fp8(args, fa, g, dev, stream, shapes, flush, world, peaks):
             call(d)
             evs[s][i][1].record(stream)
     torch.cuda.synchronize()
+    clocks = cs.stop()
     ms = [sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)) / args.steps
           for i in range(len(legs))]
     ms = max_over_ranks(ms, dev)
@@ -437,7 +448,7 @@ def time_decode_fp8(args, fa, g, dev, stream, shapes, flush, world, peaks):
                 "decode_fp8_mma_kernel", source_digest(["decode_sm103.cu", "fa512_device.cuh",
                                                         "fa512_internal.h"])),
             "l2": "flushed before every step (each shape called once per step)",
-            "per_shape": per}
+            "clocks": clocks, "per_shape": per}
 
 
 def run_ours(args):
@@ -683,12 +694,14 @@ def run_ours(args):
             torch.cuda.synchronize()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
+            cs = leg_sampler(dev)
             for e0, e1 in evs:
                 flush.zero_()
                 e0.record(stream)
                 pp_call()
                 e1.record(stream)
             torch.cuda.synchronize()
+            leg_clocks = cs.stop()
             (t_pp,) = max_over_ranks([sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3], dev)
             tf = job_rate(flops, args.steps, world, t_pp) / 1e12
             prefill_paged[name] = {
@@ -696,7 +709,7 @@ def run_ours(args):
                             "%d/%d heads, causal" % (len(seqs), seqs, PAGE, hq_p, hk_p),
                 "value": tf, "unit": "TFLOP/s", "ms": t_pp / args.steps * 1e3,
                 "flops_per_call": flops, "frac_of_measured_bf16": tf / world / peaks["bf16_tflops"],
-                "l2": "flushed before every call"}
+                "l2": "flushed before every call", "clocks": leg_clocks}
             del kp, vp, pq, pout
         assert fa.fa512_device_status() == 0
 
@@ -723,19 +736,21 @@ def run_ours(args):
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+        cs = leg_sampler(dev)
         for e0, e1 in evs:
             flush.zero_()
             e0.record(stream)
             l_call()
             e1.record(stream)
         torch.cuda.synchronize()
+        leg_clocks = cs.stop()
         (t_l,) = max_over_ranks([sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3], dev)
         tf = job_rate(lflops, args.steps, world, t_l) / 1e12
         local256 = {"workload": "local layer: %d tokens from 0, window %d, %d/%d heads, head dim 256, "
                                 "causal" % (L["seqlen"], L["window"], L["n_q_heads"], L["n_kv_heads"]),
                     "value": tf, "unit": "TFLOP/s", "ms": t_l / args.steps * 1e3,
                     "flops_per_call": lflops, "frac_of_measured_bf16": tf / world / peaks["bf16_tflops"],
-                    "l2": "flushed before every call"}
+                    "l2": "flushed before every call", "clocks": leg_clocks}
         del lq, lk, lv, lout
         assert fa.fa512_device_status() == 0
 
@@ -767,12 +782,14 @@ def run_ours(args):
             torch.cuda.synchronize()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
+            cs = leg_sampler(dev)
             for e0, e1 in evs:
                 flush.zero_()
                 e0.record(stream)
                 b_call()
                 e1.record(stream)
             torch.cuda.synchronize()
+            leg_clocks = cs.stop()
             (t_b,) = max_over_ranks([sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3], dev)
             tf = job_rate(flops, args.steps, world, t_b) / 1e12
             ach = flops / (t_b / args.steps) / 1e12
@@ -789,7 +806,7 @@ def run_ours(args):
                              "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                              "peak_kind": "%s burst bf16 (MEASURED_PEAKS.json)" % peak_kind,
                              "traffic": recorded_traffic("prefill_so_kernel_" + name, pf_src)},
-                "l2": "flushed before every call"}
+                "l2": "flushed before every call", "clocks": leg_clocks}
             del bq, bk, bv, bout, blse
         assert fa.fa512_device_status() == 0
 
@@ -831,12 +848,14 @@ def run_ours(args):
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+        cs = leg_sampler(dev)
         for e0, e1 in evs:
             flush.zero_()
             e0.record(stream)
             dq_call()
             e1.record(stream)
         torch.cuda.synchronize()
+        leg_clocks = cs.stop()
         (t_dq,) = max_over_ranks([sum(e0.elapsed_time(e1) for e0, e1 in evs) / 1e3], dev)
         dq_bytes = decode_bytes(b, n, hq, hk, ql)
         gbs = job_rate(dq_bytes, args.steps, world, t_dq) / 1e9
@@ -844,7 +863,7 @@ def run_ours(args):
                                 "%d/%d heads, page %d, num_splits auto" % (ql, b, n, hq, hk, PAGE),
                     "value": gbs, "unit": "GB/s", "ms": t_dq / args.steps * 1e3,
                     "bytes_per_call": dq_bytes, "frac_of_measured_hbm": gbs / world / peaks["hbm_gbs"],
-                    "l2": "flushed before every call"}
+                    "l2": "flushed before every call", "clocks": leg_clocks}
 
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu:
