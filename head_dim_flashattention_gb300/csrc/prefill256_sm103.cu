@@ -105,7 +105,7 @@ struct Item {
     int kvh, pair;
     int t0, ntok;                // this CTA's first token and token count (<= 0: no rows)
     int p_first, p_last;         // positions of this CTA's first and last token
-    int kt_begin, n_kt;          // key tiles of the pair's visible band
+    int key_begin, n_kt;         // first key and 128-key tiles of the pair's visible band
 };
 
 __host__ __device__ inline Item item_geometry(int idx, const Prefill256Params& p, int rank) {
@@ -124,8 +124,12 @@ __host__ __device__ inline Item item_geometry(int idx, const Prefill256Params& p
     if (p.causal && pair_last + 1 < j_hi) j_hi = pair_last + 1;
     if (p.window > 0 && pair_first - p.window + 1 > j_lo) j_lo = pair_first - p.window + 1;
     if (j_hi < j_lo) j_hi = j_lo;
-    it.kt_begin = j_lo / BN;
-    it.n_kt = j_hi > j_lo ? (j_hi + BN - 1) / BN - it.kt_begin : 0;
+    // the tiles start at the band's first key, not at a multiple of 128: a
+    // window's band of 1,024 + 2T - 1 keys then takes 9 tiles at every
+    // offset instead of 9 or 10 (the load's row coordinate has no alignment
+    // rule; keys past the band are masked, rows past the keys read zeros)
+    it.key_begin = j_lo;
+    it.n_kt = j_hi > j_lo ? (j_hi - j_lo + BN - 1) / BN : 0;
     return it;
 }
 
@@ -248,7 +252,7 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
             auto load_k = [&](const TileCursor& t) {
                 const int b = t.g & 1;
                 if (rank == 0) mbar_arrive_expect_tx(&bars[Smem::FULL_K + b], 2 * SLOT);
-                const int key0 = (t.it.kt_begin + t.j) * BN + irank * K_BOX_ROWS;
+                const int key0 = t.it.key_begin + t.j * BN + irank * K_BOX_ROWS;
                 for (int c = 0; c < 4; ++c)
                     tma2_load_3d(smem + Smem::ring + (SLOT_K0 + b) * SLOT + c * K_BOX, &tmk,
                                  leader_bar(Smem::FULL_K + b), c * 64, t.it.kvh, key0);
@@ -288,7 +292,7 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                     for (int b = 0; b < 2; ++b)
                         tma2_load_3d(smem + Smem::ring + SLOT_V * SLOT + b * V_BOX, &tmv,
                                      leader_bar(Smem::P_FULL + (g & 1)), (irank * 2 + b) * 64, vc.it.kvh,
-                                     (vc.it.kt_begin + vc.j) * BN);
+                                     vc.it.key_begin + vc.j * BN);
                     vc.advance(p, irank);
                     progress = true;
                 }
@@ -531,7 +535,7 @@ prefill256_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
                 for (int c = 0; c < BH; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
                 const int qpos = it.p_first + tok;
-                const int key0 = (it.kt_begin + j) * BN + kh * BH;
+                const int key0 = it.key_begin + j * BN + kh * BH;
                 const bool half_full = it.ntok > 0 && key0 + BH <= p.seqlen_k &&
                                        (!p.causal || key0 + BH - 1 <= it.p_first) &&
                                        (p.window <= 0 || key0 > it.p_last - p.window);
