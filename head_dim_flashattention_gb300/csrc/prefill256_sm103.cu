@@ -15,7 +15,7 @@
 //     (a pair) and issues 2-SM MMAs (cta_group::2, M = 256), each CTA holding
 //     half of every K tile (64 keys x 256) and half of every V tile's output
 //     columns (128 keys x 128).
-//   * Under a 1,024-key window a pair sees only nine or ten 128-key tiles,
+//   * Under a 1,024-key window a pair sees only nine 128-key tiles,
 //     so a per-launch setup (barriers, TMEM, the first loads) would cost
 //     about as much as the work.  The kernel is persistent: one cluster per
 //     SM pair walks a contiguous range of (KV head, pair) items, chosen on
